@@ -1,0 +1,497 @@
+#!/usr/bin/env python
+"""Throughput of the tensor-parallel MLP (column-parallel linear + GeLU -> row-parallel linear,
+forward + backward, all shards on one GB300) through the library's C ABI.
+
+One step = tp_mlp_forward + tp_mlp_backward over one batch of the workload (every kernel of the
+path: column GEMM with the bias + GeLU epilogue, row GEMM with the fused shard sum, the dY GEMM
+with the GeLU' epilogue, both weight-gradient GEMMs, the input-gradient GEMM with the fused
+shard sum, and the bias-gradient column sums). Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload gpt3|mlp2|p3|sweep:T:n]
+                  [--reduce fused|partials] [--impl native|reference]
+
+--impl reference times the fp64 CPU oracle on the host cores instead (a bounded sample of the
+same workload per step). With N > 1 (torchrun) every rank runs an independent replica of the
+workload on its own GPU: there is no exchange between the replicas (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "TP-sharded MLP fwd+bwd TFLOP/s (bf16) on 1 GB300 and % of tensor-core peak"
+UNIT = "TFLOP/s"
+KERNEL_SOURCES = ["tc_gemm.cuh", "tc_launch.cu", "tc_gemm_kmn.cu", "tc_gemm_kk.cu",
+                  "tc_gemm_mnmn.cu", "device_common.cuh"]
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemm_tc_gpt3_mlp_T2048_tp8.md")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default="gpt3")
+    ap.add_argument("--reduce", choices=["fused", "partials"], default="fused")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    return ap.parse_args()
+
+
+def workload(name: str) -> wl.MlpWorkload:
+    if name == "gpt3":
+        return wl.GPT3_MLP_T2048_TP8
+    if name == "mlp2":
+        return wl.MLP_T4096_H1024_F4096_TP2
+    if name == "p3":
+        return wl.P3_FP32_FWD
+    if name.startswith("sweep:"):
+        _, T, n = name.split(":")
+        return wl.SWEEP_H8192_F28672.with_shape(tokens=int(T), tp_degree=int(n))
+    raise SystemExit(f"unknown workload {name}")
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_setup(gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != gpus and world > 1:
+        raise SystemExit(f"--gpus {gpus} but WORLD_SIZE {world}")
+    return world, rank, local
+
+
+def dist_init(world: int, local: int):
+    import torch
+    import torch.distributed as dist
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return torch.device("cuda", local)
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_QUERY}", "--format=csv,noheader,nounits",
+                 "-i", str(device_index), "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_median": statistics.median(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- peaks / profile
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return {"bf16_sustained": p["bf16_tflops_sustained"], "bf16_burst": p["bf16_tflops"],
+                "hbm_gbs": p["hbm_gbs"], "source": "measured"}
+    return {"bf16_sustained": 1700.0, "bf16_burst": 1900.0, "hbm_gbs": 6800.0,
+            "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "tensor_sharded_linear_bias_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_name: str):
+    """DRAM bytes per launch of the tensor-core GEMM from the committed ncu summary, if that
+    summary was taken on the current kernel source and this workload; else None."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    fields = {}
+    for line in open(PROFILE_SUMMARY):
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    if fields.get("workload") != workload_name:
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------- the step
+class MlpBench:
+    def __init__(self, w: wl.MlpWorkload, reduce: int, device, keep_host: bool):
+        import numpy as np
+        import torch
+
+        import tensor_sharded_linear_bias_gb300 as tp
+
+        self.tp, self.w, self.device = tp, w, device
+        bf16 = w.dtype == "bf16"
+        cdt = torch.bfloat16 if bf16 else torch.float32
+        n, T, H, F = w.tp_degree, w.tokens, w.hidden, w.ffn
+        Fs = F // n
+        raw = wl.mlp_tensors(w)
+        host = {}
+        dev = {}
+        for k, v in raw.items():
+            if bf16:
+                t, f = wl.to_bf16(v)
+            else:
+                t, f = torch.from_numpy(np.ascontiguousarray(v)), v
+            dev[k] = t
+            if keep_host:
+                host[k] = f
+        del raw
+        self.host = host
+        self.X = dev["X"].to(device)
+        self.dZ = dev["dZ"].to(device)
+        self.X_pinned = dev["X"].pin_memory()
+        self.dZ_pinned = dev["dZ"].pin_memory()
+        self.A = [dev["A"][:, i * Fs:(i + 1) * Fs].contiguous().to(device) for i in range(n)]
+        self.a = [dev["a"][i * Fs:(i + 1) * Fs].contiguous().to(device) for i in range(n)]
+        self.B = [dev["B"][i * Fs:(i + 1) * Fs, :].contiguous().to(device) for i in range(n)]
+        self.b = dev["b"].to(device)
+        del dev
+        self.desc = tp.MlpDesc(tokens=T, hidden=H, ffn=F, tp_degree=n,
+                               dtype=tp.TP_BF16 if bf16 else tp.TP_F32,
+                               act=tp.TP_ACT_GELU_ERF, reduce=reduce)
+        self.ws = tp.new_workspace(tp.tp_mlp_workspace_size(self.desc), device)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.Z = torch.empty(T, H, **f32)
+        self.Hs = [torch.empty(T, Fs, dtype=cdt, device=device) for _ in range(n)]
+        self.Ys = [torch.empty(T, Fs, dtype=cdt, device=device) for _ in range(n)]
+        self.dX = torch.empty(T, H, **f32)
+        self.dA = [torch.empty(H, Fs, **f32) for _ in range(n)]
+        self.dB = [torch.empty(Fs, H, **f32) for _ in range(n)]
+        self.da = [torch.empty(Fs, **f32) for _ in range(n)]
+        self.db = torch.empty(H, **f32)
+        self.Z_host = torch.empty(T, H, dtype=torch.float32).pin_memory()
+        self.dX_host = torch.empty(T, H, dtype=torch.float32).pin_memory()
+        self.backward = w.backward
+        e = 2 if bf16 else 4
+        self.operand_bytes = e * (T * H * 2 + 2 * H * F) + e * 2 * T * F
+
+    def step(self):
+        tp = self.tp
+        tp.tp_mlp_forward(self.desc, self.X, self.A, self.a, self.B, self.b, self.Z, self.Hs,
+                          self.Ys, self.ws)
+        if self.backward:
+            tp.tp_mlp_backward(self.desc, self.X, self.A, self.B, self.Hs, self.Ys, self.dZ,
+                               self.dX, self.dA, self.da, self.dB, self.db, self.ws)
+
+    def step_e2e(self):
+        """The same step with its inputs copied from pinned host memory and its results
+        (Z, dX) copied back, all on the current stream."""
+        self.X.copy_(self.X_pinned, non_blocking=True)
+        self.dZ.copy_(self.dZ_pinned, non_blocking=True)
+        self.step()
+        self.Z_host.copy_(self.Z, non_blocking=True)
+        if self.backward:
+            self.dX_host.copy_(self.dX, non_blocking=True)
+
+    @property
+    def flops(self) -> int:
+        return self.w.flops_fwd_bwd if self.backward else self.w.flops_fwd
+
+    @property
+    def h2d_bytes(self) -> int:
+        return self.X.numel() * self.X.element_size() * (2 if self.backward else 1)
+
+    @property
+    def d2h_bytes(self) -> int:
+        return self.Z.numel() * 4 * (2 if self.backward else 1)
+
+
+def time_steps(fn, steps: int, world: int):
+    import torch
+
+    barrier(world)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        fn()
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    return start.elapsed_time(end)
+
+
+# ----------------------------------------------------------------------------- the oracle
+def oracle_sample(w: wl.MlpWorkload, host: dict, rows: int, cols_per_shard: int):
+    """A bounded sample of the workload for the CPU oracle: `rows` token rows and the first
+    `cols_per_shard` ffn columns of every shard (the MLP restricted to those rows and ffn
+    columns, still split into tp_degree shards). Returns (callable, flops per call, text)."""
+    import numpy as np
+
+    import oracle
+
+    n, Fs = w.tp_degree, w.ffn // w.tp_degree
+    c = min(cols_per_shard, Fs)
+    r = min(rows, w.tokens)
+    cols = np.concatenate([np.arange(i * Fs, i * Fs + c) for i in range(n)])
+    X, dZ = host["X"][:r], host["dZ"][:r]
+    A, a, B, b = host["A"][:, cols], host["a"][cols], host["B"][cols, :], host["b"]
+
+    def run():
+        fwd = oracle.mlp_forward(X, A, a, B, b, n)
+        if w.backward:
+            oracle.mlp_backward(X, A, a, B, b, dZ, n, fwd)
+
+    per = (12 if w.backward else 4) * r * w.hidden * (c * n)
+    text = (f"{r} token rows x {c} ffn columns per shard ({c * n} of {w.ffn}) of the workload, "
+            f"{'fwd+bwd' if w.backward else 'fwd'}, fp64 numpy")
+    return run, per, text
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, host, seconds: float):
+    run, per, text = oracle_sample(w, host, rows=256, cols_per_shard=64)
+    run()  # warm caches / BLAS threads
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        run()
+        reps += 1
+        el = time.perf_counter() - t0
+        if (el >= seconds and reps >= 3) or reps >= 1000:
+            break
+    value = per * reps / el / 1e12
+    return {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+            "sample": f"{text}; {reps} repetitions in {el:.1f} s"}
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return 0
+    import numpy as np  # noqa: F401
+
+    host = {}
+    raw = wl.mlp_tensors(w)
+    for k, v in raw.items():
+        host[k] = wl.to_bf16(v)[1] if w.dtype == "bf16" else v
+    del raw
+    run, per, text = oracle_sample(w, host, rows=128, cols_per_shard=32)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    el = time.perf_counter() - t0
+    value = per * args.steps / el / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "tokens": w.tokens, "hidden": w.hidden,
+                       "ffn": w.ffn, "tp_degree": w.tp_degree, "sample": text},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(),
+                             "kind": "oracle", "sample": text},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    args = parse_args()
+    w = workload(args.workload)
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        return run_reference(args, w, world, rank)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    import torch
+
+    device = dist_init(world, local)
+    import tensor_sharded_linear_bias_gb300 as tp
+
+    reduce = tp.TP_REDUCE_FUSED if args.reduce == "fused" else tp.TP_REDUCE_PARTIALS
+    keep_host = (rank == 0 and world == 1 and not args.no_cpu_baseline)
+    mb = MlpBench(w, reduce, device, keep_host)
+
+    # ---- device-resident throughput, with launch tracing over the timed region
+    for _ in range(args.warmup):
+        mb.step()
+    tp.tp_check_status(mb.ws)
+    sampler = ClockSampler(device.index if device.index is not None else 0) if rank == 0 else None
+    launches_per_step = 7 if w.backward else 2
+    tp.tp_trace_start(args.steps * (launches_per_step + 2) + 16)
+    ms = time_steps(mb.step, args.steps, world)
+    recs = tp.tp_trace_stop(args.steps * (launches_per_step + 2) + 16)
+    clocks = sampler.stop() if sampler else None
+    tp.tp_check_status(mb.ws)
+    ms = max_over_ranks(ms, world)
+    ms_per_step = ms / args.steps
+    value = mb.flops * args.steps * world / (ms / 1e3) / 1e12
+
+    # ---- end to end: host inputs in, host results out, every step
+    e2e = None
+    if not args.no_e2e:
+        for _ in range(args.warmup):
+            mb.step_e2e()
+        ms_e = max_over_ranks(time_steps(mb.step_e2e, args.steps, world), world)
+        e2e = {"value": mb.flops * args.steps * world / (ms_e / 1e3) / 1e12, "unit": UNIT,
+               "ms_per_step": ms_e / args.steps, "h2d_bytes_per_step": mb.h2d_bytes,
+               "d2h_bytes_per_step": mb.d2h_bytes}
+        tp.tp_check_status(mb.ws)
+
+    if rank != 0:
+        return 0
+
+    # ---- roofline of the dominant kernel (largest total device time in the timed region)
+    pk = peaks()
+    by_kernel, by_tag = {}, {}
+    for r in recs:
+        k = by_kernel.setdefault(r["kernel"], {"ms": 0.0, "flops": 0.0, "bytes": 0.0, "n": 0})
+        k["ms"] += r["ms"]
+        k["flops"] += r["flops"]
+        k["bytes"] += r["bytes"]
+        k["n"] += 1
+        t = by_tag.setdefault(f'{r["kernel"]}:{r["tag"]}', {"ms": 0.0, "flops": 0.0, "n": 0})
+        t["ms"] += r["ms"]
+        t["flops"] += r["flops"]
+        t["n"] += 1
+    dom = max(by_kernel, key=lambda k: by_kernel[k]["ms"])
+    d = by_kernel[dom]
+    total_ms = sum(v["ms"] for v in by_kernel.values())
+    if dom in ("gemm_tc", "gemm_ffma"):
+        achieved = d["flops"] / (d["ms"] / 1e3) / 1e12
+        peak = pk["bf16_sustained"] if dom == "gemm_tc" else None
+        roof = {"bound": "tensor" if dom == "gemm_tc" else "alu", "kernel": dom,
+                "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": (achieved / peak) if peak else None,
+                "peak_source": (f"MEASURED_PEAKS.json bf16_tflops_sustained (of {pk['source']})"
+                                if dom == "gemm_tc" else None)}
+    else:
+        achieved = d["bytes"] / (d["ms"] / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                "peak_source": f"MEASURED_PEAKS.json hbm_gbs (of {pk['source']})"}
+    roof["launches"] = d["n"]
+    roof["avg_launch_ms"] = d["ms"] / d["n"]
+    roof["share_of_kernel_time"] = d["ms"] / total_ms
+    traffic = profiled_traffic(w.name)
+    roof["traffic"] = traffic
+    roof["traffic_note"] = ("dram__bytes_read.sum + dram__bytes_write.sum per launch from the "
+                            "committed ncu summary" if traffic is not None else
+                            "null: no ncu capture of the current kernel source for this workload")
+    kernels = {k: {"launches": v["n"], "avg_ms": v["ms"] / v["n"],
+                   "tflops": (v["flops"] / (v["ms"] / 1e3) / 1e12) if v["flops"] else None,
+                   "share": v["ms"] / total_ms} for k, v in sorted(by_tag.items())}
+
+    cpu = None
+    if keep_host:
+        cpu = cpu_baseline(w, mb.host, args.cpu_seconds)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": w.tokens, "hidden": w.hidden, "ffn": w.ffn,
+                   "tp_degree": w.tp_degree, "reduce": args.reduce,
+                   "pass": "fwd+bwd" if w.backward else "fwd",
+                   "parallelism": "single GPU, all shards on it" if world == 1 else
+                   f"{world} independent replicas (no exchange)",
+                   "l2": f"no flush: {mb.operand_bytes / 1e9:.2f} GB of operands per step vs "
+                         "126 MB of L2"},
+        "pct_of_peak": value / pk["bf16_sustained"] * 100.0 if w.dtype == "bf16" else None,
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": len(recs),
+        "roofline": roof,
+        "kernels": kernels,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -52,7 +52,7 @@ from scipy.special import erf
 
 __all__ = [
     "gelu", "gelu_grad", "shard_size", "split_columns", "split_rows", "split_vector",
-    "concat_columns", "qkv_head_shards", "linear", "column_parallel_forward",
+    "concat_columns", "qkv_head_shards", "linear", "bias_grad", "column_parallel_forward",
     "column_parallel_backward", "row_parallel_forward", "row_parallel_backward",
     "mlp_forward", "mlp_backward", "mlp_columns", "attn_forward", "attn_backward",
 ]
@@ -128,6 +128,11 @@ def linear(X, W, bias=None) -> np.ndarray:
     return out
 
 
+def bias_grad(G) -> np.ndarray:
+    """Gradient of a bias broadcast over the token rows: the sum over tokens of G."""
+    return _f64(G).sum(axis=0)
+
+
 # ----------------------------------------------------------------------------- column parallel
 def column_parallel_forward(X, W_shards, b_shards=None, act: str = "none"):
     """Y_i = act(X W_i + b_i) for every shard i; X is replicated ([Lansai]; [CSDN]).
@@ -155,7 +160,7 @@ def column_parallel_backward(X, W_shards, H_shards, dY_shards, act: str = "none"
     for i, dYi in enumerate(dY_shards):
         dH.append(_f64(dYi) * gelu_grad(H_shards[i]) if act == "gelu" else _f64(dYi))
     dW = [X.T @ dHi for dHi in dH]
-    dbias = [dHi.sum(axis=0) for dHi in dH]
+    dbias = [bias_grad(dHi) for dHi in dH]
     dX = None
     for dHi, Wi in zip(dH, W_shards):
         term = dHi @ _f64(Wi).T
@@ -184,7 +189,7 @@ def row_parallel_backward(X_shards, W_shards, dZ):
     dZ = _f64(dZ)
     dX = [dZ @ _f64(Wi).T for Wi in W_shards]
     dW = [_f64(Xi).T @ dZ for Xi in X_shards]
-    return dX, dW, dZ.sum(axis=0)
+    return dX, dW, bias_grad(dZ)
 
 
 # ----------------------------------------------------------------------------- the MLP

@@ -1,0 +1,79 @@
+// Host-side interface between the C ABI layer (tp_api.cu) and the kernel launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "tp_mlp.h"
+
+namespace tpk {
+
+constexpr int kMaxShards = 64;
+
+// Workspace layout: a 256-byte status block, then scratch (256-byte aligned).
+constexpr size_t kStatusBytes = 256;
+
+// Device status codes written by kernels (first error wins).
+constexpr int kDevTimeoutBase = 0x100;  // | (role << 4) | wait site
+
+enum EpiKind : int {
+  EPI_STORE_F32 = 0,      // D (fp32) = acc (+ bias[n] once, when bias != nullptr)
+  EPI_BIAS_ACT = 1,       // H = acc + bias[n] -> D (optional), Y = act(H) -> D2  (bf16 / fp32)
+  EPI_DACT = 2,           // D = acc * act'(aux[m,n])                               (bf16 / fp32)
+};
+
+// One launch of a (grouped) GEMM: D_g[M,N] = A_g[M,K] * B_g[K,N] for every group g, or,
+// with ksum, one D[M,N] = sum_g A_g B_g (K spans the groups in group order).
+//  A element (m,k) at A[g] + (a_mn ? k*lda + m : m*lda + k)
+//  B element (k,n) at B[g] + (b_mn ? k*ldb + n : n*ldb + k)
+//  D element (m,n) at D[g] + m*ldd + n
+struct GemmSpec {
+  int64_t M = 0, N = 0, K = 0;
+  int groups = 1;
+  int ksum = 0;
+  int a_mn = 0, b_mn = 0;
+  const void* A[kMaxShards] = {};
+  const void* B[kMaxShards] = {};
+  void* D[kMaxShards] = {};
+  void* D2[kMaxShards] = {};
+  const void* bias[kMaxShards] = {};
+  const void* aux[kMaxShards] = {};
+  int64_t lda = 0, ldb = 0, ldd = 0, ldd2 = 0, ldaux = 0;
+  int epi = EPI_STORE_F32;
+  int act = TP_ACT_NONE;
+  int* status = nullptr;
+};
+
+// bf16 inputs, tcgen05 tensor cores (sm_103a). Returns cudaSuccess or the launch error.
+cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st);
+// fp32 inputs, FFMA (no TF32).
+cudaError_t launch_simt_gemm(const GemmSpec& s, cudaStream_t st);
+
+// Z[T,N] = sum_{i<n} P[i][T,N] + bias (bias may be null; bias dtype: bf16 if bias_bf16).
+cudaError_t launch_shard_reduce(const float* P, int n, int64_t T, int64_t N,
+                                const void* bias, int bias_bf16, float* Z, cudaStream_t st);
+
+// Column sums: out_s[c] = sum_{r<rows} in_s[r*ld_s + c] for every segment s.
+struct ColsumSeg {
+  const void* in;
+  float* out;
+  int64_t cols;
+  int64_t ld;
+};
+cudaError_t launch_colsum(const ColsumSeg* segs, int nseg, int64_t rows, int in_bf16,
+                          cudaStream_t st);
+
+// dH = dY * act'(H) elementwise over n shards of [T, w] (ld for dY may differ: gathered).
+cudaError_t launch_dact(const void* const* dY, int64_t ld_dy, const void* const* H,
+                        void* const* dH, int n, int64_t T, int64_t w, int act, int bf16,
+                        cudaStream_t st);
+
+// One-block self-test of the bounded wait (see tp_selftest_wait_timeout).
+cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t st);
+
+// Device facts (cached per device).
+int device_sm_count();
+
+}  // namespace tpk

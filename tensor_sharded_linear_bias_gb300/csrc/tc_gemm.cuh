@@ -1,0 +1,413 @@
+// Persistent, warp-specialised bf16 GEMM on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// One CTA per SM loops over output tiles of 128 x 256. Roles:
+//   warp 0 (one lane)  : TMA producer -- streams 64-wide K slices of A and B into a
+//                        4-stage ring of 128B-swizzled shared-memory tiles.
+//   warp 1 (one lane)  : MMA issuer  -- tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32)
+//                        into one of two TMEM accumulators (2 x 256 columns), so the
+//                        epilogue of tile i overlaps the main loop of tile i+1.
+//   warps 2..5         : epilogue    -- tcgen05.ld of the accumulator (one row per thread),
+//                        the fused epilogue (bias, GeLU, GeLU', fp32 or bf16 store).
+//
+// Grouping: the tp_degree shards are groups of one launch. Either every group has its own
+// output (tiles enumerate group x m x n), or -- the on-device form of the pages' All-Reduce
+// -- one output accumulates every group's K range into the same TMEM accumulator, in group
+// order ("ksum").
+//
+// Operand layouts: A is K-major ([M,K] row-major) or MN-major ([K,M] row-major); likewise
+// B ([N,K] or [K,N]). The MN-major forms let the backward use X^T, Y_i^T, B_i^T and A_i^T
+// straight from the forward's row-major buffers without a transpose.
+//
+// Every mbarrier wait is bounded (kWaitLimitNs); a wait that runs out records an error code
+// in the status word, raises a CTA-wide abort flag, drains the copies and MMAs in flight,
+// frees TMEM and returns.
+#pragma once
+
+#include <cuda.h>
+#include <cstdint>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace tpk {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;                       // one 128-byte swizzle row of bf16
+constexpr int STAGES = 4;
+constexpr int ACC_BUFS = 2;
+constexpr int TMEM_COLS = ACC_BUFS * BN;     // 512 (all of TMEM)
+constexpr int A_BYTES = BM * BK * 2;         // 16 KiB
+constexpr int B_BYTES = BN * BK * 2;         // 32 KiB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int MN_BOX_BYTES = 64 * BK * 2;    // one [64 K rows][64 MN] box: 8 KiB
+constexpr int NUM_THREADS = 192;
+constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+
+struct __align__(128) TcParams {
+  CUtensorMap tmA[kMaxShards];
+  CUtensorMap tmB[kMaxShards];
+  void* D[kMaxShards];
+  void* D2[kMaxShards];
+  const void* bias[kMaxShards];
+  const void* aux[kMaxShards];
+  long long ldd, ldd2, ldaux;
+  int M, N;
+  int kblocks;      // K blocks of 64 per group
+  int groups;
+  int ksum;
+  int tiles_m, tiles_n, num_tiles;
+  int epi, act;
+  int* status;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor of a 128B-swizzled operand tile (tcgen05 format:
+// start >> 4 at bit 0, leading byte offset >> 4 at bit 16, stride byte offset >> 4 at bit
+// 32, descriptor version 1 at bit 46, swizzle mode "128B" = 2 at bit 61).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, operand majors,
+// N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns: thread t of the warp gets row (quadrant + t).
+// The wait is in the same asm statement, so no use of r[] can be scheduled before it.
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+      "[%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ------------------------------------------------------------------ tile decode
+__device__ __forceinline__ void decode_tile(const TcParams& p, int t, int& g, int& mb, int& nb) {
+  const int per = p.tiles_m * p.tiles_n;
+  g = t / per;
+  const int r = t - g * per;
+  mb = r % p.tiles_m;
+  nb = r / p.tiles_m;
+}
+
+// ------------------------------------------------------------------ epilogue (one row, 32 cols)
+// bias / aux / outputs are bf16 here (this GEMM's inputs are bf16), except EPI_STORE_F32's D.
+// Loads the first `valid_cols` (a multiple of 8) of 32 bf16 values; the rest read as 0.
+__device__ __forceinline__ void load_bf16x32(const uint16_t* src, float* out, int valid_cols) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 u = (q * 8 < valid_cols) ? s[q] : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = unpack_bf16x2(w[j]);
+      out[q * 8 + 2 * j] = f.x;
+      out[q * 8 + 2 * j + 1] = f.y;
+    }
+  }
+}
+
+__device__ __forceinline__ void store_bf16_row(uint16_t* dst, const float* v, int valid_cols) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (q * 8 < valid_cols) {
+      uint4 u;
+      u.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
+      u.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
+      u.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
+      u.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+      reinterpret_cast<uint4*>(dst)[q] = u;
+    }
+  }
+}
+
+__device__ __forceinline__ void epilogue_chunk(const TcParams& p, int g, int row, int col0,
+                                               float* v) {
+  const int valid = min(32, p.N - col0);  // a multiple of 8 (N % 8 == 0)
+  const int og = p.ksum ? 0 : g;
+  if (p.epi == EPI_STORE_F32) {
+    if (p.bias[og] != nullptr) {
+      float bv[32];
+      load_bf16x32(static_cast<const uint16_t*>(p.bias[og]) + col0, bv, valid);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] += bv[i];
+    }
+    float* d = static_cast<float*>(p.D[og]) + static_cast<long long>(row) * p.ldd + col0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (q * 4 < valid)
+        reinterpret_cast<float4*>(d)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2],
+                                                      v[4 * q + 3]);
+    }
+  } else if (p.epi == EPI_BIAS_ACT) {
+    if (p.bias[og] != nullptr) {
+      float bv[32];
+      load_bf16x32(static_cast<const uint16_t*>(p.bias[og]) + col0, bv, valid);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] += bv[i];
+    }
+    if (p.D[og] != nullptr)
+      store_bf16_row(static_cast<uint16_t*>(p.D[og]) + static_cast<long long>(row) * p.ldd + col0,
+                     v, valid);
+    if (p.act == TP_ACT_GELU_ERF) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+    }
+    store_bf16_row(static_cast<uint16_t*>(p.D2[og]) + static_cast<long long>(row) * p.ldd2 + col0,
+                   v, valid);
+  } else {  // EPI_DACT (aux = the saved pre-activation, read only with an activation)
+    if (p.act == TP_ACT_GELU_ERF) {
+      float h[32];
+      load_bf16x32(static_cast<const uint16_t*>(p.aux[og]) + static_cast<long long>(row) * p.ldaux +
+                       col0,
+                   h, valid);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] *= gelu_erf_grad(h[i]);
+    }
+    store_bf16_row(static_cast<uint16_t*>(p.D[og]) + static_cast<long long>(row) * p.ldd + col0, v,
+                   valid);
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const uint32_t smem_base = smem_addr(smem);
+  const uint32_t bar_base = smem_addr(bars);
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + ACC_BUFS + a); };
+  const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 2 * ACC_BUFS);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < ACC_BUFS; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int total_kb = p.ksum ? p.kblocks * p.groups : p.kblocks;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      uint32_t stage = 0, phase = 0;
+      long long issued = 0;
+      bool failed = false;
+      for (int t = blockIdx.x; t < p.num_tiles && !failed; t += gridDim.x) {
+        int g, mb, nb;
+        decode_tile(p, t, g, mb, nb);
+        for (int kb = 0; kb < total_kb; ++kb) {
+          if (*abort_flag) { failed = true; break; }
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, kWaitLimitNs)) {
+            report_status(p.status, kDevTimeoutBase | 0x10);
+            *abort_flag = 1;
+            failed = true;
+            break;
+          }
+          const int kg = p.ksum ? kb / p.kblocks : g;
+          const int kk = (p.ksum ? kb % p.kblocks : kb) * BK;
+          const uint32_t fb = full_bar(stage);
+          const uint32_t sa = smem_base + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          if (!A_MN) {
+            tma_load_2d(sa, &p.tmA[kg], kk, mb * BM, fb);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BM / 64; ++j)
+              tma_load_2d(sa + j * MN_BOX_BYTES, &p.tmA[kg], mb * BM + 64 * j, kk, fb);
+          }
+          if (!B_MN) {
+            tma_load_2d(sb, &p.tmB[kg], kk, nb * BN, fb);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(sb + j * MN_BOX_BYTES, &p.tmB[kg], nb * BN + 64 * j, kk, fb);
+          }
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (failed) {
+        // Drain: wait (bounded) until every copy this thread issued has landed.
+        for (int s = 0; s < STAGES; ++s) {
+          if (issued > s) {
+            const long long last = s + ((issued - 1 - s) / STAGES) * STAGES;
+            mbar_wait_bounded(full_bar(s), static_cast<uint32_t>((last / STAGES) & 1), 100000000ull);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = idesc_bf16(BM, BN, A_MN, B_MN);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool failed = false;
+      for (int t = blockIdx.x; t < p.num_tiles && !failed; t += gridDim.x) {
+        if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, kWaitLimitNs)) {
+          report_status(p.status, kDevTimeoutBase | 0x20);
+          *abort_flag = 1;
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < total_kb; ++kb) {
+          if (*abort_flag) { failed = true; break; }
+          if (!mbar_wait_bounded(full_bar(stage), phase, kWaitLimitNs)) {
+            report_status(p.status, kDevTimeoutBase | 0x21);
+            *abort_flag = 1;
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_base + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = A_MN ? sdesc_sw128(sa + k * 2048, MN_BOX_BYTES, 1024)
+                                     : sdesc_sw128(sa + k * 32, 16, 1024);
+            const uint64_t bd = B_MN ? sdesc_sw128(sb + k * 2048, MN_BOX_BYTES, 1024)
+                                     : sdesc_sw128(sb + k * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          umma_commit(empty_bar(stage));
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (failed) break;
+        umma_commit(tfull_bar(acc));
+        if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1u; }
+      }
+      if (failed) {
+        // Drain: all MMAs issued so far complete before TMEM is freed.
+        umma_commit(drain_bar);
+        mbar_wait_bounded(drain_bar, 0, 100000000ull);
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue warps 2..5
+    const int quad = warp & 3;  // TMEM lanes this warp may read: 32*quad .. 32*quad+31
+    uint32_t acc = 0, acc_phase = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+      int g, mb, nb;
+      decode_tile(p, t, g, mb, nb);
+      if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, kWaitLimitNs)) {
+        if (lane == 0) report_status(p.status, kDevTimeoutBase | 0x30);
+        *abort_flag = 1;
+        break;
+      }
+      if (*abort_flag) break;
+      tc_fence_after();
+      const int row = mb * BM + quad * 32 + lane;
+      const uint32_t trow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        const int col0 = nb * BN + c0;
+        if (col0 >= p.N) break;  // uniform across the warp
+        float v[32];
+        tmem_ld_32cols(trow + c0, v);
+        if (row < p.M) epilogue_chunk(p, g, row, col0, v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+}  // namespace tc
+}  // namespace tpk

@@ -1,0 +1,97 @@
+// Host side of the tcgen05 GEMM: TMA descriptor encoding, tile counts, grid sizing.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "tc_gemm.cuh"
+
+namespace tpk {
+namespace tc {
+cudaError_t run_kmn(const TcParams& p, int grid, cudaStream_t st);
+cudaError_t run_kk(const TcParams& p, int grid, cudaStream_t st);
+cudaError_t run_mnmn(const TcParams& p, int grid, cudaStream_t st);
+}  // namespace tc
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// 2-D bf16 row-major tensor [outer][inner] with row pitch ld (elements), 128B swizzle.
+bool encode_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
+                 uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {ld * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
+  using namespace tc;
+  if (s.M <= 0 || s.N <= 0 || s.K <= 0) return cudaSuccess;
+  if (s.groups < 1 || s.groups > kMaxShards) return cudaErrorInvalidValue;
+  static_assert(sizeof(TcParams) <= 32764, "kernel parameter block too large");
+
+  alignas(128) static thread_local TcParams p;
+  std::memset(static_cast<void*>(&p), 0, sizeof(p));
+  for (int g = 0; g < s.groups; ++g) {
+    const bool okA = s.a_mn ? encode_bf16(&p.tmA[g], s.A[g], s.M, s.K, s.lda, 64, 64)
+                            : encode_bf16(&p.tmA[g], s.A[g], s.K, s.M, s.lda, 64, BM);
+    const bool okB = s.b_mn ? encode_bf16(&p.tmB[g], s.B[g], s.N, s.K, s.ldb, 64, 64)
+                            : encode_bf16(&p.tmB[g], s.B[g], s.K, s.N, s.ldb, 64, BN);
+    if (!okA || !okB) return cudaErrorInvalidValue;
+    p.D[g] = s.D[g];
+    p.D2[g] = s.D2[g];
+    p.bias[g] = s.bias[g];
+    p.aux[g] = s.aux[g];
+  }
+  p.ldd = s.ldd;
+  p.ldd2 = s.ldd2;
+  p.ldaux = s.ldaux;
+  p.M = static_cast<int>(s.M);
+  p.N = static_cast<int>(s.N);
+  p.kblocks = static_cast<int>((s.K + BK - 1) / BK);
+  p.groups = s.groups;
+  p.ksum = s.ksum;
+  p.tiles_m = static_cast<int>((s.M + BM - 1) / BM);
+  p.tiles_n = static_cast<int>((s.N + BN - 1) / BN);
+  p.num_tiles = (s.ksum ? 1 : s.groups) * p.tiles_m * p.tiles_n;
+  p.epi = s.epi;
+  p.act = s.act;
+  p.status = s.status;
+
+  const int grid = std::min(p.num_tiles, device_sm_count());
+  if (!s.a_mn && s.b_mn) return run_kmn(p, grid, st);
+  if (!s.a_mn && !s.b_mn) return run_kk(p, grid, st);
+  if (s.a_mn && s.b_mn) return run_mnmn(p, grid, st);
+  return cudaErrorNotSupported;
+}
+
+}  // namespace tpk

@@ -1,0 +1,178 @@
+"""Host-side checks of the C ABI: the library builds and loads, exports every symbol the header
+declares, and rejects bad arguments with the documented status before touching the GPU.
+
+No test here launches a kernel or dereferences a pointer: every call either fails validation
+(which runs before any CUDA call) or, on a machine without a CUDA device, stops at the
+device check.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tp_mlp.h")
+
+
+@pytest.fixture(scope="module")
+def tp():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import tensor_sharded_linear_bias_gb300 as mod
+
+    return mod
+
+
+def header_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tp_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_what_the_binding_exports(tp):
+    assert header_functions() == sorted(tp.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(tp):
+    out = subprocess.run(["nm", "-D", "--defined-only", tp.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s(tp_\w+)", out))
+    for name in header_functions():
+        assert name in exported, name
+        assert hasattr(tp.lib, name)
+
+
+def test_version_and_error_string(tp):
+    assert tp.tp_version() == 100
+    assert isinstance(tp.tp_last_error(), str)
+
+
+def mlp(tp, **kw):
+    d = dict(tokens=64, hidden=128, ffn=512, tp_degree=4, dtype=tp.TP_BF16,
+             act=tp.TP_ACT_GELU_ERF, reduce=tp.TP_REDUCE_FUSED)
+    d.update(kw)
+    return tp.MlpDesc(**d)
+
+
+def status_of(fn):
+    from tensor_sharded_linear_bias_gb300 import TpError
+
+    try:
+        fn()
+    except TpError as e:
+        return e.name
+    return "TP_OK"
+
+
+def test_workspace_sizes(tp):
+    T, H, F, n = 64, 128, 512, 4
+    assert tp.tp_mlp_workspace_size(mlp(tp)) == 256 + T * F * 2
+    assert tp.tp_mlp_workspace_size(mlp(tp, dtype=tp.TP_F32)) == 256 + T * F * 4
+    part = n * T * H * 4
+    assert tp.tp_mlp_workspace_size(mlp(tp, reduce=tp.TP_REDUCE_PARTIALS)) == 256 + T * F * 2 + part
+    col = tp.LinearDesc(tokens=32, in_features=768, out_features=3072, tp_degree=4,
+                        dtype=tp.TP_F32, act=0, reduce=0, gather=1)
+    assert tp.tp_linear_workspace_size(col, tp.TP_COLUMN) == 256
+    row = tp.LinearDesc(tokens=32, in_features=3072, out_features=768, tp_degree=4,
+                        dtype=tp.TP_F32, act=0, reduce=tp.TP_REDUCE_PARTIALS, gather=0)
+    assert tp.tp_linear_workspace_size(row, tp.TP_ROW) == 256 + 4 * 32 * 768 * 4
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(tp_degree=0), "TP_ERR_SHAPE"),
+    (dict(tp_degree=65), "TP_ERR_SHAPE"),
+    (dict(ffn=510), "TP_ERR_INDIVISIBLE"),
+    (dict(hidden=0), "TP_ERR_SHAPE"),
+    (dict(tokens=-1), "TP_ERR_SHAPE"),
+    (dict(hidden=130), "TP_ERR_ALIGN"),          # bf16 widths must be multiples of 8
+    (dict(ffn=4 * 130), "TP_ERR_ALIGN"),         # ... including the shard width
+    (dict(dtype=7), "TP_ERR_DTYPE"),
+    (dict(act=3), "TP_ERR_DTYPE"),
+    (dict(reduce=2), "TP_ERR_DTYPE"),
+])
+def test_mlp_desc_validation(tp, kw, expected):
+    assert status_of(lambda: tp.tp_mlp_workspace_size(mlp(tp, **kw))) == expected
+
+
+def test_fp32_has_no_width_rule(tp):
+    assert tp.tp_mlp_workspace_size(mlp(tp, hidden=130, ffn=4 * 131, dtype=tp.TP_F32)) > 0
+
+
+def test_linear_desc_validation(tp):
+    base = dict(tokens=8, in_features=64, out_features=96, tp_degree=4, dtype=tp.TP_BF16,
+                act=0, reduce=0, gather=0)
+    ok = tp.LinearDesc(**base)
+    assert tp.tp_linear_workspace_size(ok, tp.TP_COLUMN) == 256
+    assert status_of(lambda: tp.tp_linear_workspace_size(
+        tp.LinearDesc(**{**base, "out_features": 98}), tp.TP_COLUMN)) == "TP_ERR_INDIVISIBLE"
+    assert status_of(lambda: tp.tp_linear_workspace_size(
+        tp.LinearDesc(**{**base, "in_features": 66}), tp.TP_ROW)) == "TP_ERR_INDIVISIBLE"
+    assert status_of(lambda: tp.tp_linear_workspace_size(
+        tp.LinearDesc(**{**base, "act": 1}), tp.TP_ROW)) == "TP_ERR_DTYPE"
+    assert status_of(lambda: tp.tp_linear_workspace_size(
+        tp.LinearDesc(**{**base, "gather": 1}), tp.TP_ROW)) == "TP_ERR_DTYPE"
+    assert status_of(lambda: tp.tp_linear_workspace_size(ok, 5)) == "TP_ERR_DTYPE"
+
+
+# Fake device addresses: validation rejects the call before anything could use them.
+ALIGNED = 0x7F0000000000
+WS = 0x7F0000100000
+
+
+def forward_args(tp, desc, **over):
+    n = desc.tp_degree
+    args = dict(X=ALIGNED, A=[ALIGNED] * n, a=None, B=[ALIGNED] * n, b=None, Z=ALIGNED,
+                Hsave=[ALIGNED] * n, Ysave=[ALIGNED] * n, ws=None)
+    args.update(over)
+    return args
+
+
+def call_forward(tp, desc, ws_bytes, **over):
+    a = forward_args(tp, desc, **over)
+    p = tp._arr
+    st = tp.lib.tp_mlp_forward(ctypes.byref(desc), a["X"], p(a["A"]), p(a["a"]), p(a["B"]),
+                               a["b"], a["Z"], p(a["Hsave"]), p(a["Ysave"]),
+                               a.get("wsp", WS), ws_bytes, 0)
+    return tp.STATUS_NAMES[st]
+
+
+def test_forward_argument_checks(tp):
+    d = mlp(tp)
+    need = tp.tp_mlp_workspace_size(d)
+    assert call_forward(tp, d, need, X=None) == "TP_ERR_NULL"
+    assert call_forward(tp, d, need, A=None) == "TP_ERR_NULL"
+    assert call_forward(tp, d, need, A=[ALIGNED, ALIGNED, None, ALIGNED]) == "TP_ERR_NULL"
+    assert call_forward(tp, d, need, Ysave=None) == "TP_ERR_NULL"
+    assert call_forward(tp, d, need, Hsave=None) == "TP_ERR_NULL"   # GeLU needs H saved
+    assert call_forward(tp, d, need, X=ALIGNED + 8) == "TP_ERR_ALIGN"
+    assert call_forward(tp, d, need, B=[ALIGNED] * 3 + [ALIGNED + 2]) == "TP_ERR_ALIGN"
+    assert call_forward(tp, d, need - 1) == "TP_ERR_WORKSPACE"
+    assert call_forward(tp, d, need, wsp=None) == "TP_ERR_WORKSPACE"
+    assert call_forward(tp, d, need, wsp=WS + 16) == "TP_ERR_ALIGN"
+    assert "workspace" in tp.tp_last_error()
+
+
+def test_valid_call_without_a_device_is_refused(tp):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present: fake pointers must not reach it")
+    d = mlp(tp)
+    assert call_forward(tp, d, tp.tp_mlp_workspace_size(d)) == "TP_ERR_ARCH"
+
+
+def test_selftest_argument_checks(tp):
+    assert tp.STATUS_NAMES[tp.lib.tp_selftest_wait_timeout(WS, 256, 0, 0)] == "TP_ERR_SHAPE"
+    assert tp.STATUS_NAMES[tp.lib.tp_selftest_wait_timeout(None, 256, 10, 0)] == "TP_ERR_WORKSPACE"
+    assert tp.STATUS_NAMES[tp.lib.tp_check_status(WS, 16, 0)] == "TP_ERR_WORKSPACE"
+
+
+def test_product_path_does_not_touch_the_oracle():
+    pkg = os.path.join(ROOT, "tensor_sharded_linear_bias_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in src.replace("oracle-free", ""), f

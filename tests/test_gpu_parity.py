@@ -1,0 +1,350 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle, element by element.
+
+Small and ragged shapes are compared in full (several 128 x 256 output tiles, partial tiles in
+M, N and K); the full-size workloads are compared on sampled token rows and ffn columns that
+the oracle computes one by one; plus the invariants (sharded vs unsharded, fused vs partials,
+run-to-run determinism, every output element written, zero tokens).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from harness import (TOL_BF16, TOL_F32, TOL_SHARDED_VS_UNSHARDED, MlpCase, compare_full, np64,
+                     prepare, rel, rel_shards, sample_rows_cols, sampled_gpu, sampled_reference)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tp():
+    import torch
+
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import tensor_sharded_linear_bias_gb300 as mod
+
+    return mod
+
+
+SMALL = wl.MLP_T4096_H1024_F4096_TP2
+
+
+def full_reference(case):
+    f = case.f
+    rf = oracle.mlp_forward(f["X"], f["A"], f["a"], f["B"], f["b"], case.n)
+    rb = oracle.mlp_backward(f["X"], f["A"], f["a"], f["B"], f["b"], f["dZ"], case.n, rf)
+    return rf, rb
+
+
+# ----------------------------------------------------------------------------- device status
+def test_wait_timeout_is_reported(tp):
+    import torch
+
+    ws = tp.new_workspace(256)
+    tp.tp_check_status(ws)
+    tp.tp_selftest_wait_timeout(ws, 2000)
+    with pytest.raises(tp.TpError) as e:
+        tp.tp_check_status(ws)
+    assert e.value.name == "TP_ERR_DEVICE_TIMEOUT"
+    tp.tp_workspace_init(ws)
+    tp.tp_check_status(ws)
+    # the context is still usable
+    x = torch.ones(4, device="cuda")
+    assert float(x.sum()) == 4.0
+
+
+# ----------------------------------------------------------------------------- small MLPs
+@pytest.mark.parametrize("T,H,F,n", [
+    (128, 64, 512, 2),        # one tile in M, exact K block
+    (300, 136, 2 * 296, 2),   # ragged M (300), ragged N (296 of 256), ragged K (136 of 64)
+    (513, 264, 4 * 136, 4),   # 4 shards, ragged everywhere
+    (64, 512, 520, 1),        # one shard: the unsharded layer
+    (1, 8, 16, 2),            # a single token, widths at the minimum
+    (130, 72, 8 * 40, 8),     # 8 shards of 40 columns
+])
+@pytest.mark.parametrize("reduce", [0, 1])
+def test_mlp_bf16_small(tp, T, H, F, n, reduce):
+    w = SMALL.with_shape(tokens=T, hidden=H, ffn=F, tp_degree=n)
+    case = MlpCase(w, reduce).run()
+    errs = compare_full(case.outputs(), *full_reference(case))
+    assert max(errs.values()) <= TOL_BF16, errs
+
+
+def test_mlp_fp32_small(tp):
+    w = wl.P3_FP32_FWD.with_shape(tokens=70, hidden=100, ffn=4 * 33, tp_degree=4)
+    w = wl.dataclasses.replace(w, sigma={**w.sigma, "a": 0.05, "b": 0.05})
+    for reduce in (0, 1):
+        case = MlpCase(w, reduce).run()
+        errs = compare_full(case.outputs(), *full_reference(case))
+        assert max(errs.values()) <= TOL_F32, errs
+
+
+def test_p3_shapes_fp32_forward(tp):
+    """The pages' example shapes (768 -> 3072, batch 32, 4 shards) closed by the row layer."""
+    w = wl.P3_FP32_FWD
+    for reduce in (0, 1):
+        case = MlpCase(w, reduce).run(backward=False)
+        f = case.f
+        rf = oracle.mlp_forward(f["X"], f["A"], f["a"], f["B"], f["b"], w.tp_degree)
+        errs = compare_full(case.outputs(backward=False), rf)
+        assert max(errs.values()) <= TOL_F32, errs
+
+
+# ----------------------------------------------------------------------------- invariants
+def test_sharded_matches_unsharded(tp):
+    T, H, F = 384, 256, 1024
+    outs = {}
+    for n in (1, 2, 4, 8):
+        w = SMALL.with_shape(tokens=T, hidden=H, ffn=F, tp_degree=n)
+        c = MlpCase(w, 0).run()
+        o = c.outputs()
+        outs[n] = {"Z": o["Z"], "dX": o["dX"], "dA": np.concatenate(o["dA"], 1),
+                   "dB": np.concatenate(o["dB"], 0), "da": np.concatenate(o["da"]),
+                   "db": o["db"], "H": np.concatenate(o["H"], 1), "Y": np.concatenate(o["Y"], 1)}
+    for n in (2, 4, 8):
+        for k in outs[1]:
+            e = rel(outs[n][k], outs[1][k])
+            assert e <= TOL_SHARDED_VS_UNSHARDED, (n, k, e)
+        # the column layer's K order does not depend on n: saved activations are identical
+        assert np.array_equal(outs[n]["H"], outs[1]["H"])
+        assert np.array_equal(outs[n]["Y"], outs[1]["Y"])
+
+
+def test_fused_matches_partials(tp):
+    w = SMALL.with_shape(tokens=320, hidden=200, ffn=4 * 264, tp_degree=4)
+    a = MlpCase(w, 0).run().outputs()
+    b = MlpCase(w, 1).run().outputs()
+    for k in ("Z", "dX"):
+        assert rel(a[k], b[k]) <= 1e-5, k
+    for k in ("dA", "dB", "da", "H", "Y"):
+        assert all(np.array_equal(x, y) for x, y in zip(a[k], b[k])), k
+
+
+def test_deterministic(tp):
+    w = SMALL.with_shape(tokens=257, hidden=128, ffn=2 * 384, tp_degree=2)
+    for reduce in (0, 1):
+        c = MlpCase(w, reduce)
+        c.run()
+        first = c.outputs()
+        c.run()
+        second = c.outputs()
+        for k, v in first.items():
+            if isinstance(v, list):
+                assert all(np.array_equal(x, y) for x, y in zip(v, second[k])), k
+            else:
+                assert np.array_equal(v, second[k]), k
+
+
+def test_every_output_written(tp):
+    w = SMALL.with_shape(tokens=200, hidden=136, ffn=2 * 264, tp_degree=2)
+    for reduce in (0, 1):
+        o = MlpCase(w, reduce).run().outputs()   # outputs start as NaN
+        for k, v in o.items():
+            vs = v if isinstance(v, list) else [v]
+            assert all(np.isfinite(x).all() for x in vs), k
+
+
+def test_zero_tokens(tp):
+    import torch
+
+    w = SMALL.with_shape(tokens=0, hidden=64, ffn=2 * 64, tp_degree=2)
+    c = MlpCase(w, 0).run()
+    assert torch.all(torch.cat([x.flatten() for x in c.dA + c.dB + c.da]) == 0)
+    assert torch.all(c.db == 0)
+
+
+# ----------------------------------------------------------------------------- parallel linears
+def _lin_inputs(seed, T, K, N, dtype, device):
+    raw = {"X": wl.normal(seed, (T, K), 1.0), "W": wl.normal(seed + 1, (K, N), 0.05),
+           "bias": wl.normal(seed + 2, (N,), 0.1), "G": wl.normal(seed + 3, (T, N), 1.0)}
+    return prepare(raw, dtype, device)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("gather", [0, 1])
+@pytest.mark.parametrize("act", [0, 1])
+def test_column_linear(tp, dtype, gather, act):
+    import torch
+
+    T, K, N, n = 200, 136, 4 * 72, 4
+    t, f = _lin_inputs(31, T, K, N, dtype, "cuda")
+    Ns = N // n
+    cdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    W = [t["W"][:, i * Ns:(i + 1) * Ns].contiguous() for i in range(n)]
+    bias = [t["bias"][i * Ns:(i + 1) * Ns].contiguous() for i in range(n)]
+    desc = tp.LinearDesc(tokens=T, in_features=K, out_features=N, tp_degree=n,
+                         dtype=tp.TP_BF16 if dtype == "bf16" else tp.TP_F32, act=act,
+                         reduce=0, gather=gather)
+    ws = tp.new_workspace(tp.tp_linear_workspace_size(desc, tp.TP_COLUMN))
+    Y = [torch.empty(T, N, dtype=cdt, device="cuda")] if gather else \
+        [torch.empty(T, Ns, dtype=cdt, device="cuda") for _ in range(n)]
+    Hs = [torch.empty(T, Ns, dtype=cdt, device="cuda") for _ in range(n)] if act else None
+    tp.tp_linear_column_forward(desc, t["X"], W, bias, Y, Hs, ws)
+    G = t["G"]
+    dY = [G] if gather else [G[:, i * Ns:(i + 1) * Ns].contiguous() for i in range(n)]
+    dX = torch.empty(T, K, dtype=torch.float32, device="cuda")
+    dW = [torch.empty(K, Ns, dtype=torch.float32, device="cuda") for _ in range(n)]
+    db = [torch.empty(Ns, dtype=torch.float32, device="cuda") for _ in range(n)]
+    tp.tp_linear_column_backward(desc, t["X"], W, Hs, dY, dX, dW, db, ws)
+    tp.tp_check_status(ws)
+    torch.cuda.synchronize()
+
+    a = "gelu" if act else "none"
+    Wr = oracle.split_columns(f["W"], n)
+    Hr, Yr = oracle.column_parallel_forward(f["X"], Wr, oracle.split_vector(f["bias"], n), a)
+    dXr, dWr, dbr, _ = oracle.column_parallel_backward(f["X"], Wr, Hr,
+                                                       oracle.split_columns(f["G"], n), a)
+    tol = TOL_BF16 if dtype == "bf16" else TOL_F32
+    ygpu = [np64(Y[0])[:, i * Ns:(i + 1) * Ns] for i in range(n)] if gather else \
+        [np64(y) for y in Y]
+    assert rel_shards(ygpu, Yr) <= tol
+    if act:
+        assert rel_shards([np64(h) for h in Hs], Hr) <= tol
+    assert rel(np64(dX), dXr) <= tol
+    assert rel_shards([np64(x) for x in dW], dWr) <= tol
+    assert rel_shards([np64(x) for x in db], dbr) <= tol
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("reduce", [0, 1])
+def test_row_linear(tp, dtype, reduce):
+    import torch
+
+    T, K, N, n = 190, 4 * 88, 264, 4
+    t, f = _lin_inputs(41, T, K, N, dtype, "cuda")
+    Ks = K // n
+    X = [t["X"][:, i * Ks:(i + 1) * Ks].contiguous() for i in range(n)]
+    W = [t["W"][i * Ks:(i + 1) * Ks, :].contiguous() for i in range(n)]
+    desc = tp.LinearDesc(tokens=T, in_features=K, out_features=N, tp_degree=n,
+                         dtype=tp.TP_BF16 if dtype == "bf16" else tp.TP_F32, act=0,
+                         reduce=reduce, gather=0)
+    ws = tp.new_workspace(tp.tp_linear_workspace_size(desc, tp.TP_ROW))
+    Z = torch.empty(T, N, dtype=torch.float32, device="cuda")
+    tp.tp_linear_row_forward(desc, X, W, t["bias"], Z, ws)
+    dX = [torch.empty(T, Ks, dtype=torch.float32, device="cuda") for _ in range(n)]
+    dW = [torch.empty(Ks, N, dtype=torch.float32, device="cuda") for _ in range(n)]
+    db = torch.empty(N, dtype=torch.float32, device="cuda")
+    tp.tp_linear_row_backward(desc, X, W, t["G"], dX, dW, db, ws)
+    tp.tp_check_status(ws)
+    torch.cuda.synchronize()
+
+    Xr, Wr = oracle.split_columns(f["X"], n), oracle.split_rows(f["W"], n)
+    Zr = oracle.row_parallel_forward(Xr, Wr, f["bias"])
+    dXr, dWr, dbr = oracle.row_parallel_backward(Xr, Wr, f["G"])
+    tol = TOL_BF16 if dtype == "bf16" else TOL_F32
+    assert rel(np64(Z), Zr) <= tol
+    assert rel_shards([np64(x) for x in dX], dXr) <= tol
+    assert rel_shards([np64(x) for x in dW], dWr) <= tol
+    assert rel(np64(db), dbr) <= tol
+
+
+def test_many_shards(tp):
+    w = SMALL.with_shape(tokens=96, hidden=64, ffn=64 * 8, tp_degree=64)
+    case = MlpCase(w, 0).run()
+    errs = compare_full(case.outputs(), *full_reference(case))
+    assert max(errs.values()) <= TOL_BF16, errs
+
+
+# ----------------------------------------------------------------------------- full-size workloads
+@pytest.mark.slow
+def test_workload_mlp_4096_1024_4096_tp2_full(tp):
+    w = wl.MLP_T4096_H1024_F4096_TP2
+    case = MlpCase(w, 0).run()
+    errs = compare_full(case.outputs(), *full_reference(case))
+    assert max(errs.values()) <= TOL_BF16, errs
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("reduce", [0, 1])
+def test_workload_gpt3_mlp_slice_sampled(tp, reduce):
+    w = wl.GPT3_MLP_T2048_TP8
+    case = MlpCase(w, reduce).run()
+    rows, cols = sample_rows_cols(w)
+    ref = sampled_reference(oracle, case.f, w.tp_degree, rows, cols)
+    got = sampled_gpu(case, rows, cols)
+    errs = {k: rel(got[k], ref[k]) for k in ref}
+    assert max(errs.values()) <= TOL_BF16, errs
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("n,T", [(1, 512), (8, 16384), (2, 2048), (4, 8192)])
+def test_workload_sweep_sampled(tp, n, T):
+    w = wl.SWEEP_H8192_F28672.with_shape(tokens=T, tp_degree=n)
+    case = MlpCase(w, 0).run()
+    rows, cols = sample_rows_cols(w, nrows=4, ncols=4)
+    ref = sampled_reference(oracle, case.f, n, rows, cols)
+    got = sampled_gpu(case, rows, cols)
+    errs = {k: rel(got[k], ref[k]) for k in ref}
+    assert max(errs.values()) <= TOL_BF16, errs
+
+
+@pytest.mark.slow
+def test_workload_attention_projections(tp):
+    """Fused QKV (column parallel over heads) and output projection (row parallel)."""
+    import torch
+
+    w = wl.ATTN_T4096_H5120_TP8
+    n, T, Hm, hd, heads = w.tp_degree, w.tokens, w.hidden, w.head_dim, w.heads
+    raw = wl.attn_tensors(w)
+    t, f = prepare(raw, "bf16", "cuda")
+    # shard buffers (head-split of the fused [Q|K|V] weight), made on the device by slicing
+    hw = heads // n * hd
+    Wq = [torch.cat([t["Wqkv"][:, blk * Hm + s * hw: blk * Hm + (s + 1) * hw] for blk in range(3)],
+                    1).contiguous() for s in range(n)]
+    dQ = [torch.cat([t["dQKV"][:, blk * Hm + s * hw: blk * Hm + (s + 1) * hw] for blk in range(3)],
+                    1).contiguous() for s in range(n)]
+    Cs = [t["C"][:, s * hw:(s + 1) * hw].contiguous() for s in range(n)]
+    Wo = [t["Wo"][s * hw:(s + 1) * hw, :].contiguous() for s in range(n)]
+    f32 = dict(dtype=torch.float32, device="cuda")
+    col = tp.LinearDesc(tokens=T, in_features=Hm, out_features=3 * Hm, tp_degree=n,
+                        dtype=tp.TP_BF16, act=0, reduce=0, gather=0)
+    row = tp.LinearDesc(tokens=T, in_features=Hm, out_features=Hm, tp_degree=n,
+                        dtype=tp.TP_BF16, act=0, reduce=0, gather=0)
+    ws = tp.new_workspace(max(tp.tp_linear_workspace_size(col, tp.TP_COLUMN),
+                              tp.tp_linear_workspace_size(row, tp.TP_ROW)))
+    QKV = [torch.empty(T, 3 * hw, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    tp.tp_linear_column_forward(col, t["X"], Wq, None, QKV, None, ws)
+    O = torch.empty(T, Hm, **f32)
+    tp.tp_linear_row_forward(row, Cs, Wo, None, O, ws)
+    dX = torch.empty(T, Hm, **f32)
+    dWq = [torch.empty(Hm, 3 * hw, **f32) for _ in range(n)]
+    tp.tp_linear_column_backward(col, t["X"], Wq, None, dQ, dX, dWq, None, ws)
+    dC = [torch.empty(T, hw, **f32) for _ in range(n)]
+    dWo = [torch.empty(hw, Hm, **f32) for _ in range(n)]
+    tp.tp_linear_row_backward(row, Cs, Wo, t["dO"], dC, dWo, None, ws)
+    tp.tp_check_status(ws)
+    torch.cuda.synchronize()
+
+    rows = wl.sample_indices(9004, 8, T, must=[0, T - 1])
+    fr = oracle.attn_forward(f["X"][rows], f["Wqkv"], f["C"][rows], f["Wo"], heads, hd, n)
+    br = oracle.attn_backward(f["X"][rows], f["Wqkv"], f["C"][rows], f["Wo"], f["dQKV"][rows],
+                              f["dO"][rows], heads, hd, n)
+    errs = {"QKV": rel_shards([np64(q)[rows] for q in QKV], fr["QKV"]),
+            "O": rel(np64(O)[rows], fr["O"]),
+            "dX": rel(np64(dX)[rows], br["dX"]),
+            "dC": rel_shards([np64(c)[rows] for c in dC], br["dC"])}
+    # weight gradients: full oracle over all tokens for a few columns of each shard
+    Wsh = oracle.qkv_head_shards(f["Wqkv"], heads, hd, n)
+    dQsh = oracle.qkv_head_shards(f["dQKV"], heads, hd, n)
+    cols = [0, 1, 3 * hw - 1]
+    for s in (0, n - 1):
+        _, (dw,), _, _ = oracle.column_parallel_backward(f["X"], [Wsh[s][:, cols]], None,
+                                                         [dQsh[s][:, cols]], "none")
+        errs[f"dWqkv{s}"] = rel(np64(dWq[s])[:, cols], dw)
+        Csh = oracle.split_columns(f["C"], n)[s]
+        Wosh = oracle.split_rows(f["Wo"], n)[s]
+        _, (dwo,), _ = oracle.row_parallel_backward([Csh[:, cols]], [Wosh[cols, :]], f["dO"])
+        errs[f"dWo{s}"] = rel(np64(dWo[s])[cols], dwo)
+    assert max(errs.values()) <= TOL_BF16, errs
+
+
+def test_trace_records_every_launch(tp):
+    T, H, F, n = 256, 128, 2 * 256, 2
+    c = MlpCase(SMALL.with_shape(tokens=T, hidden=H, ffn=F, tp_degree=n), 0)
+    tp.tp_trace_start(64)
+    c.run()
+    recs = tp.tp_trace_stop(64)
+    assert [r["tag"] for r in recs] == ["column_fwd", "row_fwd", "row_dgrad", "row_wgrad",
+                                        "column_wgrad", "column_dgrad", "bias_grad"]
+    assert sum(r["flops"] for r in recs if r["kernel"] == "gemm_tc") == 12 * T * H * F
+    assert all(r["ms"] > 0 for r in recs)
