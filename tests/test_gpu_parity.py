@@ -326,15 +326,16 @@ def test_workload_attention_projections(tp):
     # weight gradients: full oracle over all tokens for a few columns of each shard
     Wsh = oracle.qkv_head_shards(f["Wqkv"], heads, hd, n)
     dQsh = oracle.qkv_head_shards(f["dQKV"], heads, hd, n)
-    cols = [0, 1, 3 * hw - 1]
+    qcols = [0, 1, hw, 2 * hw, 3 * hw - 1]   # first / last column of Q, K and V blocks
+    ocols = [0, 1, hw - 1]
     for s in (0, n - 1):
-        _, (dw,), _, _ = oracle.column_parallel_backward(f["X"], [Wsh[s][:, cols]], None,
-                                                         [dQsh[s][:, cols]], "none")
-        errs[f"dWqkv{s}"] = rel(np64(dWq[s])[:, cols], dw)
+        _, (dw,), _, _ = oracle.column_parallel_backward(f["X"], [Wsh[s][:, qcols]], None,
+                                                         [dQsh[s][:, qcols]], "none")
+        errs[f"dWqkv{s}"] = rel(np64(dWq[s])[:, qcols], dw)
         Csh = oracle.split_columns(f["C"], n)[s]
         Wosh = oracle.split_rows(f["Wo"], n)[s]
-        _, (dwo,), _ = oracle.row_parallel_backward([Csh[:, cols]], [Wosh[cols, :]], f["dO"])
-        errs[f"dWo{s}"] = rel(np64(dWo[s])[cols], dwo)
+        _, (dwo,), _ = oracle.row_parallel_backward([Csh[:, ocols]], [Wosh[ocols, :]], f["dO"])
+        errs[f"dWo{s}"] = rel(np64(dWo[s])[ocols], dwo)
     assert max(errs.values()) <= TOL_BF16, errs
 
 
