@@ -222,6 +222,31 @@ typedef struct tp_trace_record {
 tp_status tp_trace_start(int32_t capacity);
 tp_status tp_trace_stop(tp_trace_record* out, int32_t capacity, int32_t* count);
 
+/* Row-parallel linear forward for callers that cannot allocate device memory. The pages have
+ * no counterpart to this entry point.
+ *
+ * Some callers have no way to call cudaMalloc: a plug-in running inside a host application
+ * that owns every device allocation and forbids side allocations, or a process whose device
+ * memory budget is fixed when it starts. This entry point takes no workspace: it computes the
+ * same Z = sum_i X_i W_i + bias as tp_linear_row_forward in TP_REDUCE_PARTIALS form (desc->
+ * reduce is ignored), with its status word and the per-shard fp32 partials in one static
+ * device array of 32 MiB inside the library (every GPU that loads the library holds it until
+ * the process exits). It allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * call.
+ *  - Limit: 256 + tp_degree * tokens * out_features * 4 bytes must fit in 32 MiB; larger calls
+ *    return TP_ERR_WORKSPACE before anything is enqueued.
+ *  - The first call on each device looks up the array's device address (once per device,
+ *    with that device current); make that first call before any stream capture.
+ *  - Every call on a device shares the one array and leaves its partials there; each call
+ *    clears the status word itself. Calls whose work overlaps on the GPU (on different
+ *    streams, or from different threads) race on the array: order them on one stream.
+ *  - A device-side wait that runs out writes its code into the array's status word, which no
+ *    entry point reads back; the next call clears it.
+ * Arguments, layouts, dtypes and the other errors are those of tp_linear_row_forward. */
+tp_status tp_linear_row_forward_noalloc(const tp_linear_desc* desc, const void* const* X,
+                                        const void* const* W, const void* bias, void* Z,
+                                        void* stream);
+
 /* Self-test of the device-side timeout path: launches one block that waits on a barrier
  * nothing completes, with a limit of limit_us microseconds (1..1000000). The wait runs
  * out, the kernel writes TP_ERR_DEVICE_TIMEOUT's code into the workspace status word and

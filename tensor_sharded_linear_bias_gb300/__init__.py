@@ -20,7 +20,7 @@ __all__ = [
     "tp_mlp_backward", "tp_linear_column_forward", "tp_linear_column_backward",
     "tp_linear_row_forward", "tp_linear_row_backward", "tp_selftest_wait_timeout",
     "new_workspace", "EXPORTED_SYMBOLS", "tp_trace_start", "tp_trace_stop", "TraceRecord",
-    "KERNEL_NAMES", "TAG_NAMES",
+    "KERNEL_NAMES", "TAG_NAMES", "tp_linear_row_forward_noalloc",
 ]
 
 TP_F32, TP_BF16 = 0, 1
@@ -39,6 +39,7 @@ EXPORTED_SYMBOLS = (
     "tp_workspace_init", "tp_check_status", "tp_mlp_forward", "tp_mlp_backward",
     "tp_linear_column_forward", "tp_linear_column_backward", "tp_linear_row_forward",
     "tp_linear_row_backward", "tp_selftest_wait_timeout", "tp_trace_start", "tp_trace_stop",
+    "tp_linear_row_forward_noalloc",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -102,6 +103,8 @@ _SIGS = {
                                               _PP, _P, _P, ctypes.c_size_t, _P]),
     "tp_selftest_wait_timeout": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_uint32, _P]),
     "tp_trace_start": (ctypes.c_int, [ctypes.c_int32]),
+    "tp_linear_row_forward_noalloc": (ctypes.c_int, [ctypes.POINTER(LinearDesc), _PP, _PP, _P,
+                                                     _P, _P]),
     "tp_trace_stop": (ctypes.c_int, [ctypes.POINTER(TraceRecord), ctypes.c_int32,
                                      ctypes.POINTER(ctypes.c_int32)]),
 }
@@ -245,6 +248,11 @@ def tp_linear_row_backward(desc, X, W, dZ, dX, dW, dbias, ws, stream=None):
     p, n = _ws(ws)
     _check(lib.tp_linear_row_backward(ctypes.byref(_desc_lin(desc)), _arr(X), _arr(W), _ptr(dZ),
                                       _arr(dX), _arr(dW), _ptr(dbias), p, n, _stream(stream)))
+
+
+def tp_linear_row_forward_noalloc(desc, X, W, bias, Z, stream=None):
+    _check(lib.tp_linear_row_forward_noalloc(ctypes.byref(_desc_lin(desc)), _arr(X), _arr(W),
+                                             _ptr(bias), _ptr(Z), _stream(stream)))
 
 
 def tp_trace_start(capacity: int):

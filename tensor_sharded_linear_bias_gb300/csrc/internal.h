@@ -76,4 +76,7 @@ cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t st
 // Device facts (cached per device).
 int device_sm_count();
 
+// Sets the thread-local message that tp_last_error() returns.
+void set_last_error(const char* msg);
+
 }  // namespace tpk

@@ -20,6 +20,12 @@ namespace {
 
 thread_local std::string g_last_error;
 
+}  // namespace
+
+void tpk::set_last_error(const char* msg) { g_last_error = msg; }
+
+namespace {
+
 tp_status fail(tp_status st, const char* fmt, ...) {
   char buf[512];
   va_list ap;
