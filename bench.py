@@ -45,7 +45,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="gpt3")
-    ap.add_argument("--reduce", choices=["fused", "partials"], default="fused")
+    ap.add_argument("--reduce", choices=["fused", "partials", "auto"], default="auto")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -387,7 +387,8 @@ def main():
     device = dist_init(world, local)
     import tensor_sharded_linear_bias_gb300 as tp
 
-    reduce = tp.TP_REDUCE_FUSED if args.reduce == "fused" else tp.TP_REDUCE_PARTIALS
+    reduce = {"fused": tp.TP_REDUCE_FUSED, "partials": tp.TP_REDUCE_PARTIALS,
+              "auto": tp.TP_REDUCE_AUTO}[args.reduce]
     keep_host = (rank == 0 and world == 1 and not args.no_cpu_baseline)
     mb = MlpBench(w, reduce, device, keep_host)
 

@@ -59,8 +59,18 @@ typedef enum tp_dtype { TP_F32 = 0, TP_BF16 = 1 } tp_dtype;
  * form h * (1 + erf(h / sqrt 2)) / 2. */
 typedef enum tp_act { TP_ACT_NONE = 0, TP_ACT_GELU_ERF = 1 } tp_act;
 
-/* How the shard sum (the pages' All-Reduce) is done on the device. */
-typedef enum tp_reduce { TP_REDUCE_FUSED = 0, TP_REDUCE_PARTIALS = 1 } tp_reduce;
+/* How the shard sum (the pages' All-Reduce) is done on the device.
+ *  FUSED:    one accumulator sums every shard's K range (no scratch).
+ *  PARTIALS: one fp32 partial per shard, then a reduction kernel.
+ *  AUTO:     the shards are summed in S groups (S a divisor of tp_degree chosen from the
+ *            shape and the SM count to balance tile waves against reduction traffic; S = 1 is
+ *            FUSED), then a reduction of the S partials. bf16 only; fp32 uses FUSED.
+ *            Workspace is sized as for PARTIALS. */
+typedef enum tp_reduce {
+  TP_REDUCE_FUSED = 0,
+  TP_REDUCE_PARTIALS = 1,
+  TP_REDUCE_AUTO = 2
+} tp_reduce;
 
 typedef enum tp_status {
   TP_OK = 0,

@@ -32,7 +32,8 @@ enum EpiKind : int {
 struct GemmSpec {
   int64_t M = 0, N = 0, K = 0;
   int groups = 1;
-  int ksum = 0;
+  int ksum = 0;   // 1: one output, sum over all groups (shorthand for kpo = groups)
+  int kpo = 0;    // groups summed per output (tensor-core GEMM only; 0: from ksum)
   int a_mn = 0, b_mn = 0;
   const void* A[kMaxShards] = {};
   const void* B[kMaxShards] = {};
@@ -72,6 +73,10 @@ cudaError_t launch_dact(const void* const* dY, int64_t ld_dy, const void* const*
 
 // One-block self-test of the bounded wait (see tp_selftest_wait_timeout).
 cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t st);
+
+// Number of partial outputs to split a shard-summed GEMM into (a divisor of n; 1 = fully
+// fused): balances the tile waves against the extra reduction traffic.
+int plan_shard_split(int64_t M, int64_t N, int64_t K_per_group, int n);
 
 // Device facts (cached per device).
 int device_sm_count();

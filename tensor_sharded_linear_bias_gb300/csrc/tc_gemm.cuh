@@ -7,12 +7,14 @@
 //                        into one of two TMEM accumulators (2 x 256 columns), so the
 //                        epilogue of tile i overlaps the main loop of tile i+1.
 //   warps 2..5         : epilogue    -- tcgen05.ld of the accumulator (one row per thread),
-//                        the fused epilogue (bias, GeLU, GeLU', fp32 or bf16 store).
+//                        the fused epilogue (bias, GeLU, GeLU'), coalesced fp32 / bf16 stores
+//                        through a per-warp shared-memory staging buffer.
 //
-// Grouping: the tp_degree shards are groups of one launch. Either every group has its own
-// output (tiles enumerate group x m x n), or -- the on-device form of the pages' All-Reduce
-// -- one output accumulates every group's K range into the same TMEM accumulator, in group
-// order ("ksum").
+// Grouping: the tp_degree shards are groups of one launch. Output og accumulates the K ranges
+// of groups og*kpo .. og*kpo + kpo - 1 into one TMEM accumulator, in group order: kpo = 1
+// gives every group its own output; kpo = groups is the on-device form of the pages'
+// All-Reduce (one output, the shard sum inside the accumulator); in between, the shard sum
+// is split into groups/kpo partial outputs that a reduction kernel adds.
 //
 // Operand layouts: A is K-major ([M,K] row-major) or MN-major ([K,M] row-major); likewise
 // B ([N,K] or [K,N]). The MN-major forms let the backward use X^T, Y_i^T, B_i^T and A_i^T
@@ -44,7 +46,8 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int MN_BOX_BYTES = 64 * BK * 2;    // one [64 K rows][64 MN] box: 8 KiB
 constexpr int NUM_THREADS = 192;
 constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr int EPI_WARPS = 4;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_WARPS * 32 * 128 + 1024 + 256;
 
 struct __align__(128) TcParams {
   CUtensorMap tmA[kMaxShards];
@@ -57,7 +60,7 @@ struct __align__(128) TcParams {
   int M, N;
   int kblocks;      // K blocks of 64 per group
   int groups;
-  int ksum;
+  int kpo;          // groups summed into each output (1: one output per group)
   int tiles_m, tiles_n, num_tiles;
   int epi, act;
   int* status;
@@ -135,6 +138,7 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, float* v) {
 }
 
 // ------------------------------------------------------------------ tile decode
+// Tile t -> output index og, m block, n block (m fastest, for reuse of the B block).
 __device__ __forceinline__ void decode_tile(const TcParams& p, int t, int& g, int& mb, int& nb) {
   const int per = p.tiles_m * p.tiles_n;
   g = t / per;
@@ -143,14 +147,80 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int t, int& g, in
   nb = r / p.tiles_m;
 }
 
-// ------------------------------------------------------------------ epilogue (one row, 32 cols)
-// bias / aux / outputs are bf16 here (this GEMM's inputs are bf16), except EPI_STORE_F32's D.
-// Loads the first `valid_cols` (a multiple of 8) of 32 bf16 values; the rest read as 0.
-__device__ __forceinline__ void load_bf16x32(const uint16_t* src, float* out, int valid_cols) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
+// ------------------------------------------------------------------ epilogue (32 rows x 32 cols per warp)
+// Each lane of an epilogue warp holds 32 consecutive accumulator columns of one row
+// (row = row0 + lane). Global memory is touched through the warp's 4 KiB staging buffer so
+// that every store (and the GeLU' input load) moves whole row segments: 4 rows x 128 B per
+// instruction for fp32, 8 rows x 64 B for bf16. 16-byte chunks are XOR-swizzled by row in the
+// staging buffer, which keeps both the row-wise and the column-wise accesses free of bank
+// conflicts.
+constexpr int STAGE_WARP_BYTES = 32 * 128;
+
+__device__ __forceinline__ void warp_store_f32(uint8_t* stage, const float* v, float* D,
+                                               long long ldd, int row0, int col0, int M,
+                                               int valid) {
+  const int lane = threadIdx.x & 31;
+  float4* s4 = reinterpret_cast<float4*>(stage);
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    s4[lane * 8 + (q ^ (lane & 7))] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int r = 4 * it + (lane >> 3);
+    const int c = lane & 7;
+    const float4 x = s4[r * 8 + (c ^ (r & 7))];
+    if (row0 + r < M && 4 * c < valid)
+      *reinterpret_cast<float4*>(D + static_cast<long long>(row0 + r) * ldd + col0 + 4 * c) = x;
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ void warp_store_bf16(uint8_t* stage, const float* v, uint16_t* D,
+                                                long long ldd, int row0, int col0, int M,
+                                                int valid) {
+  const int lane = threadIdx.x & 31;
+  uint4* s = reinterpret_cast<uint4*>(stage);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const uint4 u = (q * 8 < valid_cols) ? s[q] : make_uint4(0u, 0u, 0u, 0u);
+    uint4 u;
+    u.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
+    u.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
+    u.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
+    u.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+    s[lane * 4 + (q ^ ((lane >> 1) & 3))] = u;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int r = 8 * it + (lane >> 2);
+    const int c = lane & 3;
+    const uint4 x = s[r * 4 + (c ^ ((r >> 1) & 3))];
+    if (row0 + r < M && 8 * c < valid)
+      *reinterpret_cast<uint4*>(D + static_cast<long long>(row0 + r) * ldd + col0 + 8 * c) = x;
+  }
+  __syncwarp();
+}
+
+// The transpose of warp_store_bf16: coalesced loads of the 32 x 32 bf16 block at
+// src[row0.., col0..], then lane l gets the 32 values of row row0 + l (0 outside the matrix).
+__device__ __forceinline__ void warp_load_bf16(uint8_t* stage, const uint16_t* src, long long ld,
+                                               int row0, int col0, int M, int valid, float* out) {
+  const int lane = threadIdx.x & 31;
+  uint4* s = reinterpret_cast<uint4*>(stage);
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int r = 8 * it + (lane >> 2);
+    const int c = lane & 3;
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+    if (row0 + r < M && 8 * c < valid)
+      x = *reinterpret_cast<const uint4*>(src + static_cast<long long>(row0 + r) * ld + col0 + 8 * c);
+    s[r * 4 + (c ^ ((r >> 1) & 3))] = x;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 u = s[lane * 4 + (q ^ ((lane >> 1) & 3))];
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -159,67 +229,54 @@ __device__ __forceinline__ void load_bf16x32(const uint16_t* src, float* out, in
       out[q * 8 + 2 * j + 1] = f.y;
     }
   }
+  __syncwarp();
 }
 
-__device__ __forceinline__ void store_bf16_row(uint16_t* dst, const float* v, int valid_cols) {
+// Per-column bias (bf16), the same 32 values for every lane: broadcast loads. Columns at or
+// beyond `valid` (a multiple of 8) read as 0.
+__device__ __forceinline__ void add_bias_bf16x32(const uint16_t* bias, int valid, float* v) {
+  const uint4* s = reinterpret_cast<const uint4*>(bias);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    if (q * 8 < valid_cols) {
-      uint4 u;
-      u.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
-      u.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
-      u.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
-      u.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
-      reinterpret_cast<uint4*>(dst)[q] = u;
+    if (q * 8 < valid) {
+      const uint4 u = s[q];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = unpack_bf16x2(w[j]);
+        v[q * 8 + 2 * j] += f.x;
+        v[q * 8 + 2 * j + 1] += f.y;
+      }
     }
   }
 }
 
-__device__ __forceinline__ void epilogue_chunk(const TcParams& p, int g, int row, int col0,
-                                               float* v) {
+// Warp-wide: all 32 lanes call this for the same (row0, col0).
+__device__ __forceinline__ void epilogue_chunk(const TcParams& p, int g, int row0, int col0,
+                                               float* v, uint8_t* stage) {
   const int valid = min(32, p.N - col0);  // a multiple of 8 (N % 8 == 0)
-  const int og = p.ksum ? 0 : g;
+  const int og = g;
   if (p.epi == EPI_STORE_F32) {
-    if (p.bias[og] != nullptr) {
-      float bv[32];
-      load_bf16x32(static_cast<const uint16_t*>(p.bias[og]) + col0, bv, valid);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] += bv[i];
-    }
-    float* d = static_cast<float*>(p.D[og]) + static_cast<long long>(row) * p.ldd + col0;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      if (q * 4 < valid)
-        reinterpret_cast<float4*>(d)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2],
-                                                      v[4 * q + 3]);
-    }
+    if (p.bias[og] != nullptr) add_bias_bf16x32(static_cast<const uint16_t*>(p.bias[og]) + col0, valid, v);
+    warp_store_f32(stage, v, static_cast<float*>(p.D[og]), p.ldd, row0, col0, p.M, valid);
   } else if (p.epi == EPI_BIAS_ACT) {
-    if (p.bias[og] != nullptr) {
-      float bv[32];
-      load_bf16x32(static_cast<const uint16_t*>(p.bias[og]) + col0, bv, valid);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] += bv[i];
-    }
+    if (p.bias[og] != nullptr) add_bias_bf16x32(static_cast<const uint16_t*>(p.bias[og]) + col0, valid, v);
     if (p.D[og] != nullptr)
-      store_bf16_row(static_cast<uint16_t*>(p.D[og]) + static_cast<long long>(row) * p.ldd + col0,
-                     v, valid);
+      warp_store_bf16(stage, v, static_cast<uint16_t*>(p.D[og]), p.ldd, row0, col0, p.M, valid);
     if (p.act == TP_ACT_GELU_ERF) {
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
     }
-    store_bf16_row(static_cast<uint16_t*>(p.D2[og]) + static_cast<long long>(row) * p.ldd2 + col0,
-                   v, valid);
+    warp_store_bf16(stage, v, static_cast<uint16_t*>(p.D2[og]), p.ldd2, row0, col0, p.M, valid);
   } else {  // EPI_DACT (aux = the saved pre-activation, read only with an activation)
     if (p.act == TP_ACT_GELU_ERF) {
       float h[32];
-      load_bf16x32(static_cast<const uint16_t*>(p.aux[og]) + static_cast<long long>(row) * p.ldaux +
-                       col0,
-                   h, valid);
+      warp_load_bf16(stage, static_cast<const uint16_t*>(p.aux[og]), p.ldaux, row0, col0, p.M,
+                     valid, h);
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] *= gelu_erf_grad(h[i]);
     }
-    store_bf16_row(static_cast<uint16_t*>(p.D[og]) + static_cast<long long>(row) * p.ldd + col0, v,
-                   valid);
+    warp_store_bf16(stage, v, static_cast<uint16_t*>(p.D[og]), p.ldd, row0, col0, p.M, valid);
   }
 }
 
@@ -229,7 +286,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* epi_stage = smem + STAGES * STAGE_BYTES;  // EPI_WARPS x 4 KiB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + EPI_WARPS * STAGE_WARP_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -269,7 +327,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int total_kb = p.ksum ? p.kblocks * p.groups : p.kblocks;
+  const int total_kb = p.kblocks * p.kpo;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -288,8 +346,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             failed = true;
             break;
           }
-          const int kg = p.ksum ? kb / p.kblocks : g;
-          const int kk = (p.ksum ? kb % p.kblocks : kb) * BK;
+          const int kg = g * p.kpo + kb / p.kblocks;
+          const int kk = (kb % p.kblocks) * BK;
           const uint32_t fb = full_bar(stage);
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
@@ -383,14 +441,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       }
       if (*abort_flag) break;
       tc_fence_after();
-      const int row = mb * BM + quad * 32 + lane;
+      const int row0 = mb * BM + quad * 32;  // this warp's 32 rows
       const uint32_t trow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+      uint8_t* stage = epi_stage + (warp - 2) * STAGE_WARP_BYTES;
       for (int c0 = 0; c0 < BN; c0 += 32) {
         const int col0 = nb * BN + c0;
         if (col0 >= p.N) break;  // uniform across the warp
         float v[32];
         tmem_ld_32cols(trow + c0, v);
-        if (row < p.M) epilogue_chunk(p, g, row, col0, v);
+        epilogue_chunk(p, g, row0, col0, v, stage);
       }
       tc_fence_before();
       __syncwarp();

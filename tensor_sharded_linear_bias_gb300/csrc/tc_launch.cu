@@ -3,6 +3,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -53,6 +55,37 @@ bool encode_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer
 
 }  // namespace
 
+int plan_shard_split(int64_t M, int64_t N, int64_t K_per_group, int n) {
+  using namespace tc;
+  if (const char* env = std::getenv("TPMLP_SHARD_SPLIT")) {  // tuning override
+    const int v = std::atoi(env);
+    if (v >= 1 && v <= n && n % v == 0) return v;
+  }
+  const double sms = device_sm_count();
+  const double tiles = double((M + BM - 1) / BM) * double((N + BN - 1) / BN);
+  const double kb = double((K_per_group + BK - 1) / BK);
+  // Model: a 64-deep K block of a 128 x 256 tile costs ~512 tensor cycles (~0.27 us); a
+  // reduction of S fp32 partials moves (4 S + 4) M N bytes at ~6.5 TB/s; tiles whose K range
+  // is deeper than 256 blocks lose ~25 % (the running tiles' operands no longer fit in L2).
+  const double t_kb_us = 512.0 / 1.9e3;
+  const double hbm_bytes_per_us = 6.5e6;
+  int best = 1;
+  double best_cost = 1e300;
+  for (int S = 1; S <= n; ++S) {
+    if (n % S != 0) continue;
+    const double per_tile_kb = kb * (n / S);
+    const double waves = std::ceil(S * tiles / sms);
+    double cost = waves * per_tile_kb * t_kb_us;
+    if (per_tile_kb > 256.0) cost *= 1.25;
+    if (S > 1) cost += (4.0 * S + 4.0) * double(M) * double(N) / hbm_bytes_per_us;
+    if (cost < best_cost * 0.995) {
+      best_cost = cost;
+      best = S;
+    }
+  }
+  return best;
+}
+
 cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
   using namespace tc;
   if (s.M <= 0 || s.N <= 0 || s.K <= 0) return cudaSuccess;
@@ -79,10 +112,12 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
   p.N = static_cast<int>(s.N);
   p.kblocks = static_cast<int>((s.K + BK - 1) / BK);
   p.groups = s.groups;
-  p.ksum = s.ksum;
+  const int kpo = s.kpo > 0 ? s.kpo : (s.ksum ? s.groups : 1);
+  if (s.groups % kpo != 0) return cudaErrorInvalidValue;
+  p.kpo = kpo;
   p.tiles_m = static_cast<int>((s.M + BM - 1) / BM);
   p.tiles_n = static_cast<int>((s.N + BN - 1) / BN);
-  p.num_tiles = (s.ksum ? 1 : s.groups) * p.tiles_m * p.tiles_n;
+  p.num_tiles = (s.groups / kpo) * p.tiles_m * p.tiles_n;
   p.epi = s.epi;
   p.act = s.act;
   p.status = s.status;

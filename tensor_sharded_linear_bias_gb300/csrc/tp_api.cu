@@ -51,7 +51,7 @@ tp_status check_common(int64_t tokens, int tp, int dtype, int act, int reduce) {
   if (dtype != TP_F32 && dtype != TP_BF16) return fail(TP_ERR_DTYPE, "unknown dtype %d", dtype);
   if (act != TP_ACT_NONE && act != TP_ACT_GELU_ERF)
     return fail(TP_ERR_DTYPE, "unknown activation %d", act);
-  if (reduce != TP_REDUCE_FUSED && reduce != TP_REDUCE_PARTIALS)
+  if (reduce != TP_REDUCE_FUSED && reduce != TP_REDUCE_PARTIALS && reduce != TP_REDUCE_AUTO)
     return fail(TP_ERR_DTYPE, "unknown reduce mode %d", reduce);
   if (tp < 1 || tp > kMaxShards)
     return fail(TP_ERR_SHAPE, "tp_degree %d outside 1..%d", tp, kMaxShards);
@@ -208,7 +208,7 @@ void gemm_work(const GemmSpec& s, int dtype, double* flops, double* bytes) {
     distinctA += !seenA;
     distinctB += !seenB;
   }
-  const int outs = s.ksum ? 1 : s.groups;
+  const int outs = s.groups / (s.kpo > 0 ? s.kpo : (s.ksum ? s.groups : 1));
   double out_e = 4.0;
   if (s.epi != EPI_STORE_F32) out_e = e * ((s.epi == EPI_BIAS_ACT && s.D[0] != nullptr) ? 2 : 1);
   double aux = (s.epi == EPI_DACT && s.act != TP_ACT_NONE) ? e * M * N * outs : 0.0;
@@ -266,7 +266,7 @@ tp_status mlp_validate(const tp_mlp_desc* d, MlpSizes* z) {
   TP_TRY(check_width(d->dtype, "ffn / tp_degree", z->Fs));
   const size_t e = elem_size(d->dtype);
   z->partials_fwd =
-      d->reduce == TP_REDUCE_PARTIALS ? align256(size_t(z->n) * z->T * z->H * 4) : 0;
+      d->reduce != TP_REDUCE_FUSED ? align256(size_t(z->n) * z->T * z->H * 4) : 0;
   z->dH = align256(size_t(z->T) * z->F * e);
   z->partials_bwd = z->partials_fwd;
   z->total = kStatusBytes + std::max(z->partials_fwd, z->dH + z->partials_bwd);
@@ -303,7 +303,7 @@ tp_status lin_validate(const tp_linear_desc* d, int kind, LinSizes* z) {
     z->partials_fwd = 0;
     z->dH = d->act != TP_ACT_NONE ? align256(size_t(z->T) * z->N * e) : 0;
     z->partials_bwd =
-        d->reduce == TP_REDUCE_PARTIALS ? align256(size_t(z->n) * z->T * z->K * 4) : 0;
+        d->reduce != TP_REDUCE_FUSED ? align256(size_t(z->n) * z->T * z->K * 4) : 0;
   } else {
     if (d->act != TP_ACT_NONE) return fail(TP_ERR_DTYPE, "a row-parallel linear has no activation");
     if (d->gather != 0) return fail(TP_ERR_DTYPE, "gather applies to column-parallel linears only");
@@ -315,12 +315,20 @@ tp_status lin_validate(const tp_linear_desc* d, int kind, LinSizes* z) {
     TP_TRY(check_width(d->dtype, "in_features / tp_degree", z->Ks));
     TP_TRY(check_width(d->dtype, "out_features", z->N));
     z->partials_fwd =
-        d->reduce == TP_REDUCE_PARTIALS ? align256(size_t(z->n) * z->T * z->N * 4) : 0;
+        d->reduce != TP_REDUCE_FUSED ? align256(size_t(z->n) * z->T * z->N * 4) : 0;
     z->dH = 0;
     z->partials_bwd = 0;
   }
   z->total = kStatusBytes + std::max(z->partials_fwd, z->dH + z->partials_bwd);
   return TP_OK;
+}
+
+// Number of partial outputs of a shard-summed product: 1 (fused), n (partials), or the
+// planner's choice (bf16 AUTO).
+int shard_split(int reduce, int dtype, int64_t M, int64_t N, int64_t K, int n) {
+  if (reduce == TP_REDUCE_FUSED) return 1;
+  if (reduce == TP_REDUCE_PARTIALS) return n;
+  return dtype == TP_BF16 ? plan_shard_split(M, N, K, n) : 1;
 }
 
 cudaError_t reduce_traced(const float* P, int n, int64_t T, int64_t N, const void* bias,
@@ -351,16 +359,18 @@ tp_status row_product(int dtype, int reduce, int n, int64_t T, int64_t Ks, int64
     s.A[i] = X[i];
     s.B[i] = W[i];
   }
-  if (reduce == TP_REDUCE_FUSED) {
+  const int S = shard_split(reduce, dtype, T, N, Ks, n);
+  if (S == 1) {
     s.ksum = 1;
     s.D[0] = Z;
     s.bias[0] = bias;
     TP_CUDA(run_gemm(s, dtype, st, TP_TAG_ROW_FWD), what);
   } else {
     float* P = ws_at<float>(ws, partials_off);
-    for (int i = 0; i < n; ++i) s.D[i] = P + size_t(i) * T * N;
+    s.kpo = n / S;
+    for (int i = 0; i < S; ++i) s.D[i] = P + size_t(i) * T * N;
     TP_CUDA(run_gemm(s, dtype, st, TP_TAG_ROW_FWD), what);
-    TP_CUDA(reduce_traced(P, n, T, N, bias, dtype == TP_BF16, Z, st), "shard reduce");
+    TP_CUDA(reduce_traced(P, S, T, N, bias, dtype == TP_BF16, Z, st), "shard reduce");
   }
   return TP_OK;
 }
@@ -385,15 +395,17 @@ tp_status input_grad_sum(int dtype, int reduce, int n, int64_t T, int64_t w, int
     s.A[i] = dH[i];
     s.B[i] = W[i];
   }
-  if (reduce == TP_REDUCE_FUSED) {
+  const int S = shard_split(reduce, dtype, T, Kd, w, n);
+  if (S == 1) {
     s.ksum = 1;
     s.D[0] = dX;
     TP_CUDA(run_gemm(s, dtype, st, TP_TAG_COLUMN_DGRAD), "input-gradient GEMM");
   } else {
     float* P = ws_at<float>(ws, partials_off);
-    for (int i = 0; i < n; ++i) s.D[i] = P + size_t(i) * T * Kd;
+    s.kpo = n / S;
+    for (int i = 0; i < S; ++i) s.D[i] = P + size_t(i) * T * Kd;
     TP_CUDA(run_gemm(s, dtype, st, TP_TAG_COLUMN_DGRAD), "input-gradient GEMM");
-    TP_CUDA(reduce_traced(P, n, T, Kd, nullptr, 0, dX, st), "shard reduce");
+    TP_CUDA(reduce_traced(P, S, T, Kd, nullptr, 0, dX, st), "shard reduce");
   }
   return TP_OK;
 }

@@ -62,10 +62,20 @@ def test_wait_timeout_is_reported(tp):
     (1, 8, 16, 2),            # a single token, widths at the minimum
     (130, 72, 8 * 40, 8),     # 8 shards of 40 columns
 ])
-@pytest.mark.parametrize("reduce", [0, 1])
+@pytest.mark.parametrize("reduce", [0, 1, 2])
 def test_mlp_bf16_small(tp, T, H, F, n, reduce):
     w = SMALL.with_shape(tokens=T, hidden=H, ffn=F, tp_degree=n)
     case = MlpCase(w, reduce).run()
+    errs = compare_full(case.outputs(), *full_reference(case))
+    assert max(errs.values()) <= TOL_BF16, errs
+
+
+@pytest.mark.parametrize("split", ["1", "2", "4", "8"])
+def test_shard_sum_in_groups(tp, monkeypatch, split):
+    """The shard sum split into `split` partial outputs (groups of 8 / split shards each)."""
+    monkeypatch.setenv("TPMLP_SHARD_SPLIT", split)
+    w = SMALL.with_shape(tokens=300, hidden=136, ffn=8 * 136, tp_degree=8)
+    case = MlpCase(w, tp.TP_REDUCE_AUTO).run()
     errs = compare_full(case.outputs(), *full_reference(case))
     assert max(errs.values()) <= TOL_BF16, errs
 
