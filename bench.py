@@ -33,7 +33,7 @@ import workloads as wl  # noqa: E402
 
 METRIC = "TP-sharded MLP fwd+bwd TFLOP/s (bf16) on 1 GB300 and % of tensor-core peak"
 UNIT = "TFLOP/s"
-KERNEL_SOURCES = ["tc_gemm.cuh", "tc_launch.cu", "tc_gemm_kmn.cu", "tc_gemm_kk.cu",
+KERNEL_SOURCES = ["tc_gemm.cuh", "tc2_gemm.cuh", "tc_launch.cu", "tc_gemm_kmn.cu", "tc_gemm_kk.cu",
                   "tc_gemm_mnmn.cu", "device_common.cuh"]
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemm_tc_gpt3_mlp_T2048_tp8.md")
 

@@ -19,7 +19,7 @@ LIB = os.path.join(PKG, "libtpmlp.so")
 
 SOURCES = ["tp_api.cu", "tc_launch.cu", "tc_gemm_kmn.cu", "tc_gemm_kk.cu", "tc_gemm_mnmn.cu",
            "simt_gemm.cu", "reduce.cu", "noalloc.cu"]
-HEADERS = ["internal.h", "device_common.cuh", "tc_gemm.cuh"]
+HEADERS = ["internal.h", "device_common.cuh", "tc_gemm.cuh", "tc2_gemm.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -1,0 +1,301 @@
+// The same grouped bf16 GEMM on pairs of SMs: tcgen05.mma.cta_group::2.
+//
+// A cluster of two CTAs (one per SM) computes a 256 x 256 output tile. Each CTA stages its own
+// 128 rows of A and its own 128-column half of B (32 KiB per stage, 6 stages); one MMA issued
+// by the even CTA reads both CTAs' shared memory and writes each CTA's 128 accumulator rows
+// (all 256 columns) into that CTA's TMEM. Per k block an SM takes in 32 KiB instead of the
+// 48 KiB of the one-SM 128 x 256 tile, for the same tensor work per SM.
+//
+// Synchronisation (mbarriers; the even CTA is the "leader"):
+//   full[s]   leader only: the leader's producer posts expect_tx for both halves (64 KiB);
+//             both CTAs' TMA loads complete their bytes on it (.cta_group::2 loads).
+//   empty[s]  in both CTAs: the leader's MMA commit arrives on both (multicast).
+//   tfull[a]  in both CTAs: the leader's commit after a tile's last MMA (multicast).
+//   tempty[a] leader only: the 4 epilogue warps of both CTAs arrive (count 8).
+// TMEM (all 512 columns, two 256-column accumulators) is allocated and freed by warp 1 of
+// both CTAs together (cta_group::2). Cluster barriers after set-up and before the end keep
+// either CTA from touching the other's shared memory before it is ready or after it is gone.
+//
+// Every mbarrier wait is bounded as in the one-SM kernel; a wait that runs out records a
+// code in the status word, raises the CTA's abort flag and lets the CTA wind down.
+#pragma once
+
+#include "tc_gemm.cuh"
+
+namespace tpk {
+namespace tc2 {
+
+using tc::BK;
+using tc::TcParams;
+
+constexpr int BM = 256;                      // rows per CTA pair (128 per CTA)
+constexpr int BN = 256;                      // columns per tile (128 of B staged per CTA)
+constexpr int HALF = 128;
+constexpr int STAGES = 6;
+constexpr int ACC_BUFS = 2;
+constexpr int TMEM_COLS = ACC_BUFS * BN;     // 512
+constexpr int A_BYTES = HALF * BK * 2;       // 16 KiB
+constexpr int B_BYTES = HALF * BK * 2;       // 16 KiB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int MN_BOX_BYTES = 64 * BK * 2;    // 8 KiB
+constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARPS = 4;
+constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_WARPS * tc::STAGE_WARP_BYTES + 1024 + 256;
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t num_clusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+
+// Shared::cluster address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion is counted on an mbarrier that may
+// live in the peer CTA (`bar` is a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+// Arrives on the mbarrier at shared offset `bar` in every CTA of `mask` once all MMAs issued
+// so far by this thread have completed.
+__device__ __forceinline__ void umma_commit_pair_multicast(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* epi_stage = smem + STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + EPI_WARPS * tc::STAGE_WARP_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const uint32_t smem_base = smem_addr(smem);
+  const uint32_t bar_base = smem_addr(bars);
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + ACC_BUFS + a); };
+  const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 2 * ACC_BUFS);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();      // 0: leader (issues the MMAs), 1: peer
+  const int cluster = static_cast<int>(cluster_id_x());
+  const int nclusters = static_cast<int>(num_clusters_x());
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < ACC_BUFS; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 2 * EPI_WARPS);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int total_kb = p.kblocks * p.kpo;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer (both CTAs)
+      uint32_t stage = 0, phase = 0;
+      bool failed = false;
+      long long issued = 0;
+      for (int t = cluster; t < p.num_tiles && !failed; t += nclusters) {
+        int g, mb, nb;
+        tc::decode_tile(p, t, g, mb, nb);
+        const int arow = mb * BM + static_cast<int>(rank) * HALF;   // this CTA's A rows
+        const int bcol = nb * BN + static_cast<int>(rank) * HALF;   // this CTA's B half
+        for (int kb = 0; kb < total_kb; ++kb) {
+          if (*abort_flag) { failed = true; break; }
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, kWaitLimitNs)) {
+            report_status(p.status, kDevTimeoutBase | 0x40);
+            *abort_flag = 1;
+            failed = true;
+            break;
+          }
+          const int kg = g * p.kpo + kb / p.kblocks;
+          const int kk = (kb % p.kblocks) * BK;
+          const uint32_t fb = map_to_rank(full_bar(stage), 0);   // the leader's barrier
+          const uint32_t sa = smem_base + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
+          if (!A_MN) {
+            tma_load_2d_pair(sa, &p.tmA[kg], kk, arow, fb);
+          } else {
+#pragma unroll
+            for (int j = 0; j < HALF / 64; ++j)
+              tma_load_2d_pair(sa + j * MN_BOX_BYTES, &p.tmA[kg], arow + 64 * j, kk, fb);
+          }
+          if (!B_MN) {
+            tma_load_2d_pair(sb, &p.tmB[kg], kk, bcol, fb);
+          } else {
+#pragma unroll
+            for (int j = 0; j < HALF / 64; ++j)
+              tma_load_2d_pair(sb + j * MN_BOX_BYTES, &p.tmB[kg], bcol + 64 * j, kk, fb);
+          }
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (failed && issued > 0) {
+        // The copies signal the leader's barriers; give any still in flight time to land
+        // before this CTA can leave.
+        const uint64_t t0 = global_ns();
+        while (global_ns() - t0 < 2000000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ------------------------------------------------------------ MMA issuer (leader)
+      constexpr uint32_t idesc = tc::idesc_bf16(BM, BN, A_MN, B_MN);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool failed = false;
+      for (int t = cluster; t < p.num_tiles && !failed; t += nclusters) {
+        if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, kWaitLimitNs)) {
+          report_status(p.status, kDevTimeoutBase | 0x50);
+          *abort_flag = 1;
+          failed = true;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < total_kb; ++kb) {
+          if (*abort_flag) { failed = true; break; }
+          if (!mbar_wait_bounded(full_bar(stage), phase, kWaitLimitNs)) {
+            report_status(p.status, kDevTimeoutBase | 0x51);
+            *abort_flag = 1;
+            failed = true;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t sa = smem_base + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = A_MN ? tc::sdesc_sw128(sa + k * 2048, MN_BOX_BYTES, 1024)
+                                     : tc::sdesc_sw128(sa + k * 32, 16, 1024);
+            const uint64_t bd = B_MN ? tc::sdesc_sw128(sb + k * 2048, MN_BOX_BYTES, 1024)
+                                     : tc::sdesc_sw128(sb + k * 32, 16, 1024);
+            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          umma_commit_pair_multicast(empty_bar(stage), 0x3);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (failed) break;
+        umma_commit_pair_multicast(tfull_bar(acc), 0x3);
+        if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1u; }
+      }
+      if (failed) {
+        umma_commit_pair_multicast(drain_bar, 0x1);
+        mbar_wait_bounded(drain_bar, 0, 100000000ull);
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue warps 2..5
+    const int quad = warp & 3;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int t = cluster; t < p.num_tiles; t += nclusters) {
+      int g, mb, nb;
+      tc::decode_tile(p, t, g, mb, nb);
+      if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, kWaitLimitNs)) {
+        if (lane == 0) report_status(p.status, kDevTimeoutBase | 0x60);
+        *abort_flag = 1;
+        break;
+      }
+      if (*abort_flag) break;
+      tc::tc_fence_after();
+      const int row0 = mb * BM + static_cast<int>(rank) * HALF + quad * 32;
+      const uint32_t trow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+      uint8_t* stg = epi_stage + (warp - 2) * tc::STAGE_WARP_BYTES;
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        const int col0 = nb * BN + c0;
+        if (col0 >= p.N) break;  // uniform across the warp
+        float v[32];
+        tc::tmem_ld_32cols(trow + c0, v);
+        tc::epilogue_chunk(p, g, row0, col0, v, stg);
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+      if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+}  // namespace tc2
+}  // namespace tpk

@@ -9,13 +9,16 @@
 #include <mutex>
 
 #include "internal.h"
-#include "tc_gemm.cuh"
+#include "tc2_gemm.cuh"
 
 namespace tpk {
 namespace tc {
 cudaError_t run_kmn(const TcParams& p, int grid, cudaStream_t st);
 cudaError_t run_kk(const TcParams& p, int grid, cudaStream_t st);
 cudaError_t run_mnmn(const TcParams& p, int grid, cudaStream_t st);
+cudaError_t run_pair_kmn(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters);
+cudaError_t run_pair_kk(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters);
+cudaError_t run_pair_mnmn(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters);
 }  // namespace tc
 
 namespace {
@@ -53,6 +56,33 @@ bool encode_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The SM-pair kernel computes 256-row tiles; below that the one-SM kernel's 128-row tiles
+// waste less. TPMLP_GEMM_PAIR=0/1 forces the choice (tuning and tests).
+bool use_pair_kernel(int64_t M) {
+  if (const char* env = std::getenv("TPMLP_GEMM_PAIR")) return std::atoi(env) != 0;
+  return M > tc::BM;
+}
+
+// Largest number of co-resident 2-CTA clusters of the pair kernel (cached per device and
+// operand layout); falls back to half the SM count.
+int pair_clusters(int layout) {
+  static int cached[64][3] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return device_sm_count() / 2;
+  if (cached[dev][layout] == 0) {
+    int n = 0;
+    cudaError_t e = layout == 0   ? tc::run_pair_kmn(tc::TcParams{}, 0, nullptr, &n)
+                    : layout == 1 ? tc::run_pair_kk(tc::TcParams{}, 0, nullptr, &n)
+                                  : tc::run_pair_mnmn(tc::TcParams{}, 0, nullptr, &n);
+    if (e != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = device_sm_count() / 2;
+    }
+    cached[dev][layout] = n;
+  }
+  return cached[dev][layout];
+}
+
 }  // namespace
 
 int plan_shard_split(int64_t M, int64_t N, int64_t K_per_group, int n) {
@@ -62,6 +92,8 @@ int plan_shard_split(int64_t M, int64_t N, int64_t K_per_group, int n) {
     if (v >= 1 && v <= n && n % v == 0) return v;
   }
   const double sms = device_sm_count();
+  // One-SM tiles of 128 x 256 on every SM, or pair tiles of 256 x 256 on every SM pair:
+  // the same count of tiles per wave in units of 128 x 256.
   const double tiles = double((M + BM - 1) / BM) * double((N + BN - 1) / BN);
   const double kb = double((K_per_group + BK - 1) / BK);
   // Model: a 64-deep K block of a 128 x 256 tile costs ~512 tensor cycles (~0.27 us); a
@@ -92,13 +124,16 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
   if (s.groups < 1 || s.groups > kMaxShards) return cudaErrorInvalidValue;
   static_assert(sizeof(TcParams) <= 32764, "kernel parameter block too large");
 
+  const bool pair = use_pair_kernel(s.M);
   alignas(128) static thread_local TcParams p;
   std::memset(static_cast<void*>(&p), 0, sizeof(p));
+  // K-major boxes: 128 rows of A; 256 rows of B (one SM) or 128 (each SM of a pair).
+  const uint32_t b_rows = pair ? static_cast<uint32_t>(tc2::HALF) : static_cast<uint32_t>(BN);
   for (int g = 0; g < s.groups; ++g) {
     const bool okA = s.a_mn ? encode_bf16(&p.tmA[g], s.A[g], s.M, s.K, s.lda, 64, 64)
                             : encode_bf16(&p.tmA[g], s.A[g], s.K, s.M, s.lda, 64, BM);
     const bool okB = s.b_mn ? encode_bf16(&p.tmB[g], s.B[g], s.N, s.K, s.ldb, 64, 64)
-                            : encode_bf16(&p.tmB[g], s.B[g], s.K, s.N, s.ldb, 64, BN);
+                            : encode_bf16(&p.tmB[g], s.B[g], s.K, s.N, s.ldb, 64, b_rows);
     if (!okA || !okB) return cudaErrorInvalidValue;
     p.D[g] = s.D[g];
     p.D2[g] = s.D2[g];
@@ -115,13 +150,22 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
   const int kpo = s.kpo > 0 ? s.kpo : (s.ksum ? s.groups : 1);
   if (s.groups % kpo != 0) return cudaErrorInvalidValue;
   p.kpo = kpo;
-  p.tiles_m = static_cast<int>((s.M + BM - 1) / BM);
+  const int tile_rows = pair ? tc2::BM : BM;
+  p.tiles_m = static_cast<int>((s.M + tile_rows - 1) / tile_rows);
   p.tiles_n = static_cast<int>((s.N + BN - 1) / BN);
   p.num_tiles = (s.groups / kpo) * p.tiles_m * p.tiles_n;
   p.epi = s.epi;
   p.act = s.act;
   p.status = s.status;
 
+  const int layout = (!s.a_mn && s.b_mn) ? 0 : (!s.a_mn && !s.b_mn) ? 1 : (s.a_mn && s.b_mn) ? 2 : -1;
+  if (layout < 0) return cudaErrorNotSupported;
+  if (pair) {
+    const int clusters = std::min(p.num_tiles, pair_clusters(layout));
+    if (layout == 0) return run_pair_kmn(p, clusters, st, nullptr);
+    if (layout == 1) return run_pair_kk(p, clusters, st, nullptr);
+    return run_pair_mnmn(p, clusters, st, nullptr);
+  }
   const int grid = std::min(p.num_tiles, device_sm_count());
   if (!s.a_mn && s.b_mn) return run_kmn(p, grid, st);
   if (!s.a_mn && !s.b_mn) return run_kk(p, grid, st);
