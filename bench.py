@@ -238,6 +238,10 @@ class MlpBench:
         self.dB = [torch.empty(Fs, H, **f32) for _ in range(n)]
         self.da = [torch.empty(Fs, **f32) for _ in range(n)]
         self.db = torch.empty(H, **f32)
+        self.copy_stream = torch.cuda.Stream(device=device)
+        self.ev_x = torch.cuda.Event()
+        self.ev_dz = torch.cuda.Event()
+        self.ev_fwd = torch.cuda.Event()
         self.Z_host = torch.empty(T, H, dtype=torch.float32).pin_memory()
         self.dX_host = torch.empty(T, H, dtype=torch.float32).pin_memory()
         self.backward = w.backward
@@ -253,14 +257,36 @@ class MlpBench:
                                self.dX, self.dA, self.da, self.dB, self.db, self.ws)
 
     def step_e2e(self):
-        """The same step with its inputs copied from pinned host memory and its results
-        (Z, dX) copied back, all on the current stream."""
-        self.X.copy_(self.X_pinned, non_blocking=True)
-        self.dZ.copy_(self.dZ_pinned, non_blocking=True)
-        self.step()
-        self.Z_host.copy_(self.Z, non_blocking=True)
+        """The same step with its inputs (X, dZ) copied from pinned host memory and its results
+        (Z, dX) copied back to pinned host memory, every step. A second stream carries the
+        copies that the data dependencies let overlap with compute: dZ's upload runs during the
+        forward, Z's download during the backward. The step ends when every copy is done."""
+        import torch
+
+        tp = self.tp
+        cur = torch.cuda.current_stream()
+        cp = self.copy_stream
+        cp.wait_stream(cur)  # the previous step no longer reads X, dZ, Z
+        with torch.cuda.stream(cp):
+            self.X.copy_(self.X_pinned, non_blocking=True)
+            self.ev_x.record(cp)
+            if self.backward:
+                self.dZ.copy_(self.dZ_pinned, non_blocking=True)
+                self.ev_dz.record(cp)
+        cur.wait_event(self.ev_x)
+        tp.tp_mlp_forward(self.desc, self.X, self.A, self.a, self.B, self.b, self.Z, self.Hs,
+                          self.Ys, self.ws)
+        self.ev_fwd.record(cur)
+        if self.backward:
+            cur.wait_event(self.ev_dz)
+            tp.tp_mlp_backward(self.desc, self.X, self.A, self.B, self.Hs, self.Ys, self.dZ,
+                               self.dX, self.dA, self.da, self.dB, self.db, self.ws)
+        with torch.cuda.stream(cp):
+            cp.wait_event(self.ev_fwd)
+            self.Z_host.copy_(self.Z, non_blocking=True)
         if self.backward:
             self.dX_host.copy_(self.dX, non_blocking=True)
+        cur.wait_stream(cp)
 
     @property
     def flops(self) -> int:

@@ -96,11 +96,13 @@ __global__ void shard_reduce_scalar(const float* __restrict__ P, int n, long lon
 }
 
 // ------------------------------------------------------------------ column sums
-// One block per (segment, strip of 256 columns). Thread lane l of warp w owns columns
-// [strip + 8l, strip + 8l + 8) and rows w, w + 8, ...; the eight warps' partial sums are
-// then added in warp order. The order of every addition is fixed: the result is the same
-// on every run.
-constexpr int kColsumWarps = 8;
+// One block per (segment, strip of 256 columns), 16 warps. Lane l of warp w owns columns
+// [strip + 8l, strip + 8l + 8) and the rows r with r % 16 == w; it keeps eight of its rows'
+// 16-byte loads in flight and adds them in row order. The 16 warps' partial sums are then
+// added in warp order. Every addition happens in a fixed order, so the result is the same on
+// every run.
+constexpr int kColsumWarps = 16;
+constexpr int kColsumUnroll = 8;
 constexpr int kMaxColsumSegs = kMaxShards + 1;
 
 struct ColsumParams {
@@ -142,7 +144,29 @@ __global__ void __launch_bounds__(kColsumWarps * 32) colsum_kernel(const __grid_
   const int valid = static_cast<int>(max(0LL, min(8LL, seg.cols - col)));
   float acc[8] = {};
   if (valid > 0) {
-    for (long long r = warp; r < p.rows; r += kColsumWarps) {
+    const long long step = kColsumWarps;
+    long long r = warp;
+    if (p.bf16 && valid == 8) {
+      // Raw 16-byte loads first (8 rows in flight), then unpack and add in row order.
+      const uint16_t* in = static_cast<const uint16_t*>(seg.in);
+      for (; r + (kColsumUnroll - 1) * step < p.rows; r += kColsumUnroll * step) {
+        uint4 raw[kColsumUnroll];
+#pragma unroll
+        for (int u = 0; u < kColsumUnroll; ++u)
+          raw[u] = *reinterpret_cast<const uint4*>(in + (r + u * step) * seg.ld + col);
+#pragma unroll
+        for (int u = 0; u < kColsumUnroll; ++u) {
+          const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f = unpack_bf16x2(w[j]);
+            acc[2 * j] += f.x;
+            acc[2 * j + 1] += f.y;
+          }
+        }
+      }
+    }
+    for (; r < p.rows; r += step) {
       float v[8];
       load8(seg.in, p.bf16, r * seg.ld + col, v, valid);
 #pragma unroll
@@ -152,12 +176,14 @@ __global__ void __launch_bounds__(kColsumWarps * 32) colsum_kernel(const __grid_
 #pragma unroll
   for (int j = 0; j < 8; ++j) part[warp][8 * lane + j] = acc[j];
   __syncthreads();
-  const long long c = c0 + threadIdx.x;
-  if (threadIdx.x < 256 && c < seg.cols) {
-    float t = 0.f;
-#pragma unroll
-    for (int w = 0; w < kColsumWarps; ++w) t += part[w][threadIdx.x];
-    seg.out[c] = t;
+  if (threadIdx.x < 256) {
+    const long long c = c0 + threadIdx.x;
+    if (c < seg.cols) {
+      float t = 0.f;
+#pragma unroll 8
+      for (int w = 0; w < kColsumWarps; ++w) t += part[w][threadIdx.x];
+      seg.out[c] = t;
+    }
   }
 }
 
