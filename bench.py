@@ -93,14 +93,23 @@ def barrier(world: int):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The largest of the ranks' values (the slowest replica's time)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_throughput(work_per_step: float, steps: int, ms_local: float, world: int):
+    """Whole-job throughput of `world` independent replicas: all replicas' work divided by the
+    slowest replica's time. Returns (max ms, TFLOP/s)."""
+    ms = max_over_ranks(ms_local, world)
+    return ms, work_per_step * steps * world / (ms / 1e3) / 1e12
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -238,10 +247,12 @@ class MlpBench:
         self.dB = [torch.empty(Fs, H, **f32) for _ in range(n)]
         self.da = [torch.empty(Fs, **f32) for _ in range(n)]
         self.db = torch.empty(H, **f32)
-        self.copy_stream = torch.cuda.Stream(device=device)
-        self.ev_x = torch.cuda.Event()
-        self.ev_dz = torch.cuda.Event()
-        self.ev_fwd = torch.cuda.Event()
+        self.h2d_stream = torch.cuda.Stream(device=device)
+        self.d2h_stream = torch.cuda.Stream(device=device)
+        self.X2 = [self.X, torch.empty_like(self.X)]
+        self.dZ2 = [self.dZ, torch.empty_like(self.dZ)]
+        self.Z2 = [self.Z, torch.empty_like(self.Z)]
+        self.dX2 = [self.dX, torch.empty_like(self.dX)]
         self.Z_host = torch.empty(T, H, dtype=torch.float32).pin_memory()
         self.dX_host = torch.empty(T, H, dtype=torch.float32).pin_memory()
         self.backward = w.backward
@@ -256,37 +267,61 @@ class MlpBench:
             tp.tp_mlp_backward(self.desc, self.X, self.A, self.B, self.Hs, self.Ys, self.dZ,
                                self.dX, self.dA, self.da, self.dB, self.db, self.ws)
 
-    def step_e2e(self):
-        """The same step with its inputs (X, dZ) copied from pinned host memory and its results
-        (Z, dX) copied back to pinned host memory, every step. A second stream carries the
-        copies that the data dependencies let overlap with compute: dZ's upload runs during the
-        forward, Z's download during the backward. The step ends when every copy is done."""
+    def run_e2e(self, steps: int) -> None:
+        """`steps` steps end to end: every step uploads its inputs (X, dZ) from pinned host
+        memory and downloads its results (Z, dX) to pinned host memory. Two device slots per
+        input and output let the copies of neighbouring steps overlap compute, as a training
+        loop's input prefetch does: step i+1's uploads run during step i, Z's download during
+        the backward, dX's download during the next step's forward. All copies are issued on
+        two copy streams (host->device, device->host) ordered by events; the caller's stream
+        runs the compute and, at the end, waits for both copy streams."""
         import torch
 
         tp = self.tp
         cur = torch.cuda.current_stream()
-        cp = self.copy_stream
-        cp.wait_stream(cur)  # the previous step no longer reads X, dZ, Z
-        with torch.cuda.stream(cp):
-            self.X.copy_(self.X_pinned, non_blocking=True)
-            self.ev_x.record(cp)
+        h2d, d2h = self.h2d_stream, self.d2h_stream
+        h2d.wait_stream(cur)
+        d2h.wait_stream(cur)
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        bwd_done, zdown, dxdown = {}, {}, {}
+        for i in range(steps):
+            s = i % 2
+            X, dZ, Z, dX = self.X2[s], self.dZ2[s], self.Z2[s], self.dX2[s]
+            x_ready, dz_ready, fwd_done = ev(), ev(), ev()
+            with torch.cuda.stream(h2d):
+                if i - 2 in bwd_done:
+                    h2d.wait_event(bwd_done[i - 2])   # slot s is no longer read
+                X.copy_(self.X_pinned, non_blocking=True)
+                x_ready.record(h2d)
+                if self.backward:
+                    dZ.copy_(self.dZ_pinned, non_blocking=True)
+                    dz_ready.record(h2d)
+            cur.wait_event(x_ready)
+            if i - 2 in zdown:
+                cur.wait_event(zdown[i - 2])          # Z slot downloaded
+            tp.tp_mlp_forward(self.desc, X, self.A, self.a, self.B, self.b, Z, self.Hs,
+                              self.Ys, self.ws)
+            fwd_done.record(cur)
             if self.backward:
-                self.dZ.copy_(self.dZ_pinned, non_blocking=True)
-                self.ev_dz.record(cp)
-        cur.wait_event(self.ev_x)
-        tp.tp_mlp_forward(self.desc, self.X, self.A, self.a, self.B, self.b, self.Z, self.Hs,
-                          self.Ys, self.ws)
-        self.ev_fwd.record(cur)
-        if self.backward:
-            cur.wait_event(self.ev_dz)
-            tp.tp_mlp_backward(self.desc, self.X, self.A, self.B, self.Hs, self.Ys, self.dZ,
-                               self.dX, self.dA, self.da, self.dB, self.db, self.ws)
-        with torch.cuda.stream(cp):
-            cp.wait_event(self.ev_fwd)
-            self.Z_host.copy_(self.Z, non_blocking=True)
-        if self.backward:
-            self.dX_host.copy_(self.dX, non_blocking=True)
-        cur.wait_stream(cp)
+                cur.wait_event(dz_ready)
+                if i - 2 in dxdown:
+                    cur.wait_event(dxdown[i - 2])     # dX slot downloaded
+                tp.tp_mlp_backward(self.desc, X, self.A, self.B, self.Hs, self.Ys, dZ, dX,
+                                   self.dA, self.da, self.dB, self.db, self.ws)
+                bwd_done[i] = ev()
+                bwd_done[i].record(cur)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(fwd_done)
+                self.Z_host.copy_(Z, non_blocking=True)
+                zdown[i] = ev()
+                zdown[i].record(d2h)
+                if self.backward:
+                    d2h.wait_event(bwd_done[i])
+                    self.dX_host.copy_(dX, non_blocking=True)
+                    dxdown[i] = ev()
+                    dxdown[i].record(d2h)
+        cur.wait_stream(h2d)
+        cur.wait_stream(d2h)
 
     @property
     def flops(self) -> int:
@@ -429,17 +464,17 @@ def main():
     recs = tp.tp_trace_stop(args.steps * (launches_per_step + 2) + 16)
     clocks = sampler.stop() if sampler else None
     tp.tp_check_status(mb.ws)
-    ms = max_over_ranks(ms, world)
+    ms, value = replica_throughput(mb.flops, args.steps, ms, world)
     ms_per_step = ms / args.steps
-    value = mb.flops * args.steps * world / (ms / 1e3) / 1e12
 
     # ---- end to end: host inputs in, host results out, every step
     e2e = None
     if not args.no_e2e:
-        for _ in range(args.warmup):
-            mb.step_e2e()
-        ms_e = max_over_ranks(time_steps(mb.step_e2e, args.steps, world), world)
-        e2e = {"value": mb.flops * args.steps * world / (ms_e / 1e3) / 1e12, "unit": UNIT,
+        mb.run_e2e(args.warmup)
+        ms_e, value_e = replica_throughput(mb.flops, args.steps,
+                                           time_steps(lambda: mb.run_e2e(args.steps), 1, world),
+                                           world)
+        e2e = {"value": value_e, "unit": UNIT,
                "ms_per_step": ms_e / args.steps, "h2d_bytes_per_step": mb.h2d_bytes,
                "d2h_bytes_per_step": mb.d2h_bytes}
         tp.tp_check_status(mb.ws)
