@@ -44,6 +44,7 @@ struct GemmSpec {
   int64_t lda = 0, ldb = 0, ldd = 0, ldd2 = 0, ldaux = 0;
   int epi = EPI_STORE_F32;
   int act = TP_ACT_NONE;
+  int raster = 0;   // tensor-core GEMM tile order: 0 = m fastest, 1 = n fastest
   int* status = nullptr;
 };
 

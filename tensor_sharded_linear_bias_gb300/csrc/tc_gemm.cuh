@@ -63,6 +63,7 @@ struct __align__(128) TcParams {
   int kpo;          // groups summed into each output (1: one output per group)
   int tiles_m, tiles_n, num_tiles;
   int epi, act;
+  int raster;       // tile order inside an output: 0 = m fastest, 1 = n fastest
   int* status;
 };
 
@@ -138,13 +139,19 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, float* v) {
 }
 
 // ------------------------------------------------------------------ tile decode
-// Tile t -> output index og, m block, n block (m fastest, for reuse of the B block).
+// Tile t -> output index og, m block, n block. With m fastest, the tiles running at the same
+// time share B blocks and sweep all of A; with n fastest, they share A blocks and sweep B.
 __device__ __forceinline__ void decode_tile(const TcParams& p, int t, int& g, int& mb, int& nb) {
   const int per = p.tiles_m * p.tiles_n;
   g = t / per;
   const int r = t - g * per;
-  mb = r % p.tiles_m;
-  nb = r / p.tiles_m;
+  if (p.raster == 0) {
+    mb = r % p.tiles_m;
+    nb = r / p.tiles_m;
+  } else {
+    nb = r % p.tiles_n;
+    mb = r / p.tiles_n;
+  }
 }
 
 // ------------------------------------------------------------------ epilogue (32 rows x 32 cols per warp)

@@ -83,6 +83,25 @@ int pair_clusters(int layout) {
   return cached[dev][layout];
 }
 
+// Tile order of a launch. The tiles running at the same time (one per SM, or per SM pair)
+// touch, in m-fastest order, all tiles_m row blocks of A plus C / tiles_m column blocks of B
+// (C = tiles in flight); in n-fastest order, the converse. Each block is 256 x K bf16 (128 x K
+// for one-SM A blocks). Keep m fastest unless its working set exceeds half of L2 and n
+// fastest needs a quarter less. (Measured on GB300: m fastest is 5 % faster for the GPT-3-
+// shaped MLP, n fastest 1.5 % faster at 8192 tokens.) TPMLP_RASTER=0/1 forces the order.
+int choose_raster(int tiles_m, int tiles_n, int64_t k_total, int sms, bool pair) {
+  if (const char* env = std::getenv("TPMLP_RASTER")) return std::atoi(env) != 0;
+  const double inflight = pair ? sms / 2.0 : double(sms);
+  const double a_block = (pair ? 256.0 : 128.0) * double(k_total) * 2.0;
+  const double b_block = 256.0 * double(k_total) * 2.0;
+  const double fm = std::min<double>(tiles_m, inflight) * a_block +
+                    std::ceil(inflight / std::max(1, tiles_m)) * b_block;
+  const double fn = std::min<double>(tiles_n, inflight) * b_block +
+                    std::ceil(inflight / std::max(1, tiles_n)) * a_block;
+  const double half_l2 = 64.0e6;
+  return (fm > half_l2 && fn < 0.75 * fm) ? 1 : 0;
+}
+
 }  // namespace
 
 int plan_shard_split(int64_t M, int64_t N, int64_t K_per_group, int n) {
@@ -156,6 +175,8 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
   p.num_tiles = (s.groups / kpo) * p.tiles_m * p.tiles_n;
   p.epi = s.epi;
   p.act = s.act;
+  p.raster = choose_raster(p.tiles_m, p.tiles_n, s.K * p.kpo,
+                           pair ? 2 * pair_clusters(0) : device_sm_count(), pair);
   p.status = s.status;
 
   const int layout = (!s.a_mn && s.b_mn) ? 0 : (!s.a_mn && !s.b_mn) ? 1 : (s.a_mn && s.b_mn) ? 2 : -1;

@@ -80,14 +80,16 @@ def test_shard_sum_in_groups(tp, monkeypatch, split):
     assert max(errs.values()) <= TOL_BF16, errs
 
 
+@pytest.mark.parametrize("raster", ["0", "1"])
 @pytest.mark.parametrize("pair", ["0", "1"])
 @pytest.mark.parametrize("T,H,F,n", [(96, 72, 2 * 136, 2), (300, 136, 2 * 296, 2),
                                      (640, 264, 4 * 392, 4)])
-def test_gemm_kernel_variants(tp, monkeypatch, pair, T, H, F, n):
+def test_gemm_kernel_variants(tp, monkeypatch, pair, raster, T, H, F, n):
     """Both tensor-core kernels on every GEMM of the MLP: one SM per 128 x 256 tile, and SM
     pairs (tcgen05 cta_group::2) per 256 x 256 tile, including pairs whose second half of
-    the rows lies beyond M."""
+    the rows lies beyond M; in both tile orders (m fastest, n fastest)."""
     monkeypatch.setenv("TPMLP_GEMM_PAIR", pair)
+    monkeypatch.setenv("TPMLP_RASTER", raster)
     for reduce in (0, 2):
         case = MlpCase(SMALL.with_shape(tokens=T, hidden=H, ffn=F, tp_degree=n), reduce).run()
         errs = compare_full(case.outputs(), *full_reference(case))
