@@ -45,7 +45,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="gpt3")
-    ap.add_argument("--reduce", choices=["fused", "partials", "auto"], default="auto")
+    ap.add_argument("--reduce", choices=["fused", "partials", "auto", "partials_bf16"],
+                    default="auto")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -433,9 +434,49 @@ def run_reference(args, w, world, rank):
     return 0
 
 
+# ----------------------------------------------------------------------------- pages' example
+def run_p3_column_latency(args, world, rank, local):
+    """Latency of the pages' column-parallel example: X [32, 768] times W [768, 3072] split
+    into 4 column shards, bias per shard, outputs gathered into one [32, 3072] tensor
+    (tp_linear_column_forward with gather = 1), fp32 as on the page and bf16."""
+    import torch
+
+    from tensor_sharded_linear_bias_gb300.modules import ColumnParallelLinear
+
+    device = dist_init(world, local)
+    w = wl.P3_FP32_FWD
+    res = {}
+    for name, dt in (("f32", torch.float32), ("bf16", torch.bfloat16)):
+        weight = torch.from_numpy(wl.normal(1000 * w.cid + 1, (w.hidden, w.ffn), 0.01))
+        layer = ColumnParallelLinear(w.hidden, w.ffn, w.tp_degree, dtype=dt, device=device,
+                                     weight=weight, gather=True)
+        x = torch.from_numpy(wl.normal(1000 * w.cid, (w.tokens, w.hidden), 1.0)).to(device, dt)
+        for _ in range(max(args.warmup, 10)):
+            layer.forward(x)
+        layer.check()
+        ms = time_steps(lambda: layer.forward(x), args.steps, world)
+        ms = max_over_ranks(ms, world)
+        res[name] = ms / args.steps * 1e3
+    if rank == 0:
+        print(json.dumps({
+            "metric": "column-parallel linear latency, the pages' example (768 -> 3072, batch 32, "
+                      "4 shards, gathered output)",
+            "value": res["f32"], "unit": "us", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": False, "dtype": "f32",
+            "data": "synthetic", "bf16_us": res["bf16"],
+            "config": {"workload": "p3_column_linear_T32_K768_N3072_tp4_gather",
+                       "calls": "tp_linear_column_forward back to back, CUDA events"},
+            "context": "the page expects ~1.5 ms on one GPU and ~1.2 ms with 4-GPU tensor "
+                       "parallelism (hardware not stated)"}), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- main
 def main():
     args = parse_args()
+    if args.workload == "p3col":
+        world, rank, local = dist_setup(args.gpus)
+        return run_p3_column_latency(args, world, rank, local)
     w = workload(args.workload)
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
@@ -449,7 +490,7 @@ def main():
     import tensor_sharded_linear_bias_gb300 as tp
 
     reduce = {"fused": tp.TP_REDUCE_FUSED, "partials": tp.TP_REDUCE_PARTIALS,
-              "auto": tp.TP_REDUCE_AUTO}[args.reduce]
+              "auto": tp.TP_REDUCE_AUTO, "partials_bf16": tp.TP_REDUCE_PARTIALS_BF16}[args.reduce]
     keep_host = (rank == 0 and world == 1 and not args.no_cpu_baseline)
     mb = MlpBench(w, reduce, device, keep_host)
 

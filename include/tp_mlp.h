@@ -65,11 +65,15 @@ typedef enum tp_act { TP_ACT_NONE = 0, TP_ACT_GELU_ERF = 1 } tp_act;
  *  AUTO:     the shards are summed in S groups (S a divisor of tp_degree chosen from the
  *            shape and the SM count to balance tile waves against reduction traffic; S = 1 is
  *            FUSED), then a reduction of the S partials. bf16 only; fp32 uses FUSED.
- *            Workspace is sized as for PARTIALS. */
+ *            Workspace is sized as for PARTIALS.
+ *  PARTIALS_BF16: one bf16 partial per shard (half the bytes of PARTIALS), summed in fp32 by
+ *            the reduction kernel -- the reduced-precision "communication" of "Tensor
+ *            Parallelism: principle and practice", section 5.2. bf16 only. */
 typedef enum tp_reduce {
   TP_REDUCE_FUSED = 0,
   TP_REDUCE_PARTIALS = 1,
-  TP_REDUCE_AUTO = 2
+  TP_REDUCE_AUTO = 2,
+  TP_REDUCE_PARTIALS_BF16 = 3
 } tp_reduce;
 
 typedef enum tp_status {

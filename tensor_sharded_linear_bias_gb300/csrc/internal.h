@@ -22,6 +22,7 @@ enum EpiKind : int {
   EPI_STORE_F32 = 0,      // D (fp32) = acc (+ bias[n] once, when bias != nullptr)
   EPI_BIAS_ACT = 1,       // H = acc + bias[n] -> D (optional), Y = act(H) -> D2  (bf16 / fp32)
   EPI_DACT = 2,           // D = acc * act'(aux[m,n])                               (bf16 / fp32)
+  EPI_STORE_BF16 = 3,     // D (bf16) = acc (+ bias[n])                   (tensor-core GEMM only)
 };
 
 // One launch of a (grouped) GEMM: D_g[M,N] = A_g[M,K] * B_g[K,N] for every group g, or,
@@ -56,6 +57,10 @@ cudaError_t launch_simt_gemm(const GemmSpec& s, cudaStream_t st);
 // Z[T,N] = sum_{i<n} P[i][T,N] + bias (bias may be null; bias dtype: bf16 if bias_bf16).
 cudaError_t launch_shard_reduce(const float* P, int n, int64_t T, int64_t N,
                                 const void* bias, int bias_bf16, float* Z, cudaStream_t st);
+
+// The same over bf16 partials (summed in fp32); N % 8 == 0.
+cudaError_t launch_shard_reduce_bf16(const uint16_t* P, int n, int64_t T, int64_t N,
+                                     const void* bias, float* Z, cudaStream_t st);
 
 // Column sums: out_s[c] = sum_{r<rows} in_s[r*ld_s + c] for every segment s.
 struct ColsumSeg {

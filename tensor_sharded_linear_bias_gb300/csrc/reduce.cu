@@ -95,6 +95,43 @@ __global__ void shard_reduce_scalar(const float* __restrict__ P, int n, long lon
   }
 }
 
+// Eight bf16 partial values per thread and shard (one 16-byte load each), summed in fp32 in
+// shard order, plus the bias; two 16-byte fp32 stores.
+__global__ void __launch_bounds__(kReduceThreads) shard_reduce_bf16_v8(
+    const uint4* __restrict__ P, int n, long long count8, long long n8, const void* bias,
+    float4* __restrict__ Z) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+       idx < count8; idx += stride) {
+    float s[8] = {};
+    for (int i = 0; i < n; ++i) {
+      uint4 u;
+      asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
+                   : "l"(P + i * count8 + idx));
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = unpack_bf16x2(w[j]);
+        s[2 * j] += f.x;
+        s[2 * j + 1] += f.y;
+      }
+    }
+    if (bias != nullptr) {
+      const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(bias) + (idx % n8) * 8);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = unpack_bf16x2(w[j]);
+        s[2 * j] += f.x;
+        s[2 * j + 1] += f.y;
+      }
+    }
+    Z[2 * idx] = make_float4(s[0], s[1], s[2], s[3]);
+    Z[2 * idx + 1] = make_float4(s[4], s[5], s[6], s[7]);
+  }
+}
+
 // ------------------------------------------------------------------ column sums
 // One block per (segment, strip of 256 columns), 16 warps. Lane l of warp w owns columns
 // [strip + 8l, strip + 8l + 8) and the rows r with r % 16 == w; it keeps eight of its rows'
@@ -267,6 +304,22 @@ cudaError_t launch_shard_reduce(const float* P, int n, int64_t T, int64_t N, con
     shard_reduce_scalar<<<static_cast<unsigned>(blocks), kReduceThreads, 0, st>>>(
         P, n, count, N, bias, bias_bf16, Z);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shard_reduce_bf16(const uint16_t* P, int n, int64_t T, int64_t N,
+                                     const void* bias, float* Z, cudaStream_t st) {
+  const long long count = static_cast<long long>(T) * N;
+  if (count == 0) return cudaSuccess;
+  if (N % 8 != 0 || reinterpret_cast<uintptr_t>(P) % 16 != 0 ||
+      reinterpret_cast<uintptr_t>(Z) % 16 != 0 ||
+      (bias != nullptr && reinterpret_cast<uintptr_t>(bias) % 16 != 0))
+    return cudaErrorInvalidValue;
+  const long long count8 = count / 8;
+  const long long blocks = std::min<long long>((count8 + kReduceThreads - 1) / kReduceThreads,
+                                               static_cast<long long>(device_sm_count()) * 8);
+  shard_reduce_bf16_v8<<<static_cast<unsigned>(blocks), kReduceThreads, 0, st>>>(
+      reinterpret_cast<const uint4*>(P), n, count8, N / 8, bias, reinterpret_cast<float4*>(Z));
   return cudaGetLastError();
 }
 

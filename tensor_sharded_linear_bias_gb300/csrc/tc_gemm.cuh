@@ -266,6 +266,9 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, int g, int row
   if (p.epi == EPI_STORE_F32) {
     if (p.bias[og] != nullptr) add_bias_bf16x32(static_cast<const uint16_t*>(p.bias[og]) + col0, valid, v);
     warp_store_f32(stage, v, static_cast<float*>(p.D[og]), p.ldd, row0, col0, p.M, valid);
+  } else if (p.epi == EPI_STORE_BF16) {
+    if (p.bias[og] != nullptr) add_bias_bf16x32(static_cast<const uint16_t*>(p.bias[og]) + col0, valid, v);
+    warp_store_bf16(stage, v, static_cast<uint16_t*>(p.D[og]), p.ldd, row0, col0, p.M, valid);
   } else if (p.epi == EPI_BIAS_ACT) {
     if (p.bias[og] != nullptr) add_bias_bf16x32(static_cast<const uint16_t*>(p.bias[og]) + col0, valid, v);
     if (p.D[og] != nullptr)

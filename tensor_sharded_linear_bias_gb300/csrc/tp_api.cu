@@ -51,8 +51,11 @@ tp_status check_common(int64_t tokens, int tp, int dtype, int act, int reduce) {
   if (dtype != TP_F32 && dtype != TP_BF16) return fail(TP_ERR_DTYPE, "unknown dtype %d", dtype);
   if (act != TP_ACT_NONE && act != TP_ACT_GELU_ERF)
     return fail(TP_ERR_DTYPE, "unknown activation %d", act);
-  if (reduce != TP_REDUCE_FUSED && reduce != TP_REDUCE_PARTIALS && reduce != TP_REDUCE_AUTO)
+  if (reduce != TP_REDUCE_FUSED && reduce != TP_REDUCE_PARTIALS && reduce != TP_REDUCE_AUTO &&
+      reduce != TP_REDUCE_PARTIALS_BF16)
     return fail(TP_ERR_DTYPE, "unknown reduce mode %d", reduce);
+  if (reduce == TP_REDUCE_PARTIALS_BF16 && dtype != TP_BF16)
+    return fail(TP_ERR_DTYPE, "bf16 partials need bf16 inputs");
   if (tp < 1 || tp > kMaxShards)
     return fail(TP_ERR_SHAPE, "tp_degree %d outside 1..%d", tp, kMaxShards);
   if (tokens < 0 || tokens > kMaxDim) return fail(TP_ERR_SHAPE, "tokens %lld out of range",
@@ -242,6 +245,9 @@ cudaError_t zero_f32(void* p, int64_t count, cudaStream_t st) {
     if (_e != cudaSuccess) return cuda_fail(_e, what); \
   } while (0)
 
+// Bytes of one element of a shard partial.
+size_t partial_bytes(int reduce) { return reduce == TP_REDUCE_PARTIALS_BF16 ? 2 : 4; }
+
 // ---------------------------------------------------------------- MLP sizes
 struct MlpSizes {
   int64_t T, H, F, Fs;
@@ -266,7 +272,7 @@ tp_status mlp_validate(const tp_mlp_desc* d, MlpSizes* z) {
   TP_TRY(check_width(d->dtype, "ffn / tp_degree", z->Fs));
   const size_t e = elem_size(d->dtype);
   z->partials_fwd =
-      d->reduce != TP_REDUCE_FUSED ? align256(size_t(z->n) * z->T * z->H * 4) : 0;
+      d->reduce != TP_REDUCE_FUSED ? align256(size_t(z->n) * z->T * z->H * partial_bytes(d->reduce)) : 0;
   z->dH = align256(size_t(z->T) * z->F * e);
   z->partials_bwd = z->partials_fwd;
   z->total = kStatusBytes + std::max(z->partials_fwd, z->dH + z->partials_bwd);
@@ -303,7 +309,7 @@ tp_status lin_validate(const tp_linear_desc* d, int kind, LinSizes* z) {
     z->partials_fwd = 0;
     z->dH = d->act != TP_ACT_NONE ? align256(size_t(z->T) * z->N * e) : 0;
     z->partials_bwd =
-        d->reduce != TP_REDUCE_FUSED ? align256(size_t(z->n) * z->T * z->K * 4) : 0;
+        d->reduce != TP_REDUCE_FUSED ? align256(size_t(z->n) * z->T * z->K * partial_bytes(d->reduce)) : 0;
   } else {
     if (d->act != TP_ACT_NONE) return fail(TP_ERR_DTYPE, "a row-parallel linear has no activation");
     if (d->gather != 0) return fail(TP_ERR_DTYPE, "gather applies to column-parallel linears only");
@@ -315,7 +321,7 @@ tp_status lin_validate(const tp_linear_desc* d, int kind, LinSizes* z) {
     TP_TRY(check_width(d->dtype, "in_features / tp_degree", z->Ks));
     TP_TRY(check_width(d->dtype, "out_features", z->N));
     z->partials_fwd =
-        d->reduce != TP_REDUCE_FUSED ? align256(size_t(z->n) * z->T * z->N * 4) : 0;
+        d->reduce != TP_REDUCE_FUSED ? align256(size_t(z->n) * z->T * z->N * partial_bytes(d->reduce)) : 0;
     z->dH = 0;
     z->partials_bwd = 0;
   }
@@ -327,7 +333,7 @@ tp_status lin_validate(const tp_linear_desc* d, int kind, LinSizes* z) {
 // planner's choice (bf16 AUTO).
 int shard_split(int reduce, int dtype, int64_t M, int64_t N, int64_t K, int n) {
   if (reduce == TP_REDUCE_FUSED) return 1;
-  if (reduce == TP_REDUCE_PARTIALS) return n;
+  if (reduce == TP_REDUCE_PARTIALS || reduce == TP_REDUCE_PARTIALS_BF16) return n;
   return dtype == TP_BF16 ? plan_shard_split(M, N, K, n) : 1;
 }
 
@@ -336,6 +342,13 @@ cudaError_t reduce_traced(const float* P, int n, int64_t T, int64_t N, const voi
   const double bytes = (4.0 * n + 4.0) * double(T) * N + (bias ? (bias_bf16 ? 2.0 : 4.0) * N : 0.0);
   return traced(TP_K_SHARD_REDUCE, TP_TAG_REDUCE, n, double(n - 1) * T * N + (bias ? T * N : 0),
                 bytes, st, [&] { return launch_shard_reduce(P, n, T, N, bias, bias_bf16, Z, st); });
+}
+
+cudaError_t reduce_bf16_traced(const uint16_t* P, int n, int64_t T, int64_t N, const void* bias,
+                               float* Z, cudaStream_t st) {
+  const double bytes = (2.0 * n + 4.0) * double(T) * N + (bias ? 2.0 * N : 0.0);
+  return traced(TP_K_SHARD_REDUCE, TP_TAG_REDUCE, n, double(n - 1) * T * N + (bias ? T * N : 0),
+                bytes, st, [&] { return launch_shard_reduce_bf16(P, n, T, N, bias, Z, st); });
 }
 
 // Row-parallel product Z = sum_i X_i W_i + bias, fused or through partials.
@@ -366,11 +379,19 @@ tp_status row_product(int dtype, int reduce, int n, int64_t T, int64_t Ks, int64
     s.bias[0] = bias;
     TP_CUDA(run_gemm(s, dtype, st, TP_TAG_ROW_FWD), what);
   } else {
-    float* P = ws_at<float>(ws, partials_off);
     s.kpo = n / S;
-    for (int i = 0; i < S; ++i) s.D[i] = P + size_t(i) * T * N;
-    TP_CUDA(run_gemm(s, dtype, st, TP_TAG_ROW_FWD), what);
-    TP_CUDA(reduce_traced(P, S, T, N, bias, dtype == TP_BF16, Z, st), "shard reduce");
+    if (reduce == TP_REDUCE_PARTIALS_BF16) {
+      uint16_t* P = ws_at<uint16_t>(ws, partials_off);
+      s.epi = EPI_STORE_BF16;
+      for (int i = 0; i < S; ++i) s.D[i] = P + size_t(i) * T * N;
+      TP_CUDA(run_gemm(s, dtype, st, TP_TAG_ROW_FWD), what);
+      TP_CUDA(reduce_bf16_traced(P, S, T, N, bias, Z, st), "shard reduce");
+    } else {
+      float* P = ws_at<float>(ws, partials_off);
+      for (int i = 0; i < S; ++i) s.D[i] = P + size_t(i) * T * N;
+      TP_CUDA(run_gemm(s, dtype, st, TP_TAG_ROW_FWD), what);
+      TP_CUDA(reduce_traced(P, S, T, N, bias, dtype == TP_BF16, Z, st), "shard reduce");
+    }
   }
   return TP_OK;
 }
@@ -401,11 +422,19 @@ tp_status input_grad_sum(int dtype, int reduce, int n, int64_t T, int64_t w, int
     s.D[0] = dX;
     TP_CUDA(run_gemm(s, dtype, st, TP_TAG_COLUMN_DGRAD), "input-gradient GEMM");
   } else {
-    float* P = ws_at<float>(ws, partials_off);
     s.kpo = n / S;
-    for (int i = 0; i < S; ++i) s.D[i] = P + size_t(i) * T * Kd;
-    TP_CUDA(run_gemm(s, dtype, st, TP_TAG_COLUMN_DGRAD), "input-gradient GEMM");
-    TP_CUDA(reduce_traced(P, S, T, Kd, nullptr, 0, dX, st), "shard reduce");
+    if (reduce == TP_REDUCE_PARTIALS_BF16) {
+      uint16_t* P = ws_at<uint16_t>(ws, partials_off);
+      s.epi = EPI_STORE_BF16;
+      for (int i = 0; i < S; ++i) s.D[i] = P + size_t(i) * T * Kd;
+      TP_CUDA(run_gemm(s, dtype, st, TP_TAG_COLUMN_DGRAD), "input-gradient GEMM");
+      TP_CUDA(reduce_bf16_traced(P, S, T, Kd, nullptr, dX, st), "shard reduce");
+    } else {
+      float* P = ws_at<float>(ws, partials_off);
+      for (int i = 0; i < S; ++i) s.D[i] = P + size_t(i) * T * Kd;
+      TP_CUDA(run_gemm(s, dtype, st, TP_TAG_COLUMN_DGRAD), "input-gradient GEMM");
+      TP_CUDA(reduce_traced(P, S, T, Kd, nullptr, 0, dX, st), "shard reduce");
+    }
   }
   return TP_OK;
 }

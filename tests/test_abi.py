@@ -74,6 +74,8 @@ def test_workspace_sizes(tp):
     part = n * T * H * 4
     assert tp.tp_mlp_workspace_size(mlp(tp, reduce=tp.TP_REDUCE_PARTIALS)) == 256 + T * F * 2 + part
     assert tp.tp_mlp_workspace_size(mlp(tp, reduce=tp.TP_REDUCE_AUTO)) == 256 + T * F * 2 + part
+    assert tp.tp_mlp_workspace_size(mlp(tp, reduce=tp.TP_REDUCE_PARTIALS_BF16)) == \
+        256 + T * F * 2 + part // 2
     col = tp.LinearDesc(tokens=32, in_features=768, out_features=3072, tp_degree=4,
                         dtype=tp.TP_F32, act=0, reduce=0, gather=1)
     assert tp.tp_linear_workspace_size(col, tp.TP_COLUMN) == 256
@@ -92,7 +94,8 @@ def test_workspace_sizes(tp):
     (dict(ffn=4 * 130), "TP_ERR_ALIGN"),         # ... including the shard width
     (dict(dtype=7), "TP_ERR_DTYPE"),
     (dict(act=3), "TP_ERR_DTYPE"),
-    (dict(reduce=3), "TP_ERR_DTYPE"),
+    (dict(reduce=4), "TP_ERR_DTYPE"),
+    (dict(reduce=3, dtype=0), "TP_ERR_DTYPE"),     # bf16 partials need bf16 inputs
 ])
 def test_mlp_desc_validation(tp, kw, expected):
     assert status_of(lambda: tp.tp_mlp_workspace_size(mlp(tp, **kw))) == expected

@@ -62,7 +62,7 @@ def test_wait_timeout_is_reported(tp):
     (1, 8, 16, 2),            # a single token, widths at the minimum
     (130, 72, 8 * 40, 8),     # 8 shards of 40 columns
 ])
-@pytest.mark.parametrize("reduce", [0, 1, 2])
+@pytest.mark.parametrize("reduce", [0, 1, 2, 3])
 def test_mlp_bf16_small(tp, T, H, F, n, reduce):
     w = SMALL.with_shape(tokens=T, hidden=H, ffn=F, tp_degree=n)
     case = MlpCase(w, reduce).run()
@@ -144,6 +144,23 @@ def test_fused_matches_partials(tp):
         assert rel(a[k], b[k]) <= 1e-5, k
     for k in ("dA", "dB", "da", "H", "Y"):
         assert all(np.array_equal(x, y) for x, y in zip(a[k], b[k])), k
+
+
+def test_bf16_partials_error_vs_bytes(tp):
+    """bf16 shard partials halve the partial bytes; their rounding error stays far inside the
+    bf16 tolerance (it is recorded against the fp32-partials error of the same inputs)."""
+    w = SMALL.with_shape(tokens=512, hidden=256, ffn=8 * 256, tp_degree=8)
+    ref_f, ref_b = None, None
+    errs = {}
+    for reduce in (1, 3):
+        case = MlpCase(w, reduce).run()
+        if ref_f is None:
+            ref_f, ref_b = full_reference(case)
+        o = case.outputs()
+        errs[reduce] = (rel(o["Z"], ref_f["Z"]), rel(o["dX"], ref_b["dX"]))
+    assert max(errs[3]) <= TOL_BF16, errs
+    # the bf16 partials add at most a few bf16 ulps (2^-8 relative) to the fp32-partials error
+    assert errs[3][0] <= errs[1][0] + 8 * 2.0 ** -8, errs
 
 
 def test_deterministic(tp):
@@ -232,8 +249,10 @@ def test_column_linear(tp, dtype, gather, act):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("reduce", [0, 1])
+@pytest.mark.parametrize("reduce", [0, 1, 2, 3])
 def test_row_linear(tp, dtype, reduce):
+    if reduce == 3 and dtype == "f32":
+        pytest.skip("bf16 partials need bf16 inputs")
     import torch
 
     T, K, N, n = 190, 4 * 88, 264, 4
@@ -281,7 +300,7 @@ def test_workload_mlp_4096_1024_4096_tp2_full(tp):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("reduce", [0, 1, 2])
+@pytest.mark.parametrize("reduce", [0, 1, 2, 3])
 def test_workload_gpt3_mlp_slice_sampled(tp, reduce):
     """The bench's workload and launch configuration (reduce=2 is the AUTO mode it times)."""
     w = wl.GPT3_MLP_T2048_TP8
