@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--workload", default="gpt3")
     ap.add_argument("--reduce", choices=["fused", "partials", "auto", "partials_bf16"],
                     default="auto")
+    ap.add_argument("--sp", action="store_true",
+                    help="sequence-parallel step: token-sharded X, dZ in and Z, dX out")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -202,7 +204,7 @@ def profiled_traffic(workload_name: str):
 
 # ----------------------------------------------------------------------------- the step
 class MlpBench:
-    def __init__(self, w: wl.MlpWorkload, reduce: int, device, keep_host: bool):
+    def __init__(self, w: wl.MlpWorkload, reduce: int, device, keep_host: bool, sp: bool = False):
         import numpy as np
         import torch
 
@@ -238,7 +240,15 @@ class MlpBench:
         self.desc = tp.MlpDesc(tokens=T, hidden=H, ffn=F, tp_degree=n,
                                dtype=tp.TP_BF16 if bf16 else tp.TP_F32,
                                act=tp.TP_ACT_GELU_ERF, reduce=reduce)
-        self.ws = tp.new_workspace(tp.tp_mlp_workspace_size(self.desc), device)
+        self.sp = sp
+        self.ws = tp.new_workspace(tp.tp_mlp_sp_workspace_size(self.desc) if sp else
+                                   tp.tp_mlp_workspace_size(self.desc), device)
+        if sp:
+            Ts = T // n
+            self.Xs = [self.X[j * Ts:(j + 1) * Ts].contiguous() for j in range(n)]
+            self.dZs = [self.dZ[j * Ts:(j + 1) * Ts].contiguous() for j in range(n)]
+            self.Zs = [torch.empty(Ts, H, dtype=torch.float32, device=device) for _ in range(n)]
+            self.dXs = [torch.empty(Ts, H, dtype=torch.float32, device=device) for _ in range(n)]
         f32 = dict(dtype=torch.float32, device=device)
         self.Z = torch.empty(T, H, **f32)
         self.Hs = [torch.empty(T, Fs, dtype=cdt, device=device) for _ in range(n)]
@@ -262,6 +272,14 @@ class MlpBench:
 
     def step(self):
         tp = self.tp
+        if self.sp:
+            tp.tp_mlp_forward_sp(self.desc, self.Xs, self.A, self.a, self.B, self.b, self.Zs,
+                                 self.Hs, self.Ys, self.ws)
+            if self.backward:
+                tp.tp_mlp_backward_sp(self.desc, self.Xs, self.A, self.B, self.Hs, self.Ys,
+                                      self.dZs, self.dXs, self.dA, self.da, self.dB, self.db,
+                                      self.ws)
+            return
         tp.tp_mlp_forward(self.desc, self.X, self.A, self.a, self.B, self.b, self.Z, self.Hs,
                           self.Ys, self.ws)
         if self.backward:
@@ -492,14 +510,16 @@ def main():
     reduce = {"fused": tp.TP_REDUCE_FUSED, "partials": tp.TP_REDUCE_PARTIALS,
               "auto": tp.TP_REDUCE_AUTO, "partials_bf16": tp.TP_REDUCE_PARTIALS_BF16}[args.reduce]
     keep_host = (rank == 0 and world == 1 and not args.no_cpu_baseline)
-    mb = MlpBench(w, reduce, device, keep_host)
+    mb = MlpBench(w, reduce, device, keep_host, sp=args.sp)
+    if args.sp:
+        args.no_e2e = True
 
     # ---- device-resident throughput, with launch tracing over the timed region
     for _ in range(args.warmup):
         mb.step()
     tp.tp_check_status(mb.ws)
     sampler = ClockSampler(device.index if device.index is not None else 0) if rank == 0 else None
-    launches_per_step = 7 if w.backward else 2
+    launches_per_step = (7 if w.backward else 2) + (5 if args.sp else 0)
     tp.tp_trace_start(args.steps * (launches_per_step + 2) + 16)
     ms = time_steps(mb.step, args.steps, world)
     recs = tp.tp_trace_stop(args.steps * (launches_per_step + 2) + 16)
@@ -575,6 +595,7 @@ def main():
         "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
         "config": {"workload": w.name, "tokens": w.tokens, "hidden": w.hidden, "ffn": w.ffn,
                    "tp_degree": w.tp_degree, "reduce": args.reduce,
+                   "sequence_parallel": bool(args.sp),
                    "pass": "fwd+bwd" if w.backward else "fwd",
                    "parallelism": "single GPU, all shards on it" if world == 1 else
                    f"{world} independent replicas (no exchange)",

@@ -162,6 +162,27 @@ tp_status tp_mlp_backward(const tp_mlp_desc* desc, const void* X, const void* co
                           void* const* dA, void* const* da, void* const* dB, void* db,
                           void* ws, size_t ws_bytes, void* stream);
 
+/* Sequence-parallel MLP ("What tensor parallelism is", section on sequence parallelism; the
+ * ReduceScatter of "PaddlePaddle tensor parallelism"). The tokens are split across the shards:
+ * X_shards[j] and Z_shards[j] (backward: dZ_shards[j], dX_shards[j]) hold rows
+ * j*T/n .. (j+1)*T/n - 1, each [T/n, H]; T must divide by tp_degree (else
+ * TP_ERR_INDIVISIBLE). The token shards are all-gathered on the device, the MLP runs as in
+ * tp_mlp_forward / tp_mlp_backward, and the shard sum Z (dX) is scattered back by token rows
+ * (a reduce-scatter: each token shard receives the full sum for its rows). Hsave, Ysave, the
+ * weight and bias gradients are as in the non-sequence-parallel calls. The workspace
+ * (tp_mlp_sp_workspace_size) adds gathered copies of X and dZ and the full Z / dX. */
+tp_status tp_mlp_sp_workspace_size(const tp_mlp_desc* desc, size_t* bytes);
+tp_status tp_mlp_forward_sp(const tp_mlp_desc* desc, const void* const* X_shards,
+                            const void* const* A, const void* const* a, const void* const* B,
+                            const void* b, void* const* Z_shards, void* const* Hsave,
+                            void* const* Ysave, void* ws, size_t ws_bytes, void* stream);
+tp_status tp_mlp_backward_sp(const tp_mlp_desc* desc, const void* const* X_shards,
+                             const void* const* A, const void* const* B,
+                             const void* const* Hsave, const void* const* Ysave,
+                             const void* const* dZ_shards, void* const* dX_shards,
+                             void* const* dA, void* const* da, void* const* dB, void* db,
+                             void* ws, size_t ws_bytes, void* stream);
+
 /* Column-parallel linear forward: Y_i = act(X W_i + bias_i). X [T,K]; W[i] [K,N/n];
  * bias[i] [N/n] or bias NULL; Y[i] [T,N/n] in the input dtype (gather=1: Y[0] is [T,N]).
  * Hsave[i] [T,N/n] receives X W_i + bias_i when act != NONE (required then), else may be
@@ -208,7 +229,8 @@ typedef enum tp_kernel_kind {
   TP_K_SHARD_REDUCE = 3,   /* sum of fp32 shard partials (+ bias) */
   TP_K_COLSUM = 4,         /* bias gradients: column sums over tokens */
   TP_K_DACT = 5,           /* dH = dY * act'(H) */
-  TP_K_SELFTEST = 6
+  TP_K_SELFTEST = 6,
+  TP_K_SHARD_COPY = 7      /* token-shard gather / scatter (sequence parallel) */
 } tp_kernel_kind;
 
 typedef enum tp_trace_tag {
@@ -221,7 +243,9 @@ typedef enum tp_trace_tag {
   TP_TAG_REDUCE = 7,       /* shard reduction of partials */
   TP_TAG_BIAS_GRAD = 8,    /* db, da_i */
   TP_TAG_ACT_GRAD = 9,     /* stand-alone dH = dY * act'(H) */
-  TP_TAG_OTHER = 10
+  TP_TAG_OTHER = 10,
+  TP_TAG_SP_GATHER = 11,   /* all-gather of token shards */
+  TP_TAG_SP_SCATTER = 12   /* scatter of the summed rows to token shards */
 } tp_trace_tag;
 
 typedef struct tp_trace_record {

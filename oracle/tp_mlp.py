@@ -55,6 +55,7 @@ __all__ = [
     "concat_columns", "qkv_head_shards", "linear", "bias_grad", "column_parallel_forward",
     "column_parallel_backward", "row_parallel_forward", "row_parallel_backward",
     "mlp_forward", "mlp_backward", "mlp_columns", "attn_forward", "attn_backward",
+    "split_tokens", "all_gather_tokens", "mlp_forward_sp", "mlp_backward_sp",
 ]
 
 _SQRT2 = math.sqrt(2.0)
@@ -253,6 +254,38 @@ def mlp_columns(X, A, a, B, dZ, n: int, cols: Sequence[int]):
         out["da"][pos] = dai[0]
         out["dB"][pos, :] = dBi[0, :]
     return out
+
+
+# ----------------------------------------------------------------------------- sequence parallel
+def split_tokens(M, n: int) -> List[np.ndarray]:
+    """Token (row) split: shard j holds rows j*T/n .. (j+1)*T/n - 1 (sequence parallelism,
+    [Lansai] "sequence parallelism", which splits the sequence dimension across devices)."""
+    return split_rows(M, n)
+
+
+def all_gather_tokens(parts: Sequence[np.ndarray]) -> np.ndarray:
+    """All-gather of token shards: their rows stacked in shard order."""
+    return np.concatenate([_f64(p) for p in parts], axis=0)
+
+
+def mlp_forward_sp(X_shards, A, a, B, b, n: int):
+    """Sequence-parallel MLP forward: the token shards X_j are all-gathered into X, the MLP
+    runs as in mlp_forward, and the shard sum Z is reduce-scattered: shard j receives rows
+    j*T/n .. (j+1)*T/n - 1 of Z ([Paddle]: ReduceScatter in place of AllReduce).
+    Returns a dict with Z (list of token shards), H, Y (lists of shard activations)."""
+    X = all_gather_tokens(X_shards)
+    out = mlp_forward(X, A, a, B, b, n)
+    return {"Z": split_tokens(out["Z"], n), "H": out["H"], "Y": out["Y"]}
+
+
+def mlp_backward_sp(X_shards, A, a, B, b, dZ_shards, n: int):
+    """Backward of mlp_forward_sp: dZ is all-gathered, the weight and bias gradients are those
+    of mlp_backward, and dX is reduce-scattered into token shards."""
+    X = all_gather_tokens(X_shards)
+    dZ = all_gather_tokens(dZ_shards)
+    g = mlp_backward(X, A, a, B, b, dZ, n)
+    g["dX"] = split_tokens(g["dX"], n)
+    return g
 
 
 # ----------------------------------------------------------------------------- attention projections

@@ -20,7 +20,8 @@ __all__ = [
     "tp_mlp_backward", "tp_linear_column_forward", "tp_linear_column_backward",
     "tp_linear_row_forward", "tp_linear_row_backward", "tp_selftest_wait_timeout",
     "new_workspace", "EXPORTED_SYMBOLS", "tp_trace_start", "tp_trace_stop", "TraceRecord",
-    "KERNEL_NAMES", "TAG_NAMES", "tp_linear_row_forward_noalloc",
+    "KERNEL_NAMES", "TAG_NAMES", "tp_linear_row_forward_noalloc", "tp_mlp_sp_workspace_size",
+    "tp_mlp_forward_sp", "tp_mlp_backward_sp",
 ]
 
 TP_F32, TP_BF16 = 0, 1
@@ -39,7 +40,8 @@ EXPORTED_SYMBOLS = (
     "tp_workspace_init", "tp_check_status", "tp_mlp_forward", "tp_mlp_backward",
     "tp_linear_column_forward", "tp_linear_column_backward", "tp_linear_row_forward",
     "tp_linear_row_backward", "tp_selftest_wait_timeout", "tp_trace_start", "tp_trace_stop",
-    "tp_linear_row_forward_noalloc",
+    "tp_linear_row_forward_noalloc", "tp_mlp_sp_workspace_size", "tp_mlp_forward_sp",
+    "tp_mlp_backward_sp",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -75,9 +77,10 @@ class TraceRecord(ctypes.Structure):
 
 
 KERNEL_NAMES = {1: "gemm_tc", 2: "gemm_ffma", 3: "shard_reduce", 4: "colsum", 5: "dact",
-                6: "selftest"}
+                6: "selftest", 7: "shard_copy"}
 TAG_NAMES = {1: "column_fwd", 2: "row_fwd", 3: "row_dgrad", 4: "row_wgrad", 5: "column_wgrad",
-             6: "column_dgrad", 7: "reduce", 8: "bias_grad", 9: "act_grad", 10: "other"}
+             6: "column_dgrad", 7: "reduce", 8: "bias_grad", 9: "act_grad", 10: "other",
+             11: "sp_gather", 12: "sp_scatter"}
 
 _P = ctypes.c_void_p
 _PP = ctypes.POINTER(ctypes.c_void_p)
@@ -103,6 +106,11 @@ _SIGS = {
                                               _PP, _P, _P, ctypes.c_size_t, _P]),
     "tp_selftest_wait_timeout": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_uint32, _P]),
     "tp_trace_start": (ctypes.c_int, [ctypes.c_int32]),
+    "tp_mlp_sp_workspace_size": (ctypes.c_int, [ctypes.POINTER(MlpDesc), ctypes.POINTER(ctypes.c_size_t)]),
+    "tp_mlp_forward_sp": (ctypes.c_int, [ctypes.POINTER(MlpDesc), _PP, _PP, _PP, _PP, _P, _PP,
+                                         _PP, _PP, _P, ctypes.c_size_t, _P]),
+    "tp_mlp_backward_sp": (ctypes.c_int, [ctypes.POINTER(MlpDesc), _PP, _PP, _PP, _PP, _PP, _PP,
+                                          _PP, _PP, _PP, _PP, _P, _P, ctypes.c_size_t, _P]),
     "tp_linear_row_forward_noalloc": (ctypes.c_int, [ctypes.POINTER(LinearDesc), _PP, _PP, _P,
                                                      _P, _P]),
     "tp_trace_stop": (ctypes.c_int, [ctypes.POINTER(TraceRecord), ctypes.c_int32,
@@ -253,6 +261,28 @@ def tp_linear_row_backward(desc, X, W, dZ, dX, dW, dbias, ws, stream=None):
 def tp_linear_row_forward_noalloc(desc, X, W, bias, Z, stream=None):
     _check(lib.tp_linear_row_forward_noalloc(ctypes.byref(_desc_lin(desc)), _arr(X), _arr(W),
                                              _ptr(bias), _ptr(Z), _stream(stream)))
+
+
+def tp_mlp_sp_workspace_size(desc) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib.tp_mlp_sp_workspace_size(ctypes.byref(_desc_mlp(desc)), ctypes.byref(out)))
+    return int(out.value)
+
+
+def tp_mlp_forward_sp(desc, X_shards, A, a, B, b, Z_shards, Hsave, Ysave, ws, stream=None):
+    p, n = _ws(ws)
+    _check(lib.tp_mlp_forward_sp(ctypes.byref(_desc_mlp(desc)), _arr(X_shards), _arr(A), _arr(a),
+                                 _arr(B), _ptr(b), _arr(Z_shards), _arr(Hsave), _arr(Ysave), p,
+                                 n, _stream(stream)))
+
+
+def tp_mlp_backward_sp(desc, X_shards, A, B, Hsave, Ysave, dZ_shards, dX_shards, dA, da, dB, db,
+                       ws, stream=None):
+    p, n = _ws(ws)
+    _check(lib.tp_mlp_backward_sp(ctypes.byref(_desc_mlp(desc)), _arr(X_shards), _arr(A),
+                                  _arr(B), _arr(Hsave), _arr(Ysave), _arr(dZ_shards),
+                                  _arr(dX_shards), _arr(dA), _arr(da), _arr(dB), _ptr(db), p, n,
+                                  _stream(stream)))
 
 
 def tp_trace_start(capacity: int):

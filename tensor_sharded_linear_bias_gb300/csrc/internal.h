@@ -62,6 +62,11 @@ cudaError_t launch_shard_reduce(const float* P, int n, int64_t T, int64_t N,
 cudaError_t launch_shard_reduce_bf16(const uint16_t* P, int n, int64_t T, int64_t N,
                                      const void* bias, float* Z, cudaStream_t st);
 
+// n equal, contiguous blocks of `bytes` each: gather (full[j*bytes..] <- shard[j]) or scatter
+// (shard[j] <- full[j*bytes..]), one launch for all blocks.
+cudaError_t launch_shard_copy(void* const* shards, void* full, int n, size_t bytes, int gather,
+                              cudaStream_t st);
+
 // Column sums: out_s[c] = sum_{r<rows} in_s[r*ld_s + c] for every segment s.
 struct ColsumSeg {
   const void* in;

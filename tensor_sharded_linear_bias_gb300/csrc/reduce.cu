@@ -132,6 +132,37 @@ __global__ void __launch_bounds__(kReduceThreads) shard_reduce_bf16_v8(
   }
 }
 
+// ------------------------------------------------------------------ token-shard copies
+struct ShardCopyParams {
+  void* shards[kMaxShards];
+  void* full;
+  long long bytes;   // per shard
+  int n;
+  int gather;
+};
+
+// Grid-stride copy over n blocks, 16 bytes per thread and step when every block allows it.
+__global__ void shard_copy_kernel(const __grid_constant__ ShardCopyParams p) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const bool vec = (p.bytes % 16 == 0) && (reinterpret_cast<uintptr_t>(p.full) % 16 == 0);
+  for (int j = 0; j < p.n; ++j) {
+    char* sh = static_cast<char*>(p.shards[j]);
+    char* fu = static_cast<char*>(p.full) + static_cast<long long>(j) * p.bytes;
+    char* dst = p.gather ? fu : sh;
+    const char* src = p.gather ? sh : fu;
+    if (vec && reinterpret_cast<uintptr_t>(sh) % 16 == 0) {
+      const long long n16 = p.bytes / 16;
+      for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+           i += stride)
+        reinterpret_cast<uint4*>(dst)[i] = reinterpret_cast<const uint4*>(src)[i];
+    } else {
+      for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+           i < p.bytes; i += stride)
+        dst[i] = src[i];
+    }
+  }
+}
+
 // ------------------------------------------------------------------ column sums
 // One block per (segment, strip of 256 columns), 16 warps. Lane l of warp w owns columns
 // [strip + 8l, strip + 8l + 8) and the rows r with r % 16 == w; it keeps eight of its rows'
@@ -320,6 +351,22 @@ cudaError_t launch_shard_reduce_bf16(const uint16_t* P, int n, int64_t T, int64_
                                                static_cast<long long>(device_sm_count()) * 8);
   shard_reduce_bf16_v8<<<static_cast<unsigned>(blocks), kReduceThreads, 0, st>>>(
       reinterpret_cast<const uint4*>(P), n, count8, N / 8, bias, reinterpret_cast<float4*>(Z));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shard_copy(void* const* shards, void* full, int n, size_t bytes, int gather,
+                              cudaStream_t st) {
+  if (n < 1 || n > kMaxShards) return cudaErrorInvalidValue;
+  if (bytes == 0) return cudaSuccess;
+  ShardCopyParams p{};
+  for (int j = 0; j < n; ++j) p.shards[j] = shards[j];
+  p.full = full;
+  p.bytes = static_cast<long long>(bytes);
+  p.n = n;
+  p.gather = gather;
+  const long long blocks = std::min<long long>((static_cast<long long>(bytes) / 16 + 255) / 256 + 1,
+                                               static_cast<long long>(device_sm_count()) * 8);
+  shard_copy_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 

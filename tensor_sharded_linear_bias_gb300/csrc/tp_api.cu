@@ -726,6 +726,112 @@ tp_status tp_mlp_backward(const tp_mlp_desc* desc, const void* X, const void* co
   return ok();
 }
 
+}  // extern "C"
+
+// ------------------------------------------------------------------ sequence-parallel MLP
+namespace {
+
+struct SpLayout {
+  size_t base, xg, zf, dzg, dxf, total;
+};
+
+tp_status sp_layout(const tp_mlp_desc* d, SpLayout* L, MlpSizes* z) {
+  TP_TRY(mlp_validate(d, z));
+  if (z->T % z->n != 0)
+    return fail(TP_ERR_INDIVISIBLE, "tokens %lld are not divisible by tp_degree %d",
+                static_cast<long long>(z->T), z->n);
+  const size_t e = elem_size(d->dtype);
+  const size_t th = size_t(z->T) * size_t(z->H);
+  L->base = align256(z->total);
+  L->xg = L->base;
+  L->zf = L->xg + align256(th * e);
+  L->dzg = L->zf + align256(th * 4);
+  L->dxf = L->dzg + align256(th * e);
+  L->total = L->dxf + align256(th * 4);
+  return TP_OK;
+}
+
+cudaError_t copy_traced(void* const* shards, void* full, int n, size_t bytes, int gather,
+                        cudaStream_t st) {
+  return traced(TP_K_SHARD_COPY, gather ? TP_TAG_SP_GATHER : TP_TAG_SP_SCATTER, n, 0.0,
+                2.0 * double(bytes) * n, st,
+                [&] { return launch_shard_copy(shards, full, n, bytes, gather, st); });
+}
+
+}  // namespace
+
+extern "C" {
+
+tp_status tp_mlp_sp_workspace_size(const tp_mlp_desc* desc, size_t* bytes) {
+  if (bytes == nullptr) return fail(TP_ERR_NULL, "bytes is NULL");
+  SpLayout L{};
+  MlpSizes z{};
+  TP_TRY(sp_layout(desc, &L, &z));
+  *bytes = L.total;
+  return ok();
+}
+
+tp_status tp_mlp_forward_sp(const tp_mlp_desc* desc, const void* const* X_shards,
+                            const void* const* A, const void* const* a, const void* const* B,
+                            const void* b, void* const* Z_shards, void* const* Hsave,
+                            void* const* Ysave, void* ws, size_t ws_bytes, void* stream) {
+  SpLayout L{};
+  MlpSizes z{};
+  TP_TRY(sp_layout(desc, &L, &z));
+  const int dt = desc->dtype;
+  TP_TRY(check_ptr_array(dt, "X_shards", X_shards, z.n, z.T > 0, z.T > 0));
+  TP_TRY(check_ptr_array(dt, "Z_shards", reinterpret_cast<const void* const*>(Z_shards), z.n,
+                         z.T > 0, z.T > 0));
+  TP_TRY(check_ws(ws, ws_bytes, L.total));
+  TP_TRY(check_arch());
+  if (z.T == 0) return ok();
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t e = elem_size(dt);
+  const size_t rows = size_t(z.T / z.n);
+  void* xg = ws_at<char>(ws, L.xg);
+  void* zf = ws_at<char>(ws, L.zf);
+  TP_CUDA(copy_traced(const_cast<void* const*>(X_shards), xg, z.n, rows * z.H * e, 1, st),
+          "all-gather of the token shards");
+  TP_TRY(tp_mlp_forward(desc, xg, A, a, B, b, zf, Hsave, Ysave, ws, L.base, stream));
+  TP_CUDA(copy_traced(Z_shards, zf, z.n, rows * z.H * 4, 0, st), "scatter of Z");
+  return ok();
+}
+
+tp_status tp_mlp_backward_sp(const tp_mlp_desc* desc, const void* const* X_shards,
+                             const void* const* A, const void* const* B,
+                             const void* const* Hsave, const void* const* Ysave,
+                             const void* const* dZ_shards, void* const* dX_shards,
+                             void* const* dA, void* const* da, void* const* dB, void* db,
+                             void* ws, size_t ws_bytes, void* stream) {
+  SpLayout L{};
+  MlpSizes z{};
+  TP_TRY(sp_layout(desc, &L, &z));
+  const int dt = desc->dtype;
+  TP_TRY(check_ptr_array(dt, "X_shards", X_shards, z.n, z.T > 0, z.T > 0));
+  TP_TRY(check_ptr_array(dt, "dZ_shards", dZ_shards, z.n, z.T > 0, z.T > 0));
+  TP_TRY(check_ptr_array(dt, "dX_shards", reinterpret_cast<const void* const*>(dX_shards), z.n,
+                         z.T > 0, z.T > 0));
+  TP_TRY(check_ws(ws, ws_bytes, L.total));
+  TP_TRY(check_arch());
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t e = elem_size(dt);
+  const size_t rows = size_t(z.T / z.n);
+  void* xg = ws_at<char>(ws, L.xg);
+  void* dzg = ws_at<char>(ws, L.dzg);
+  void* dxf = ws_at<char>(ws, L.dxf);
+  if (z.T > 0) {
+    TP_CUDA(copy_traced(const_cast<void* const*>(X_shards), xg, z.n, rows * z.H * e, 1, st),
+            "all-gather of the token shards");
+    TP_CUDA(copy_traced(const_cast<void* const*>(dZ_shards), dzg, z.n, rows * z.H * e, 1, st),
+            "all-gather of dZ");
+  }
+  TP_TRY(tp_mlp_backward(desc, xg, A, B, Hsave, Ysave, dzg, dxf, dA, da, dB, db, ws, L.base,
+                         stream));
+  if (z.T > 0)
+    TP_CUDA(copy_traced(dX_shards, dxf, z.n, rows * z.H * 4, 0, st), "scatter of dX");
+  return ok();
+}
+
 // ------------------------------------------------------------------ column-parallel linear
 tp_status tp_linear_column_forward(const tp_linear_desc* desc, const void* X,
                                    const void* const* W, const void* const* bias,

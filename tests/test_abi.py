@@ -101,6 +101,14 @@ def test_mlp_desc_validation(tp, kw, expected):
     assert status_of(lambda: tp.tp_mlp_workspace_size(mlp(tp, **kw))) == expected
 
 
+def test_sequence_parallel_workspace(tp):
+    d = mlp(tp)   # T=64, H=128, F=512, n=4, bf16
+    base = tp.tp_mlp_workspace_size(d)
+    base += (-base) % 256
+    assert tp.tp_mlp_sp_workspace_size(d) == base + 2 * (64 * 128 * 2) + 2 * (64 * 128 * 4)
+    assert status_of(lambda: tp.tp_mlp_sp_workspace_size(mlp(tp, tokens=66))) == "TP_ERR_INDIVISIBLE"
+
+
 def test_fp32_has_no_width_rule(tp):
     assert tp.tp_mlp_workspace_size(mlp(tp, hidden=130, ffn=4 * 131, dtype=tp.TP_F32)) > 0
 

@@ -163,6 +163,54 @@ def test_bf16_partials_error_vs_bytes(tp):
     assert errs[3][0] <= errs[1][0] + 8 * 2.0 ** -8, errs
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("T,H,F,n", [(300, 136, 4 * 88, 4), (4096, 1024, 4096, 2)])
+def test_sequence_parallel_mlp(tp, dtype, T, H, F, n):
+    """Token-sharded X and dZ in, token-sharded Z and dX out (all-gather before the column
+    GEMM, reduce-scatter after the row GEMM), against the oracle's sequence-parallel MLP."""
+    import torch
+
+    base = wl.P3_FP32_FWD if dtype == "f32" else SMALL
+    w = base.with_shape(tokens=T, hidden=H, ffn=F, tp_degree=n)
+    w = wl.dataclasses.replace(w, sigma={**w.sigma, "A": 0.02, "B": 0.02, "a": 0.01, "b": 0.01})
+    t, f = prepare(wl.mlp_tensors(w), w.dtype, "cuda")
+    cdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    code = tp.TP_BF16 if dtype == "bf16" else tp.TP_F32
+    Fs, Ts = F // n, T // n
+    A = [t["A"][:, i * Fs:(i + 1) * Fs].contiguous() for i in range(n)]
+    a = [t["a"][i * Fs:(i + 1) * Fs].contiguous() for i in range(n)]
+    B = [t["B"][i * Fs:(i + 1) * Fs, :].contiguous() for i in range(n)]
+    Xs = [t["X"][j * Ts:(j + 1) * Ts].contiguous() for j in range(n)]
+    dZs = [t["dZ"][j * Ts:(j + 1) * Ts].contiguous() for j in range(n)]
+    desc = tp.MlpDesc(tokens=T, hidden=H, ffn=F, tp_degree=n, dtype=code,
+                      act=tp.TP_ACT_GELU_ERF, reduce=tp.TP_REDUCE_AUTO)
+    ws = tp.new_workspace(tp.tp_mlp_sp_workspace_size(desc))
+    f32 = dict(dtype=torch.float32, device="cuda")
+    Zs = [torch.full((Ts, H), float("nan"), **f32) for _ in range(n)]
+    Hs = [torch.empty(T, Fs, dtype=cdt, device="cuda") for _ in range(n)]
+    Ys = [torch.empty(T, Fs, dtype=cdt, device="cuda") for _ in range(n)]
+    tp.tp_mlp_forward_sp(desc, Xs, A, a, B, t["b"], Zs, Hs, Ys, ws)
+    dXs = [torch.full((Ts, H), float("nan"), **f32) for _ in range(n)]
+    dA = [torch.empty(H, Fs, **f32) for _ in range(n)]
+    dB = [torch.empty(Fs, H, **f32) for _ in range(n)]
+    da = [torch.empty(Fs, **f32) for _ in range(n)]
+    db = torch.empty(H, **f32)
+    tp.tp_mlp_backward_sp(desc, Xs, A, B, Hs, Ys, dZs, dXs, dA, da, dB, db, ws)
+    tp.tp_check_status(ws)
+    torch.cuda.synchronize()
+    xs = [f["X"][j * Ts:(j + 1) * Ts] for j in range(n)]
+    dzs = [f["dZ"][j * Ts:(j + 1) * Ts] for j in range(n)]
+    rf = oracle.mlp_forward_sp(xs, f["A"], f["a"], f["B"], f["b"], n)
+    rb = oracle.mlp_backward_sp(xs, f["A"], f["a"], f["B"], f["b"], dzs, n)
+    tol = TOL_BF16 if dtype == "bf16" else TOL_F32
+    errs = {"Z": rel_shards([np64(z) for z in Zs], rf["Z"]),
+            "dX": rel_shards([np64(x) for x in dXs], rb["dX"]),
+            "dA": rel_shards([np64(x) for x in dA], rb["dA"]),
+            "dB": rel_shards([np64(x) for x in dB], rb["dB"]),
+            "da": rel_shards([np64(x) for x in da], rb["da"]), "db": rel(np64(db), rb["db"])}
+    assert max(errs.values()) <= tol, errs
+
+
 def test_deterministic(tp):
     w = SMALL.with_shape(tokens=257, hidden=128, ffn=2 * 384, tp_degree=2)
     for reduce in (0, 1):

@@ -315,6 +315,31 @@ def test_column_sampling_equals_full_columns():
     assert rel(s["H"], O.concat_columns(f["H"])[:, cols]) < 1e-14
 
 
+# ----------------------------------------------------------------------------- sequence parallel
+@pytest.mark.parametrize("n", [1, 2, 4])
+def test_sequence_parallel_against_torch_autograd(n):
+    """Token-sharded in, token-sharded out: the shards are exactly the rows of the unsharded
+    layer's outputs and input gradient, and the parameter gradients are the unsharded ones."""
+    T, H, F = 8, 12, 16
+    X, A, a = rand(300, T, H), rand(301, H, F, scale=0.3), rand(302, F, scale=0.1)
+    B, b, dZ = rand(303, F, H, scale=0.3), rand(304, H, scale=0.1), rand(305, T, H)
+    ref = _torch_reference(X, A, a, B, b, dZ)
+    xs = [X[j * T // n:(j + 1) * T // n] for j in range(n)]
+    dzs = [dZ[j * T // n:(j + 1) * T // n] for j in range(n)]
+    f = O.mlp_forward_sp(xs, A, a, B, b, n)
+    g = O.mlp_backward_sp(xs, A, a, B, b, dzs, n)
+    assert len(f["Z"]) == n and all(z.shape == (T // n, H) for z in f["Z"])
+    for j in range(n):
+        rows = slice(j * T // n, (j + 1) * T // n)
+        assert rel(f["Z"][j], ref["Z"][rows]) < 1e-12
+        assert rel(g["dX"][j], ref["dX"][rows]) < 1e-12
+    assert rel(O.concat_columns(g["dA"]), ref["dA"]) < 1e-12
+    assert rel(np.concatenate(g["dB"], axis=0), ref["dB"]) < 1e-12
+    assert rel(g["db"], ref["db"]) < 1e-12
+    with pytest.raises(ValueError):
+        O.split_tokens(np.zeros((6, 2)), 4)
+
+
 # ----------------------------------------------------------------------------- attention projections
 def test_attention_projections_against_torch():
     torch = pytest.importorskip("torch")
