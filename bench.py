@@ -45,7 +45,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="gpt3")
-    ap.add_argument("--reduce", choices=["fused", "partials", "auto", "partials_bf16"],
+    ap.add_argument("--reduce", choices=["fused", "partials", "auto", "partials_bf16", "overlap"],
                     default="auto")
     ap.add_argument("--sp", action="store_true",
                     help="sequence-parallel step: token-sharded X, dZ in and Z, dX out")
@@ -508,7 +508,8 @@ def main():
     import tensor_sharded_linear_bias_gb300 as tp
 
     reduce = {"fused": tp.TP_REDUCE_FUSED, "partials": tp.TP_REDUCE_PARTIALS,
-              "auto": tp.TP_REDUCE_AUTO, "partials_bf16": tp.TP_REDUCE_PARTIALS_BF16}[args.reduce]
+              "auto": tp.TP_REDUCE_AUTO, "partials_bf16": tp.TP_REDUCE_PARTIALS_BF16,
+              "overlap": tp.TP_REDUCE_OVERLAP}[args.reduce]
     keep_host = (rank == 0 and world == 1 and not args.no_cpu_baseline)
     mb = MlpBench(w, reduce, device, keep_host, sp=args.sp)
     if args.sp:

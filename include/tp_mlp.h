@@ -68,12 +68,19 @@ typedef enum tp_act { TP_ACT_NONE = 0, TP_ACT_GELU_ERF = 1 } tp_act;
  *            Workspace is sized as for PARTIALS.
  *  PARTIALS_BF16: one bf16 partial per shard (half the bytes of PARTIALS), summed in fp32 by
  *            the reduction kernel -- the reduced-precision "communication" of "Tensor
- *            Parallelism: principle and practice", section 5.2. bf16 only. */
+ *            Parallelism: principle and practice", section 5.2. bf16 only.
+ *  OVERLAP:  as AUTO, but with S > 1 the partials are summed inside the GEMM launch, while
+ *            other tiles still compute: the epilogue warp that writes the last partial of a
+ *            (32-row, 256-column) block adds the S partials in order, plus the bias, into the
+ *            output (the single-GPU counterpart of overlapping the All-Reduce with compute,
+ *            "Tensor Parallelism: principle and practice", section 5.2). bf16 only; the
+ *            workspace adds one counter per block. */
 typedef enum tp_reduce {
   TP_REDUCE_FUSED = 0,
   TP_REDUCE_PARTIALS = 1,
   TP_REDUCE_AUTO = 2,
-  TP_REDUCE_PARTIALS_BF16 = 3
+  TP_REDUCE_PARTIALS_BF16 = 3,
+  TP_REDUCE_OVERLAP = 4
 } tp_reduce;
 
 typedef enum tp_status {

@@ -14,7 +14,8 @@ from typing import Optional, Sequence
 
 __all__ = [
     "TP_F32", "TP_BF16", "TP_ACT_NONE", "TP_ACT_GELU_ERF", "TP_REDUCE_FUSED",
-    "TP_REDUCE_PARTIALS", "TP_REDUCE_AUTO", "TP_REDUCE_PARTIALS_BF16", "TP_COLUMN", "TP_ROW", "TpError", "MlpDesc", "LinearDesc", "lib",
+    "TP_REDUCE_PARTIALS", "TP_REDUCE_AUTO", "TP_REDUCE_PARTIALS_BF16", "TP_REDUCE_OVERLAP",
+    "TP_COLUMN", "TP_ROW", "TpError", "MlpDesc", "LinearDesc", "lib",
     "library_path", "tp_version", "tp_last_error", "tp_mlp_workspace_size",
     "tp_linear_workspace_size", "tp_workspace_init", "tp_check_status", "tp_mlp_forward",
     "tp_mlp_backward", "tp_linear_column_forward", "tp_linear_column_backward",
@@ -26,7 +27,7 @@ __all__ = [
 
 TP_F32, TP_BF16 = 0, 1
 TP_ACT_NONE, TP_ACT_GELU_ERF = 0, 1
-TP_REDUCE_FUSED, TP_REDUCE_PARTIALS, TP_REDUCE_AUTO, TP_REDUCE_PARTIALS_BF16 = 0, 1, 2, 3
+TP_REDUCE_FUSED, TP_REDUCE_PARTIALS, TP_REDUCE_AUTO, TP_REDUCE_PARTIALS_BF16, TP_REDUCE_OVERLAP = 0, 1, 2, 3, 4
 TP_COLUMN, TP_ROW = 0, 1
 
 STATUS_NAMES = {

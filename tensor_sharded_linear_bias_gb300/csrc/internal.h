@@ -23,6 +23,8 @@ enum EpiKind : int {
   EPI_BIAS_ACT = 1,       // H = acc + bias[n] -> D (optional), Y = act(H) -> D2  (bf16 / fp32)
   EPI_DACT = 2,           // D = acc * act'(aux[m,n])                               (bf16 / fp32)
   EPI_STORE_BF16 = 3,     // D (bf16) = acc (+ bias[n])                   (tensor-core GEMM only)
+  EPI_PARTIAL_REDUCE = 4, // D[og] (fp32 partial og); the last writer of each block sums the
+                          // partials into Z (+ zbias)                   (tensor-core GEMM only)
 };
 
 // One launch of a (grouped) GEMM: D_g[M,N] = A_g[M,K] * B_g[K,N] for every group g, or,
@@ -46,6 +48,10 @@ struct GemmSpec {
   int epi = EPI_STORE_F32;
   int act = TP_ACT_NONE;
   int raster = 0;   // tensor-core GEMM tile order: 0 = m fastest, 1 = n fastest
+  int* counters = nullptr;   // EPI_PARTIAL_REDUCE: one int per (32-row, 256-column) block, zero
+  float* Z = nullptr;
+  int64_t ldz = 0;
+  const void* zbias = nullptr;
   int* status = nullptr;
 };
 

@@ -282,6 +282,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_c
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+      if (p.epi == EPI_PARTIAL_REDUCE) tc::partial_reduce_rows(p, row0, nb);
       if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1u; }
     }
   }

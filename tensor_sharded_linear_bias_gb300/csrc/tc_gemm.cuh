@@ -62,8 +62,16 @@ struct __align__(128) TcParams {
   int groups;
   int kpo;          // groups summed into each output (1: one output per group)
   int tiles_m, tiles_n, num_tiles;
+  int tiles_n_out;  // 256-column blocks of one output (for the partial-sum counters)
   int epi, act;
   int raster;       // tile order inside an output: 0 = m fastest, 1 = n fastest
+  // EPI_PARTIAL_REDUCE: D[og] are the nsplit fp32 partials; the warp completing a
+  // (32-row, 256-column) block's count sums them (+ zbias, bf16) into Z.
+  int* counters;
+  float* Z;
+  long long ldz;
+  const void* zbias;
+  int nsplit;
   int* status;
 };
 
@@ -258,12 +266,70 @@ __device__ __forceinline__ void add_bias_bf16x32(const uint16_t* bias, int valid
   }
 }
 
+__device__ __forceinline__ float4 ld_cg_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
+// The shard sum overlapped with the GEMM (EPI_PARTIAL_REDUCE), warp-wide, after the warp has
+// stored its 32 rows x 256 columns of partial og: the warp makes its stores visible and counts
+// itself in for the block; the warp that completes the count (one per block, whichever
+// partial it computed) reads the nsplit partials of the block in partial order, adds the bias
+// and writes Z, then resets the counter for the next launch. No warp waits for another.
+__device__ __forceinline__ void partial_reduce_rows(const TcParams& p, int row0, int nb) {
+  const int lane = threadIdx.x & 31;
+  if (row0 >= p.M) return;  // no rows of this block exist (edge tile): nothing was stored
+  __threadfence();
+  __syncwarp();
+  const int block = (row0 >> 5) * p.tiles_n_out + nb;
+  int last = 0;
+  if (lane == 0) last = atomicAdd(p.counters + block, 1) == p.nsplit - 1;
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  __threadfence();
+  const int col = nb * 256 + lane * 8;  // N % 8 == 0: a lane's 8 columns are all in or all out
+  if (col < p.N) {
+    float b[8] = {};
+    if (p.zbias != nullptr) {
+      const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.zbias) + col);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = unpack_bf16x2(w[j]);
+        b[2 * j] = f.x;
+        b[2 * j + 1] = f.y;
+      }
+    }
+    for (int r = 0; r < 32 && row0 + r < p.M; ++r) {
+      const long long row = row0 + r;
+      float acc[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+      for (int sp = 0; sp < p.nsplit; ++sp) {
+        const float* src = static_cast<const float*>(p.D[sp]) + row * p.ldd + col;
+        const float4 x0 = ld_cg_f4(src), x1 = ld_cg_f4(src + 4);
+        acc[0] += x0.x; acc[1] += x0.y; acc[2] += x0.z; acc[3] += x0.w;
+        acc[4] += x1.x; acc[5] += x1.y; acc[6] += x1.z; acc[7] += x1.w;
+      }
+      float* dst = p.Z + row * p.ldz + col;
+      reinterpret_cast<float4*>(dst)[0] = make_float4(acc[0] + b[0], acc[1] + b[1], acc[2] + b[2], acc[3] + b[3]);
+      reinterpret_cast<float4*>(dst)[1] = make_float4(acc[4] + b[4], acc[5] + b[5], acc[6] + b[6], acc[7] + b[7]);
+    }
+  }
+  __syncwarp();
+  if (lane == 0) atomicExch(p.counters + block, 0);
+}
+
 // Warp-wide: all 32 lanes call this for the same (row0, col0).
 __device__ __forceinline__ void epilogue_chunk(const TcParams& p, int g, int row0, int col0,
                                                float* v, uint8_t* stage) {
   const int valid = min(32, p.N - col0);  // a multiple of 8 (N % 8 == 0)
   const int og = g;
-  if (p.epi == EPI_STORE_F32) {
+  if (p.epi == EPI_STORE_F32 || p.epi == EPI_PARTIAL_REDUCE) {
     if (p.bias[og] != nullptr) add_bias_bf16x32(static_cast<const uint16_t*>(p.bias[og]) + col0, valid, v);
     warp_store_f32(stage, v, static_cast<float*>(p.D[og]), p.ldd, row0, col0, p.M, valid);
   } else if (p.epi == EPI_STORE_BF16) {
@@ -464,6 +530,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (p.epi == EPI_PARTIAL_REDUCE) partial_reduce_rows(p, row0, nb);
       if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1u; }
     }
   }

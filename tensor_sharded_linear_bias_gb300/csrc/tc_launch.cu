@@ -173,6 +173,12 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
   p.tiles_m = static_cast<int>((s.M + tile_rows - 1) / tile_rows);
   p.tiles_n = static_cast<int>((s.N + BN - 1) / BN);
   p.num_tiles = (s.groups / kpo) * p.tiles_m * p.tiles_n;
+  p.tiles_n_out = p.tiles_n;
+  p.counters = s.counters;
+  p.Z = s.Z;
+  p.ldz = s.ldz;
+  p.zbias = s.zbias;
+  p.nsplit = s.groups / kpo;
   p.epi = s.epi;
   p.act = s.act;
   p.raster = choose_raster(p.tiles_m, p.tiles_n, s.K * p.kpo,

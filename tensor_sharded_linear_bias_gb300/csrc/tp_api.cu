@@ -51,11 +51,10 @@ tp_status check_common(int64_t tokens, int tp, int dtype, int act, int reduce) {
   if (dtype != TP_F32 && dtype != TP_BF16) return fail(TP_ERR_DTYPE, "unknown dtype %d", dtype);
   if (act != TP_ACT_NONE && act != TP_ACT_GELU_ERF)
     return fail(TP_ERR_DTYPE, "unknown activation %d", act);
-  if (reduce != TP_REDUCE_FUSED && reduce != TP_REDUCE_PARTIALS && reduce != TP_REDUCE_AUTO &&
-      reduce != TP_REDUCE_PARTIALS_BF16)
+  if (reduce < TP_REDUCE_FUSED || reduce > TP_REDUCE_OVERLAP)
     return fail(TP_ERR_DTYPE, "unknown reduce mode %d", reduce);
-  if (reduce == TP_REDUCE_PARTIALS_BF16 && dtype != TP_BF16)
-    return fail(TP_ERR_DTYPE, "bf16 partials need bf16 inputs");
+  if ((reduce == TP_REDUCE_PARTIALS_BF16 || reduce == TP_REDUCE_OVERLAP) && dtype != TP_BF16)
+    return fail(TP_ERR_DTYPE, "reduce mode %d needs bf16 inputs", reduce);
   if (tp < 1 || tp > kMaxShards)
     return fail(TP_ERR_SHAPE, "tp_degree %d outside 1..%d", tp, kMaxShards);
   if (tokens < 0 || tokens > kMaxDim) return fail(TP_ERR_SHAPE, "tokens %lld out of range",
@@ -248,6 +247,19 @@ cudaError_t zero_f32(void* p, int64_t count, cudaStream_t st) {
 // Bytes of one element of a shard partial.
 size_t partial_bytes(int reduce) { return reduce == TP_REDUCE_PARTIALS_BF16 ? 2 : 4; }
 
+// Counters of the overlapped reduction: one int per (32-row, 256-column) block of [M, N].
+size_t counter_bytes(int reduce, int64_t M, int64_t N) {
+  if (reduce != TP_REDUCE_OVERLAP) return 0;
+  return align256(size_t((M + 31) / 32) * size_t((N + 255) / 256) * 4);
+}
+
+// Scratch of one shard-summed product: n partials, then the counters.
+size_t partials_region(int reduce, int n, int64_t M, int64_t N) {
+  if (reduce == TP_REDUCE_FUSED) return 0;
+  return align256(size_t(n) * size_t(M) * size_t(N) * partial_bytes(reduce)) +
+         counter_bytes(reduce, M, N);
+}
+
 // ---------------------------------------------------------------- MLP sizes
 struct MlpSizes {
   int64_t T, H, F, Fs;
@@ -272,7 +284,7 @@ tp_status mlp_validate(const tp_mlp_desc* d, MlpSizes* z) {
   TP_TRY(check_width(d->dtype, "ffn / tp_degree", z->Fs));
   const size_t e = elem_size(d->dtype);
   z->partials_fwd =
-      d->reduce != TP_REDUCE_FUSED ? align256(size_t(z->n) * z->T * z->H * partial_bytes(d->reduce)) : 0;
+      partials_region(d->reduce, z->n, z->T, z->H);
   z->dH = align256(size_t(z->T) * z->F * e);
   z->partials_bwd = z->partials_fwd;
   z->total = kStatusBytes + std::max(z->partials_fwd, z->dH + z->partials_bwd);
@@ -309,7 +321,7 @@ tp_status lin_validate(const tp_linear_desc* d, int kind, LinSizes* z) {
     z->partials_fwd = 0;
     z->dH = d->act != TP_ACT_NONE ? align256(size_t(z->T) * z->N * e) : 0;
     z->partials_bwd =
-        d->reduce != TP_REDUCE_FUSED ? align256(size_t(z->n) * z->T * z->K * partial_bytes(d->reduce)) : 0;
+        partials_region(d->reduce, z->n, z->T, z->K);
   } else {
     if (d->act != TP_ACT_NONE) return fail(TP_ERR_DTYPE, "a row-parallel linear has no activation");
     if (d->gather != 0) return fail(TP_ERR_DTYPE, "gather applies to column-parallel linears only");
@@ -321,7 +333,7 @@ tp_status lin_validate(const tp_linear_desc* d, int kind, LinSizes* z) {
     TP_TRY(check_width(d->dtype, "in_features / tp_degree", z->Ks));
     TP_TRY(check_width(d->dtype, "out_features", z->N));
     z->partials_fwd =
-        d->reduce != TP_REDUCE_FUSED ? align256(size_t(z->n) * z->T * z->N * partial_bytes(d->reduce)) : 0;
+        partials_region(d->reduce, z->n, z->T, z->N);
     z->dH = 0;
     z->partials_bwd = 0;
   }
@@ -334,7 +346,27 @@ tp_status lin_validate(const tp_linear_desc* d, int kind, LinSizes* z) {
 int shard_split(int reduce, int dtype, int64_t M, int64_t N, int64_t K, int n) {
   if (reduce == TP_REDUCE_FUSED) return 1;
   if (reduce == TP_REDUCE_PARTIALS || reduce == TP_REDUCE_PARTIALS_BF16) return n;
-  return dtype == TP_BF16 ? plan_shard_split(M, N, K, n) : 1;
+  return dtype == TP_BF16 ? plan_shard_split(M, N, K, n) : 1;  // AUTO, OVERLAP
+}
+
+// The overlapped form of a split shard sum: S partials in the workspace, counters after the
+// n-partial region, Z written by the GEMM's own epilogue warps.
+tp_status overlapped_sum(GemmSpec& s, int dtype, int S, int n, int64_t M, int64_t N,
+                         const void* bias, float* Z, void* ws, size_t partials_off,
+                         cudaStream_t st, int tag, const char* what) {
+  float* P = ws_at<float>(ws, partials_off);
+  int* counters = ws_at<int>(ws, partials_off + align256(size_t(n) * M * N * 4));
+  TP_CUDA(cudaMemsetAsync(counters, 0, counter_bytes(TP_REDUCE_OVERLAP, M, N), st),
+          "clearing the partial-sum counters");
+  s.kpo = n / S;
+  s.epi = EPI_PARTIAL_REDUCE;
+  for (int i = 0; i < S; ++i) s.D[i] = P + size_t(i) * M * N;
+  s.counters = counters;
+  s.Z = Z;
+  s.ldz = N;
+  s.zbias = bias;
+  TP_CUDA(run_gemm(s, dtype, st, tag), what);
+  return TP_OK;
 }
 
 cudaError_t reduce_traced(const float* P, int n, int64_t T, int64_t N, const void* bias,
@@ -378,6 +410,9 @@ tp_status row_product(int dtype, int reduce, int n, int64_t T, int64_t Ks, int64
     s.D[0] = Z;
     s.bias[0] = bias;
     TP_CUDA(run_gemm(s, dtype, st, TP_TAG_ROW_FWD), what);
+  } else if (reduce == TP_REDUCE_OVERLAP) {
+    TP_TRY(overlapped_sum(s, dtype, S, n, T, N, bias, Z, ws, partials_off, st, TP_TAG_ROW_FWD,
+                          what));
   } else {
     s.kpo = n / S;
     if (reduce == TP_REDUCE_PARTIALS_BF16) {
@@ -421,6 +456,9 @@ tp_status input_grad_sum(int dtype, int reduce, int n, int64_t T, int64_t w, int
     s.ksum = 1;
     s.D[0] = dX;
     TP_CUDA(run_gemm(s, dtype, st, TP_TAG_COLUMN_DGRAD), "input-gradient GEMM");
+  } else if (reduce == TP_REDUCE_OVERLAP) {
+    TP_TRY(overlapped_sum(s, dtype, S, n, T, Kd, nullptr, dX, ws, partials_off, st,
+                          TP_TAG_COLUMN_DGRAD, "input-gradient GEMM"));
   } else {
     s.kpo = n / S;
     if (reduce == TP_REDUCE_PARTIALS_BF16) {

@@ -76,6 +76,9 @@ def test_workspace_sizes(tp):
     assert tp.tp_mlp_workspace_size(mlp(tp, reduce=tp.TP_REDUCE_AUTO)) == 256 + T * F * 2 + part
     assert tp.tp_mlp_workspace_size(mlp(tp, reduce=tp.TP_REDUCE_PARTIALS_BF16)) == \
         256 + T * F * 2 + part // 2
+    counters = 256   # (64 / 32) x (128 / 256 -> 1) ints, rounded up to 256 bytes
+    assert tp.tp_mlp_workspace_size(mlp(tp, reduce=tp.TP_REDUCE_OVERLAP)) == \
+        256 + T * F * 2 + part + counters
     col = tp.LinearDesc(tokens=32, in_features=768, out_features=3072, tp_degree=4,
                         dtype=tp.TP_F32, act=0, reduce=0, gather=1)
     assert tp.tp_linear_workspace_size(col, tp.TP_COLUMN) == 256
@@ -94,7 +97,8 @@ def test_workspace_sizes(tp):
     (dict(ffn=4 * 130), "TP_ERR_ALIGN"),         # ... including the shard width
     (dict(dtype=7), "TP_ERR_DTYPE"),
     (dict(act=3), "TP_ERR_DTYPE"),
-    (dict(reduce=4), "TP_ERR_DTYPE"),
+    (dict(reduce=5), "TP_ERR_DTYPE"),
+    (dict(reduce=4, dtype=0), "TP_ERR_DTYPE"),     # the overlapped sum needs bf16 inputs
     (dict(reduce=3, dtype=0), "TP_ERR_DTYPE"),     # bf16 partials need bf16 inputs
 ])
 def test_mlp_desc_validation(tp, kw, expected):

@@ -62,7 +62,7 @@ def test_wait_timeout_is_reported(tp):
     (1, 8, 16, 2),            # a single token, widths at the minimum
     (130, 72, 8 * 40, 8),     # 8 shards of 40 columns
 ])
-@pytest.mark.parametrize("reduce", [0, 1, 2, 3])
+@pytest.mark.parametrize("reduce", [0, 1, 2, 3, 4])
 def test_mlp_bf16_small(tp, T, H, F, n, reduce):
     w = SMALL.with_shape(tokens=T, hidden=H, ffn=F, tp_degree=n)
     case = MlpCase(w, reduce).run()
@@ -70,14 +70,20 @@ def test_mlp_bf16_small(tp, T, H, F, n, reduce):
     assert max(errs.values()) <= TOL_BF16, errs
 
 
+@pytest.mark.parametrize("reduce", [2, 4])
 @pytest.mark.parametrize("split", ["1", "2", "4", "8"])
-def test_shard_sum_in_groups(tp, monkeypatch, split):
-    """The shard sum split into `split` partial outputs (groups of 8 / split shards each)."""
+def test_shard_sum_in_groups(tp, monkeypatch, split, reduce):
+    """The shard sum split into `split` partial outputs (groups of 8 / split shards each),
+    reduced after the GEMM (AUTO) or inside it (OVERLAP); twice in a row, so the second launch
+    starts from counters the first one reset."""
     monkeypatch.setenv("TPMLP_SHARD_SPLIT", split)
     w = SMALL.with_shape(tokens=300, hidden=136, ffn=8 * 136, tp_degree=8)
-    case = MlpCase(w, tp.TP_REDUCE_AUTO).run()
-    errs = compare_full(case.outputs(), *full_reference(case))
+    case = MlpCase(w, reduce).run()
+    first = case.outputs()
+    errs = compare_full(first, *full_reference(case))
     assert max(errs.values()) <= TOL_BF16, errs
+    second = case.run().outputs()
+    assert np.array_equal(first["Z"], second["Z"]) and np.array_equal(first["dX"], second["dX"])
 
 
 @pytest.mark.parametrize("raster", ["0", "1"])
@@ -297,10 +303,10 @@ def test_column_linear(tp, dtype, gather, act):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("reduce", [0, 1, 2, 3])
+@pytest.mark.parametrize("reduce", [0, 1, 2, 3, 4])
 def test_row_linear(tp, dtype, reduce):
-    if reduce == 3 and dtype == "f32":
-        pytest.skip("bf16 partials need bf16 inputs")
+    if reduce in (3, 4) and dtype == "f32":
+        pytest.skip("this reduce mode needs bf16 inputs")
     import torch
 
     T, K, N, n = 190, 4 * 88, 264, 4
@@ -348,7 +354,7 @@ def test_workload_mlp_4096_1024_4096_tp2_full(tp):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("reduce", [0, 1, 2, 3])
+@pytest.mark.parametrize("reduce", [0, 1, 2, 3, 4])
 def test_workload_gpt3_mlp_slice_sampled(tp, reduce):
     """The bench's workload and launch configuration (reduce=2 is the AUTO mode it times)."""
     w = wl.GPT3_MLP_T2048_TP8
