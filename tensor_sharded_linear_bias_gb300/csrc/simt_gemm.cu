@@ -9,7 +9,8 @@
 namespace tpk {
 namespace {
 
-constexpr int TM = 64, TN = 64, TK = 16;
+constexpr int TM = 64, TN = 64, TK = 32;
+constexpr int LOADS = TM * TK / 256;  // elements of A (and of B) each thread stages per K step
 
 struct SimtParams {
   const float* A[kMaxShards];
@@ -24,9 +25,12 @@ struct SimtParams {
   int groups, ksum, epi, act;
 };
 
+// Two shared-memory buffers and a register prefetch: while the block multiplies the K step in
+// one buffer, the loads of the next step are in flight, so the K loop is not a chain of
+// load-latency-bound steps.
 __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ SimtParams p) {
-  __shared__ float As[TK][TM + 4];
-  __shared__ float Bs[TK][TN + 4];
+  __shared__ float As[2][TK][TM + 4];
+  __shared__ float Bs[2][TK][TN + 4];
   const int g = blockIdx.z;
   const long long m0 = static_cast<long long>(blockIdx.y) * TM;
   const long long n0 = static_cast<long long>(blockIdx.x) * TN;
@@ -34,37 +38,70 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ 
   float acc[4][4] = {};
 
   const int kgroups = p.ksum ? p.groups : 1;
-  for (int kg = 0; kg < kgroups; ++kg) {
+  const long long ksteps = (p.K + TK - 1) / TK;
+  const long long nsteps = ksteps * kgroups;
+  float ra[LOADS], rb[LOADS];
+
+  // element e of a step's A tile -> (mm, kk); coalesced along whichever of m, k is contiguous
+  auto a_coord = [&](int e, int& mm, int& kk) {
+    if (p.sak == 1) { kk = e % TK; mm = e / TK; } else { mm = e % TM; kk = e / TM; }
+  };
+  auto b_coord = [&](int e, int& nn, int& kk) {
+    if (p.sbk == 1) { kk = e % TK; nn = e / TK; } else { nn = e % TN; kk = e / TN; }
+  };
+  auto load = [&](long long step) {
+    const int kg = static_cast<int>(step / ksteps);
+    const long long k0 = (step % ksteps) * TK;
     const float* A = p.A[p.ksum ? kg : g];
     const float* B = p.B[p.ksum ? kg : g];
-    for (long long k0 = 0; k0 < p.K; k0 += TK) {
-      for (int i = threadIdx.x; i < TM * TK; i += 256) {
-        int mm, kk;
-        if (p.sak == 1) { kk = i % TK; mm = i / TK; } else { mm = i % TM; kk = i / TM; }
-        const long long m = m0 + mm, k = k0 + kk;
-        As[kk][mm] = (m < p.M && k < p.K) ? A[m * p.sam + k * p.sak] : 0.0f;
-      }
-      for (int i = threadIdx.x; i < TN * TK; i += 256) {
-        int nn, kk;
-        if (p.sbk == 1) { kk = i % TK; nn = i / TK; } else { nn = i % TN; kk = i / TN; }
-        const long long n = n0 + nn, k = k0 + kk;
-        Bs[kk][nn] = (n < p.N && k < p.K) ? B[k * p.sbk + n * p.sbn] : 0.0f;
-      }
-      __syncthreads();
 #pragma unroll
-      for (int kk = 0; kk < TK; ++kk) {
-        float a[4], b[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) a[r] = As[kk][ty + 16 * r];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) b[c] = Bs[kk][tx + 16 * c];
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
-      }
-      __syncthreads();
+    for (int j = 0; j < LOADS; ++j) {
+      const int e = threadIdx.x + 256 * j;
+      int mm, kk;
+      a_coord(e, mm, kk);
+      const long long m = m0 + mm, k = k0 + kk;
+      ra[j] = (m < p.M && k < p.K) ? A[m * p.sam + k * p.sak] : 0.0f;
+      int nn, kb;
+      b_coord(e, nn, kb);
+      const long long n = n0 + nn, k2 = k0 + kb;
+      rb[j] = (n < p.N && k2 < p.K) ? B[k2 * p.sbk + n * p.sbn] : 0.0f;
     }
+  };
+  auto stash = [&](int buf) {
+#pragma unroll
+    for (int j = 0; j < LOADS; ++j) {
+      const int e = threadIdx.x + 256 * j;
+      int mm, kk;
+      a_coord(e, mm, kk);
+      As[buf][kk][mm] = ra[j];
+      int nn, kb;
+      b_coord(e, nn, kb);
+      Bs[buf][kb][nn] = rb[j];
+    }
+  };
+
+  if (nsteps > 0) {
+    load(0);
+    stash(0);
+  }
+  __syncthreads();
+  for (long long step = 0; step < nsteps; ++step) {
+    const int buf = static_cast<int>(step & 1);
+    if (step + 1 < nsteps) load(step + 1);
+#pragma unroll
+    for (int kk = 0; kk < TK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) a[r] = As[buf][kk][ty + 16 * r];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) b[c] = Bs[buf][kk][tx + 16 * c];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
+    }
+    if (step + 1 < nsteps) stash(buf ^ 1);
+    __syncthreads();
   }
 
   const int og = p.ksum ? 0 : g;

@@ -87,6 +87,15 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                 int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                                uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -185,6 +194,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_c
           if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
           if (!A_MN) {
             tma_load_2d_pair(sa, &p.tmA[kg], kk, arow, fb);
+          } else if (p.a3d) {
+            tma_load_3d_pair(sa, &p.tmA[kg], 0, kk, arow / 64, fb);
           } else {
 #pragma unroll
             for (int j = 0; j < HALF / 64; ++j)
@@ -192,6 +203,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_c
           }
           if (!B_MN) {
             tma_load_2d_pair(sb, &p.tmB[kg], kk, bcol, fb);
+          } else if (p.b3d) {
+            tma_load_3d_pair(sb, &p.tmB[kg], 0, kk, bcol / 64, fb);
           } else {
 #pragma unroll
             for (int j = 0; j < HALF / 64; ++j)

@@ -65,6 +65,7 @@ struct __align__(128) TcParams {
   int tiles_n_out;  // 256-column blocks of one output (for the partial-sum counters)
   int epi, act;
   int raster;       // tile order inside an output: 0 = m fastest, 1 = n fastest
+  int a3d, b3d;     // MN-major operand mapped as [MN/64][K][64]: one TMA load per tile
   // EPI_PARTIAL_REDUCE: D[og] are the nsplit fp32 partials; the warp completing a
   // (32-row, 256-column) block's count sums them (+ zbias, bf16) into Z.
   int* counters;
@@ -89,6 +90,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// One load of `chunks` consecutive 64-wide MN chunks of an MN-major operand, through its 3-D
+// view [MN/64][K][64]: lands in shared memory exactly like `chunks` 2-D boxes of [64 K][64 MN].
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
 
@@ -430,6 +442,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
           if (!A_MN) {
             tma_load_2d(sa, &p.tmA[kg], kk, mb * BM, fb);
+          } else if (p.a3d) {
+            tma_load_3d(sa, &p.tmA[kg], 0, kk, mb * BM / 64, fb);
           } else {
 #pragma unroll
             for (int j = 0; j < BM / 64; ++j)
@@ -437,6 +451,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
           }
           if (!B_MN) {
             tma_load_2d(sb, &p.tmB[kg], kk, nb * BN, fb);
+          } else if (p.b3d) {
+            tma_load_3d(sb, &p.tmB[kg], 0, kk, nb * BN / 64, fb);
           } else {
 #pragma unroll
             for (int j = 0; j < BN / 64; ++j)

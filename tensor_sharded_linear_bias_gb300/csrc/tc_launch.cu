@@ -102,6 +102,29 @@ int choose_raster(int tiles_m, int tiles_n, int64_t k_total, int sms, bool pair)
   return (fm > half_l2 && fn < 0.75 * fm) ? 1 : 0;
 }
 
+// 3-D view of an MN-major bf16 operand [K][MN] (row pitch ld): dims {64, K, MN/64}, strides
+// {ld * 2, 128} bytes, box {64, 64, chunks}. One load then brings `chunks` 64-wide MN chunks
+// of 64 K rows, laid out in shared memory like `chunks` 2-D boxes. Only for MN % 64 == 0 (a
+// partial last chunk would read past the rows). Returns false if the driver refuses it.
+bool encode_bf16_mn3d(CUtensorMap* m, const void* ptr, uint64_t mn, uint64_t k, uint64_t ld,
+                      uint32_t chunks) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || mn % 64 != 0) return false;
+  const cuuint64_t dims[3] = {64, k, mn / 64};
+  const cuuint64_t strides[2] = {ld * 2, 128};
+  const cuuint32_t box[3] = {64, 64, chunks};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// One-load MN-major tiles (3-D maps); TPMLP_TMA_3D=0 keeps the 2-D boxes.
+bool mn3d_enabled() {
+  if (const char* env = std::getenv("TPMLP_TMA_3D")) return std::atoi(env) != 0;
+  return true;
+}
+
 }  // namespace
 
 int plan_shard_split(int64_t M, int64_t N, int64_t K_per_group, int n) {
@@ -148,11 +171,22 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
   std::memset(static_cast<void*>(&p), 0, sizeof(p));
   // K-major boxes: 128 rows of A; 256 rows of B (one SM) or 128 (each SM of a pair).
   const uint32_t b_rows = pair ? static_cast<uint32_t>(tc2::HALF) : static_cast<uint32_t>(BN);
+  // MN chunks per CTA tile: A 128 rows (one SM or each SM of a pair); B 256 or 128 columns.
+  const uint32_t a_chunks = 2;
+  const uint32_t b_chunks = pair ? 2 : 4;
+  p.a3d = s.a_mn && mn3d_enabled() && s.M % 64 == 0;
+  p.b3d = s.b_mn && mn3d_enabled() && s.N % 64 == 0;
+  for (int g = 0; g < s.groups && p.a3d; ++g)
+    p.a3d = encode_bf16_mn3d(&p.tmA[g], s.A[g], s.M, s.K, s.lda, a_chunks);
+  for (int g = 0; g < s.groups && p.b3d; ++g)
+    p.b3d = encode_bf16_mn3d(&p.tmB[g], s.B[g], s.N, s.K, s.ldb, b_chunks);
   for (int g = 0; g < s.groups; ++g) {
-    const bool okA = s.a_mn ? encode_bf16(&p.tmA[g], s.A[g], s.M, s.K, s.lda, 64, 64)
-                            : encode_bf16(&p.tmA[g], s.A[g], s.K, s.M, s.lda, 64, BM);
-    const bool okB = s.b_mn ? encode_bf16(&p.tmB[g], s.B[g], s.N, s.K, s.ldb, 64, 64)
-                            : encode_bf16(&p.tmB[g], s.B[g], s.K, s.N, s.ldb, 64, b_rows);
+    const bool okA = p.a3d ? true
+                     : s.a_mn ? encode_bf16(&p.tmA[g], s.A[g], s.M, s.K, s.lda, 64, 64)
+                              : encode_bf16(&p.tmA[g], s.A[g], s.K, s.M, s.lda, 64, BM);
+    const bool okB = p.b3d ? true
+                     : s.b_mn ? encode_bf16(&p.tmB[g], s.B[g], s.N, s.K, s.ldb, 64, 64)
+                              : encode_bf16(&p.tmB[g], s.B[g], s.K, s.N, s.ldb, 64, b_rows);
     if (!okA || !okB) return cudaErrorInvalidValue;
     p.D[g] = s.D[g];
     p.D2[g] = s.D2[g];

@@ -86,16 +86,21 @@ def test_shard_sum_in_groups(tp, monkeypatch, split, reduce):
     assert np.array_equal(first["Z"], second["Z"]) and np.array_equal(first["dX"], second["dX"])
 
 
+@pytest.mark.parametrize("tma3d", ["0", "1"])
 @pytest.mark.parametrize("raster", ["0", "1"])
 @pytest.mark.parametrize("pair", ["0", "1"])
 @pytest.mark.parametrize("T,H,F,n", [(96, 72, 2 * 136, 2), (300, 136, 2 * 296, 2),
-                                     (640, 264, 4 * 392, 4)])
-def test_gemm_kernel_variants(tp, monkeypatch, pair, raster, T, H, F, n):
+                                     (640, 264, 4 * 392, 4), (392, 192, 2 * 320, 2),
+                                     (520, 320, 4 * 448, 4)])
+def test_gemm_kernel_variants(tp, monkeypatch, pair, raster, tma3d, T, H, F, n):
     """Both tensor-core kernels on every GEMM of the MLP: one SM per 128 x 256 tile, and SM
     pairs (tcgen05 cta_group::2) per 256 x 256 tile, including pairs whose second half of
     the rows lies beyond M; in both tile orders (m fastest, n fastest)."""
     monkeypatch.setenv("TPMLP_GEMM_PAIR", pair)
     monkeypatch.setenv("TPMLP_RASTER", raster)
+    # MN-major operands whose MN size is a multiple of 64 (H = 192, 320; F/n = 320, 448) are
+    # loaded as one 3-D TMA box per tile, or as 64-wide 2-D boxes
+    monkeypatch.setenv("TPMLP_TMA_3D", tma3d)
     for reduce in (0, 2):
         case = MlpCase(SMALL.with_shape(tokens=T, hidden=H, ffn=F, tp_degree=n), reduce).run()
         errs = compare_full(case.outputs(), *full_reference(case))
