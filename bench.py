@@ -452,6 +452,90 @@ def run_reference(args, w, world, rank):
     return 0
 
 
+# ----------------------------------------------------------------------------- attention projections
+class AttnBench:
+    """The attention-projection workload: the fused QKV projection split by heads (column
+    parallel, no bias, no activation) and the output projection split by rows (row parallel),
+    forward and backward, through the linear entry points."""
+
+    def __init__(self, w: wl.AttnWorkload, reduce: int, device):
+        import torch
+
+        import tensor_sharded_linear_bias_gb300 as tp
+
+        self.tp, self.w = tp, w
+        n, T, Hm, hd, heads = w.tp_degree, w.tokens, w.hidden, w.head_dim, w.heads
+        hw = heads // n * hd
+        t = {k: wl.to_bf16(v)[0].to(device) for k, v in wl.attn_tensors(w).items()}
+        blk = lambda M, s: torch.cat([M[:, b * Hm + s * hw: b * Hm + (s + 1) * hw]  # noqa: E731
+                                      for b in range(3)], 1).contiguous()
+        self.X, self.dO = t["X"], t["dO"]
+        self.Wq = [blk(t["Wqkv"], s) for s in range(n)]
+        self.dQ = [blk(t["dQKV"], s) for s in range(n)]
+        self.Cs = [t["C"][:, s * hw:(s + 1) * hw].contiguous() for s in range(n)]
+        self.Wo = [t["Wo"][s * hw:(s + 1) * hw, :].contiguous() for s in range(n)]
+        self.col = tp.LinearDesc(tokens=T, in_features=Hm, out_features=3 * Hm, tp_degree=n,
+                                 dtype=tp.TP_BF16, act=0, reduce=reduce, gather=0)
+        self.row = tp.LinearDesc(tokens=T, in_features=Hm, out_features=Hm, tp_degree=n,
+                                 dtype=tp.TP_BF16, act=0, reduce=reduce, gather=0)
+        self.ws = tp.new_workspace(max(tp.tp_linear_workspace_size(self.col, tp.TP_COLUMN),
+                                       tp.tp_linear_workspace_size(self.row, tp.TP_ROW)), device)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.QKV = [torch.empty(T, 3 * hw, dtype=torch.bfloat16, device=device) for _ in range(n)]
+        self.O = torch.empty(T, Hm, **f32)
+        self.dX = torch.empty(T, Hm, **f32)
+        self.dWq = [torch.empty(Hm, 3 * hw, **f32) for _ in range(n)]
+        self.dC = [torch.empty(T, hw, **f32) for _ in range(n)]
+        self.dWo = [torch.empty(hw, Hm, **f32) for _ in range(n)]
+        self.flops = w.flops_fwd_bwd
+
+    def step(self):
+        tp = self.tp
+        tp.tp_linear_column_forward(self.col, self.X, self.Wq, None, self.QKV, None, self.ws)
+        tp.tp_linear_row_forward(self.row, self.Cs, self.Wo, None, self.O, self.ws)
+        tp.tp_linear_column_backward(self.col, self.X, self.Wq, None, self.dQ, self.dX, self.dWq,
+                                     None, self.ws)
+        tp.tp_linear_row_backward(self.row, self.Cs, self.Wo, self.dO, self.dC, self.dWo, None,
+                                  self.ws)
+
+
+def run_attention(args, world, rank, local):
+    import torch  # noqa: F401
+
+    import tensor_sharded_linear_bias_gb300 as tp
+
+    device = dist_init(world, local)
+    w = wl.ATTN_T4096_H5120_TP8
+    reduce = {"fused": tp.TP_REDUCE_FUSED, "partials": tp.TP_REDUCE_PARTIALS,
+              "auto": tp.TP_REDUCE_AUTO, "partials_bf16": tp.TP_REDUCE_PARTIALS_BF16,
+              "overlap": tp.TP_REDUCE_OVERLAP}[args.reduce]
+    ab = AttnBench(w, reduce, device)
+    for _ in range(args.warmup):
+        ab.step()
+    tp.tp_check_status(ab.ws)
+    sampler = ClockSampler(device.index or 0) if rank == 0 else None
+    tp.tp_trace_start(args.steps * 12 + 16)
+    ms = time_steps(ab.step, args.steps, world)
+    recs = tp.tp_trace_stop(args.steps * 12 + 16)
+    clocks = sampler.stop() if sampler else None
+    tp.tp_check_status(ab.ws)
+    ms, value = replica_throughput(ab.flops, args.steps, ms, world)
+    if rank == 0:
+        pk = peaks()
+        print(json.dumps({
+            "metric": "attention projections (QKV split by heads + output projection) fwd+bwd "
+                      "TFLOP/s (bf16)",
+            "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "tokens": w.tokens, "hidden": w.hidden,
+                       "heads": w.heads, "head_dim": w.head_dim, "tp_degree": w.tp_degree,
+                       "reduce": args.reduce},
+            "pct_of_peak": value / pk["bf16_sustained"] * 100.0, "clocks": clocks,
+            "gpu_launches": len(recs)}), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- pages' example
 def run_p3_column_latency(args, world, rank, local):
     """Latency of the pages' column-parallel example: X [32, 768] times W [768, 3072] split
@@ -495,6 +579,11 @@ def main():
     if args.workload == "p3col":
         world, rank, local = dist_setup(args.gpus)
         return run_p3_column_latency(args, world, rank, local)
+    if args.workload == "attn":
+        if args.impl != "native":
+            raise SystemExit("--impl reference times the MLP workloads only")
+        world, rank, local = dist_setup(args.gpus)
+        return run_attention(args, world, rank, local)
     w = workload(args.workload)
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
