@@ -35,6 +35,9 @@ METRIC = "TP-sharded MLP fwd+bwd TFLOP/s (bf16) on 1 GB300 and % of tensor-core 
 UNIT = "TFLOP/s"
 KERNEL_SOURCES = ["tc_gemm.cuh", "tc2_gemm.cuh", "tc_launch.cu", "tc_gemm_kmn.cu", "tc_gemm_kk.cu",
                   "tc_gemm_mnmn.cu", "device_common.cuh"]
+# fp32 FFMA peak: 152 SMs x 128 lanes x 2 flops per FFMA x 2.07 GHz (maximum SM clock).
+FFMA_F32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+TRACE_PER_STEP = 24  # trace slots per step (launches per step are at most 16)
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemm_tc_gpt3_mlp_T2048_tp8.md")
 
 
@@ -170,9 +173,9 @@ def peaks():
     if os.path.exists(path):
         p = json.load(open(path))
         return {"bf16_sustained": p["bf16_tflops_sustained"], "bf16_burst": p["bf16_tflops"],
-                "hbm_gbs": p["hbm_gbs"], "source": "measured"}
+                "hbm_gbs": p["hbm_gbs"], "source": "measured", "ffma_f32": FFMA_F32_TFLOPS}
     return {"bf16_sustained": 1700.0, "bf16_burst": 1900.0, "hbm_gbs": 6800.0,
-            "source": "fallback"}
+            "source": "fallback", "ffma_f32": FFMA_F32_TFLOPS}
 
 
 def kernel_source_hash() -> str:
@@ -342,6 +345,21 @@ class MlpBench:
         cur.wait_stream(h2d)
         cur.wait_stream(d2h)
 
+    def e2e_step(self):
+        """One step end to end, serially on the current stream: upload X (and dZ) from pinned
+        host memory, forward (and backward), download Z (and dX) to pinned host memory."""
+        tp = self.tp
+        self.X.copy_(self.X_pinned, non_blocking=True)
+        if self.backward:
+            self.dZ.copy_(self.dZ_pinned, non_blocking=True)
+        tp.tp_mlp_forward(self.desc, self.X, self.A, self.a, self.B, self.b, self.Z, self.Hs,
+                          self.Ys, self.ws)
+        self.Z_host.copy_(self.Z, non_blocking=True)
+        if self.backward:
+            tp.tp_mlp_backward(self.desc, self.X, self.A, self.B, self.Hs, self.Ys, self.dZ,
+                               self.dX, self.dA, self.da, self.dB, self.db, self.ws)
+            self.dX_host.copy_(self.dX, non_blocking=True)
+
     @property
     def flops(self) -> int:
         return self.w.flops_fwd_bwd if self.backward else self.w.flops_fwd
@@ -355,20 +373,124 @@ class MlpBench:
         return self.Z.numel() * 4 * (2 if self.backward else 1)
 
 
-def time_steps(fn, steps: int, world: int):
+L2_FLUSH_FACTOR = 4  # flush between steps unless a step reads this many L2 sizes of operands
+
+
+class L2Flush:
+    """Writes a buffer of twice the L2 size (a different value each time) before a timed step,
+    outside the step's events, so that a step whose operands would fit in L2 starts cold."""
+
+    def __init__(self, device):
+        import torch
+
+        props = torch.cuda.get_device_properties(device)
+        self.l2 = int(getattr(props, "L2_cache_size", 0) or (126 << 20))
+        self.buf = torch.empty(2 * self.l2 // 4, dtype=torch.float32, device=device)
+        self.k = 0
+
+    def __call__(self):
+        self.k += 1
+        self.buf.fill_(float(self.k))
+
+    def describe(self) -> str:
+        return (f"flushed: {self.buf.numel() * 4 / 1e6:.0f} MB written before every timed step, "
+                f"outside the step's events (L2 {self.l2 / 1e6:.0f} MB)")
+
+
+def make_flush(device, operand_bytes: int):
+    """An L2 flush when the step's operands are fewer than L2_FLUSH_FACTOR L2 sizes, else None."""
+    f = L2Flush(device)
+    if operand_bytes >= L2_FLUSH_FACTOR * f.l2:
+        return None, (f"no flush: {operand_bytes / 1e9:.2f} GB of operands per step vs "
+                      f"{f.l2 / 1e6:.0f} MB of L2")
+    return f, f.describe()
+
+
+def time_steps(fn, steps: int, world: int, flush=None):
+    """Device time of `steps` calls of fn (ms), barrier + synchronize on both sides. Without a
+    flush: one event pair around all steps. With one: flush, then an event pair around each
+    step; the sum of the steps' times."""
     import torch
 
     barrier(world)
     torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record()
-    for _ in range(steps):
+    if flush is None:
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record()
+        for _ in range(steps):
+            fn()
+        end.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        return start.elapsed_time(end)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evs:
+        flush()
+        a.record()
         fn()
-    end.record()
+        b.record()
     torch.cuda.synchronize()
     barrier(world)
-    return start.elapsed_time(end)
+    return sum(a.elapsed_time(b) for a, b in evs)
+
+
+def timed_then_traced(tp, fn, steps: int, world: int, flush, trace_capacity: int, sampler):
+    """Times `steps` steps with tracing off (the reported throughput), then the same number of
+    steps with the library's per-launch trace on (per-kernel times for the roofline).
+    Returns (ms of the untraced steps, trace records, clocks sampled during the untraced
+    steps)."""
+    ms = time_steps(fn, steps, world, flush)
+    clocks = sampler.stop() if sampler else None
+    tp.tp_trace_start(trace_capacity)
+    time_steps(fn, steps, world, flush)
+    recs = tp.tp_trace_stop(trace_capacity)
+    return ms, recs, clocks
+
+
+def roofline_from_trace(recs, pk, workload_name=None):
+    """The dominant kernel (largest total traced device time) against its roofline, and the
+    per-(kernel, tag) breakdown."""
+    by_kernel, by_tag = {}, {}
+    for r in recs:
+        k = by_kernel.setdefault(r["kernel"], {"ms": 0.0, "flops": 0.0, "bytes": 0.0, "n": 0})
+        k["ms"] += r["ms"]
+        k["flops"] += r["flops"]
+        k["bytes"] += r["bytes"]
+        k["n"] += 1
+        t = by_tag.setdefault(f'{r["kernel"]}:{r["tag"]}', {"ms": 0.0, "flops": 0.0, "n": 0})
+        t["ms"] += r["ms"]
+        t["flops"] += r["flops"]
+        t["n"] += 1
+    dom = max(by_kernel, key=lambda k: by_kernel[k]["ms"])
+    d = by_kernel[dom]
+    total_ms = sum(v["ms"] for v in by_kernel.values())
+    if dom in ("gemm_tc", "gemm_ffma"):
+        achieved = d["flops"] / (d["ms"] / 1e3) / 1e12
+        peak = pk["bf16_sustained"] if dom == "gemm_tc" else pk["ffma_f32"]
+        roof = {"bound": "tensor" if dom == "gemm_tc" else "alu", "kernel": dom,
+                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": (f"MEASURED_PEAKS.json bf16_tflops_sustained (of {pk['source']})"
+                                if dom == "gemm_tc" else
+                                "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz")}
+    else:
+        achieved = d["bytes"] / (d["ms"] / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                "peak_source": f"MEASURED_PEAKS.json hbm_gbs (of {pk['source']})"}
+    roof["launches"] = d["n"]
+    roof["avg_launch_ms"] = d["ms"] / d["n"]
+    roof["share_of_kernel_time"] = d["ms"] / total_ms
+    traffic = profiled_traffic(workload_name) if workload_name else None
+    roof["traffic"] = traffic
+    roof["traffic_note"] = ("dram__bytes_read.sum + dram__bytes_write.sum per launch from the "
+                            "committed ncu summary" if traffic is not None else
+                            "null: no ncu capture of the current kernel source for this workload")
+    kernels = {k: {"launches": v["n"], "avg_ms": v["ms"] / v["n"],
+                   "tflops": (v["flops"] / (v["ms"] / 1e3) / 1e12) if v["flops"] else None,
+                   "share": v["ms"] / total_ms} for k, v in sorted(by_tag.items())}
+    return roof, kernels
 
 
 # ----------------------------------------------------------------------------- the oracle
@@ -488,6 +610,7 @@ class AttnBench:
         self.dC = [torch.empty(T, hw, **f32) for _ in range(n)]
         self.dWo = [torch.empty(hw, Hm, **f32) for _ in range(n)]
         self.flops = w.flops_fwd_bwd
+        self.operand_bytes = 2 * (2 * T * Hm + 3 * Hm * Hm + T * 3 * Hm + T * Hm + Hm * Hm)
 
     def step(self):
         tp = self.tp
@@ -513,15 +636,15 @@ def run_attention(args, world, rank, local):
     for _ in range(args.warmup):
         ab.step()
     tp.tp_check_status(ab.ws)
+    flush, l2_note = make_flush(device, ab.operand_bytes)
     sampler = ClockSampler(device.index or 0) if rank == 0 else None
-    tp.tp_trace_start(args.steps * 12 + 16)
-    ms = time_steps(ab.step, args.steps, world)
-    recs = tp.tp_trace_stop(args.steps * 12 + 16)
-    clocks = sampler.stop() if sampler else None
+    ms, recs, clocks = timed_then_traced(tp, ab.step, args.steps, world, flush,
+                                         args.steps * TRACE_PER_STEP + 16, sampler)
     tp.tp_check_status(ab.ws)
     ms, value = replica_throughput(ab.flops, args.steps, ms, world)
     if rank == 0:
         pk = peaks()
+        roof, kernels = roofline_from_trace(recs, pk)
         print(json.dumps({
             "metric": "attention projections (QKV split by heads + output projection) fwd+bwd "
                       "TFLOP/s (bf16)",
@@ -530,9 +653,9 @@ def run_attention(args, world, rank, local):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "tokens": w.tokens, "hidden": w.hidden,
                        "heads": w.heads, "head_dim": w.head_dim, "tp_degree": w.tp_degree,
-                       "reduce": args.reduce},
+                       "reduce": args.reduce, "l2": l2_note},
             "pct_of_peak": value / pk["bf16_sustained"] * 100.0, "clocks": clocks,
-            "gpu_launches": len(recs)}), flush=True)
+            "gpu_launches": len(recs), "roofline": roof, "kernels": kernels}), flush=True)
     return 0
 
 
@@ -556,7 +679,7 @@ def run_p3_column_latency(args, world, rank, local):
         for _ in range(max(args.warmup, 10)):
             layer.forward(x)
         layer.check()
-        ms = time_steps(lambda: layer.forward(x), args.steps, world)
+        ms = time_steps(lambda: layer.forward(x), args.steps, world, L2Flush(device))
         ms = max_over_ranks(ms, world)
         res[name] = ms / args.steps * 1e3
     if rank == 0:
@@ -567,7 +690,8 @@ def run_p3_column_latency(args, world, rank, local):
             "warmup": args.warmup, "higher_is_better": False, "dtype": "f32",
             "data": "synthetic", "bf16_us": res["bf16"],
             "config": {"workload": "p3_column_linear_T32_K768_N3072_tp4_gather",
-                       "calls": "tp_linear_column_forward back to back, CUDA events"},
+                       "calls": "tp_linear_column_forward, one CUDA event pair per call, L2 "
+                                "flushed before each call outside its events"},
             "context": "the page expects ~1.5 ms on one GPU and ~1.2 ms with 4-GPU tensor "
                        "parallelism (hardware not stated)"}), flush=True)
     return 0
@@ -604,16 +728,14 @@ def main():
     if args.sp:
         args.no_e2e = True
 
-    # ---- device-resident throughput, with launch tracing over the timed region
+    # ---- device-resident throughput (untraced), then the same steps traced for the roofline
     for _ in range(args.warmup):
         mb.step()
     tp.tp_check_status(mb.ws)
+    flush, l2_note = make_flush(device, mb.operand_bytes)
     sampler = ClockSampler(device.index if device.index is not None else 0) if rank == 0 else None
-    launches_per_step = (7 if w.backward else 2) + (5 if args.sp else 0)
-    tp.tp_trace_start(args.steps * (launches_per_step + 2) + 16)
-    ms = time_steps(mb.step, args.steps, world)
-    recs = tp.tp_trace_stop(args.steps * (launches_per_step + 2) + 16)
-    clocks = sampler.stop() if sampler else None
+    ms, recs, clocks = timed_then_traced(tp, mb.step, args.steps, world, flush,
+                                         args.steps * TRACE_PER_STEP + 16, sampler)
     tp.tp_check_status(mb.ws)
     ms, value = replica_throughput(mb.flops, args.steps, ms, world)
     ms_per_step = ms / args.steps
@@ -621,58 +743,27 @@ def main():
     # ---- end to end: host inputs in, host results out, every step
     e2e = None
     if not args.no_e2e:
-        mb.run_e2e(args.warmup)
-        ms_e, value_e = replica_throughput(mb.flops, args.steps,
-                                           time_steps(lambda: mb.run_e2e(args.steps), 1, world),
-                                           world)
+        if flush is None:
+            mb.run_e2e(args.warmup)
+            ms_e = time_steps(lambda: mb.run_e2e(args.steps), 1, world)
+        else:
+            for _ in range(args.warmup):
+                mb.e2e_step()
+            ms_e = time_steps(mb.e2e_step, args.steps, world, flush)
+        ms_e, value_e = replica_throughput(mb.flops, args.steps, ms_e, world)
         e2e = {"value": value_e, "unit": UNIT,
                "ms_per_step": ms_e / args.steps, "h2d_bytes_per_step": mb.h2d_bytes,
-               "d2h_bytes_per_step": mb.d2h_bytes}
+               "d2h_bytes_per_step": mb.d2h_bytes,
+               "mode": ("two copy streams, neighbouring steps' copies overlap compute"
+                        if flush is None else "serial per step on one stream, L2 flushed "
+                        "before each step outside its events")}
         tp.tp_check_status(mb.ws)
 
     if rank != 0:
         return 0
 
-    # ---- roofline of the dominant kernel (largest total device time in the timed region)
     pk = peaks()
-    by_kernel, by_tag = {}, {}
-    for r in recs:
-        k = by_kernel.setdefault(r["kernel"], {"ms": 0.0, "flops": 0.0, "bytes": 0.0, "n": 0})
-        k["ms"] += r["ms"]
-        k["flops"] += r["flops"]
-        k["bytes"] += r["bytes"]
-        k["n"] += 1
-        t = by_tag.setdefault(f'{r["kernel"]}:{r["tag"]}', {"ms": 0.0, "flops": 0.0, "n": 0})
-        t["ms"] += r["ms"]
-        t["flops"] += r["flops"]
-        t["n"] += 1
-    dom = max(by_kernel, key=lambda k: by_kernel[k]["ms"])
-    d = by_kernel[dom]
-    total_ms = sum(v["ms"] for v in by_kernel.values())
-    if dom in ("gemm_tc", "gemm_ffma"):
-        achieved = d["flops"] / (d["ms"] / 1e3) / 1e12
-        peak = pk["bf16_sustained"] if dom == "gemm_tc" else None
-        roof = {"bound": "tensor" if dom == "gemm_tc" else "alu", "kernel": dom,
-                "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": (achieved / peak) if peak else None,
-                "peak_source": (f"MEASURED_PEAKS.json bf16_tflops_sustained (of {pk['source']})"
-                                if dom == "gemm_tc" else None)}
-    else:
-        achieved = d["bytes"] / (d["ms"] / 1e3) / 1e9
-        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": pk["hbm_gbs"],
-                "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
-                "peak_source": f"MEASURED_PEAKS.json hbm_gbs (of {pk['source']})"}
-    roof["launches"] = d["n"]
-    roof["avg_launch_ms"] = d["ms"] / d["n"]
-    roof["share_of_kernel_time"] = d["ms"] / total_ms
-    traffic = profiled_traffic(w.name)
-    roof["traffic"] = traffic
-    roof["traffic_note"] = ("dram__bytes_read.sum + dram__bytes_write.sum per launch from the "
-                            "committed ncu summary" if traffic is not None else
-                            "null: no ncu capture of the current kernel source for this workload")
-    kernels = {k: {"launches": v["n"], "avg_ms": v["ms"] / v["n"],
-                   "tflops": (v["flops"] / (v["ms"] / 1e3) / 1e12) if v["flops"] else None,
-                   "share": v["ms"] / total_ms} for k, v in sorted(by_tag.items())}
+    roof, kernels = roofline_from_trace(recs, pk, w.name)
 
     cpu = None
     if keep_host:
@@ -689,12 +780,14 @@ def main():
                    "pass": "fwd+bwd" if w.backward else "fwd",
                    "parallelism": "single GPU, all shards on it" if world == 1 else
                    f"{world} independent replicas (no exchange)",
-                   "l2": f"no flush: {mb.operand_bytes / 1e9:.2f} GB of operands per step vs "
-                         "126 MB of L2"},
+                   "l2": l2_note,
+                   "timing": "throughput from untraced steps; per-kernel figures from the "
+                             "same number of steps traced with per-launch events"},
         "pct_of_peak": value / pk["bf16_sustained"] * 100.0 if w.dtype == "bf16" else None,
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": len(recs),
+        "gpu_launches_per_step": len(recs) / args.steps,
         "roofline": roof,
         "kernels": kernels,
         "cpu_baseline": cpu,

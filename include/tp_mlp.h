@@ -39,7 +39,11 @@
  *    TP_F32: everything is fp32 and computed with fp32 FMA (no TF32); pointers 4-byte
  *    aligned, no other size rule.
  *  - The workspace (see the *_workspace_size calls) holds a device status word followed by
- *    scratch; call tp_workspace_init once after allocating it. A device-side wait that
+ *    scratch; call tp_workspace_init once after allocating it. TP_F32 calls reserve
+ *    TP_F32_SPLIT_SCRATCH_BYTES of it, right after the status block, for the K-slice
+ *    partial sums of their GEMMs: when a product has too few output tiles to fill the GPU
+ *    (few tokens), its K range is cut into slices computed in parallel and the slices are
+ *    added in slice order (deterministic) by a second kernel. A device-side wait that
  *    runs out writes an error code into the status word; tp_check_status reports it.
  *  - Requires an sm_103 device (GB300); on any other device calls return TP_ERR_ARCH.
  */
@@ -128,6 +132,9 @@ typedef struct tp_linear_desc {
 
 typedef enum tp_linear_kind { TP_COLUMN = 0, TP_ROW = 1 } tp_linear_kind;
 
+/* Workspace bytes that every TP_F32 call reserves after the 256-byte status block. */
+#define TP_F32_SPLIT_SCRATCH_BYTES ((size_t)320 * 64 * 64 * 4)
+
 /* Version of this ABI (major * 100 + minor). */
 int32_t tp_version(void);
 
@@ -135,8 +142,9 @@ int32_t tp_version(void);
 const char* tp_last_error(void);
 
 /* Bytes of workspace that tp_mlp_forward and tp_mlp_backward need for *desc (the larger of
- * the two): a 256-byte status block, plus n fp32 partials [T,H] in TP_REDUCE_PARTIALS
- * mode, or the backward's per-shard gradients dH_i [T,F/n] at the pre-activation. */
+ * the two): a 256-byte status block, TP_F32_SPLIT_SCRATCH_BYTES for TP_F32, plus n fp32
+ * partials [T,H] in TP_REDUCE_PARTIALS mode, or the backward's per-shard gradients
+ * dH_i [T,F/n] at the pre-activation. */
 tp_status tp_mlp_workspace_size(const tp_mlp_desc* desc, size_t* bytes);
 
 /* Bytes of workspace that the forward and backward of one column or row linear need. */
@@ -237,7 +245,8 @@ typedef enum tp_kernel_kind {
   TP_K_COLSUM = 4,         /* bias gradients: column sums over tokens */
   TP_K_DACT = 5,           /* dH = dY * act'(H) */
   TP_K_SELFTEST = 6,
-  TP_K_SHARD_COPY = 7      /* token-shard gather / scatter (sequence parallel) */
+  TP_K_SHARD_COPY = 7,     /* token-shard gather / scatter (sequence parallel) */
+  TP_K_SPLIT_SUM = 8       /* fp32: sum of a GEMM's K-slice partials + its epilogue */
 } tp_kernel_kind;
 
 typedef enum tp_trace_tag {

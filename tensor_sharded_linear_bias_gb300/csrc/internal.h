@@ -12,8 +12,11 @@ namespace tpk {
 
 constexpr int kMaxShards = 64;
 
-// Workspace layout: a 256-byte status block, then scratch (256-byte aligned).
+// Workspace layout: a 256-byte status block, then scratch (256-byte aligned). fp32 calls
+// reserve kSplitBytes right after the status block for the K-slice partials of the FFMA GEMM
+// (320 tiles of 64 x 64 fp32: the most a split plan ever uses).
 constexpr size_t kStatusBytes = 256;
+constexpr size_t kSplitBytes = TP_F32_SPLIT_SCRATCH_BYTES;
 
 // Device status codes written by kernels (first error wins).
 constexpr int kDevTimeoutBase = 0x100;  // | (role << 4) | wait site
@@ -53,12 +56,19 @@ struct GemmSpec {
   int64_t ldz = 0;
   const void* zbias = nullptr;
   int* status = nullptr;
+  int kslices = 1;         // FFMA GEMM: K steps split over this many CTAs per tile (1: none)
+  float* split = nullptr;  // ... their partial tiles, kslices x outputs x M x N fp32
 };
 
 // bf16 inputs, tcgen05 tensor cores (sm_103a). Returns cudaSuccess or the launch error.
 cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st);
-// fp32 inputs, FFMA (no TF32).
+// fp32 inputs, FFMA (no TF32). With kslices > 1 it writes raw partials to `split` and
+// launch_simt_split_sum finishes the product (sum in slice order + epilogue).
 cudaError_t launch_simt_gemm(const GemmSpec& s, cudaStream_t st);
+cudaError_t launch_simt_split_sum(const GemmSpec& s, cudaStream_t st);
+// K slices for an FFMA GEMM whose tiles alone would leave SMs idle (1: no split); the
+// partials must fit in scratch_bytes.
+int plan_simt_split(const GemmSpec& s, size_t scratch_bytes);
 
 // Z[T,N] = sum_{i<n} P[i][T,N] + bias (bias may be null; bias dtype: bf16 if bias_bf16).
 cudaError_t launch_shard_reduce(const float* P, int n, int64_t T, int64_t N,

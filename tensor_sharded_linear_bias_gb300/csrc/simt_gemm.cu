@@ -1,7 +1,15 @@
 // fp32 GEMM on the CUDA cores (FFMA): the fp32 path, where tensor-core TF32 would not keep
 // fp32 accuracy. Same grouping (per-shard outputs or a shard-summed output) and epilogues as
 // the tensor-core GEMM, with fp32 everywhere.
+//
+// Split K: when the output tiles alone cannot fill the GPU (few tokens, as in the pages'
+// batch-32 example), the K steps of every tile (over all summed shards) are cut into
+// `slices` contiguous ranges, one CTA each. Each CTA writes its raw partial tile to scratch;
+// simt_split_sum_kernel then adds the slices in slice order (a fixed order: the result does
+// not depend on scheduling) and applies the epilogue.
 #include <cuda_runtime.h>
+
+#include <algorithm>
 
 #include "device_common.cuh"
 #include "internal.h"
@@ -11,6 +19,8 @@ namespace {
 
 constexpr int TM = 64, TN = 64, TK = 32;
 constexpr int LOADS = TM * TK / 256;  // elements of A (and of B) each thread stages per K step
+constexpr long long kMinSplitSteps = 4;    // K steps (of TK) a split slice keeps at least
+constexpr long long kMaxSplitSlices = 64;
 
 struct SimtParams {
   const float* A[kMaxShards];
@@ -23,7 +33,25 @@ struct SimtParams {
   long long ldd, ldd2, ldaux;
   long long M, N, K;
   int groups, ksum, epi, act;
+  float* P;    // split K: partial tiles [slices][outs][M][N]
+  int slices;  // 1: no split
 };
+
+// The epilogue of output element (m, n) of output og, given its accumulated value v.
+__device__ __forceinline__ void epilogue(const SimtParams& p, int og, long long m, long long n,
+                                         float v) {
+  if (p.epi == EPI_STORE_F32) {
+    if (p.bias[og] != nullptr) v += p.bias[og][n];
+    p.D[og][m * p.ldd + n] = v;
+  } else if (p.epi == EPI_BIAS_ACT) {
+    if (p.bias[og] != nullptr) v += p.bias[og][n];
+    if (p.D[og] != nullptr) p.D[og][m * p.ldd + n] = v;
+    p.D2[og][m * p.ldd2 + n] = (p.act == TP_ACT_GELU_ERF) ? gelu_erf(v) : v;
+  } else {  // EPI_DACT
+    if (p.act == TP_ACT_GELU_ERF) v *= gelu_erf_grad(p.aux[og][m * p.ldaux + n]);
+    p.D[og][m * p.ldd + n] = v;
+  }
+}
 
 // Two shared-memory buffers and a register prefetch: while the block multiplies the K step in
 // one buffer, the loads of the next step are in flight, so the K loop is not a chain of
@@ -31,7 +59,9 @@ struct SimtParams {
 __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ SimtParams p) {
   __shared__ float As[2][TK][TM + 4];
   __shared__ float Bs[2][TK][TN + 4];
-  const int g = blockIdx.z;
+  const int zg = p.ksum ? 1 : p.groups;  // outputs
+  const int g = static_cast<int>(blockIdx.z % zg);
+  const int slice = static_cast<int>(blockIdx.z / zg);
   const long long m0 = static_cast<long long>(blockIdx.y) * TM;
   const long long n0 = static_cast<long long>(blockIdx.x) * TN;
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
@@ -39,7 +69,10 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ 
 
   const int kgroups = p.ksum ? p.groups : 1;
   const long long ksteps = (p.K + TK - 1) / TK;
-  const long long nsteps = ksteps * kgroups;
+  const long long all_steps = ksteps * kgroups;
+  // this CTA's contiguous range of K steps (all of them without a split)
+  const long long s_begin = all_steps * slice / p.slices;
+  const long long s_end = all_steps * (slice + 1) / p.slices;
   float ra[LOADS], rb[LOADS];
 
   // element e of a step's A tile -> (mm, kk); coalesced along whichever of m, k is contiguous
@@ -80,14 +113,14 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ 
     }
   };
 
-  if (nsteps > 0) {
-    load(0);
+  if (s_begin < s_end) {
+    load(s_begin);
     stash(0);
   }
   __syncthreads();
-  for (long long step = 0; step < nsteps; ++step) {
-    const int buf = static_cast<int>(step & 1);
-    if (step + 1 < nsteps) load(step + 1);
+  for (long long step = s_begin; step < s_end; ++step) {
+    const int buf = static_cast<int>((step - s_begin) & 1);
+    if (step + 1 < s_end) load(step + 1);
 #pragma unroll
     for (int kk = 0; kk < TK; ++kk) {
       float a[4], b[4];
@@ -100,11 +133,12 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ 
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
     }
-    if (step + 1 < nsteps) stash(buf ^ 1);
+    if (step + 1 < s_end) stash(buf ^ 1);
     __syncthreads();
   }
 
   const int og = p.ksum ? 0 : g;
+  float* part = p.slices > 1 ? p.P + (static_cast<long long>(slice) * zg + og) * p.M * p.N : nullptr;
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const long long m = m0 + ty + 16 * r;
@@ -113,27 +147,30 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ 
     for (int c = 0; c < 4; ++c) {
       const long long n = n0 + tx + 16 * c;
       if (n >= p.N) continue;
-      float v = acc[r][c];
-      if (p.epi == EPI_STORE_F32) {
-        if (p.bias[og] != nullptr) v += p.bias[og][n];
-        p.D[og][m * p.ldd + n] = v;
-      } else if (p.epi == EPI_BIAS_ACT) {
-        if (p.bias[og] != nullptr) v += p.bias[og][n];
-        if (p.D[og] != nullptr) p.D[og][m * p.ldd + n] = v;
-        p.D2[og][m * p.ldd2 + n] = (p.act == TP_ACT_GELU_ERF) ? gelu_erf(v) : v;
-      } else {  // EPI_DACT
-        if (p.act == TP_ACT_GELU_ERF) v *= gelu_erf_grad(p.aux[og][m * p.ldaux + n]);
-        p.D[og][m * p.ldd + n] = v;
-      }
+      if (part != nullptr)
+        part[m * p.N + n] = acc[r][c];
+      else
+        epilogue(p, og, m, n, acc[r][c]);
     }
   }
 }
 
-}  // namespace
+// Sum of the K-slice partials in slice order, then the epilogue; one thread per element of
+// [outs][M][N] (consecutive threads along n: coalesced).
+__global__ void __launch_bounds__(256) simt_split_sum_kernel(const __grid_constant__ SimtParams p) {
+  const int zg = p.ksum ? 1 : p.groups;
+  const long long mn = p.M * p.N;
+  const long long total = zg * mn;
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += 256LL * gridDim.x) {
+    const int og = static_cast<int>(i / mn);
+    const long long r = i - og * mn;
+    float v = 0.0f;
+    for (int s = 0; s < p.slices; ++s) v += p.P[(static_cast<long long>(s) * zg + og) * mn + r];
+    epilogue(p, og, r / p.N, r % p.N, v);
+  }
+}
 
-cudaError_t launch_simt_gemm(const GemmSpec& s, cudaStream_t st) {
-  if (s.M <= 0 || s.N <= 0 || s.K <= 0) return cudaSuccess;
-  if (s.groups < 1 || s.groups > kMaxShards) return cudaErrorInvalidValue;
+SimtParams make_params(const GemmSpec& s) {
   SimtParams p{};
   for (int g = 0; g < s.groups; ++g) {
     p.A[g] = static_cast<const float*>(s.A[g]);
@@ -157,10 +194,48 @@ cudaError_t launch_simt_gemm(const GemmSpec& s, cudaStream_t st) {
   p.ksum = s.ksum;
   p.epi = s.epi;
   p.act = s.act;
+  p.slices = s.kslices > 1 ? s.kslices : 1;
+  p.P = p.slices > 1 ? s.split : nullptr;
+  return p;
+}
+
+}  // namespace
+
+int plan_simt_split(const GemmSpec& s, size_t scratch_bytes) {
+  if (s.M <= 0 || s.N <= 0 || s.K <= 0) return 1;
+  const long long outs = s.ksum ? 1 : s.groups;
+  const long long tiles = ((s.N + TN - 1) / TN) * ((s.M + TM - 1) / TM) * outs;
+  const long long target = 2LL * device_sm_count();  // CTAs: two per SM
+  if (tiles >= target) return 1;
+  const long long steps = ((s.K + TK - 1) / TK) * (s.ksum ? s.groups : 1);
+  long long S = (target + tiles - 1) / tiles;
+  S = std::min(S, steps / kMinSplitSteps);                        // enough K steps per slice
+  S = std::min<long long>(S, kMaxSplitSlices);
+  const long long per_slice = outs * s.M * s.N * 4;
+  if (per_slice > 0) S = std::min<long long>(S, static_cast<long long>(scratch_bytes) / per_slice);
+  return S > 1 ? static_cast<int>(S) : 1;
+}
+
+cudaError_t launch_simt_gemm(const GemmSpec& s, cudaStream_t st) {
+  if (s.M <= 0 || s.N <= 0 || s.K <= 0) return cudaSuccess;
+  if (s.groups < 1 || s.groups > kMaxShards) return cudaErrorInvalidValue;
+  if (s.kslices > 1 && s.split == nullptr) return cudaErrorInvalidValue;
+  const SimtParams p = make_params(s);
+  const unsigned zg = s.ksum ? 1u : static_cast<unsigned>(s.groups);
   const dim3 grid(static_cast<unsigned>((s.N + TN - 1) / TN),
-                  static_cast<unsigned>((s.M + TM - 1) / TM), s.ksum ? 1u : s.groups);
-  if (grid.y > 65535u) return cudaErrorInvalidValue;
+                  static_cast<unsigned>((s.M + TM - 1) / TM), zg * static_cast<unsigned>(p.slices));
+  if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidValue;
   simt_gemm_kernel<<<grid, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_simt_split_sum(const GemmSpec& s, cudaStream_t st) {
+  if (s.M <= 0 || s.N <= 0 || s.kslices <= 1) return cudaSuccess;
+  if (s.split == nullptr) return cudaErrorInvalidValue;
+  const SimtParams p = make_params(s);
+  const long long total = (s.ksum ? 1LL : s.groups) * s.M * s.N;
+  const long long blocks = std::min<long long>((total + 255) / 256, 8LL * device_sm_count());
+  simt_split_sum_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 

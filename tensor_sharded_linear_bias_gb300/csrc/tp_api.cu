@@ -144,6 +144,16 @@ tp_status cuda_fail(cudaError_t e, const char* what) {
 
 int* status_word(void* ws) { return static_cast<int*>(ws); }
 
+// First byte of a call's scratch: after the status block and, for fp32, the split-K region.
+size_t scratch_base(int dtype) { return kStatusBytes + (dtype == TP_F32 ? kSplitBytes : 0); }
+
+// A GEMM's view of the workspace: the status word, and the split-K scratch of fp32 calls.
+void bind_ws(GemmSpec& s, void* ws, int dtype) {
+  s.status = status_word(ws);
+  s.split = dtype == TP_F32 ? reinterpret_cast<float*>(static_cast<char*>(ws) + kStatusBytes)
+                            : nullptr;
+}
+
 template <typename T>
 T* ws_at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
@@ -222,8 +232,21 @@ cudaError_t run_gemm(const GemmSpec& s, int dtype, cudaStream_t st, int tag) {
   gemm_work(s, dtype, &flops, &bytes);
   if (dtype == TP_BF16)
     return traced(TP_K_GEMM_TC, tag, s.groups, flops, bytes, st, [&] { return launch_tc_gemm(s, st); });
-  return traced(TP_K_GEMM_FFMA, tag, s.groups, flops, bytes, st,
-                [&] { return launch_simt_gemm(s, st); });
+  if (s.split == nullptr)
+    return traced(TP_K_GEMM_FFMA, tag, s.groups, flops, bytes, st,
+                  [&] { return launch_simt_gemm(s, st); });
+  GemmSpec t = s;
+  t.kslices = plan_simt_split(s, kSplitBytes);
+  cudaError_t e = traced(TP_K_GEMM_FFMA, tag, s.groups, flops, bytes, st,
+                         [&] { return launch_simt_gemm(t, st); });
+  if (e != cudaSuccess || t.kslices <= 1) return e;
+  // the slices' sum: every partial read once, every output (and GeLU' input) touched once
+  const double outs = double(s.ksum ? 1 : s.groups), mn = double(s.M) * double(s.N);
+  const double out_e = (s.epi == EPI_BIAS_ACT && s.D[0] != nullptr) ? 8.0 : 4.0;
+  const double aux = (s.epi == EPI_DACT && s.act != TP_ACT_NONE) ? 4.0 : 0.0;
+  return traced(TP_K_SPLIT_SUM, tag, s.groups, (t.kslices - 1) * outs * mn,
+                outs * mn * (4.0 * t.kslices + out_e + aux), st,
+                [&] { return launch_simt_split_sum(t, st); });
 }
 
 // Zero `rows` x `cols` fp32 outputs (a GEMM over zero tokens).
@@ -287,7 +310,7 @@ tp_status mlp_validate(const tp_mlp_desc* d, MlpSizes* z) {
       partials_region(d->reduce, z->n, z->T, z->H);
   z->dH = align256(size_t(z->T) * z->F * e);
   z->partials_bwd = z->partials_fwd;
-  z->total = kStatusBytes + std::max(z->partials_fwd, z->dH + z->partials_bwd);
+  z->total = scratch_base(d->dtype) + std::max(z->partials_fwd, z->dH + z->partials_bwd);
   return TP_OK;
 }
 
@@ -337,7 +360,7 @@ tp_status lin_validate(const tp_linear_desc* d, int kind, LinSizes* z) {
     z->dH = 0;
     z->partials_bwd = 0;
   }
-  z->total = kStatusBytes + std::max(z->partials_fwd, z->dH + z->partials_bwd);
+  z->total = scratch_base(d->dtype) + std::max(z->partials_fwd, z->dH + z->partials_bwd);
   return TP_OK;
 }
 
@@ -399,7 +422,7 @@ tp_status row_product(int dtype, int reduce, int n, int64_t T, int64_t Ks, int64
   s.ldb = N;
   s.ldd = N;
   s.epi = EPI_STORE_F32;
-  s.status = status_word(ws);
+  bind_ws(s, ws, dtype);
   for (int i = 0; i < n; ++i) {
     s.A[i] = X[i];
     s.B[i] = W[i];
@@ -446,7 +469,7 @@ tp_status input_grad_sum(int dtype, int reduce, int n, int64_t T, int64_t w, int
   s.ldb = w;
   s.ldd = Kd;
   s.epi = EPI_STORE_F32;
-  s.status = status_word(ws);
+  bind_ws(s, ws, dtype);
   for (int i = 0; i < n; ++i) {
     s.A[i] = dH[i];
     s.B[i] = W[i];
@@ -497,7 +520,7 @@ tp_status weight_grads(int dtype, int n, int64_t T, int64_t M, int64_t N,
   s.ldb = ldb;
   s.ldd = N;
   s.epi = EPI_STORE_F32;
-  s.status = status_word(ws);
+  bind_ws(s, ws, dtype);
   for (int i = 0; i < n; ++i) {
     s.A[i] = Xa[i];
     s.B[i] = Gb[i];
@@ -670,7 +693,7 @@ tp_status tp_mlp_forward(const tp_mlp_desc* desc, const void* X, const void* con
   c.ldd2 = z.Fs;
   c.epi = EPI_BIAS_ACT;
   c.act = desc->act;
-  c.status = status_word(ws);
+  bind_ws(c, ws, dt);
   for (int i = 0; i < n; ++i) {
     c.A[i] = X;
     c.B[i] = A[i];
@@ -683,7 +706,7 @@ tp_status tp_mlp_forward(const tp_mlp_desc* desc, const void* X, const void* con
   // Row-parallel linear: Z = sum_i Y_i B_i + b.
   TP_TRY(row_product(dt, desc->reduce, n, z.T, z.Fs, z.H,
                      reinterpret_cast<const void* const*>(Ysave), z.Fs, B, b,
-                     static_cast<float*>(Z), ws, kStatusBytes, st, "row GEMM"));
+                     static_cast<float*>(Z), ws, scratch_base(dt), st, "row GEMM"));
   return ok();
 }
 
@@ -713,7 +736,7 @@ tp_status tp_mlp_backward(const tp_mlp_desc* desc, const void* X, const void* co
   const size_t e = elem_size(dt);
 
   // dH_i = (dZ B_i^T) * act'(H_i), kept in the workspace in the input dtype.
-  const size_t dh_off = kStatusBytes;
+  const size_t dh_off = scratch_base(dt);
   const void* dHp[kMaxShards] = {};
   if (z.T > 0) {
     GemmSpec s;
@@ -729,7 +752,7 @@ tp_status tp_mlp_backward(const tp_mlp_desc* desc, const void* X, const void* co
     s.ldaux = z.Fs;
     s.epi = EPI_DACT;
     s.act = desc->act;
-    s.status = status_word(ws);
+    bind_ws(s, ws, dt);
     for (int i = 0; i < n; ++i) {
       s.A[i] = dZ;
       s.B[i] = B[i];
@@ -904,7 +927,7 @@ tp_status tp_linear_column_forward(const tp_linear_desc* desc, const void* X,
   c.ldd2 = desc->gather ? z.N : z.Ns;
   c.epi = EPI_BIAS_ACT;
   c.act = desc->act;
-  c.status = status_word(ws);
+  bind_ws(c, ws, dt);
   for (int i = 0; i < n; ++i) {
     c.A[i] = X;
     c.B[i] = W[i];
@@ -945,7 +968,7 @@ tp_status tp_linear_column_backward(const tp_linear_desc* desc, const void* X,
 
   const void* dHp[kMaxShards] = {};
   int64_t ldh = ld_dy;
-  const size_t dh_off = kStatusBytes;
+  const size_t dh_off = scratch_base(dt);
   if (desc->act != TP_ACT_NONE) {
     void* dHw[kMaxShards] = {};
     for (int i = 0; i < n; ++i) {
@@ -993,7 +1016,7 @@ tp_status tp_linear_row_forward(const tp_linear_desc* desc, const void* const* X
   TP_TRY(check_arch());
   if (z.T == 0) return ok();
   TP_TRY(row_product(dt, desc->reduce, n, z.T, z.Ks, z.N, X, z.Ks, W, bias,
-                     static_cast<float*>(Z), ws, kStatusBytes, static_cast<cudaStream_t>(stream),
+                     static_cast<float*>(Z), ws, scratch_base(dt), static_cast<cudaStream_t>(stream),
                      "row GEMM"));
   return ok();
 }
@@ -1028,7 +1051,7 @@ tp_status tp_linear_row_backward(const tp_linear_desc* desc, const void* const* 
     s.ldb = z.N;
     s.ldd = z.Ks;
     s.epi = EPI_STORE_F32;
-    s.status = status_word(ws);
+    bind_ws(s, ws, dt);
     for (int i = 0; i < n; ++i) {
       s.A[i] = dZ;
       s.B[i] = W[i];

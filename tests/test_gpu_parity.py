@@ -127,6 +127,28 @@ def test_p3_shapes_fp32_forward(tp):
         assert max(errs.values()) <= TOL_F32, errs
 
 
+def test_fp32_split_k(tp):
+    """Few tokens: the FFMA GEMMs whose tiles cannot fill the GPU cut their K range into slices
+    (split_sum launches in the trace: column forward, row forward with the shard sum, the dY
+    GEMM with the GeLU' epilogue, the input gradient); ragged K per slice and ragged tiles still
+    match the oracle to fp32 accuracy, and the slice order makes repeated runs bit-identical."""
+    import torch
+
+    w = wl.P3_FP32_FWD.with_shape(tokens=9, hidden=1000, ffn=4 * 300, tp_degree=4)
+    w = wl.dataclasses.replace(w, sigma={**w.sigma, "a": 0.05, "b": 0.05})
+    case = MlpCase(w, 0)
+    tp.tp_trace_start(64)
+    case.run()
+    recs = tp.tp_trace_stop(64)
+    split_tags = sorted(r["tag"] for r in recs if r["kernel"] == "split_sum")
+    assert split_tags == sorted(["column_fwd", "row_fwd", "row_dgrad", "column_dgrad"]), split_tags
+    errs = compare_full(case.outputs(), *full_reference(case))
+    assert max(errs.values()) <= TOL_F32, errs
+    Z1, dX1 = case.Z.clone(), case.dX.clone()
+    case.run()
+    assert torch.equal(Z1, case.Z) and torch.equal(dX1, case.dX)
+
+
 # ----------------------------------------------------------------------------- invariants
 def test_sharded_matches_unsharded(tp):
     T, H, F = 384, 256, 1024
