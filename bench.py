@@ -377,8 +377,10 @@ L2_FLUSH_FACTOR = 4  # flush between steps unless a step reads this many L2 size
 
 
 class L2Flush:
-    """Writes a buffer of twice the L2 size (a different value each time) before a timed step,
-    outside the step's events, so that a step whose operands would fit in L2 starts cold."""
+    """Before a timed step, outside the step's events: writes a buffer of twice the L2 size (a
+    different value each time), then reads a second one of the same size. The write evicts the
+    previous step's data; the read evicts the written lines again, so that their write-back to
+    HBM is not charged to the timed step. The step then starts with a cold, clean L2."""
 
     def __init__(self, device):
         import torch
@@ -386,15 +388,21 @@ class L2Flush:
         props = torch.cuda.get_device_properties(device)
         self.l2 = int(getattr(props, "L2_cache_size", 0) or (126 << 20))
         self.buf = torch.empty(2 * self.l2 // 4, dtype=torch.float32, device=device)
+        self.clean = torch.ones(2 * self.l2 // 4, dtype=torch.float32, device=device)
+        self.sink = torch.empty((), dtype=torch.float32, device=device)
         self.k = 0
 
     def __call__(self):
+        import torch
+
         self.k += 1
         self.buf.fill_(float(self.k))
+        torch.sum(self.clean, out=self.sink)
 
     def describe(self) -> str:
-        return (f"flushed: {self.buf.numel() * 4 / 1e6:.0f} MB written before every timed step, "
-                f"outside the step's events (L2 {self.l2 / 1e6:.0f} MB)")
+        return (f"flushed: {self.buf.numel() * 4 / 1e6:.0f} MB written, then another "
+                f"{self.clean.numel() * 4 / 1e6:.0f} MB read, before every timed step, outside "
+                f"the step's events (L2 {self.l2 / 1e6:.0f} MB)")
 
 
 def make_flush(device, operand_bytes: int):

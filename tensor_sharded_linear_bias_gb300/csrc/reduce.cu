@@ -6,10 +6,14 @@
 //  * the one-block self-test of the bounded wait.
 #include <cuda_runtime.h>
 
+#include <cooperative_groups.h>
+
 #include <algorithm>
 
 #include "device_common.cuh"
 #include "internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace tpk {
 
@@ -164,11 +168,14 @@ __global__ void shard_copy_kernel(const __grid_constant__ ShardCopyParams p) {
 }
 
 // ------------------------------------------------------------------ column sums
-// One block per (segment, strip of 256 columns), 16 warps. Lane l of warp w owns columns
-// [strip + 8l, strip + 8l + 8) and the rows r with r % 16 == w; it keeps eight of its rows'
-// 16-byte loads in flight and adds them in row order. The 16 warps' partial sums are then
-// added in warp order. Every addition happens in a fixed order, so the result is the same on
-// every run.
+// One cluster of R blocks per (segment, strip of 256 columns); block q of the cluster sums
+// rows [q*rows/R, (q+1)*rows/R) with 16 warps. Lane l of warp w owns columns
+// [strip + 8l, strip + 8l + 8) and every 16th row of the block's range from w; it keeps eight
+// of its rows' 16-byte loads in flight and adds them in row order. The 16 warps' sums are
+// added in warp order, then block 0 adds the R blocks' sums in block order, reading them from
+// the other blocks' shared memory (distributed shared memory of the cluster). R > 1 only when
+// the strips alone would leave SMs idle (few columns). Every addition happens in a fixed order
+// for a given shape, so the result is the same on every run.
 constexpr int kColsumWarps = 16;
 constexpr int kColsumUnroll = 8;
 constexpr int kMaxColsumSegs = kMaxShards + 1;
@@ -203,6 +210,7 @@ __device__ __forceinline__ void load8(const void* base, int bf16, long long off,
 
 __global__ void __launch_bounds__(kColsumWarps * 32) colsum_kernel(const __grid_constant__ ColsumParams p) {
   __shared__ float part[kColsumWarps][256];
+  __shared__ float block_sum[256];
   int s = 0;
   while (s + 1 < p.nseg && static_cast<int>(blockIdx.x) >= p.strip_start[s + 1]) ++s;
   const ColsumSeg seg = p.seg[s];
@@ -210,14 +218,17 @@ __global__ void __launch_bounds__(kColsumWarps * 32) colsum_kernel(const __grid_
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const long long col = c0 + 8 * lane;
   const int valid = static_cast<int>(max(0LL, min(8LL, seg.cols - col)));
+  const int R = static_cast<int>(gridDim.y);  // blocks per cluster (cluster dims 1 x R x 1)
+  const int q = static_cast<int>(blockIdx.y);
+  const long long r_end = p.rows * (q + 1) / R;
   float acc[8] = {};
   if (valid > 0) {
     const long long step = kColsumWarps;
-    long long r = warp;
+    long long r = p.rows * q / R + warp;
     if (p.bf16 && valid == 8) {
       // Raw 16-byte loads first (8 rows in flight), then unpack and add in row order.
       const uint16_t* in = static_cast<const uint16_t*>(seg.in);
-      for (; r + (kColsumUnroll - 1) * step < p.rows; r += kColsumUnroll * step) {
+      for (; r + (kColsumUnroll - 1) * step < r_end; r += kColsumUnroll * step) {
         uint4 raw[kColsumUnroll];
 #pragma unroll
         for (int u = 0; u < kColsumUnroll; ++u)
@@ -234,7 +245,7 @@ __global__ void __launch_bounds__(kColsumWarps * 32) colsum_kernel(const __grid_
         }
       }
     }
-    for (; r < p.rows; r += step) {
+    for (; r < r_end; r += step) {
       float v[8];
       load8(seg.in, p.bf16, r * seg.ld + col, v, valid);
 #pragma unroll
@@ -244,15 +255,26 @@ __global__ void __launch_bounds__(kColsumWarps * 32) colsum_kernel(const __grid_
 #pragma unroll
   for (int j = 0; j < 8; ++j) part[warp][8 * lane + j] = acc[j];
   __syncthreads();
+  const long long c = c0 + threadIdx.x;
   if (threadIdx.x < 256) {
-    const long long c = c0 + threadIdx.x;
-    if (c < seg.cols) {
-      float t = 0.f;
+    float t = 0.f;
 #pragma unroll 8
-      for (int w = 0; w < kColsumWarps; ++w) t += part[w][threadIdx.x];
-      seg.out[c] = t;
+    for (int w = 0; w < kColsumWarps; ++w) t += part[w][threadIdx.x];
+    if (R == 1) {
+      if (c < seg.cols) seg.out[c] = t;
+    } else {
+      block_sum[threadIdx.x] = t;
     }
   }
+  if (R == 1) return;
+  cg::cluster_group cluster = cg::this_cluster();
+  cluster.sync();  // every block's sums are in its shared memory
+  if (q == 0 && threadIdx.x < 256 && c < seg.cols) {
+    float t = 0.f;
+    for (int b = 0; b < R; ++b) t += cluster.map_shared_rank(block_sum, b)[threadIdx.x];
+    seg.out[c] = t;
+  }
+  cluster.sync();  // no block leaves while block 0 may still read its shared memory
 }
 
 // ------------------------------------------------------------------ dH = dY * act'(H)
@@ -386,8 +408,23 @@ cudaError_t launch_colsum(const ColsumSeg* segs, int nseg, int64_t rows, int in_
   }
   p.strip_start[nseg] = strips;
   if (strips == 0) return cudaSuccess;
-  colsum_kernel<<<strips, kColsumWarps * 32, 0, st>>>(p);
-  return cudaGetLastError();
+  // Blocks per strip: enough for about four blocks per SM, at least 256 rows each, at most a
+  // portable cluster of 8.
+  const long long want = (4LL * device_sm_count() + strips - 1) / strips;
+  const int R = static_cast<int>(std::max(1LL, std::min({want, static_cast<long long>(rows) / 256, 8LL})));
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(strips), static_cast<unsigned>(R), 1);
+  cfg.blockDim = dim3(kColsumWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = static_cast<unsigned>(R);
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, colsum_kernel, p);
 }
 
 cudaError_t launch_dact(const void* const* dY, int64_t ld_dy, const void* const* H,

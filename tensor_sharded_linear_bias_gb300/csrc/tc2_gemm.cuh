@@ -272,9 +272,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_c
     // -------------------------------------------------------------- epilogue warps 2..5
     const int quad = warp & 3;
     uint32_t acc = 0, acc_phase = 0;
+    // With the GeLU' epilogue, each tile's pre-activation rows are requested into L2 one tile
+    // ahead (the first tile's here), while the tile before it is being finished.
+    const bool aux_ahead = tc::dact_reads_aux(p);
+    const int my_rows = static_cast<int>(rank) * HALF + quad * 32;
+    if (aux_ahead && cluster < p.num_tiles) {
+      int g1, mb1, nb1;
+      tc::decode_tile(p, cluster, g1, mb1, nb1);
+      tc::prefetch_aux_rows(p, g1, mb1 * BM + my_rows, nb1 * BN, BN);
+    }
     for (int t = cluster; t < p.num_tiles; t += nclusters) {
       int g, mb, nb;
       tc::decode_tile(p, t, g, mb, nb);
+      if (aux_ahead && t + nclusters < p.num_tiles) {
+        int g1, mb1, nb1;
+        tc::decode_tile(p, t + nclusters, g1, mb1, nb1);
+        tc::prefetch_aux_rows(p, g1, mb1 * BM + my_rows, nb1 * BN, BN);
+      }
       if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, kWaitLimitNs)) {
         if (lane == 0) report_status(p.status, kDevTimeoutBase | 0x60);
         *abort_flag = 1;
@@ -285,13 +299,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_c
       const int row0 = mb * BM + static_cast<int>(rank) * HALF + quad * 32;
       const uint32_t trow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
       uint8_t* stg = epi_stage + (warp - 2) * tc::STAGE_WARP_BYTES;
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        const int col0 = nb * BN + c0;
-        if (col0 >= p.N) break;  // uniform across the warp
-        float v[32];
-        tc::tmem_ld_32cols(trow + c0, v);
-        tc::epilogue_chunk(p, g, row0, col0, v, stg);
-      }
+      tc::epilogue_rows<BN>(p, g, row0, nb * BN, trow, stg);
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));

@@ -229,20 +229,32 @@ __device__ __forceinline__ void warp_store_bf16(uint8_t* stage, const float* v, 
   __syncwarp();
 }
 
-// The transpose of warp_store_bf16: coalesced loads of the 32 x 32 bf16 block at
-// src[row0.., col0..], then lane l gets the 32 values of row row0 + l (0 outside the matrix).
-__device__ __forceinline__ void warp_load_bf16(uint8_t* stage, const uint16_t* src, long long ld,
-                                               int row0, int col0, int M, int valid, float* out) {
+// The transpose of warp_store_bf16, in two halves so that the loads can be issued ahead of
+// their use. warp_fetch_bf16: coalesced 16-byte loads of the 32 x 32 bf16 block at
+// src[row0.., col0..] into four registers per lane (0 outside the matrix).
+__device__ __forceinline__ void warp_fetch_bf16(const uint16_t* src, long long ld, int row0,
+                                                int col0, int M, int valid, uint4* raw) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int r = 8 * it + (lane >> 2);
+    const int c = lane & 3;
+    raw[it] = make_uint4(0u, 0u, 0u, 0u);
+    if (row0 + r < M && 8 * c < valid)
+      raw[it] = *reinterpret_cast<const uint4*>(src + static_cast<long long>(row0 + r) * ld + col0 + 8 * c);
+  }
+}
+
+// warp_unpack_bf16: through the warp's staging buffer, lane l gets the 32 values of row
+// row0 + l of a fetched block, as fp32.
+__device__ __forceinline__ void warp_unpack_bf16(uint8_t* stage, const uint4* raw, float* out) {
   const int lane = threadIdx.x & 31;
   uint4* s = reinterpret_cast<uint4*>(stage);
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
     const int r = 8 * it + (lane >> 2);
     const int c = lane & 3;
-    uint4 x = make_uint4(0u, 0u, 0u, 0u);
-    if (row0 + r < M && 8 * c < valid)
-      x = *reinterpret_cast<const uint4*>(src + static_cast<long long>(row0 + r) * ld + col0 + 8 * c);
-    s[r * 4 + (c ^ ((r >> 1) & 3))] = x;
+    s[r * 4 + (c ^ ((r >> 1) & 3))] = raw[it];
   }
   __syncwarp();
 #pragma unroll
@@ -257,6 +269,30 @@ __device__ __forceinline__ void warp_load_bf16(uint8_t* stage, const uint16_t* s
     }
   }
   __syncwarp();
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(__cvta_generic_to_global(ptr)),
+               "r"(bytes)
+               : "memory");
+}
+
+// EPI_DACT with an activation reads the saved pre-activation at every output element.
+__device__ __forceinline__ bool dact_reads_aux(const TcParams& p) {
+  return p.epi == EPI_DACT && p.act == TP_ACT_GELU_ERF;
+}
+
+// Lane l asks L2 for row row0 + l of the pre-activation block [row0.., col0.., up to ncols
+// columns] of group g: one bulk prefetch per row (16-byte aligned start, a multiple of 16
+// bytes long: bf16 rows and N are multiples of 8, col0 of 256).
+__device__ __forceinline__ void prefetch_aux_rows(const TcParams& p, int g, int row0, int col0,
+                                                  int ncols) {
+  const int lane = threadIdx.x & 31;
+  const int row = row0 + lane;
+  const int cols = min(ncols, p.N - col0);
+  if (row < p.M && cols > 0)
+    prefetch_l2(static_cast<const uint16_t*>(p.aux[g]) + static_cast<long long>(row) * p.ldaux + col0,
+                static_cast<uint32_t>(cols) * 2u);
 }
 
 // Per-column bias (bf16), the same 32 values for every lane: broadcast loads. Columns at or
@@ -359,12 +395,49 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, int g, int row
   } else {  // EPI_DACT (aux = the saved pre-activation, read only with an activation)
     if (p.act == TP_ACT_GELU_ERF) {
       float h[32];
-      warp_load_bf16(stage, static_cast<const uint16_t*>(p.aux[og]), p.ldaux, row0, col0, p.M,
-                     valid, h);
+      uint4 raw[4];
+      warp_fetch_bf16(static_cast<const uint16_t*>(p.aux[og]), p.ldaux, row0, col0, p.M, valid, raw);
+      warp_unpack_bf16(stage, raw, h);
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] *= gelu_erf_grad(h[i]);
     }
     warp_store_bf16(stage, v, static_cast<uint16_t*>(p.D[og]), p.ldd, row0, col0, p.M, valid);
+  }
+}
+
+// One warp's 32 rows x NCOLS columns (from colbase) of a finished accumulator at TMEM address
+// trow, 32 columns at a time. With EPI_DACT + activation, the pre-activation loads of the
+// next 32 columns are issued before the current ones are used, so each chunk's DRAM/L2 round
+// trip overlaps the previous chunk's work instead of stalling the warp.
+template <int NCOLS>
+__device__ __forceinline__ void epilogue_rows(const TcParams& p, int g, int row0, int colbase,
+                                              uint32_t trow, uint8_t* stage) {
+  if (!dact_reads_aux(p)) {
+    for (int c0 = 0; c0 < NCOLS; c0 += 32) {
+      const int col0 = colbase + c0;
+      if (col0 >= p.N) break;  // uniform across the warp
+      float v[32];
+      tmem_ld_32cols(trow + c0, v);
+      epilogue_chunk(p, g, row0, col0, v, stage);
+    }
+    return;
+  }
+  const uint16_t* aux = static_cast<const uint16_t*>(p.aux[g]);
+  uint4 nxt[4];
+  warp_fetch_bf16(aux, p.ldaux, row0, colbase, p.M, min(32, p.N - colbase), nxt);
+  for (int c0 = 0; c0 < NCOLS; c0 += 32) {
+    const int col0 = colbase + c0;
+    if (col0 >= p.N) break;
+    const uint4 cur[4] = {nxt[0], nxt[1], nxt[2], nxt[3]};
+    if (c0 + 32 < NCOLS && col0 + 32 < p.N)
+      warp_fetch_bf16(aux, p.ldaux, row0, col0 + 32, p.M, min(32, p.N - col0 - 32), nxt);
+    float v[32], h[32];
+    tmem_ld_32cols(trow + c0, v);
+    warp_unpack_bf16(stage, cur, h);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] *= gelu_erf_grad(h[i]);
+    warp_store_bf16(stage, v, static_cast<uint16_t*>(p.D[g]), p.ldd, row0, col0, p.M,
+                    min(32, p.N - col0));
   }
 }
 
@@ -523,9 +596,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     // -------------------------------------------------------------- epilogue warps 2..5
     const int quad = warp & 3;  // TMEM lanes this warp may read: 32*quad .. 32*quad+31
     uint32_t acc = 0, acc_phase = 0;
+    // With the GeLU' epilogue, each tile's pre-activation rows are requested into L2 one tile
+    // ahead (the first tile's here), while the tile before it is being finished.
+    const bool aux_ahead = dact_reads_aux(p);
+    if (aux_ahead && static_cast<int>(blockIdx.x) < p.num_tiles) {
+      int g1, mb1, nb1;
+      decode_tile(p, blockIdx.x, g1, mb1, nb1);
+      prefetch_aux_rows(p, g1, mb1 * BM + quad * 32, nb1 * BN, BN);
+    }
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
       int g, mb, nb;
       decode_tile(p, t, g, mb, nb);
+      if (aux_ahead && t + static_cast<int>(gridDim.x) < p.num_tiles) {
+        int g1, mb1, nb1;
+        decode_tile(p, t + gridDim.x, g1, mb1, nb1);
+        prefetch_aux_rows(p, g1, mb1 * BM + quad * 32, nb1 * BN, BN);
+      }
       if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, kWaitLimitNs)) {
         if (lane == 0) report_status(p.status, kDevTimeoutBase | 0x30);
         *abort_flag = 1;
@@ -536,13 +622,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       const int row0 = mb * BM + quad * 32;  // this warp's 32 rows
       const uint32_t trow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
       uint8_t* stage = epi_stage + (warp - 2) * STAGE_WARP_BYTES;
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        const int col0 = nb * BN + c0;
-        if (col0 >= p.N) break;  // uniform across the warp
-        float v[32];
-        tmem_ld_32cols(trow + c0, v);
-        epilogue_chunk(p, g, row0, col0, v, stage);
-      }
+      epilogue_rows<BN>(p, g, row0, nb * BN, trow, stage);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));

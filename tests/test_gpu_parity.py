@@ -149,6 +149,22 @@ def test_fp32_split_k(tp):
     assert torch.equal(Z1, case.Z) and torch.equal(dX1, case.dX)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_bias_grads_many_tokens(tp, dtype):
+    """Column sums over many tokens and few columns: each 256-column strip is summed by a
+    cluster of blocks (ragged row ranges per block, a ragged last strip), then the blocks'
+    sums are added in block order; matches the oracle's bias gradients."""
+    base = wl.P3_FP32_FWD if dtype == "f32" else SMALL
+    w = base.with_shape(tokens=3000, hidden=264, ffn=4 * 72, tp_degree=4)
+    case = MlpCase(w, 0).run()
+    f = case.f
+    fr = oracle.mlp_forward(f["X"], f["A"], f["a"], f["B"], f["b"], case.n)
+    br = oracle.mlp_backward(f["X"], f["A"], f["a"], f["B"], f["b"], f["dZ"], case.n, fr)
+    tol = TOL_BF16 if dtype == "bf16" else TOL_F32
+    errs = {"db": rel(np64(case.db), br["db"]), "da": rel_shards([np64(x) for x in case.da], br["da"])}
+    assert max(errs.values()) <= tol, errs
+
+
 # ----------------------------------------------------------------------------- invariants
 def test_sharded_matches_unsharded(tp):
     T, H, F = 384, 256, 1024
