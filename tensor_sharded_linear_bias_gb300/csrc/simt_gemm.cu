@@ -164,8 +164,19 @@ __global__ void __launch_bounds__(256) simt_split_sum_kernel(const __grid_consta
   for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += 256LL * gridDim.x) {
     const int og = static_cast<int>(i / mn);
     const long long r = i - og * mn;
+    // eight slices' loads in flight at a time, added in slice order
+    const float* src = p.P + static_cast<long long>(og) * mn + r;
+    const long long slice_stride = zg * mn;
     float v = 0.0f;
-    for (int s = 0; s < p.slices; ++s) v += p.P[(static_cast<long long>(s) * zg + og) * mn + r];
+    int s = 0;
+    for (; s + 8 <= p.slices; s += 8) {
+      float t[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) t[u] = src[(s + u) * slice_stride];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v += t[u];
+    }
+    for (; s < p.slices; ++s) v += src[s * slice_stride];
     epilogue(p, og, r / p.N, r % p.N, v);
   }
 }
