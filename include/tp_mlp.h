@@ -43,7 +43,10 @@
  *    TP_F32_SPLIT_SCRATCH_BYTES of it, right after the status block, for the K-slice
  *    partial sums of their GEMMs: when a product has too few output tiles to fill the GPU
  *    (few tokens), its K range is cut into slices computed in parallel and the slices are
- *    added in slice order (deterministic) by a second kernel. A device-side wait that
+ *    added in slice order (deterministic) by a second kernel. TP_BF16 calls reserve
+ *    TP_BF16_TAIL_SCRATCH_BYTES there instead: when a GEMM's tiles leave its last wave of SM
+ *    pairs partly idle, each tile of that wave is computed as K pieces on otherwise idle
+ *    pairs, and the pieces are added in piece order (deterministic) before the epilogue. A device-side wait that
  *    runs out writes an error code into the status word; tp_check_status reports it.
  *  - Requires an sm_103 device (GB300); on any other device calls return TP_ERR_ARCH.
  */
@@ -134,6 +137,9 @@ typedef enum tp_linear_kind { TP_COLUMN = 0, TP_ROW = 1 } tp_linear_kind;
 
 /* Workspace bytes that every TP_F32 call reserves after the 256-byte status block. */
 #define TP_F32_SPLIT_SCRATCH_BYTES ((size_t)320 * 64 * 64 * 4)
+/* Workspace bytes that every TP_BF16 call reserves after the 256-byte status block: up to 80
+ * fp32 accumulator pieces of 256 x 256 for the GEMM's split last wave, and their counters. */
+#define TP_BF16_TAIL_SCRATCH_BYTES ((size_t)80 * 256 * 256 * 4 + 4096)
 
 /* Version of this ABI (major * 100 + minor). */
 int32_t tp_version(void);
@@ -142,7 +148,8 @@ int32_t tp_version(void);
 const char* tp_last_error(void);
 
 /* Bytes of workspace that tp_mlp_forward and tp_mlp_backward need for *desc (the larger of
- * the two): a 256-byte status block, TP_F32_SPLIT_SCRATCH_BYTES for TP_F32, plus n fp32
+ * the two): a 256-byte status block, TP_F32_SPLIT_SCRATCH_BYTES for TP_F32 (or
+ * TP_BF16_TAIL_SCRATCH_BYTES for TP_BF16), plus n fp32
  * partials [T,H] in TP_REDUCE_PARTIALS mode, or the backward's per-shard gradients
  * dH_i [T,F/n] at the pre-activation. */
 tp_status tp_mlp_workspace_size(const tp_mlp_desc* desc, size_t* bytes);

@@ -30,6 +30,7 @@ TP_ACT_NONE, TP_ACT_GELU_ERF = 0, 1
 TP_REDUCE_FUSED, TP_REDUCE_PARTIALS, TP_REDUCE_AUTO, TP_REDUCE_PARTIALS_BF16, TP_REDUCE_OVERLAP = 0, 1, 2, 3, 4
 TP_COLUMN, TP_ROW = 0, 1
 TP_F32_SPLIT_SCRATCH_BYTES = 320 * 64 * 64 * 4
+TP_BF16_TAIL_SCRATCH_BYTES = 80 * 256 * 256 * 4 + 4096
 
 STATUS_NAMES = {
     0: "TP_OK", 1: "TP_ERR_NULL", 2: "TP_ERR_SHAPE", 3: "TP_ERR_INDIVISIBLE",

@@ -17,6 +17,14 @@ constexpr int kMaxShards = 64;
 // (320 tiles of 64 x 64 fp32: the most a split plan ever uses).
 constexpr size_t kStatusBytes = 256;
 constexpr size_t kSplitBytes = TP_F32_SPLIT_SCRATCH_BYTES;
+// bf16 calls reserve kTailBytes there instead: the fp32 pieces of the tensor-core GEMM's split
+// tail tiles (at most kTailUnits pieces of 256 x 256 fp32), then one counter per (tile, 32-row
+// block) of the split tiles.
+constexpr int kTailUnits = 80;
+constexpr size_t kTailPieceBytes = size_t(256) * 256 * 4;
+constexpr size_t kTailCounterBytes = 4096;
+constexpr size_t kTailBytes = TP_BF16_TAIL_SCRATCH_BYTES;
+static_assert(kTailBytes == kTailUnits * kTailPieceBytes + kTailCounterBytes, "tail region");
 
 // Device status codes written by kernels (first error wins).
 constexpr int kDevTimeoutBase = 0x100;  // | (role << 4) | wait site
@@ -58,6 +66,9 @@ struct GemmSpec {
   int* status = nullptr;
   int kslices = 1;         // FFMA GEMM: K steps split over this many CTAs per tile (1: none)
   float* split = nullptr;  // ... their partial tiles, kslices x outputs x M x N fp32
+  // tensor-core GEMM on SM pairs: scratch for split tail tiles (nullptr: never split)
+  float* tail_ws = nullptr;
+  int* tail_counters = nullptr;
 };
 
 // bf16 inputs, tcgen05 tensor cores (sm_103a). Returns cudaSuccess or the launch error.

@@ -115,6 +115,62 @@ __device__ __forceinline__ void umma_commit_pair_multicast(uint32_t bar, uint16_
       : "memory");
 }
 
+// ------------------------------------------------------------------ tail split
+// A piece's accumulator in the tail workspace: [piece][256 rows][256 columns] fp32 per tile.
+constexpr int PIECE_FLOATS = BM * BN;
+
+// One warp stores its 32 accumulator rows (tile-local rows lrow0..lrow0+31, all 256 columns) of
+// a piece, through its staging buffer (coalesced rows).
+__device__ __forceinline__ void store_piece_rows(float* piece_ws, int lrow0, uint32_t trow,
+                                                 uint8_t* stage) {
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    float v[32];
+    tc::tmem_ld_32cols(trow + c0, v);
+    tc::warp_store_f32(stage, v, piece_ws, BN, lrow0, c0, BM, 32);
+  }
+}
+
+// Warp-wide, after the warp's piece rows are stored: make them visible and count the warp in
+// for its (tile, 32-row block). True for the warp that completes the count (it then sees every
+// piece's rows).
+__device__ __forceinline__ bool tail_last_arrival(int* counter, int pieces) {
+  const int lane = threadIdx.x & 31;
+  __threadfence();
+  __syncwarp();
+  int last = 0;
+  if (lane == 0) last = atomicAdd(counter, 1) == pieces - 1;
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (last) __threadfence();
+  return last != 0;
+}
+
+// The completing warp: lane l adds row lrow0 + l of every piece in piece order (L2 reads, 32
+// columns at a time) and runs the tile's epilogue on the sums, as for an unsplit tile.
+__device__ __forceinline__ void tail_fixup_rows(const TcParams& p, int g, int row0, int colbase,
+                                                const float* tile_ws, int lrow0, uint8_t* stage) {
+  const int lane = threadIdx.x & 31;
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    const int col0 = colbase + c0;
+    if (col0 >= p.N) break;  // uniform across the warp
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = 0.f;
+    const float* src = tile_ws + static_cast<long long>(lrow0 + lane) * BN + c0;
+    for (int pc = 0; pc < p.ksplit; ++pc) {
+      const float* sp = src + static_cast<long long>(pc) * PIECE_FLOATS;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 x = tc::ld_cg_f4(sp + 4 * j);
+        v[4 * j] += x.x;
+        v[4 * j + 1] += x.y;
+        v[4 * j + 2] += x.z;
+        v[4 * j + 3] += x.w;
+      }
+    }
+    tc::epilogue_chunk(p, g, row0, col0, v, stage);
+  }
+}
+
 template <bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -173,12 +229,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_c
       uint32_t stage = 0, phase = 0;
       bool failed = false;
       long long issued = 0;
-      for (int t = cluster; t < p.num_tiles && !failed; t += nclusters) {
+      for (int u = cluster; u < p.num_units && !failed; u += nclusters) {
+        int t, kb0, kb1, piece;
+        tc::decode_unit(p, u, total_kb, t, kb0, kb1, piece);
         int g, mb, nb;
         tc::decode_tile(p, t, g, mb, nb);
         const int arow = mb * BM + static_cast<int>(rank) * HALF;   // this CTA's A rows
         const int bcol = nb * BN + static_cast<int>(rank) * HALF;   // this CTA's B half
-        for (int kb = 0; kb < total_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (*abort_flag) { failed = true; break; }
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, kWaitLimitNs)) {
             report_status(p.status, kDevTimeoutBase | 0x40);
@@ -228,7 +286,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_c
       constexpr uint32_t idesc = tc::idesc_bf16(BM, BN, A_MN, B_MN);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool failed = false;
-      for (int t = cluster; t < p.num_tiles && !failed; t += nclusters) {
+      for (int u = cluster; u < p.num_units && !failed; u += nclusters) {
+        int t, kb0, kb1, piece;
+        tc::decode_unit(p, u, total_kb, t, kb0, kb1, piece);
         if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, kWaitLimitNs)) {
           report_status(p.status, kDevTimeoutBase | 0x50);
           *abort_flag = 1;
@@ -237,7 +297,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_c
         }
         tc::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < total_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (*abort_flag) { failed = true; break; }
           if (!mbar_wait_bounded(full_bar(stage), phase, kWaitLimitNs)) {
             report_status(p.status, kDevTimeoutBase | 0x51);
@@ -254,7 +314,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_c
                                      : tc::sdesc_sw128(sa + k * 32, 16, 1024);
             const uint64_t bd = B_MN ? tc::sdesc_sw128(sb + k * 2048, MN_BOX_BYTES, 1024)
                                      : tc::sdesc_sw128(sb + k * 32, 16, 1024);
-            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
           }
           umma_commit_pair_multicast(empty_bar(stage), 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -276,19 +336,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_c
     // ahead (the first tile's here), while the tile before it is being finished.
     const bool aux_ahead = tc::dact_reads_aux(p);
     const int my_rows = static_cast<int>(rank) * HALF + quad * 32;
-    if (aux_ahead && cluster < p.num_tiles) {
-      int g1, mb1, nb1;
-      tc::decode_tile(p, cluster, g1, mb1, nb1);
+    const int total_kb_e = p.kblocks * p.kpo;
+    auto prefetch_unit = [&](int u) {
+      int t1, a0, a1, pc1, g1, mb1, nb1;
+      tc::decode_unit(p, u, total_kb_e, t1, a0, a1, pc1);
+      tc::decode_tile(p, t1, g1, mb1, nb1);
       tc::prefetch_aux_rows(p, g1, mb1 * BM + my_rows, nb1 * BN, BN);
-    }
-    for (int t = cluster; t < p.num_tiles; t += nclusters) {
+    };
+    if (aux_ahead && cluster < p.num_units) prefetch_unit(cluster);
+    for (int u = cluster; u < p.num_units; u += nclusters) {
+      int t, kb0, kb1, piece;
+      tc::decode_unit(p, u, total_kb_e, t, kb0, kb1, piece);
       int g, mb, nb;
       tc::decode_tile(p, t, g, mb, nb);
-      if (aux_ahead && t + nclusters < p.num_tiles) {
-        int g1, mb1, nb1;
-        tc::decode_tile(p, t + nclusters, g1, mb1, nb1);
-        tc::prefetch_aux_rows(p, g1, mb1 * BM + my_rows, nb1 * BN, BN);
-      }
+      if (aux_ahead && u + nclusters < p.num_units) prefetch_unit(u + nclusters);
       if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, kWaitLimitNs)) {
         if (lane == 0) report_status(p.status, kDevTimeoutBase | 0x60);
         *abort_flag = 1;
@@ -299,11 +360,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_c
       const int row0 = mb * BM + static_cast<int>(rank) * HALF + quad * 32;
       const uint32_t trow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
       uint8_t* stg = epi_stage + (warp - 2) * tc::STAGE_WARP_BYTES;
-      tc::epilogue_rows<BN>(p, g, row0, nb * BN, trow, stg);
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
-      if (p.epi == EPI_PARTIAL_REDUCE) tc::partial_reduce_rows(p, row0, nb);
+      if (piece < 0) {
+        tc::epilogue_rows<BN>(p, g, row0, nb * BN, trow, stg);
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+        if (p.epi == EPI_PARTIAL_REDUCE) tc::partial_reduce_rows(p, row0, nb);
+      } else {
+        // one piece of a split tile: park the accumulator rows, free TMEM, and finish the
+        // tile's rows if this warp completes their count
+        const int split_tile = t - p.full_tiles;
+        float* tile_ws = p.tail_ws + static_cast<long long>(split_tile) * p.ksplit * PIECE_FLOATS;
+        store_piece_rows(tile_ws + static_cast<long long>(piece) * PIECE_FLOATS, my_rows, trow, stg);
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+        int* counter = p.tail_counters + split_tile * 8 + static_cast<int>(rank) * 4 + quad;
+        if (tail_last_arrival(counter, p.ksplit)) {
+          tail_fixup_rows(p, g, row0, nb * BN, tile_ws, my_rows, stg);
+          if (p.epi == EPI_PARTIAL_REDUCE) tc::partial_reduce_rows(p, row0, nb);
+          __syncwarp();
+          if (lane == 0) atomicExch(counter, 0);
+        }
+      }
       if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1u; }
     }
   }

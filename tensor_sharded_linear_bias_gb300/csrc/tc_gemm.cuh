@@ -73,6 +73,13 @@ struct __align__(128) TcParams {
   long long ldz;
   const void* zbias;
   int nsplit;
+  // Tail split (SM-pair kernel): units [0, full_tiles) are whole tiles; every tile t >=
+  // full_tiles is computed as ksplit units ("pieces") of consecutive K blocks. A piece stores
+  // its fp32 accumulator in tail_ws; the warp completing a (tile, 32-row block) count in
+  // tail_counters adds the pieces in piece order and runs the tile's epilogue.
+  int full_tiles, ksplit, num_units;
+  float* tail_ws;
+  int* tail_counters;
   int* status;
 };
 
@@ -172,6 +179,23 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int t, int& g, in
     nb = r % p.tiles_n;
     mb = r / p.tiles_n;
   }
+}
+
+// Work unit u -> tile t and its K blocks [kb0, kb1); piece = -1 for a whole tile.
+__device__ __forceinline__ void decode_unit(const TcParams& p, int u, int total_kb, int& t,
+                                            int& kb0, int& kb1, int& piece) {
+  if (u < p.full_tiles) {
+    t = u;
+    kb0 = 0;
+    kb1 = total_kb;
+    piece = -1;
+    return;
+  }
+  const int v = u - p.full_tiles;
+  t = p.full_tiles + v / p.ksplit;
+  piece = v % p.ksplit;
+  kb0 = static_cast<int>(static_cast<long long>(total_kb) * piece / p.ksplit);
+  kb1 = static_cast<int>(static_cast<long long>(total_kb) * (piece + 1) / p.ksplit);
 }
 
 // ------------------------------------------------------------------ epilogue (32 rows x 32 cols per warp)

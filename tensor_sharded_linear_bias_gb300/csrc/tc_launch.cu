@@ -125,6 +125,36 @@ bool mn3d_enabled() {
   return true;
 }
 
+// Split tail; TPMLP_TAIL_SPLIT=0 turns it off.
+bool tail_split_enabled() {
+  if (const char* env = std::getenv("TPMLP_TAIL_SPLIT")) return std::atoi(env) != 0;
+  return true;
+}
+
+constexpr int kMinPieceKb = 8;  // K blocks of 64 a piece keeps at least
+
+// Work units of an SM-pair launch over `clusters` pairs. Tiles are dealt to the pairs round
+// robin, so the last wave holds L = num_tiles mod clusters tiles (all of them when there are
+// fewer tiles than pairs) and leaves the other pairs idle for a whole tile. Each of those L
+// tiles is cut into S = clusters / L pieces of consecutive K blocks (capped by kMinPieceKb and
+// the kTailUnits pieces the workspace holds), which run side by side on the idle pairs: the
+// last wave takes about 1/S of a tile's time, plus the pieces' fp32 round trip through L2.
+void plan_tail(tc::TcParams& p, int clusters, int total_kb, bool have_ws) {
+  p.full_tiles = p.num_tiles;
+  p.ksplit = 1;
+  p.num_units = p.num_tiles;
+  if (!have_ws || !tail_split_enabled() || clusters < 2) return;
+  const int L = p.num_tiles % clusters;
+  if (L == 0) return;
+  int S = clusters / L;
+  S = std::min(S, total_kb / kMinPieceKb);
+  S = std::min(S, kTailUnits / L);
+  if (S < 2) return;
+  p.full_tiles = p.num_tiles - L;
+  p.ksplit = S;
+  p.num_units = p.full_tiles + L * S;
+}
+
 }  // namespace
 
 int plan_shard_split(int64_t M, int64_t N, int64_t K_per_group, int n) {
@@ -221,8 +251,20 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
 
   const int layout = (!s.a_mn && s.b_mn) ? 0 : (!s.a_mn && !s.b_mn) ? 1 : (s.a_mn && s.b_mn) ? 2 : -1;
   if (layout < 0) return cudaErrorNotSupported;
+  p.full_tiles = p.num_tiles;
+  p.ksplit = 1;
+  p.num_units = p.num_tiles;
   if (pair) {
-    const int clusters = std::min(p.num_tiles, pair_clusters(layout));
+    const int max_clusters = pair_clusters(layout);
+    plan_tail(p, max_clusters, p.kblocks * p.kpo, s.tail_ws != nullptr && s.tail_counters != nullptr);
+    if (p.ksplit > 1) {
+      p.tail_ws = s.tail_ws;
+      p.tail_counters = s.tail_counters;
+      const size_t counters = size_t(p.num_tiles - p.full_tiles) * 8 * sizeof(int);
+      cudaError_t e = cudaMemsetAsync(s.tail_counters, 0, counters, st);
+      if (e != cudaSuccess) return e;
+    }
+    const int clusters = std::min(p.num_units, max_clusters);
     if (layout == 0) return run_pair_kmn(p, clusters, st, nullptr);
     if (layout == 1) return run_pair_kk(p, clusters, st, nullptr);
     return run_pair_mnmn(p, clusters, st, nullptr);

@@ -144,14 +144,20 @@ tp_status cuda_fail(cudaError_t e, const char* what) {
 
 int* status_word(void* ws) { return static_cast<int*>(ws); }
 
-// First byte of a call's scratch: after the status block and, for fp32, the split-K region.
-size_t scratch_base(int dtype) { return kStatusBytes + (dtype == TP_F32 ? kSplitBytes : 0); }
+// First byte of a call's scratch: after the status block and the dtype's GEMM region (fp32:
+// split-K slices; bf16: split tail tiles).
+size_t scratch_base(int dtype) {
+  return kStatusBytes + (dtype == TP_F32 ? kSplitBytes : kTailBytes);
+}
 
-// A GEMM's view of the workspace: the status word, and the split-K scratch of fp32 calls.
+// A GEMM's view of the workspace: the status word and its dtype's GEMM region.
 void bind_ws(GemmSpec& s, void* ws, int dtype) {
+  char* region = static_cast<char*>(ws) + kStatusBytes;
   s.status = status_word(ws);
-  s.split = dtype == TP_F32 ? reinterpret_cast<float*>(static_cast<char*>(ws) + kStatusBytes)
-                            : nullptr;
+  s.split = dtype == TP_F32 ? reinterpret_cast<float*>(region) : nullptr;
+  s.tail_ws = dtype == TP_BF16 ? reinterpret_cast<float*>(region) : nullptr;
+  s.tail_counters =
+      dtype == TP_BF16 ? reinterpret_cast<int*>(region + kTailUnits * kTailPieceBytes) : nullptr;
 }
 
 template <typename T>

@@ -69,18 +69,20 @@ def status_of(fn):
 
 def test_workspace_sizes(tp):
     T, H, F, n = 64, 128, 512, 4
-    assert tp.tp_mlp_workspace_size(mlp(tp)) == 256 + T * F * 2
+    tail = tp.TP_BF16_TAIL_SCRATCH_BYTES   # bf16: split tail tiles after the status block
+    assert tail == 80 * 256 * 256 * 4 + 4096
+    assert tp.tp_mlp_workspace_size(mlp(tp)) == 256 + tail + T * F * 2
     split = tp.TP_F32_SPLIT_SCRATCH_BYTES   # fp32: K-slice partials after the status block
     assert split == 320 * 64 * 64 * 4
     assert tp.tp_mlp_workspace_size(mlp(tp, dtype=tp.TP_F32)) == 256 + split + T * F * 4
     part = n * T * H * 4
-    assert tp.tp_mlp_workspace_size(mlp(tp, reduce=tp.TP_REDUCE_PARTIALS)) == 256 + T * F * 2 + part
-    assert tp.tp_mlp_workspace_size(mlp(tp, reduce=tp.TP_REDUCE_AUTO)) == 256 + T * F * 2 + part
+    assert tp.tp_mlp_workspace_size(mlp(tp, reduce=tp.TP_REDUCE_PARTIALS)) == 256 + tail + T * F * 2 + part
+    assert tp.tp_mlp_workspace_size(mlp(tp, reduce=tp.TP_REDUCE_AUTO)) == 256 + tail + T * F * 2 + part
     assert tp.tp_mlp_workspace_size(mlp(tp, reduce=tp.TP_REDUCE_PARTIALS_BF16)) == \
-        256 + T * F * 2 + part // 2
+        256 + tail + T * F * 2 + part // 2
     counters = 256   # (64 / 32) x (128 / 256 -> 1) ints, rounded up to 256 bytes
     assert tp.tp_mlp_workspace_size(mlp(tp, reduce=tp.TP_REDUCE_OVERLAP)) == \
-        256 + T * F * 2 + part + counters
+        256 + tail + T * F * 2 + part + counters
     col = tp.LinearDesc(tokens=32, in_features=768, out_features=3072, tp_degree=4,
                         dtype=tp.TP_F32, act=0, reduce=0, gather=1)
     assert tp.tp_linear_workspace_size(col, tp.TP_COLUMN) == 256 + split
@@ -123,7 +125,7 @@ def test_linear_desc_validation(tp):
     base = dict(tokens=8, in_features=64, out_features=96, tp_degree=4, dtype=tp.TP_BF16,
                 act=0, reduce=0, gather=0)
     ok = tp.LinearDesc(**base)
-    assert tp.tp_linear_workspace_size(ok, tp.TP_COLUMN) == 256
+    assert tp.tp_linear_workspace_size(ok, tp.TP_COLUMN) == 256 + tp.TP_BF16_TAIL_SCRATCH_BYTES
     assert status_of(lambda: tp.tp_linear_workspace_size(
         tp.LinearDesc(**{**base, "out_features": 98}), tp.TP_COLUMN)) == "TP_ERR_INDIVISIBLE"
     assert status_of(lambda: tp.tp_linear_workspace_size(
@@ -203,5 +205,8 @@ def test_header_split_scratch_matches_binding(tp):
     m = re.search(r"#define TP_F32_SPLIT_SCRATCH_BYTES \(\(size_t\)([0-9 *]+)\)", text)
     assert m is not None
     assert eval(m.group(1)) == tp.TP_F32_SPLIT_SCRATCH_BYTES
+    m = re.search(r"#define TP_BF16_TAIL_SCRATCH_BYTES \(\(size_t\)([0-9 *+]+)\)", text)
+    assert m is not None
+    assert eval(m.group(1)) == tp.TP_BF16_TAIL_SCRATCH_BYTES
     kinds = dict((int(v), k) for k, v in re.findall(r"(TP_K_\w+) = (\d+)", text))
     assert kinds[8] == "TP_K_SPLIT_SUM" and tp.KERNEL_NAMES[8] == "split_sum"

@@ -165,6 +165,36 @@ def test_bias_grads_many_tokens(tp, dtype):
     assert max(errs.values()) <= tol, errs
 
 
+@pytest.mark.parametrize("reduce", [0, 2, 4])
+def test_tail_split(tp, monkeypatch, reduce):
+    """Tiles of a GEMM's partial last wave of SM pairs run as K pieces on the idle pairs and are
+    added in piece order before the epilogue. Ragged tiles in M and N, ragged K per piece, and
+    every epilogue (bias + GeLU, fused or grouped shard sum, overlapped sum, GeLU', plain fp32):
+    matches the oracle, matches the unsplit kernel (TPMLP_TAIL_SPLIT=0) to fp32 rounding, and
+    repeats bit for bit."""
+    import torch
+
+    w = SMALL.with_shape(tokens=1040, hidden=1032, ffn=2 * 520, tp_degree=2)
+    outs = {}
+    for split in ("1", "0"):
+        monkeypatch.setenv("TPMLP_TAIL_SPLIT", split)
+        case = MlpCase(w, reduce).run()
+        outs[split] = case.outputs()
+        if split == "1":
+            errs = compare_full(outs[split], *full_reference(case))
+            assert max(errs.values()) <= TOL_BF16, errs
+            Z1, dA1 = case.Z.clone(), [x.clone() for x in case.dA]
+            case.run()
+            assert torch.equal(Z1, case.Z) and all(torch.equal(a, b) for a, b in zip(dA1, case.dA))
+    a, b = outs["1"], outs["0"]
+    for k in ("Z", "dX", "db"):
+        assert rel(a[k], b[k]) <= TOL_SHARDED_VS_UNSHARDED, k
+    for k in ("dA", "dB", "da"):
+        assert rel_shards(a[k], b[k]) <= TOL_SHARDED_VS_UNSHARDED, k
+    for k in ("H", "Y"):
+        assert rel_shards(a[k], b[k]) <= 1e-2, k
+
+
 # ----------------------------------------------------------------------------- invariants
 def test_sharded_matches_unsharded(tp):
     T, H, F = 384, 256, 1024
