@@ -144,29 +144,57 @@ __device__ __forceinline__ bool tail_last_arrival(int* counter, int pieces) {
   return last != 0;
 }
 
-// The completing warp: lane l adds row lrow0 + l of every piece in piece order (L2 reads, 32
-// columns at a time) and runs the tile's epilogue on the sums, as for an unsplit tile.
+// The completing warp adds its 32 rows of every piece in piece order, 32 columns at a time, and
+// runs the tile's epilogue on the sums as for an unsplit tile. Reads are coalesced (each
+// instruction covers 4 rows x 128 bytes) and two pieces' loads are in flight at once; the
+// 32 x 32 sum is turned into one row per lane through the warp's staging buffer.
 __device__ __forceinline__ void tail_fixup_rows(const TcParams& p, int g, int row0, int colbase,
                                                 const float* tile_ws, int lrow0, uint8_t* stage) {
   const int lane = threadIdx.x & 31;
+  const int rr = lane >> 3, cc = lane & 7;  // row (of 4) and float4 column (of 8) per step
+  float4* s4 = reinterpret_cast<float4*>(stage);
   for (int c0 = 0; c0 < BN; c0 += 32) {
     const int col0 = colbase + c0;
     if (col0 >= p.N) break;  // uniform across the warp
-    float v[32];
+    float4 acc[8];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = 0.f;
-    const float* src = tile_ws + static_cast<long long>(lrow0 + lane) * BN + c0;
-    for (int pc = 0; pc < p.ksplit; ++pc) {
-      const float* sp = src + static_cast<long long>(pc) * PIECE_FLOATS;
+    for (int it = 0; it < 8; ++it) acc[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float* src = tile_ws + static_cast<long long>(lrow0 + rr) * BN + c0 + 4 * cc;
+    int pc = 0;
+    for (; pc + 2 <= p.ksplit; pc += 2) {
+      float4 x0[8], x1[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float4 x = tc::ld_cg_f4(sp + 4 * j);
-        v[4 * j] += x.x;
-        v[4 * j + 1] += x.y;
-        v[4 * j + 2] += x.z;
-        v[4 * j + 3] += x.w;
+      for (int it = 0; it < 8; ++it) {
+        x0[it] = tc::ld_cg_f4(src + static_cast<long long>(pc) * PIECE_FLOATS + 4 * it * BN);
+        x1[it] = tc::ld_cg_f4(src + static_cast<long long>(pc + 1) * PIECE_FLOATS + 4 * it * BN);
+      }
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        acc[it].x += x0[it].x; acc[it].y += x0[it].y; acc[it].z += x0[it].z; acc[it].w += x0[it].w;
+        acc[it].x += x1[it].x; acc[it].y += x1[it].y; acc[it].z += x1[it].z; acc[it].w += x1[it].w;
       }
     }
+    for (; pc < p.ksplit; ++pc) {
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const float4 x = tc::ld_cg_f4(src + static_cast<long long>(pc) * PIECE_FLOATS + 4 * it * BN);
+        acc[it].x += x.x; acc[it].y += x.y; acc[it].z += x.z; acc[it].w += x.w;
+      }
+    }
+    // element (row 4*it + rr, columns 4*cc..) -> the swizzled slot warp_store_f32 uses
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int r = 4 * it + rr;
+      s4[r * 8 + (cc ^ (r & 7))] = acc[it];
+    }
+    __syncwarp();
+    float v[32];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 x = s4[lane * 8 + (q ^ (lane & 7))];
+      v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+    }
+    __syncwarp();
     tc::epilogue_chunk(p, g, row0, col0, v, stage);
   }
 }

@@ -131,7 +131,8 @@ bool tail_split_enabled() {
   return true;
 }
 
-constexpr int kMinPieceKb = 8;  // K blocks of 64 a piece keeps at least
+constexpr int kMinPieceKb = 16;  // K blocks of 64 a piece keeps at least
+constexpr int kMaxSplitWaves = 8;  // deeper queues: the partly idle last wave matters little
 
 // Work units of an SM-pair launch over `clusters` pairs. Tiles are dealt to the pairs round
 // robin, so the last wave holds L = num_tiles mod clusters tiles (all of them when there are
@@ -144,6 +145,7 @@ void plan_tail(tc::TcParams& p, int clusters, int total_kb, bool have_ws) {
   p.ksplit = 1;
   p.num_units = p.num_tiles;
   if (!have_ws || !tail_split_enabled() || clusters < 2) return;
+  if (p.num_tiles > kMaxSplitWaves * clusters) return;
   const int L = p.num_tiles % clusters;
   if (L == 0) return;
   int S = clusters / L;
