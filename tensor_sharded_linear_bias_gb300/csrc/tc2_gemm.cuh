@@ -11,7 +11,7 @@
 //             both CTAs' TMA loads complete their bytes on it (.cta_group::2 loads).
 //   empty[s]  in both CTAs: the leader's MMA commit arrives on both (multicast).
 //   tfull[a]  in both CTAs: the leader's commit after a tile's last MMA (multicast).
-//   tempty[a] leader only: the 4 epilogue warps of both CTAs arrive (count 8).
+//   tempty[a] leader only: the 8 epilogue warps of both CTAs arrive (count 16).
 // TMEM (all 512 columns, two 256-column accumulators) is allocated and freed by warp 1 of
 // both CTAs together (cta_group::2). Cluster barriers after set-up and before the end keep
 // either CTA from touching the other's shared memory before it is ready or after it is gone.
@@ -38,8 +38,12 @@ constexpr int A_BYTES = HALF * BK * 2;       // 16 KiB
 constexpr int B_BYTES = HALF * BK * 2;       // 16 KiB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int MN_BOX_BYTES = 64 * BK * 2;    // 8 KiB
-constexpr int NUM_THREADS = 192;
-constexpr int EPI_WARPS = 4;
+// Warp 0: TMA producer; warp 1: MMA issuer; warps 2..9: epilogue, two per TMEM lane quadrant
+// (a warp may only read the 32 TMEM lanes of quadrant warp % 4), each taking 128 of the tile's
+// 256 columns, so that epilogue-heavy tiles (GeLU, GeLU') keep up with short K loops.
+constexpr int NUM_THREADS = 320;
+constexpr int EPI_WARPS = 8;
+constexpr int EPI_COLS = BN / 2;
 constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_WARPS * tc::STAGE_WARP_BYTES + 1024 + 256;
 
@@ -118,15 +122,17 @@ __device__ __forceinline__ void umma_commit_pair_multicast(uint32_t bar, uint16_
 // ------------------------------------------------------------------ tail split
 // A piece's accumulator in the tail workspace: [piece][256 rows][256 columns] fp32 per tile.
 constexpr int PIECE_FLOATS = BM * BN;
+// one counter per (tile, CTA, column half, lane quadrant): the rows and columns of one warp
+constexpr int TAIL_COUNTERS_PER_TILE = 2 * (BN / EPI_COLS) * 4;
 
-// One warp stores its 32 accumulator rows (tile-local rows lrow0..lrow0+31, all 256 columns) of
-// a piece, through its staging buffer (coalesced rows).
-__device__ __forceinline__ void store_piece_rows(float* piece_ws, int lrow0, uint32_t trow,
-                                                 uint8_t* stage) {
-  for (int c0 = 0; c0 < BN; c0 += 32) {
+// One warp stores its 32 accumulator rows (tile-local rows lrow0..lrow0+31) x EPI_COLS columns
+// (from tile column cofs; trow addresses that column) of a piece, through its staging buffer.
+__device__ __forceinline__ void store_piece_rows(float* piece_ws, int lrow0, int cofs,
+                                                 uint32_t trow, uint8_t* stage) {
+  for (int c0 = 0; c0 < EPI_COLS; c0 += 32) {
     float v[32];
     tc::tmem_ld_32cols(trow + c0, v);
-    tc::warp_store_f32(stage, v, piece_ws, BN, lrow0, c0, BM, 32);
+    tc::warp_store_f32(stage, v, piece_ws, BN, lrow0, cofs + c0, BM, 32);
   }
 }
 
@@ -149,11 +155,12 @@ __device__ __forceinline__ bool tail_last_arrival(int* counter, int pieces) {
 // instruction covers 4 rows x 128 bytes) and two pieces' loads are in flight at once; the
 // 32 x 32 sum is turned into one row per lane through the warp's staging buffer.
 __device__ __forceinline__ void tail_fixup_rows(const TcParams& p, int g, int row0, int colbase,
-                                                const float* tile_ws, int lrow0, uint8_t* stage) {
+                                                const float* tile_ws, int lrow0, int cofs,
+                                                uint8_t* stage) {
   const int lane = threadIdx.x & 31;
   const int rr = lane >> 3, cc = lane & 7;  // row (of 4) and float4 column (of 8) per step
   float4* s4 = reinterpret_cast<float4*>(stage);
-  for (int c0 = 0; c0 < BN; c0 += 32) {
+  for (int c0 = cofs; c0 < cofs + EPI_COLS; c0 += 32) {
     const int col0 = colbase + c0;
     if (col0 >= p.N) break;  // uniform across the warp
     float4 acc[8];
@@ -357,8 +364,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_c
       }
     }
   } else {
-    // -------------------------------------------------------------- epilogue warps 2..5
+    // -------------------------------------------------------------- epilogue warps 2..9
     const int quad = warp & 3;
+    const int cofs = ((warp - 2) >> 2) * EPI_COLS;  // this warp's columns of the tile
     uint32_t acc = 0, acc_phase = 0;
     // With the GeLU' epilogue, each tile's pre-activation rows are requested into L2 one tile
     // ahead (the first tile's here), while the tile before it is being finished.
@@ -369,7 +377,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_c
       int t1, a0, a1, pc1, g1, mb1, nb1;
       tc::decode_unit(p, u, total_kb_e, t1, a0, a1, pc1);
       tc::decode_tile(p, t1, g1, mb1, nb1);
-      tc::prefetch_aux_rows(p, g1, mb1 * BM + my_rows, nb1 * BN, BN);
+      tc::prefetch_aux_rows(p, g1, mb1 * BM + my_rows, nb1 * BN + cofs, EPI_COLS);
     };
     if (aux_ahead && cluster < p.num_units) prefetch_unit(cluster);
     for (int u = cluster; u < p.num_units; u += nclusters) {
@@ -386,27 +394,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_c
       if (*abort_flag) break;
       tc::tc_fence_after();
       const int row0 = mb * BM + static_cast<int>(rank) * HALF + quad * 32;
-      const uint32_t trow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+      const uint32_t trow =
+          tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + static_cast<uint32_t>(cofs);
       uint8_t* stg = epi_stage + (warp - 2) * tc::STAGE_WARP_BYTES;
       if (piece < 0) {
-        tc::epilogue_rows<BN>(p, g, row0, nb * BN, trow, stg);
+        tc::epilogue_rows<EPI_COLS>(p, g, row0, nb * BN + cofs, trow, stg);
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
-        if (p.epi == EPI_PARTIAL_REDUCE) tc::partial_reduce_rows(p, row0, nb);
+        if (p.epi == EPI_PARTIAL_REDUCE) tc::partial_reduce_rows(p, row0, nb, BN / EPI_COLS);
       } else {
         // one piece of a split tile: park the accumulator rows, free TMEM, and finish the
         // tile's rows if this warp completes their count
         const int split_tile = t - p.full_tiles;
         float* tile_ws = p.tail_ws + static_cast<long long>(split_tile) * p.ksplit * PIECE_FLOATS;
-        store_piece_rows(tile_ws + static_cast<long long>(piece) * PIECE_FLOATS, my_rows, trow, stg);
+        store_piece_rows(tile_ws + static_cast<long long>(piece) * PIECE_FLOATS, my_rows, cofs, trow,
+                         stg);
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
-        int* counter = p.tail_counters + split_tile * 8 + static_cast<int>(rank) * 4 + quad;
+        int* counter = p.tail_counters + split_tile * TAIL_COUNTERS_PER_TILE +
+                       static_cast<int>(rank) * 8 + (cofs / EPI_COLS) * 4 + quad;
         if (tail_last_arrival(counter, p.ksplit)) {
-          tail_fixup_rows(p, g, row0, nb * BN, tile_ws, my_rows, stg);
-          if (p.epi == EPI_PARTIAL_REDUCE) tc::partial_reduce_rows(p, row0, nb);
+          tail_fixup_rows(p, g, row0, nb * BN, tile_ws, my_rows, cofs, stg);
+          if (p.epi == EPI_PARTIAL_REDUCE) tc::partial_reduce_rows(p, row0, nb, BN / EPI_COLS);
           __syncwarp();
           if (lane == 0) atomicExch(counter, 0);
         }

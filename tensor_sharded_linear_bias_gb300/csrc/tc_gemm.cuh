@@ -348,18 +348,20 @@ __device__ __forceinline__ float4 ld_cg_f4(const float* p) {
 }
 
 // The shard sum overlapped with the GEMM (EPI_PARTIAL_REDUCE), warp-wide, after the warp has
-// stored its 32 rows x 256 columns of partial og: the warp makes its stores visible and counts
+// stored its 32 rows of partial og (all 256 columns of the block, or its share of them when
+// warps_per_block warps split the columns): the warp makes its stores visible and counts
 // itself in for the block; the warp that completes the count (one per block, whichever
 // partial it computed) reads the nsplit partials of the block in partial order, adds the bias
 // and writes Z, then resets the counter for the next launch. No warp waits for another.
-__device__ __forceinline__ void partial_reduce_rows(const TcParams& p, int row0, int nb) {
+__device__ __forceinline__ void partial_reduce_rows(const TcParams& p, int row0, int nb,
+                                                   int warps_per_block = 1) {
   const int lane = threadIdx.x & 31;
   if (row0 >= p.M) return;  // no rows of this block exist (edge tile): nothing was stored
   __threadfence();
   __syncwarp();
   const int block = (row0 >> 5) * p.tiles_n_out + nb;
   int last = 0;
-  if (lane == 0) last = atomicAdd(p.counters + block, 1) == p.nsplit - 1;
+  if (lane == 0) last = atomicAdd(p.counters + block, 1) == p.nsplit * warps_per_block - 1;
   last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return;
   __threadfence();

@@ -262,7 +262,9 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
     if (p.ksplit > 1) {
       p.tail_ws = s.tail_ws;
       p.tail_counters = s.tail_counters;
-      const size_t counters = size_t(p.num_tiles - p.full_tiles) * 8 * sizeof(int);
+      const size_t counters =
+          size_t(p.num_tiles - p.full_tiles) * tc2::TAIL_COUNTERS_PER_TILE * sizeof(int);
+      if (counters > kTailCounterBytes) return cudaErrorInvalidValue;
       cudaError_t e = cudaMemsetAsync(s.tail_counters, 0, counters, st);
       if (e != cudaSuccess) return e;
     }
