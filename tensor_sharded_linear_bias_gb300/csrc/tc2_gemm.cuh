@@ -38,14 +38,19 @@ constexpr int A_BYTES = HALF * BK * 2;       // 16 KiB
 constexpr int B_BYTES = HALF * BK * 2;       // 16 KiB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int MN_BOX_BYTES = 64 * BK * 2;    // 8 KiB
-// Warp 0: TMA producer; warp 1: MMA issuer; warps 2..9: epilogue, two per TMEM lane quadrant
-// (a warp may only read the 32 TMEM lanes of quadrant warp % 4), each taking 128 of the tile's
-// 256 columns, so that epilogue-heavy tiles (GeLU, GeLU') keep up with short K loops.
-constexpr int NUM_THREADS = 320;
-constexpr int EPI_WARPS = 8;
-constexpr int EPI_COLS = BN / 2;
+// Warp 0: TMA producer; warp 1: MMA issuer; warps 2..: EPI_W epilogue warps. A warp may only
+// read the 32 TMEM lanes of quadrant warp % 4, so with 4 epilogue warps each takes all 256
+// columns of its 32 rows, and with 8 two warps share a quadrant and take 128 columns each
+// (for epilogue-heavy tiles, GeLU or GeLU', whose K loops are too short to hide 4 warps' work).
+template <int EPI_W>
+struct EpiShape {
+  static_assert(EPI_W == 4 || EPI_W == 8, "4 or 8 epilogue warps");
+  static constexpr int WARPS = EPI_W;
+  static constexpr int COLS = BN * 4 / EPI_W;  // columns per epilogue warp
+  static constexpr int THREADS = 64 + 32 * EPI_W;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_W * tc::STAGE_WARP_BYTES + 1024 + 256;
+};
 constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_WARPS * tc::STAGE_WARP_BYTES + 1024 + 256;
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -122,14 +127,15 @@ __device__ __forceinline__ void umma_commit_pair_multicast(uint32_t bar, uint16_
 // ------------------------------------------------------------------ tail split
 // A piece's accumulator in the tail workspace: [piece][256 rows][256 columns] fp32 per tile.
 constexpr int PIECE_FLOATS = BM * BN;
-// one counter per (tile, CTA, column half, lane quadrant): the rows and columns of one warp
-constexpr int TAIL_COUNTERS_PER_TILE = 2 * (BN / EPI_COLS) * 4;
+// one counter per (tile, CTA, column part, lane quadrant): the rows and columns of one warp
+constexpr int TAIL_COUNTERS_PER_TILE = 2 * 2 * 4;
 
-// One warp stores its 32 accumulator rows (tile-local rows lrow0..lrow0+31) x EPI_COLS columns
+// One warp stores its 32 accumulator rows (tile-local rows lrow0..lrow0+31) x COLS columns
 // (from tile column cofs; trow addresses that column) of a piece, through its staging buffer.
+template <int COLS>
 __device__ __forceinline__ void store_piece_rows(float* piece_ws, int lrow0, int cofs,
                                                  uint32_t trow, uint8_t* stage) {
-  for (int c0 = 0; c0 < EPI_COLS; c0 += 32) {
+  for (int c0 = 0; c0 < COLS; c0 += 32) {
     float v[32];
     tc::tmem_ld_32cols(trow + c0, v);
     tc::warp_store_f32(stage, v, piece_ws, BN, lrow0, cofs + c0, BM, 32);
@@ -154,13 +160,14 @@ __device__ __forceinline__ bool tail_last_arrival(int* counter, int pieces) {
 // runs the tile's epilogue on the sums as for an unsplit tile. Reads are coalesced (each
 // instruction covers 4 rows x 128 bytes) and two pieces' loads are in flight at once; the
 // 32 x 32 sum is turned into one row per lane through the warp's staging buffer.
+template <int COLS>
 __device__ __forceinline__ void tail_fixup_rows(const TcParams& p, int g, int row0, int colbase,
                                                 const float* tile_ws, int lrow0, int cofs,
                                                 uint8_t* stage) {
   const int lane = threadIdx.x & 31;
   const int rr = lane >> 3, cc = lane & 7;  // row (of 4) and float4 column (of 8) per step
   float4* s4 = reinterpret_cast<float4*>(stage);
-  for (int c0 = cofs; c0 < cofs + EPI_COLS; c0 += 32) {
+  for (int c0 = cofs; c0 < cofs + COLS; c0 += 32) {
     const int col0 = colbase + c0;
     if (col0 >= p.N) break;  // uniform across the warp
     float4 acc[8];
@@ -206,13 +213,15 @@ __device__ __forceinline__ void tail_fixup_rows(const TcParams& p, int g, int ro
   }
 }
 
-template <bool A_MN, bool B_MN>
-__global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_constant__ TcParams p) {
+template <bool A_MN, bool B_MN, int EPI_W>
+__global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
+    tc2_gemm_kernel(const __grid_constant__ TcParams p) {
+  using E = EpiShape<EPI_W>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* epi_stage = smem + STAGES * STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + EPI_WARPS * tc::STAGE_WARP_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + E::WARPS * tc::STAGE_WARP_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -237,7 +246,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_c
     }
     for (int a = 0; a < ACC_BUFS; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 2 * EPI_WARPS);
+      mbar_init(tempty_bar(a), 2 * E::WARPS);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -364,9 +373,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_c
       }
     }
   } else {
-    // -------------------------------------------------------------- epilogue warps 2..9
+    // -------------------------------------------------------------- epilogue warps 2..
     const int quad = warp & 3;
-    const int cofs = ((warp - 2) >> 2) * EPI_COLS;  // this warp's columns of the tile
+    const int cofs = ((warp - 2) >> 2) * E::COLS;  // this warp's columns of the tile
     uint32_t acc = 0, acc_phase = 0;
     // With the GeLU' epilogue, each tile's pre-activation rows are requested into L2 one tile
     // ahead (the first tile's here), while the tile before it is being finished.
@@ -377,7 +386,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_c
       int t1, a0, a1, pc1, g1, mb1, nb1;
       tc::decode_unit(p, u, total_kb_e, t1, a0, a1, pc1);
       tc::decode_tile(p, t1, g1, mb1, nb1);
-      tc::prefetch_aux_rows(p, g1, mb1 * BM + my_rows, nb1 * BN + cofs, EPI_COLS);
+      tc::prefetch_aux_rows(p, g1, mb1 * BM + my_rows, nb1 * BN + cofs, E::COLS);
     };
     if (aux_ahead && cluster < p.num_units) prefetch_unit(cluster);
     for (int u = cluster; u < p.num_units; u += nclusters) {
@@ -398,26 +407,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_c
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + static_cast<uint32_t>(cofs);
       uint8_t* stg = epi_stage + (warp - 2) * tc::STAGE_WARP_BYTES;
       if (piece < 0) {
-        tc::epilogue_rows<EPI_COLS>(p, g, row0, nb * BN + cofs, trow, stg);
+        tc::epilogue_rows<E::COLS>(p, g, row0, nb * BN + cofs, trow, stg);
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
-        if (p.epi == EPI_PARTIAL_REDUCE) tc::partial_reduce_rows(p, row0, nb, BN / EPI_COLS);
+        if (p.epi == EPI_PARTIAL_REDUCE) tc::partial_reduce_rows(p, row0, nb, BN / E::COLS);
       } else {
         // one piece of a split tile: park the accumulator rows, free TMEM, and finish the
         // tile's rows if this warp completes their count
         const int split_tile = t - p.full_tiles;
         float* tile_ws = p.tail_ws + static_cast<long long>(split_tile) * p.ksplit * PIECE_FLOATS;
-        store_piece_rows(tile_ws + static_cast<long long>(piece) * PIECE_FLOATS, my_rows, cofs, trow,
-                         stg);
+        store_piece_rows<E::COLS>(tile_ws + static_cast<long long>(piece) * PIECE_FLOATS, my_rows,
+                                  cofs, trow, stg);
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
         int* counter = p.tail_counters + split_tile * TAIL_COUNTERS_PER_TILE +
-                       static_cast<int>(rank) * 8 + (cofs / EPI_COLS) * 4 + quad;
+                       static_cast<int>(rank) * 8 + (cofs / E::COLS) * 4 + quad;
         if (tail_last_arrival(counter, p.ksplit)) {
-          tail_fixup_rows(p, g, row0, nb * BN, tile_ws, my_rows, cofs, stg);
-          if (p.epi == EPI_PARTIAL_REDUCE) tc::partial_reduce_rows(p, row0, nb, BN / EPI_COLS);
+          tail_fixup_rows<E::COLS>(p, g, row0, nb * BN, tile_ws, my_rows, cofs, stg);
+          if (p.epi == EPI_PARTIAL_REDUCE) tc::partial_reduce_rows(p, row0, nb, BN / E::COLS);
           __syncwarp();
           if (lane == 0) atomicExch(counter, 0);
         }
@@ -435,6 +444,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc2_gemm_kernel(const __grid_c
                  "r"(TMEM_COLS)
                  : "memory");
   }
+}
+
+// Launch on clusters of two CTAs; max_clusters != nullptr asks for the occupancy limit only.
+template <bool A_MN, bool B_MN, int EPI_W>
+cudaError_t launch_pair(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters) {
+  using E = EpiShape<EPI_W>;
+  auto kern = tc2_gemm_kernel<A_MN, B_MN, EPI_W>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, E::SMEM);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(E::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = E::SMEM;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_clusters != nullptr) {
+    cfg.gridDim = dim3(2, 1, 1);
+    return cudaOccupancyMaxActiveClusters(max_clusters, kern, &cfg);
+  }
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 }  // namespace tc2

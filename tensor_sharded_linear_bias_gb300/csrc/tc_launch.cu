@@ -16,9 +16,12 @@ namespace tc {
 cudaError_t run_kmn(const TcParams& p, int grid, cudaStream_t st);
 cudaError_t run_kk(const TcParams& p, int grid, cudaStream_t st);
 cudaError_t run_mnmn(const TcParams& p, int grid, cudaStream_t st);
-cudaError_t run_pair_kmn(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters);
-cudaError_t run_pair_kk(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters);
-cudaError_t run_pair_mnmn(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters);
+cudaError_t run_pair_kmn(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters,
+                         int epi_warps);
+cudaError_t run_pair_kk(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters,
+                        int epi_warps);
+cudaError_t run_pair_mnmn(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters,
+                          int epi_warps);
 }  // namespace tc
 
 namespace {
@@ -63,24 +66,39 @@ bool use_pair_kernel(int64_t M) {
   return M > tc::BM;
 }
 
-// Largest number of co-resident 2-CTA clusters of the pair kernel (cached per device and
-// operand layout); falls back to half the SM count.
-int pair_clusters(int layout) {
-  static int cached[64][3] = {};
+cudaError_t run_pair(int layout, const tc::TcParams& p, int clusters, cudaStream_t st,
+                     int* max_clusters, int epi_warps) {
+  if (layout == 0) return tc::run_pair_kmn(p, clusters, st, max_clusters, epi_warps);
+  if (layout == 1) return tc::run_pair_kk(p, clusters, st, max_clusters, epi_warps);
+  return tc::run_pair_mnmn(p, clusters, st, max_clusters, epi_warps);
+}
+
+// Largest number of co-resident 2-CTA clusters of the pair kernel (cached per device, operand
+// layout and epilogue warp count); falls back to half the SM count.
+int pair_clusters(int layout, int epi_warps = 4) {
+  static int cached[64][3][2] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return device_sm_count() / 2;
-  if (cached[dev][layout] == 0) {
+  const int v = epi_warps == 8 ? 1 : 0;
+  if (cached[dev][layout][v] == 0) {
     int n = 0;
-    cudaError_t e = layout == 0   ? tc::run_pair_kmn(tc::TcParams{}, 0, nullptr, &n)
-                    : layout == 1 ? tc::run_pair_kk(tc::TcParams{}, 0, nullptr, &n)
-                                  : tc::run_pair_mnmn(tc::TcParams{}, 0, nullptr, &n);
+    cudaError_t e = run_pair(layout, tc::TcParams{}, 0, nullptr, &n, epi_warps);
     if (e != cudaSuccess || n <= 0) {
       cudaGetLastError();
       n = device_sm_count() / 2;
     }
-    cached[dev][layout] = n;
+    cached[dev][layout][v] = n;
   }
-  return cached[dev][layout];
+  return cached[dev][layout][v];
+}
+
+// Epilogue warps of the pair kernel: 8 when the tile's epilogue is heavy (GeLU or GeLU') and its
+// K loop short (at most 64 blocks of 64), where 4 warps' epilogue outlasts the next tile's main
+// loop; else 4. TPMLP_EPI_WARPS=4/8 forces the count.
+int pair_epi_warps(int epi, int act, int total_kb) {
+  if (const char* env = std::getenv("TPMLP_EPI_WARPS")) return std::atoi(env) == 8 ? 8 : 4;
+  const bool heavy = (epi == EPI_BIAS_ACT || epi == EPI_DACT) && act == TP_ACT_GELU_ERF;
+  return heavy && total_kb <= 64 ? 8 : 4;
 }
 
 // Tile order of a launch. The tiles running at the same time (one per SM, or per SM pair)
@@ -257,7 +275,8 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
   p.ksplit = 1;
   p.num_units = p.num_tiles;
   if (pair) {
-    const int max_clusters = pair_clusters(layout);
+    const int epi_warps = pair_epi_warps(p.epi, p.act, p.kblocks * p.kpo);
+    const int max_clusters = pair_clusters(layout, epi_warps);
     plan_tail(p, max_clusters, p.kblocks * p.kpo, s.tail_ws != nullptr && s.tail_counters != nullptr);
     if (p.ksplit > 1) {
       p.tail_ws = s.tail_ws;
@@ -269,9 +288,7 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
       if (e != cudaSuccess) return e;
     }
     const int clusters = std::min(p.num_units, max_clusters);
-    if (layout == 0) return run_pair_kmn(p, clusters, st, nullptr);
-    if (layout == 1) return run_pair_kk(p, clusters, st, nullptr);
-    return run_pair_mnmn(p, clusters, st, nullptr);
+    return run_pair(layout, p, clusters, st, nullptr, epi_warps);
   }
   const int grid = std::min(p.num_tiles, device_sm_count());
   if (!s.a_mn && s.b_mn) return run_kmn(p, grid, st);

@@ -165,6 +165,20 @@ def test_bias_grads_many_tokens(tp, dtype):
     assert max(errs.values()) <= tol, errs
 
 
+@pytest.mark.parametrize("epi_warps", ["4", "8"])
+@pytest.mark.parametrize("T,H,F,n", [(300, 264, 2 * 392, 2), (520, 136, 4 * 136, 4)])
+def test_epilogue_warps(tp, monkeypatch, epi_warps, T, H, F, n):
+    """The SM-pair kernel with 4 epilogue warps (each on all 256 columns of its 32 rows) or 8
+    (two per TMEM lane quadrant, 128 columns each), every epilogue and reduce mode, ragged
+    tiles: matches the oracle."""
+    monkeypatch.setenv("TPMLP_EPI_WARPS", epi_warps)
+    monkeypatch.setenv("TPMLP_GEMM_PAIR", "1")
+    for reduce in (0, 2, 4):
+        case = MlpCase(SMALL.with_shape(tokens=T, hidden=H, ffn=F, tp_degree=n), reduce).run()
+        errs = compare_full(case.outputs(), *full_reference(case))
+        assert max(errs.values()) <= TOL_BF16, (reduce, errs)
+
+
 _TAIL_REF = {}
 
 
