@@ -92,13 +92,16 @@ int pair_clusters(int layout, int epi_warps = 4) {
   return cached[dev][layout][v];
 }
 
-// Epilogue warps of the pair kernel: 8 when the tile's epilogue is heavy (GeLU or GeLU') and its
-// K loop short (at most 64 blocks of 64), where 4 warps' epilogue outlasts the next tile's main
-// loop; else 4. TPMLP_EPI_WARPS=4/8 forces the count.
+// Epilogue warps of the pair kernel: 8 where 4 warps' epilogue of a tile would outlast the next
+// tile's main loop: GeLU or GeLU' tiles with at most 64 K blocks of 64, any tile with at most
+// 16; else 4, which is faster for deep tiles (measured on GB300, same box: the GPT-3-shaped
+// step 1494 vs 1484 TFLOP/s with 4; the 4096 x 1024 x 4096 step 753 vs 710 with 8 on its
+// GeLU / GeLU' GEMMs; weight gradients over 512 tokens 0.253 vs 0.265 ms with 8).
+// TPMLP_EPI_WARPS=4/8 forces the count.
 int pair_epi_warps(int epi, int act, int total_kb) {
   if (const char* env = std::getenv("TPMLP_EPI_WARPS")) return std::atoi(env) == 8 ? 8 : 4;
   const bool heavy = (epi == EPI_BIAS_ACT || epi == EPI_DACT) && act == TP_ACT_GELU_ERF;
-  return heavy && total_kb <= 64 ? 8 : 4;
+  return (heavy && total_kb <= 64) || total_kb <= 16 ? 8 : 4;
 }
 
 // Tile order of a launch. The tiles running at the same time (one per SM, or per SM pair)
