@@ -17,8 +17,10 @@
 namespace tpk {
 namespace {
 
-constexpr int TM = 64, TN = 64, TK = 32;
-constexpr int LOADS = TM * TK / 256;  // elements of A (and of B) each thread stages per K step
+// Tiles of TM x 64 outputs (TM = 64, or 32 when the product has at most 32 rows), K steps of 32.
+// 256 threads: thread (ty, tx) owns rows RM*ty .. RM*ty+RM-1 (RM = TM/16) and columns
+// 4tx .. 4tx+3, so each K element costs one vector shared load of A, one of B and 4*RM FFMAs.
+constexpr int TN = 64, TK = 32;
 constexpr long long kMinSplitSteps = 4;    // K steps (of TK) a split slice keeps at least
 constexpr long long kMaxSplitSlices = 64;
 
@@ -53,19 +55,44 @@ __device__ __forceinline__ void epilogue(const SimtParams& p, int og, long long 
   }
 }
 
+template <int RM>
+struct RowVec;
+template <>
+struct RowVec<2> {
+  __device__ static void load(const float* p, float* a) {
+    const float2 v = *reinterpret_cast<const float2*>(p);
+    a[0] = v.x;
+    a[1] = v.y;
+  }
+};
+template <>
+struct RowVec<4> {
+  __device__ static void load(const float* p, float* a) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    a[0] = v.x;
+    a[1] = v.y;
+    a[2] = v.z;
+    a[3] = v.w;
+  }
+};
+
 // Two shared-memory buffers and a register prefetch: while the block multiplies the K step in
 // one buffer, the loads of the next step are in flight, so the K loop is not a chain of
 // load-latency-bound steps.
+template <int TM>
 __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ SimtParams p) {
-  __shared__ float As[2][TK][TM + 4];
-  __shared__ float Bs[2][TK][TN + 4];
+  constexpr int RM = TM / 16;
+  constexpr int LOADS_A = TM * TK / 256;  // elements of A each thread stages per K step
+  constexpr int LOADS_B = TK * TN / 256;  // elements of B
+  __shared__ __align__(16) float As[2][TK][TM + 4];
+  __shared__ __align__(16) float Bs[2][TK][TN + 4];
   const int zg = p.ksum ? 1 : p.groups;  // outputs
   const int g = static_cast<int>(blockIdx.z % zg);
   const int slice = static_cast<int>(blockIdx.z / zg);
   const long long m0 = static_cast<long long>(blockIdx.y) * TM;
   const long long n0 = static_cast<long long>(blockIdx.x) * TN;
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-  float acc[4][4] = {};
+  float acc[RM][4] = {};
 
   const int kgroups = p.ksum ? p.groups : 1;
   const long long ksteps = (p.K + TK - 1) / TK;
@@ -73,7 +100,7 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ 
   // this CTA's contiguous range of K steps (all of them without a split)
   const long long s_begin = all_steps * slice / p.slices;
   const long long s_end = all_steps * (slice + 1) / p.slices;
-  float ra[LOADS], rb[LOADS];
+  float ra[LOADS_A], rb[LOADS_B];
 
   // element e of a step's A tile -> (mm, kk); coalesced along whichever of m, k is contiguous
   auto a_coord = [&](int e, int& mm, int& kk) {
@@ -88,27 +115,31 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ 
     const float* A = p.A[p.ksum ? kg : g];
     const float* B = p.B[p.ksum ? kg : g];
 #pragma unroll
-    for (int j = 0; j < LOADS; ++j) {
-      const int e = threadIdx.x + 256 * j;
+    for (int j = 0; j < LOADS_A; ++j) {
       int mm, kk;
-      a_coord(e, mm, kk);
+      a_coord(threadIdx.x + 256 * j, mm, kk);
       const long long m = m0 + mm, k = k0 + kk;
       ra[j] = (m < p.M && k < p.K) ? A[m * p.sam + k * p.sak] : 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < LOADS_B; ++j) {
       int nn, kb;
-      b_coord(e, nn, kb);
+      b_coord(threadIdx.x + 256 * j, nn, kb);
       const long long n = n0 + nn, k2 = k0 + kb;
       rb[j] = (n < p.N && k2 < p.K) ? B[k2 * p.sbk + n * p.sbn] : 0.0f;
     }
   };
   auto stash = [&](int buf) {
 #pragma unroll
-    for (int j = 0; j < LOADS; ++j) {
-      const int e = threadIdx.x + 256 * j;
+    for (int j = 0; j < LOADS_A; ++j) {
       int mm, kk;
-      a_coord(e, mm, kk);
+      a_coord(threadIdx.x + 256 * j, mm, kk);
       As[buf][kk][mm] = ra[j];
+    }
+#pragma unroll
+    for (int j = 0; j < LOADS_B; ++j) {
       int nn, kb;
-      b_coord(e, nn, kb);
+      b_coord(threadIdx.x + 256 * j, nn, kb);
       Bs[buf][kb][nn] = rb[j];
     }
   };
@@ -123,13 +154,11 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ 
     if (step + 1 < s_end) load(step + 1);
 #pragma unroll
     for (int kk = 0; kk < TK; ++kk) {
-      float a[4], b[4];
+      float a[RM], b[4];
+      RowVec<RM>::load(&As[buf][kk][RM * ty], a);
+      RowVec<4>::load(&Bs[buf][kk][4 * tx], b);
 #pragma unroll
-      for (int r = 0; r < 4; ++r) a[r] = As[buf][kk][ty + 16 * r];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) b[c] = Bs[buf][kk][tx + 16 * c];
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
+      for (int r = 0; r < RM; ++r)
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
     }
@@ -140,12 +169,12 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ 
   const int og = p.ksum ? 0 : g;
   float* part = p.slices > 1 ? p.P + (static_cast<long long>(slice) * zg + og) * p.M * p.N : nullptr;
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const long long m = m0 + ty + 16 * r;
+  for (int r = 0; r < RM; ++r) {
+    const long long m = m0 + RM * ty + r;
     if (m >= p.M) continue;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const long long n = n0 + tx + 16 * c;
+      const long long n = n0 + 4 * tx + c;
       if (n >= p.N) continue;
       if (part != nullptr)
         part[m * p.N + n] = acc[r][c];
@@ -212,9 +241,14 @@ SimtParams make_params(const GemmSpec& s) {
 
 }  // namespace
 
+namespace {
+int tile_rows(int64_t M) { return M <= 32 ? 32 : 64; }
+}  // namespace
+
 int plan_simt_split(const GemmSpec& s, size_t scratch_bytes) {
   if (s.M <= 0 || s.N <= 0 || s.K <= 0) return 1;
   const long long outs = s.ksum ? 1 : s.groups;
+  const long long TM = tile_rows(s.M);
   const long long tiles = ((s.N + TN - 1) / TN) * ((s.M + TM - 1) / TM) * outs;
   const long long target = 2LL * device_sm_count();  // CTAs: two per SM
   if (tiles >= target) return 1;
@@ -233,10 +267,14 @@ cudaError_t launch_simt_gemm(const GemmSpec& s, cudaStream_t st) {
   if (s.kslices > 1 && s.split == nullptr) return cudaErrorInvalidValue;
   const SimtParams p = make_params(s);
   const unsigned zg = s.ksum ? 1u : static_cast<unsigned>(s.groups);
+  const int TM = tile_rows(s.M);
   const dim3 grid(static_cast<unsigned>((s.N + TN - 1) / TN),
                   static_cast<unsigned>((s.M + TM - 1) / TM), zg * static_cast<unsigned>(p.slices));
   if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidValue;
-  simt_gemm_kernel<<<grid, 256, 0, st>>>(p);
+  if (TM == 32)
+    simt_gemm_kernel<32><<<grid, 256, 0, st>>>(p);
+  else
+    simt_gemm_kernel<64><<<grid, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 
