@@ -39,15 +39,12 @@
  *    TP_F32: everything is fp32 and computed with fp32 FMA (no TF32); pointers 4-byte
  *    aligned, no other size rule.
  *  - The workspace (see the *_workspace_size calls) holds a device status word followed by
- *    scratch; call tp_workspace_init once after allocating it. TP_F32 calls reserve
- *    TP_F32_SPLIT_SCRATCH_BYTES of it, right after the status block, for the K-slice
- *    partial sums of their GEMMs: when a product has too few output tiles to fill the GPU
- *    (few tokens), its K range is cut into slices computed in parallel and the slices are
- *    added in slice order (deterministic) by a second kernel. TP_BF16 calls reserve
- *    TP_BF16_TAIL_SCRATCH_BYTES there instead: when a GEMM's tiles leave its last wave of SM
- *    pairs partly idle, each tile of that wave is computed as K pieces on otherwise idle
- *    pairs, and the pieces are added in piece order (deterministic) before the epilogue. A device-side wait that
+ *    scratch; call tp_workspace_init once after allocating it. A device-side wait that
  *    runs out writes an error code into the status word; tp_check_status reports it.
+ *    TP_BF16 calls reserve TP_BF16_TAIL_SCRATCH_BYTES of the workspace right after the
+ *    status block: when a GEMM's tiles leave its last wave of SM pairs partly idle, each tile
+ *    of that wave is computed as K pieces on otherwise idle pairs, and the pieces are added
+ *    in piece order (deterministic) before the epilogue.
  *  - Requires an sm_103 device (GB300); on any other device calls return TP_ERR_ARCH.
  */
 #ifndef TP_MLP_H
@@ -135,8 +132,6 @@ typedef struct tp_linear_desc {
 
 typedef enum tp_linear_kind { TP_COLUMN = 0, TP_ROW = 1 } tp_linear_kind;
 
-/* Workspace bytes that every TP_F32 call reserves after the 256-byte status block. */
-#define TP_F32_SPLIT_SCRATCH_BYTES ((size_t)320 * 64 * 64 * 4)
 /* Workspace bytes that every TP_BF16 call reserves after the 256-byte status block: up to 80
  * fp32 accumulator pieces of 256 x 256 for the GEMM's split last wave, and their counters. */
 #define TP_BF16_TAIL_SCRATCH_BYTES ((size_t)80 * 256 * 256 * 4 + 4096)
@@ -148,8 +143,7 @@ int32_t tp_version(void);
 const char* tp_last_error(void);
 
 /* Bytes of workspace that tp_mlp_forward and tp_mlp_backward need for *desc (the larger of
- * the two): a 256-byte status block, TP_F32_SPLIT_SCRATCH_BYTES for TP_F32 (or
- * TP_BF16_TAIL_SCRATCH_BYTES for TP_BF16), plus n fp32
+ * the two): a 256-byte status block, TP_BF16_TAIL_SCRATCH_BYTES for TP_BF16, plus n fp32
  * partials [T,H] in TP_REDUCE_PARTIALS mode, or the backward's per-shard gradients
  * dH_i [T,F/n] at the pre-activation. */
 tp_status tp_mlp_workspace_size(const tp_mlp_desc* desc, size_t* bytes);
@@ -252,8 +246,7 @@ typedef enum tp_kernel_kind {
   TP_K_COLSUM = 4,         /* bias gradients: column sums over tokens */
   TP_K_DACT = 5,           /* dH = dY * act'(H) */
   TP_K_SELFTEST = 6,
-  TP_K_SHARD_COPY = 7,     /* token-shard gather / scatter (sequence parallel) */
-  TP_K_SPLIT_SUM = 8       /* fp32: sum of a GEMM's K-slice partials + its epilogue */
+  TP_K_SHARD_COPY = 7      /* token-shard gather / scatter (sequence parallel) */
 } tp_kernel_kind;
 
 typedef enum tp_trace_tag {

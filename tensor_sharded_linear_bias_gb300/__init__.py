@@ -29,7 +29,6 @@ TP_F32, TP_BF16 = 0, 1
 TP_ACT_NONE, TP_ACT_GELU_ERF = 0, 1
 TP_REDUCE_FUSED, TP_REDUCE_PARTIALS, TP_REDUCE_AUTO, TP_REDUCE_PARTIALS_BF16, TP_REDUCE_OVERLAP = 0, 1, 2, 3, 4
 TP_COLUMN, TP_ROW = 0, 1
-TP_F32_SPLIT_SCRATCH_BYTES = 320 * 64 * 64 * 4
 TP_BF16_TAIL_SCRATCH_BYTES = 80 * 256 * 256 * 4 + 4096
 
 STATUS_NAMES = {
@@ -80,7 +79,7 @@ class TraceRecord(ctypes.Structure):
 
 
 KERNEL_NAMES = {1: "gemm_tc", 2: "gemm_ffma", 3: "shard_reduce", 4: "colsum", 5: "dact",
-                6: "selftest", 7: "shard_copy", 8: "split_sum"}
+                6: "selftest", 7: "shard_copy"}
 TAG_NAMES = {1: "column_fwd", 2: "row_fwd", 3: "row_dgrad", 4: "row_wgrad", 5: "column_wgrad",
              6: "column_dgrad", 7: "reduce", 8: "bias_grad", 9: "act_grad", 10: "other",
              11: "sp_gather", 12: "sp_scatter"}

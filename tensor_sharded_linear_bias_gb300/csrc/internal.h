@@ -12,12 +12,9 @@ namespace tpk {
 
 constexpr int kMaxShards = 64;
 
-// Workspace layout: a 256-byte status block, then scratch (256-byte aligned). fp32 calls
-// reserve kSplitBytes right after the status block for the K-slice partials of the FFMA GEMM
-// (320 tiles of 64 x 64 fp32: the most a split plan ever uses).
+// Workspace layout: a 256-byte status block, then scratch (256-byte aligned).
 constexpr size_t kStatusBytes = 256;
-constexpr size_t kSplitBytes = TP_F32_SPLIT_SCRATCH_BYTES;
-// bf16 calls reserve kTailBytes there instead: the fp32 pieces of the tensor-core GEMM's split
+// bf16 calls reserve kTailBytes right after the status block: the fp32 pieces of the tensor-core GEMM's split
 // tail tiles (at most kTailUnits pieces of 256 x 256 fp32), then one counter per (tile, 32-row
 // block) of the split tiles.
 constexpr int kTailUnits = 80;
@@ -64,8 +61,7 @@ struct GemmSpec {
   int64_t ldz = 0;
   const void* zbias = nullptr;
   int* status = nullptr;
-  int kslices = 1;         // FFMA GEMM: K steps split over this many CTAs per tile (1: none)
-  float* split = nullptr;  // ... their partial tiles, kslices x outputs x M x N fp32
+  int kslices = 1;  // FFMA GEMM: K steps split over a cluster of this many CTAs per tile (1: none)
   // tensor-core GEMM on SM pairs: scratch for split tail tiles (nullptr: never split)
   float* tail_ws = nullptr;
   int* tail_counters = nullptr;
@@ -73,13 +69,11 @@ struct GemmSpec {
 
 // bf16 inputs, tcgen05 tensor cores (sm_103a). Returns cudaSuccess or the launch error.
 cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st);
-// fp32 inputs, FFMA (no TF32). With kslices > 1 it writes raw partials to `split` and
-// launch_simt_split_sum finishes the product (sum in slice order + epilogue).
+// fp32 inputs, FFMA (no TF32); kslices > 1 splits every tile's K steps over a cluster.
 cudaError_t launch_simt_gemm(const GemmSpec& s, cudaStream_t st);
-cudaError_t launch_simt_split_sum(const GemmSpec& s, cudaStream_t st);
-// K slices for an FFMA GEMM whose tiles alone would leave SMs idle (1: no split); the
-// partials must fit in scratch_bytes.
-int plan_simt_split(const GemmSpec& s, size_t scratch_bytes);
+// K slices (cluster size, <= 8) for an FFMA GEMM whose tiles alone would leave SMs idle
+// (1: no split). TPMLP_SIMT_SPLIT=0 turns the split off.
+int plan_simt_split(const GemmSpec& s);
 
 // Z[T,N] = sum_{i<n} P[i][T,N] + bias (bias may be null; bias dtype: bf16 if bias_bf16).
 cudaError_t launch_shard_reduce(const float* P, int n, int64_t T, int64_t N,

@@ -2,27 +2,36 @@
 // fp32 accuracy. Same grouping (per-shard outputs or a shard-summed output) and epilogues as
 // the tensor-core GEMM, with fp32 everywhere.
 //
+// Tiles of TM x 64 outputs (TM = 64, or 32 when the product has at most 32 rows), K steps of
+// 32, a ring of STAGES shared-memory buffers filled by cp.async, so that several K steps' loads
+// are in flight while one is multiplied. 256 threads: thread (ty, tx) owns rows RM*ty ..
+// RM*ty+RM-1 (RM = TM/16) and columns 4tx .. 4tx+3; each K element costs one vector shared load
+// of A, one of B and 4*RM FFMAs.
+//
 // Split K: when the output tiles alone cannot fill the GPU (few tokens, as in the pages'
-// batch-32 example), the K steps of every tile (over all summed shards) are cut into
-// `slices` contiguous ranges, one CTA each. Each CTA writes its raw partial tile to scratch;
-// simt_split_sum_kernel then adds the slices in slice order (a fixed order: the result does
-// not depend on scheduling) and applies the epilogue.
+// batch-32 example), the K steps of every tile (over all summed shards) are cut into S <= 8
+// contiguous ranges computed by the S CTAs of one thread-block cluster. Each CTA parks its
+// partial tile in its shared memory; after a cluster barrier, CTA q adds rows q*TM/S ..
+// (q+1)*TM/S-1 of all S partial tiles in CTA order (distributed shared memory), applies the
+// epilogue and stores them. The order is fixed for a shape, so results repeat bit for bit;
+// no partial tile goes through global memory.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "device_common.cuh"
 #include "internal.h"
 
+namespace cg = cooperative_groups;
+
 namespace tpk {
 namespace {
 
-// Tiles of TM x 64 outputs (TM = 64, or 32 when the product has at most 32 rows), K steps of 32.
-// 256 threads: thread (ty, tx) owns rows RM*ty .. RM*ty+RM-1 (RM = TM/16) and columns
-// 4tx .. 4tx+3, so each K element costs one vector shared load of A, one of B and 4*RM FFMAs.
-constexpr int TN = 64, TK = 32;
-constexpr long long kMinSplitSteps = 4;    // K steps (of TK) a split slice keeps at least
-constexpr long long kMaxSplitSlices = 64;
+constexpr int TN = 64, TK = 32, STAGES = 4;
+constexpr long long kMinSplitSteps = 4;  // K steps (of TK) a split slice keeps at least
+constexpr int kMaxSplit = 8;             // CTAs of a portable cluster
 
 struct SimtParams {
   const float* A[kMaxShards];
@@ -35,8 +44,7 @@ struct SimtParams {
   long long ldd, ldd2, ldaux;
   long long M, N, K;
   int groups, ksum, epi, act;
-  float* P;    // split K: partial tiles [slices][outs][M][N]
-  int slices;  // 1: no split
+  int slices;  // CTAs (one cluster) per output tile; 1: no split
 };
 
 // The epilogue of output element (m, n) of output og, given its accumulated value v.
@@ -53,6 +61,23 @@ __device__ __forceinline__ void epilogue(const SimtParams& p, int og, long long 
     if (p.act == TP_ACT_GELU_ERF) v *= gelu_erf_grad(p.aux[og][m * p.ldaux + n]);
     p.D[og][m * p.ldd + n] = v;
   }
+}
+
+// 4-byte asynchronous copy global -> shared; with pred false nothing is read (src-size 0) and
+// the 4 bytes are zero-filled (src must still be a valid address: the operand's base).
+__device__ __forceinline__ void cp_async4(float* dst, const float* src, bool pred) {
+  const uint32_t d = smem_addr(dst);
+  const int bytes = pred ? 4 : 0;
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(d),
+               "l"(__cvta_generic_to_global(src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 template <int RM>
@@ -76,19 +101,22 @@ struct RowVec<4> {
   }
 };
 
-// Two shared-memory buffers and a register prefetch: while the block multiplies the K step in
-// one buffer, the loads of the next step are in flight, so the K loop is not a chain of
-// load-latency-bound steps.
+template <int TM>
+struct SimtSmem {
+  float A[STAGES][TK][TM + 4];  // [k][m]: rows of 16-byte multiples for the vector reads
+  float B[STAGES][TK][TN + 4];  // [k][n]
+};
+
 template <int TM>
 __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ SimtParams p) {
   constexpr int RM = TM / 16;
-  constexpr int LOADS_A = TM * TK / 256;  // elements of A each thread stages per K step
+  constexpr int LOADS_A = TM * TK / 256;  // elements of A each thread copies per K step
   constexpr int LOADS_B = TK * TN / 256;  // elements of B
-  __shared__ __align__(16) float As[2][TK][TM + 4];
-  __shared__ __align__(16) float Bs[2][TK][TN + 4];
-  const int zg = p.ksum ? 1 : p.groups;  // outputs
-  const int g = static_cast<int>(blockIdx.z % zg);
-  const int slice = static_cast<int>(blockIdx.z / zg);
+  extern __shared__ __align__(16) unsigned char simt_smem_raw[];
+  SimtSmem<TM>& sm = *reinterpret_cast<SimtSmem<TM>*>(simt_smem_raw);
+  const int S = p.slices;
+  const int g = static_cast<int>(blockIdx.z) / S;      // output (or group)
+  const int slice = static_cast<int>(blockIdx.z) % S;  // = rank in the cluster when S > 1
   const long long m0 = static_cast<long long>(blockIdx.y) * TM;
   const long long n0 = static_cast<long long>(blockIdx.x) * TN;
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
@@ -97,19 +125,18 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ 
   const int kgroups = p.ksum ? p.groups : 1;
   const long long ksteps = (p.K + TK - 1) / TK;
   const long long all_steps = ksteps * kgroups;
-  // this CTA's contiguous range of K steps (all of them without a split)
-  const long long s_begin = all_steps * slice / p.slices;
-  const long long s_end = all_steps * (slice + 1) / p.slices;
-  float ra[LOADS_A], rb[LOADS_B];
+  const long long s_begin = all_steps * slice / S;
+  const long long s_end = all_steps * (slice + 1) / S;
 
-  // element e of a step's A tile -> (mm, kk); coalesced along whichever of m, k is contiguous
+  // element e of a step's tile -> coordinates; consecutive threads follow whichever of the two
+  // coordinates is contiguous in global memory (coalesced)
   auto a_coord = [&](int e, int& mm, int& kk) {
     if (p.sak == 1) { kk = e % TK; mm = e / TK; } else { mm = e % TM; kk = e / TM; }
   };
   auto b_coord = [&](int e, int& nn, int& kk) {
     if (p.sbk == 1) { kk = e % TK; nn = e / TK; } else { nn = e % TN; kk = e / TN; }
   };
-  auto load = [&](long long step) {
+  auto issue = [&](long long step, int buf) {
     const int kg = static_cast<int>(step / ksteps);
     const long long k0 = (step % ksteps) * TK;
     const float* A = p.A[p.ksum ? kg : g];
@@ -119,96 +146,83 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ 
       int mm, kk;
       a_coord(threadIdx.x + 256 * j, mm, kk);
       const long long m = m0 + mm, k = k0 + kk;
-      ra[j] = (m < p.M && k < p.K) ? A[m * p.sam + k * p.sak] : 0.0f;
+      const bool in = m < p.M && k < p.K;
+      cp_async4(&sm.A[buf][kk][mm], in ? A + m * p.sam + k * p.sak : A, in);
     }
 #pragma unroll
     for (int j = 0; j < LOADS_B; ++j) {
-      int nn, kb;
-      b_coord(threadIdx.x + 256 * j, nn, kb);
-      const long long n = n0 + nn, k2 = k0 + kb;
-      rb[j] = (n < p.N && k2 < p.K) ? B[k2 * p.sbk + n * p.sbn] : 0.0f;
-    }
-  };
-  auto stash = [&](int buf) {
-#pragma unroll
-    for (int j = 0; j < LOADS_A; ++j) {
-      int mm, kk;
-      a_coord(threadIdx.x + 256 * j, mm, kk);
-      As[buf][kk][mm] = ra[j];
-    }
-#pragma unroll
-    for (int j = 0; j < LOADS_B; ++j) {
-      int nn, kb;
-      b_coord(threadIdx.x + 256 * j, nn, kb);
-      Bs[buf][kb][nn] = rb[j];
+      int nn, kk;
+      b_coord(threadIdx.x + 256 * j, nn, kk);
+      const long long n = n0 + nn, k = k0 + kk;
+      const bool in = n < p.N && k < p.K;
+      cp_async4(&sm.B[buf][kk][nn], in ? B + k * p.sbk + n * p.sbn : B, in);
     }
   };
 
-  if (s_begin < s_end) {
-    load(s_begin);
-    stash(0);
+  // prologue: the first STAGES-1 steps in flight (one commit group per step, empty past the end)
+#pragma unroll
+  for (int i = 0; i < STAGES - 1; ++i) {
+    if (s_begin + i < s_end) issue(s_begin + i, i);
+    cp_async_commit();
   }
-  __syncthreads();
   for (long long step = s_begin; step < s_end; ++step) {
-    const int buf = static_cast<int>((step - s_begin) & 1);
-    if (step + 1 < s_end) load(step + 1);
+    const int buf = static_cast<int>((step - s_begin) % STAGES);
+    cp_async_wait<STAGES - 2>();  // this step's group has landed (this thread's copies)
+    __syncthreads();              // ... everyone's; and the buffer refilled below is free
+    const long long nxt = step + STAGES - 1;
+    if (nxt < s_end) issue(nxt, static_cast<int>((nxt - s_begin) % STAGES));
+    cp_async_commit();
 #pragma unroll
     for (int kk = 0; kk < TK; ++kk) {
       float a[RM], b[4];
-      RowVec<RM>::load(&As[buf][kk][RM * ty], a);
-      RowVec<4>::load(&Bs[buf][kk][4 * tx], b);
+      RowVec<RM>::load(&sm.A[buf][kk][RM * ty], a);
+      RowVec<4>::load(&sm.B[buf][kk][4 * tx], b);
 #pragma unroll
       for (int r = 0; r < RM; ++r)
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
     }
-    if (step + 1 < s_end) stash(buf ^ 1);
-    __syncthreads();
   }
+  cp_async_wait<0>();
 
   const int og = p.ksum ? 0 : g;
-  float* part = p.slices > 1 ? p.P + (static_cast<long long>(slice) * zg + og) * p.M * p.N : nullptr;
+  if (S == 1) {
 #pragma unroll
-  for (int r = 0; r < RM; ++r) {
-    const long long m = m0 + RM * ty + r;
-    if (m >= p.M) continue;
+    for (int r = 0; r < RM; ++r) {
+      const long long m = m0 + RM * ty + r;
+      if (m >= p.M) continue;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const long long n = n0 + 4 * tx + c;
-      if (n >= p.N) continue;
-      if (part != nullptr)
-        part[m * p.N + n] = acc[r][c];
-      else
-        epilogue(p, og, m, n, acc[r][c]);
+      for (int c = 0; c < 4; ++c) {
+        const long long n = n0 + 4 * tx + c;
+        if (n < p.N) epilogue(p, og, m, n, acc[r][c]);
+      }
     }
+    return;
   }
+
+  // split K: park the partial tile in shared memory (the ring's A buffers, TM x TN floats),
+  // then sum this CTA's share of rows over the cluster's CTAs in CTA order
+  __syncthreads();  // every thread is done reading the ring
+  float* part = &sm.A[0][0][0];
+  static_assert(sizeof(sm.A) >= sizeof(float) * TM * TN, "partial tile fits the A ring");
+#pragma unroll
+  for (int r = 0; r < RM; ++r)
+    *reinterpret_cast<float4*>(part + (RM * ty + r) * TN + 4 * tx) =
+        make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+  cg::cluster_group cluster = cg::this_cluster();
+  cluster.sync();
+  const int r0 = TM * slice / S, r1 = TM * (slice + 1) / S;
+  for (int e = threadIdx.x; e < (r1 - r0) * TN; e += 256) {
+    const int rr = r0 + e / TN, cc = e % TN;
+    const long long m = m0 + rr, n = n0 + cc;
+    float v = 0.0f;
+    for (int q = 0; q < S; ++q) v += cluster.map_shared_rank(part, q)[rr * TN + cc];
+    if (m < p.M && n < p.N) epilogue(p, og, m, n, v);
+  }
+  cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
-// Sum of the K-slice partials in slice order, then the epilogue; one thread per element of
-// [outs][M][N] (consecutive threads along n: coalesced).
-__global__ void __launch_bounds__(256) simt_split_sum_kernel(const __grid_constant__ SimtParams p) {
-  const int zg = p.ksum ? 1 : p.groups;
-  const long long mn = p.M * p.N;
-  const long long total = zg * mn;
-  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += 256LL * gridDim.x) {
-    const int og = static_cast<int>(i / mn);
-    const long long r = i - og * mn;
-    // eight slices' loads in flight at a time, added in slice order
-    const float* src = p.P + static_cast<long long>(og) * mn + r;
-    const long long slice_stride = zg * mn;
-    float v = 0.0f;
-    int s = 0;
-    for (; s + 8 <= p.slices; s += 8) {
-      float t[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) t[u] = src[(s + u) * slice_stride];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) v += t[u];
-    }
-    for (; s < p.slices; ++s) v += src[s * slice_stride];
-    epilogue(p, og, r / p.N, r % p.N, v);
-  }
-}
+int tile_rows(int64_t M) { return M <= 32 ? 32 : 64; }
 
 SimtParams make_params(const GemmSpec& s) {
   SimtParams p{};
@@ -234,19 +248,41 @@ SimtParams make_params(const GemmSpec& s) {
   p.ksum = s.ksum;
   p.epi = s.epi;
   p.act = s.act;
-  p.slices = s.kslices > 1 ? s.kslices : 1;
-  p.P = p.slices > 1 ? s.split : nullptr;
+  p.slices = 1;
   return p;
+}
+
+template <int TM>
+cudaError_t launch(const SimtParams& p, dim3 grid, cudaStream_t st) {
+  constexpr int smem = static_cast<int>(sizeof(SimtSmem<TM>));  // > 48 KiB: opt in
+  cudaError_t e =
+      cudaFuncSetAttribute(simt_gemm_kernel<TM>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  if (p.slices == 1) {
+    simt_gemm_kernel<TM><<<grid, 256, smem, st>>>(p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = static_cast<unsigned>(p.slices);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, simt_gemm_kernel<TM>, p);
 }
 
 }  // namespace
 
-namespace {
-int tile_rows(int64_t M) { return M <= 32 ? 32 : 64; }
-}  // namespace
-
-int plan_simt_split(const GemmSpec& s, size_t scratch_bytes) {
+int plan_simt_split(const GemmSpec& s) {
   if (s.M <= 0 || s.N <= 0 || s.K <= 0) return 1;
+  if (const char* env = std::getenv("TPMLP_SIMT_SPLIT"))
+    if (std::atoi(env) == 0) return 1;
   const long long outs = s.ksum ? 1 : s.groups;
   const long long TM = tile_rows(s.M);
   const long long tiles = ((s.N + TN - 1) / TN) * ((s.M + TM - 1) / TM) * outs;
@@ -254,38 +290,23 @@ int plan_simt_split(const GemmSpec& s, size_t scratch_bytes) {
   if (tiles >= target) return 1;
   const long long steps = ((s.K + TK - 1) / TK) * (s.ksum ? s.groups : 1);
   long long S = (target + tiles - 1) / tiles;
-  S = std::min(S, steps / kMinSplitSteps);                        // enough K steps per slice
-  S = std::min<long long>(S, kMaxSplitSlices);
-  const long long per_slice = outs * s.M * s.N * 4;
-  if (per_slice > 0) S = std::min<long long>(S, static_cast<long long>(scratch_bytes) / per_slice);
+  S = std::min(S, steps / kMinSplitSteps);  // enough K steps per slice
+  S = std::min<long long>(S, kMaxSplit);
   return S > 1 ? static_cast<int>(S) : 1;
 }
 
 cudaError_t launch_simt_gemm(const GemmSpec& s, cudaStream_t st) {
   if (s.M <= 0 || s.N <= 0 || s.K <= 0) return cudaSuccess;
   if (s.groups < 1 || s.groups > kMaxShards) return cudaErrorInvalidValue;
-  if (s.kslices > 1 && s.split == nullptr) return cudaErrorInvalidValue;
-  const SimtParams p = make_params(s);
+  if (s.kslices < 1 || s.kslices > kMaxSplit) return cudaErrorInvalidValue;
+  SimtParams p = make_params(s);
+  p.slices = s.kslices;
   const unsigned zg = s.ksum ? 1u : static_cast<unsigned>(s.groups);
   const int TM = tile_rows(s.M);
   const dim3 grid(static_cast<unsigned>((s.N + TN - 1) / TN),
                   static_cast<unsigned>((s.M + TM - 1) / TM), zg * static_cast<unsigned>(p.slices));
   if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidValue;
-  if (TM == 32)
-    simt_gemm_kernel<32><<<grid, 256, 0, st>>>(p);
-  else
-    simt_gemm_kernel<64><<<grid, 256, 0, st>>>(p);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_simt_split_sum(const GemmSpec& s, cudaStream_t st) {
-  if (s.M <= 0 || s.N <= 0 || s.kslices <= 1) return cudaSuccess;
-  if (s.split == nullptr) return cudaErrorInvalidValue;
-  const SimtParams p = make_params(s);
-  const long long total = (s.ksum ? 1LL : s.groups) * s.M * s.N;
-  const long long blocks = std::min<long long>((total + 255) / 256, 8LL * device_sm_count());
-  simt_split_sum_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(p);
-  return cudaGetLastError();
+  return TM == 32 ? launch<32>(p, grid, st) : launch<64>(p, grid, st);
 }
 
 }  // namespace tpk

@@ -144,17 +144,13 @@ tp_status cuda_fail(cudaError_t e, const char* what) {
 
 int* status_word(void* ws) { return static_cast<int*>(ws); }
 
-// First byte of a call's scratch: after the status block and the dtype's GEMM region (fp32:
-// split-K slices; bf16: split tail tiles).
-size_t scratch_base(int dtype) {
-  return kStatusBytes + (dtype == TP_F32 ? kSplitBytes : kTailBytes);
-}
+// First byte of a call's scratch: after the status block and, for bf16, the split tail tiles.
+size_t scratch_base(int dtype) { return kStatusBytes + (dtype == TP_BF16 ? kTailBytes : 0); }
 
-// A GEMM's view of the workspace: the status word and its dtype's GEMM region.
+// A GEMM's view of the workspace: the status word and, for bf16, the tail-split region.
 void bind_ws(GemmSpec& s, void* ws, int dtype) {
   char* region = static_cast<char*>(ws) + kStatusBytes;
   s.status = status_word(ws);
-  s.split = dtype == TP_F32 ? reinterpret_cast<float*>(region) : nullptr;
   s.tail_ws = dtype == TP_BF16 ? reinterpret_cast<float*>(region) : nullptr;
   s.tail_counters =
       dtype == TP_BF16 ? reinterpret_cast<int*>(region + kTailUnits * kTailPieceBytes) : nullptr;
@@ -238,21 +234,10 @@ cudaError_t run_gemm(const GemmSpec& s, int dtype, cudaStream_t st, int tag) {
   gemm_work(s, dtype, &flops, &bytes);
   if (dtype == TP_BF16)
     return traced(TP_K_GEMM_TC, tag, s.groups, flops, bytes, st, [&] { return launch_tc_gemm(s, st); });
-  if (s.split == nullptr)
-    return traced(TP_K_GEMM_FFMA, tag, s.groups, flops, bytes, st,
-                  [&] { return launch_simt_gemm(s, st); });
   GemmSpec t = s;
-  t.kslices = plan_simt_split(s, kSplitBytes);
-  cudaError_t e = traced(TP_K_GEMM_FFMA, tag, s.groups, flops, bytes, st,
-                         [&] { return launch_simt_gemm(t, st); });
-  if (e != cudaSuccess || t.kslices <= 1) return e;
-  // the slices' sum: every partial read once, every output (and GeLU' input) touched once
-  const double outs = double(s.ksum ? 1 : s.groups), mn = double(s.M) * double(s.N);
-  const double out_e = (s.epi == EPI_BIAS_ACT && s.D[0] != nullptr) ? 8.0 : 4.0;
-  const double aux = (s.epi == EPI_DACT && s.act != TP_ACT_NONE) ? 4.0 : 0.0;
-  return traced(TP_K_SPLIT_SUM, tag, s.groups, (t.kslices - 1) * outs * mn,
-                outs * mn * (4.0 * t.kslices + out_e + aux), st,
-                [&] { return launch_simt_split_sum(t, st); });
+  t.kslices = plan_simt_split(s);
+  return traced(TP_K_GEMM_FFMA, tag, s.groups, flops, bytes, st,
+                [&] { return launch_simt_gemm(t, st); });
 }
 
 // Zero `rows` x `cols` fp32 outputs (a GEMM over zero tokens).

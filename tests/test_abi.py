@@ -72,9 +72,7 @@ def test_workspace_sizes(tp):
     tail = tp.TP_BF16_TAIL_SCRATCH_BYTES   # bf16: split tail tiles after the status block
     assert tail == 80 * 256 * 256 * 4 + 4096
     assert tp.tp_mlp_workspace_size(mlp(tp)) == 256 + tail + T * F * 2
-    split = tp.TP_F32_SPLIT_SCRATCH_BYTES   # fp32: K-slice partials after the status block
-    assert split == 320 * 64 * 64 * 4
-    assert tp.tp_mlp_workspace_size(mlp(tp, dtype=tp.TP_F32)) == 256 + split + T * F * 4
+    assert tp.tp_mlp_workspace_size(mlp(tp, dtype=tp.TP_F32)) == 256 + T * F * 4
     part = n * T * H * 4
     assert tp.tp_mlp_workspace_size(mlp(tp, reduce=tp.TP_REDUCE_PARTIALS)) == 256 + tail + T * F * 2 + part
     assert tp.tp_mlp_workspace_size(mlp(tp, reduce=tp.TP_REDUCE_AUTO)) == 256 + tail + T * F * 2 + part
@@ -85,10 +83,10 @@ def test_workspace_sizes(tp):
         256 + tail + T * F * 2 + part + counters
     col = tp.LinearDesc(tokens=32, in_features=768, out_features=3072, tp_degree=4,
                         dtype=tp.TP_F32, act=0, reduce=0, gather=1)
-    assert tp.tp_linear_workspace_size(col, tp.TP_COLUMN) == 256 + split
+    assert tp.tp_linear_workspace_size(col, tp.TP_COLUMN) == 256
     row = tp.LinearDesc(tokens=32, in_features=3072, out_features=768, tp_degree=4,
                         dtype=tp.TP_F32, act=0, reduce=tp.TP_REDUCE_PARTIALS, gather=0)
-    assert tp.tp_linear_workspace_size(row, tp.TP_ROW) == 256 + split + 4 * 32 * 768 * 4
+    assert tp.tp_linear_workspace_size(row, tp.TP_ROW) == 256 + 4 * 32 * 768 * 4
 
 
 @pytest.mark.parametrize("kw,expected", [
@@ -198,15 +196,13 @@ def test_product_path_does_not_touch_the_oracle():
                 assert "oracle" not in src.replace("oracle-free", ""), f
 
 
-def test_header_split_scratch_matches_binding(tp):
+def test_header_tail_scratch_matches_binding(tp):
     import re
 
     text = open(os.path.join(ROOT, "include", "tp_mlp.h")).read()
-    m = re.search(r"#define TP_F32_SPLIT_SCRATCH_BYTES \(\(size_t\)([0-9 *]+)\)", text)
-    assert m is not None
-    assert eval(m.group(1)) == tp.TP_F32_SPLIT_SCRATCH_BYTES
     m = re.search(r"#define TP_BF16_TAIL_SCRATCH_BYTES \(\(size_t\)([0-9 *+]+)\)", text)
     assert m is not None
     assert eval(m.group(1)) == tp.TP_BF16_TAIL_SCRATCH_BYTES
     kinds = dict((int(v), k) for k, v in re.findall(r"(TP_K_\w+) = (\d+)", text))
-    assert kinds[8] == "TP_K_SPLIT_SUM" and tp.KERNEL_NAMES[8] == "split_sum"
+    assert {k: v.lower()[5:] for k, v in kinds.items()} == {
+        k: v for k, v in tp.KERNEL_NAMES.items()}
