@@ -146,7 +146,7 @@ def test_fp32_split_k(tp, monkeypatch):
     assert torch.equal(Z1, case.Z) and torch.equal(dX1, case.dX)
     monkeypatch.setenv("TPMLP_SIMT_SPLIT", "0")
     case.run()
-    assert rel(np64(case.Z), np64(Z1)) <= 1e-6 and rel(np64(case.dX), np64(dX1)) <= 1e-6
+    assert rel(np64(case.Z), np64(Z1)) <= TOL_F32 and rel(np64(case.dX), np64(dX1)) <= TOL_F32
     assert not (torch.equal(Z1, case.Z) and torch.equal(dX1, case.dX)
                 and all(torch.equal(a, b) for a, b in zip(Y1, case.Ys)))
 
