@@ -65,8 +65,7 @@ __device__ __forceinline__ void epilogue(const SimtParams& p, int og, long long 
 
 // 4-byte asynchronous copy global -> shared; with pred false nothing is read (src-size 0) and
 // the 4 bytes are zero-filled (src must still be a valid address: the operand's base).
-__device__ __forceinline__ void cp_async4(float* dst, const float* src, bool pred) {
-  const uint32_t d = smem_addr(dst);
+__device__ __forceinline__ void cp_async4(uint32_t d, const float* src, bool pred) {
   const int bytes = pred ? 4 : 0;
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(d),
                "l"(__cvta_generic_to_global(src)), "r"(bytes)
@@ -128,34 +127,50 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ 
   const long long s_begin = all_steps * slice / S;
   const long long s_end = all_steps * (slice + 1) / S;
 
-  // element e of a step's tile -> coordinates; consecutive threads follow whichever of the two
-  // coordinates is contiguous in global memory (coalesced)
-  auto a_coord = [&](int e, int& mm, int& kk) {
+  // Element e of a step's tile -> coordinates; consecutive threads follow whichever of the two
+  // coordinates is contiguous in global memory (coalesced). A thread's elements keep their
+  // coordinates from step to step, so their offsets are computed once: per step only the K
+  // origin (and, summing shards, the operand) moves.
+  long long a_off[LOADS_A], b_off[LOADS_B];
+  int a_kk[LOADS_A], b_kk[LOADS_B];  // K coordinate inside the step; -1: row/column outside
+  uint32_t a_dst[LOADS_A], b_dst[LOADS_B];  // shared addresses in stage 0
+#pragma unroll
+  for (int j = 0; j < LOADS_A; ++j) {
+    const int e = threadIdx.x + 256 * j;
+    int mm, kk;
     if (p.sak == 1) { kk = e % TK; mm = e / TK; } else { mm = e % TM; kk = e / TM; }
-  };
-  auto b_coord = [&](int e, int& nn, int& kk) {
+    const long long m = m0 + mm;
+    a_off[j] = m * p.sam + kk * p.sak;
+    a_kk[j] = m < p.M ? kk : -1;
+    a_dst[j] = smem_addr(&sm.A[0][kk][mm]);
+  }
+#pragma unroll
+  for (int j = 0; j < LOADS_B; ++j) {
+    const int e = threadIdx.x + 256 * j;
+    int nn, kk;
     if (p.sbk == 1) { kk = e % TK; nn = e / TK; } else { nn = e % TN; kk = e / TN; }
-  };
+    const long long n = n0 + nn;
+    b_off[j] = kk * p.sbk + n * p.sbn;
+    b_kk[j] = n < p.N ? kk : -1;
+    b_dst[j] = smem_addr(&sm.B[0][kk][nn]);
+  }
+  constexpr uint32_t A_STAGE = sizeof(float) * TK * (TM + 4);
+  constexpr uint32_t B_STAGE = sizeof(float) * TK * (TN + 4);
   auto issue = [&](long long step, int buf) {
     const int kg = static_cast<int>(step / ksteps);
     const long long k0 = (step % ksteps) * TK;
-    const float* A = p.A[p.ksum ? kg : g];
-    const float* B = p.B[p.ksum ? kg : g];
+    const int kmax = static_cast<int>(min(static_cast<long long>(TK), p.K - k0));
+    const float* A = p.A[p.ksum ? kg : g] + k0 * p.sak;
+    const float* B = p.B[p.ksum ? kg : g] + k0 * p.sbk;
 #pragma unroll
     for (int j = 0; j < LOADS_A; ++j) {
-      int mm, kk;
-      a_coord(threadIdx.x + 256 * j, mm, kk);
-      const long long m = m0 + mm, k = k0 + kk;
-      const bool in = m < p.M && k < p.K;
-      cp_async4(&sm.A[buf][kk][mm], in ? A + m * p.sam + k * p.sak : A, in);
+      const bool in = a_kk[j] >= 0 && a_kk[j] < kmax;
+      cp_async4(a_dst[j] + buf * A_STAGE, in ? A + a_off[j] : A, in);
     }
 #pragma unroll
     for (int j = 0; j < LOADS_B; ++j) {
-      int nn, kk;
-      b_coord(threadIdx.x + 256 * j, nn, kk);
-      const long long n = n0 + nn, k = k0 + kk;
-      const bool in = n < p.N && k < p.K;
-      cp_async4(&sm.B[buf][kk][nn], in ? B + k * p.sbk + n * p.sbn : B, in);
+      const bool in = b_kk[j] >= 0 && b_kk[j] < kmax;
+      cp_async4(b_dst[j] + buf * B_STAGE, in ? B + b_off[j] : B, in);
     }
   };
 
