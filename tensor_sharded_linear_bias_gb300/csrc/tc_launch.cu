@@ -186,14 +186,16 @@ int plan_shard_split(int64_t M, int64_t N, int64_t K_per_group, int n) {
     const int v = std::atoi(env);
     if (v >= 1 && v <= n && n % v == 0) return v;
   }
-  const double sms = device_sm_count();
-  // One-SM tiles of 128 x 256 on every SM, or pair tiles of 256 x 256 on every SM pair:
-  // the same count of tiles per wave in units of 128 x 256.
-  const double tiles = double((M + BM - 1) / BM) * double((N + BN - 1) / BN);
+  // Model on SM pairs (the kernel for every M > 128): 256 x 256 tiles dealt to C = SMs / 2
+  // pairs; a 64-deep K block of a pair tile costs ~512 tensor cycles (~0.27 us). A last wave
+  // that leaves pairs idle costs a whole tile, unless the tail split applies (at most 8 waves,
+  // >= 32 K blocks per tile), which cuts its L tiles into P pieces (~1/P of a tile, plus a
+  // little for the piece sums). A reduction of S fp32 partials moves (4 S + 4) M N bytes at
+  // ~6.5 TB/s. (Measured on GB300, GPT-3-shaped step: fused 1525-1528 TFLOP/s with the tail
+  // split vs 1499-1506 for S = 4 and 1499 fused without it.)
+  const double C = std::max(1, device_sm_count() / 2);
+  const double tiles1 = double((M + 255) / 256) * double((N + BN - 1) / BN);
   const double kb = double((K_per_group + BK - 1) / BK);
-  // Model: a 64-deep K block of a 128 x 256 tile costs ~512 tensor cycles (~0.27 us); a
-  // reduction of S fp32 partials moves (4 S + 4) M N bytes at ~6.5 TB/s; tiles whose K range
-  // is deeper than 256 blocks lose ~25 % (the running tiles' operands no longer fit in L2).
   const double t_kb_us = 512.0 / 1.9e3;
   const double hbm_bytes_per_us = 6.5e6;
   int best = 1;
@@ -201,9 +203,15 @@ int plan_shard_split(int64_t M, int64_t N, int64_t K_per_group, int n) {
   for (int S = 1; S <= n; ++S) {
     if (n % S != 0) continue;
     const double per_tile_kb = kb * (n / S);
-    const double waves = std::ceil(S * tiles / sms);
+    const double tiles = S * tiles1;
+    double waves = std::ceil(tiles / C);
+    const double L = tiles - C * std::floor(tiles / C);
+    if (L > 0 && tiles <= kMaxSplitWaves * C && tail_split_enabled()) {
+      const double P = std::min({std::floor(C / L), std::floor(per_tile_kb / kMinPieceKb),
+                                 std::floor(kTailUnits / L)});
+      if (P >= 2) waves = std::floor(tiles / C) + 1.0 / P + 0.05;
+    }
     double cost = waves * per_tile_kb * t_kb_us;
-    if (per_tile_kb > 256.0) cost *= 1.25;
     if (S > 1) cost += (4.0 * S + 4.0) * double(M) * double(N) / hbm_bytes_per_us;
     if (cost < best_cost * 0.995) {
       best_cost = cost;
