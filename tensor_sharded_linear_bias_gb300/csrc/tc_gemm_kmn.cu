@@ -1,5 +1,5 @@
-// Instantiations of the tcgen05 GEMM (one-SM, SM-pair and two-pair kernels) for A K-major, B MN-major.
-#include "tc4_gemm.cuh"
+// Instantiations of the tcgen05 GEMM (one-SM and SM-pair kernels) for A K-major, B MN-major.
+#include "tc2_gemm.cuh"
 
 namespace tpk {
 namespace tc {
@@ -18,12 +18,6 @@ cudaError_t run_pair_kmn(const TcParams& p, int clusters, cudaStream_t st, int* 
                          int epi_warps) {
   return epi_warps == 8 ? tc2::launch_pair<false, true, 8>(p, clusters, st, max_clusters)
                         : tc2::launch_pair<false, true, 4>(p, clusters, st, max_clusters);
-}
-
-// Clusters of two SM pairs sharing B tiles. max_clusters != nullptr asks for the occupancy
-// limit only.
-cudaError_t run_quad_kmn(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters) {
-  return tc4::launch_quad<false, true>(p, clusters, st, max_clusters);
 }
 
 }  // namespace tc

@@ -9,7 +9,7 @@
 #include <mutex>
 
 #include "internal.h"
-#include "tc4_gemm.cuh"
+#include "tc2_gemm.cuh"
 
 namespace tpk {
 namespace tc {
@@ -22,9 +22,6 @@ cudaError_t run_pair_kk(const TcParams& p, int clusters, cudaStream_t st, int* m
                         int epi_warps);
 cudaError_t run_pair_mnmn(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters,
                           int epi_warps);
-cudaError_t run_quad_kmn(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters);
-cudaError_t run_quad_kk(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters);
-cudaError_t run_quad_mnmn(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters);
 }  // namespace tc
 
 namespace {
@@ -93,38 +90,6 @@ int pair_clusters(int layout, int epi_warps = 4) {
     cached[dev][layout][v] = n;
   }
   return cached[dev][layout][v];
-}
-
-cudaError_t run_quad(int layout, const tc::TcParams& p, int clusters, cudaStream_t st,
-                     int* max_clusters) {
-  if (layout == 0) return tc::run_quad_kmn(p, clusters, st, max_clusters);
-  if (layout == 1) return tc::run_quad_kk(p, clusters, st, max_clusters);
-  return tc::run_quad_mnmn(p, clusters, st, max_clusters);
-}
-
-// Largest number of co-resident 4-CTA clusters of the two-pair kernel (cached per device and
-// operand layout); 0 if the device cannot place any.
-int quad_clusters(int layout) {
-  static int cached[64][3] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cached[dev][layout] == 0) {
-    int n = 0;
-    if (run_quad(layout, tc::TcParams{}, 0, nullptr, &n) != cudaSuccess || n <= 0) {
-      cudaGetLastError();
-      n = -1;
-    }
-    cached[dev][layout] = n;
-  }
-  return std::max(0, cached[dev][layout]);
-}
-
-// Two pairs sharing B tiles (clusters of four): TPMLP_GEMM_QUAD=1 turns it on for products of
-// more than 256 rows whose epilogue is not the overlapped shard sum.
-bool use_quad_kernel(int64_t M, int epi) {
-  const char* env = std::getenv("TPMLP_GEMM_QUAD");
-  if (env == nullptr || std::atoi(env) == 0) return false;
-  return M > 256 && epi != EPI_PARTIAL_REDUCE;
 }
 
 // Epilogue warps of the pair kernel: 8 where 4 warps' epilogue of a tile would outlast the next
@@ -262,19 +227,14 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
   if (s.groups < 1 || s.groups > kMaxShards) return cudaErrorInvalidValue;
   static_assert(sizeof(TcParams) <= 32764, "kernel parameter block too large");
 
-  const int layout = (!s.a_mn && s.b_mn) ? 0 : (!s.a_mn && !s.b_mn) ? 1 : (s.a_mn && s.b_mn) ? 2 : -1;
-  if (layout < 0) return cudaErrorNotSupported;
-  const bool quad = use_quad_kernel(s.M, s.epi) && quad_clusters(layout) > 0;
-  const bool pair = quad || use_pair_kernel(s.M);
+  const bool pair = use_pair_kernel(s.M);
   alignas(128) static thread_local TcParams p;
   std::memset(static_cast<void*>(&p), 0, sizeof(p));
-  // K-major boxes: 128 rows of A; B 256 rows (one SM), 128 (each SM of a pair) or 64 (each
-  // SM's quarter in a two-pair cluster).
-  const uint32_t b_rows = quad ? static_cast<uint32_t>(tc4::QUARTER)
-                          : pair ? static_cast<uint32_t>(tc2::HALF) : static_cast<uint32_t>(BN);
-  // MN chunks per CTA load: A 128 rows; B 256, 128 or 64 columns.
+  // K-major boxes: 128 rows of A; 256 rows of B (one SM) or 128 (each SM of a pair).
+  const uint32_t b_rows = pair ? static_cast<uint32_t>(tc2::HALF) : static_cast<uint32_t>(BN);
+  // MN chunks per CTA tile: A 128 rows (one SM or each SM of a pair); B 256 or 128 columns.
   const uint32_t a_chunks = 2;
-  const uint32_t b_chunks = quad ? 1 : pair ? 2 : 4;
+  const uint32_t b_chunks = pair ? 2 : 4;
   p.a3d = s.a_mn && mn3d_enabled() && s.M % 64 == 0;
   p.b3d = s.b_mn && mn3d_enabled() && s.N % 64 == 0;
   for (int g = 0; g < s.groups && p.a3d; ++g)
@@ -304,7 +264,7 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
   const int kpo = s.kpo > 0 ? s.kpo : (s.ksum ? s.groups : 1);
   if (s.groups % kpo != 0) return cudaErrorInvalidValue;
   p.kpo = kpo;
-  const int tile_rows = quad ? tc4::BM : pair ? tc2::BM : BM;
+  const int tile_rows = pair ? tc2::BM : BM;
   p.tiles_m = static_cast<int>((s.M + tile_rows - 1) / tile_rows);
   p.tiles_n = static_cast<int>((s.N + BN - 1) / BN);
   p.num_tiles = (s.groups / kpo) * p.tiles_m * p.tiles_n;
@@ -320,13 +280,11 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
                            pair ? 2 * pair_clusters(0) : device_sm_count(), pair);
   p.status = s.status;
 
+  const int layout = (!s.a_mn && s.b_mn) ? 0 : (!s.a_mn && !s.b_mn) ? 1 : (s.a_mn && s.b_mn) ? 2 : -1;
+  if (layout < 0) return cudaErrorNotSupported;
   p.full_tiles = p.num_tiles;
   p.ksplit = 1;
   p.num_units = p.num_tiles;
-  if (quad) {
-    const int clusters = std::min(p.num_tiles, quad_clusters(layout));
-    return run_quad(layout, p, clusters, st, nullptr);
-  }
   if (pair) {
     const int epi_warps = pair_epi_warps(p.epi, p.act, p.kblocks * p.kpo);
     const int max_clusters = pair_clusters(layout, epi_warps);

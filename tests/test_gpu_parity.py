@@ -181,23 +181,6 @@ def test_epilogue_warps(tp, monkeypatch, epi_warps, T, H, F, n):
         assert max(errs.values()) <= TOL_BF16, (reduce, errs)
 
 
-@pytest.mark.parametrize("T,H,F,n", [(520, 264, 2 * 392, 2), (1100, 520, 4 * 264, 4)])
-def test_two_pair_kernel(tp, monkeypatch, T, H, F, n):
-    """Clusters of two SM pairs sharing B tiles through TMA multicast (TPMLP_GEMM_QUAD=1):
-    512-row cluster tiles with a ragged last one, every operand layout and epilogue of the
-    MLP, fused and grouped shard sums: matches the oracle and repeats bit for bit."""
-    import torch
-
-    monkeypatch.setenv("TPMLP_GEMM_QUAD", "1")
-    for reduce in (0, 2):
-        case = MlpCase(SMALL.with_shape(tokens=T, hidden=H, ffn=F, tp_degree=n), reduce).run()
-        errs = compare_full(case.outputs(), *full_reference(case))
-        assert max(errs.values()) <= TOL_BF16, (reduce, errs)
-        Z1, dA1 = case.Z.clone(), [x.clone() for x in case.dA]
-        case.run()
-        assert torch.equal(Z1, case.Z) and all(torch.equal(a, b) for a, b in zip(dA1, case.dA))
-
-
 _TAIL_REF = {}
 
 
