@@ -21,7 +21,8 @@ struct NormalTail {
 
 __device__ __forceinline__ NormalTail normal_tail(float h) {
   const float z = fabsf(h) * 0.7071067811865475f;
-  const float t = __frcp_rn(fmaf(0.3275911f, z, 1.0f));
+  // fast division (2 ulp): the divisor 1 + p z lies in [1, 2^126)
+  const float t = __fdividef(1.0f, fmaf(0.3275911f, z, 1.0f));
   const float poly =
       t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f),
                        -0.284496736f),
