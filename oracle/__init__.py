@@ -1,4 +1,5 @@
-"""CPU fp64 oracle for the tensor-parallel MLP path. TEST INFRASTRUCTURE ONLY.
+"""CPU fp64 oracle for the tensor-parallel MLP path and the hidden-split LayerNorm.
+TEST INFRASTRUCTURE ONLY.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py`` (its ``cpu_baseline`` leg and
 ``--impl reference``) may import this package. The library under
@@ -6,3 +7,4 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py`` (its ``cpu_baselin
 from there.
 """
 from .tp_mlp import *  # noqa: F401,F403
+from .tp_layernorm import *  # noqa: F401,F403
