@@ -7,7 +7,8 @@ path: column GEMM with the bias + GeLU epilogue, row GEMM with the fused shard s
 with the GeLU' epilogue, both weight-gradient GEMMs, the input-gradient GEMM with the fused
 shard sum, and the bias-gradient column sums). Prints ONE JSON line (rank 0).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload gpt3|mlp2|p3|sweep:T:n]
+  python bench.py [--gpus N] [--steps K] [--warmup W]
+                  [--workload gpt3|mlp2|p3|attn|p3col|ln|sweep:T:n]
                   [--reduce fused|partials] [--impl native|reference]
 
 --impl reference times the fp64 CPU oracle on the host cores instead (a bounded sample of the
@@ -672,6 +673,65 @@ def run_attention(args, world, rank, local):
     return 0
 
 
+# ----------------------------------------------------------------------------- hidden-split LayerNorm
+def run_layernorm(args, world, rank, local):
+    """LayerNorm over a hidden dimension split into tp_degree shards (the statistics combined
+    over the shards on the device), forward + backward (dX, dgamma, dbeta), bf16, GPT-3-sized
+    rows: T 2048, H 12288, 8 shards. HBM-bound: reported in GB/s of algorithmic traffic."""
+    import numpy as np
+    import torch
+
+    import tensor_sharded_linear_bias_gb300 as tp
+
+    device = dist_init(world, local)
+    T, H, n = 2048, 12288, 8
+    Hs = H // n
+    g = np.random.Generator(np.random.PCG64(9000))
+    mk = lambda *shape, s=1.0, m=0.0: [  # noqa: E731
+        torch.from_numpy((g.standard_normal(shape) * s + m).astype(np.float32)).to(device, torch.bfloat16)
+        for _ in range(n)]
+    X, dY = mk(T, Hs), mk(T, Hs)
+    gam, bet = mk(Hs, s=0.5, m=1.0), mk(Hs, s=0.5)
+    Y = [torch.empty(T, Hs, dtype=torch.bfloat16, device=device) for _ in range(n)]
+    dX = [torch.empty(T, Hs, dtype=torch.bfloat16, device=device) for _ in range(n)]
+    f32 = dict(dtype=torch.float32, device=device)
+    mean, rstd = torch.empty(T, **f32), torch.empty(T, **f32)
+    dg = [torch.empty(Hs, **f32) for _ in range(n)]
+    db = [torch.empty(Hs, **f32) for _ in range(n)]
+    desc = tp.LayerNormDesc(tokens=T, hidden=H, tp_degree=n, dtype=tp.TP_BF16, eps=1e-5)
+
+    def step():
+        tp.tp_layernorm_forward(desc, X, gam, bet, Y, mean, rstd)
+        tp.tp_layernorm_backward(desc, X, gam, mean, rstd, dY, dX, dg, db)
+
+    # algorithmic bytes: fwd reads X, writes Y; dX reads X, dY, writes dX; dgamma/dbeta read
+    # X, dY (gamma, beta, statistics and parameter gradients are < 0.1 %)
+    step_bytes = 7.0 * T * H * 2
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    flush, l2_note = make_flush(device, int(4 * T * H * 2))
+    sampler = ClockSampler(device.index or 0) if rank == 0 else None
+    ms, recs, clocks = timed_then_traced(tp, step, args.steps, world, flush,
+                                         args.steps * TRACE_PER_STEP + 16, sampler)
+    ms = max_over_ranks(ms, world)
+    if rank == 0:
+        pk = peaks()
+        roof, kernels = roofline_from_trace(recs, pk)
+        value = step_bytes * args.steps * world / (ms / 1e3) / 1e9
+        print(json.dumps({
+            "metric": "hidden-split LayerNorm fwd+bwd (8 shards, statistics combined on the "
+                      "device) GB/s of algorithmic traffic (bf16)",
+            "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "layernorm_bf16_T2048_H12288_tp8", "tokens": T, "hidden": H,
+                       "tp_degree": n, "l2": l2_note},
+            "pct_of_hbm": value / pk["hbm_gbs"] * 100.0, "clocks": clocks,
+            "gpu_launches": len(recs), "roofline": roof, "kernels": kernels}), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- pages' example
 def run_p3_column_latency(args, world, rank, local):
     """Latency of the pages' column-parallel example: X [32, 768] times W [768, 3072] split
@@ -716,6 +776,11 @@ def main():
     if args.workload == "p3col":
         world, rank, local = dist_setup(args.gpus)
         return run_p3_column_latency(args, world, rank, local)
+    if args.workload == "ln":
+        if args.impl != "native":
+            raise SystemExit("--impl reference times the MLP workloads only")
+        world, rank, local = dist_setup(args.gpus)
+        return run_layernorm(args, world, rank, local)
     if args.workload == "attn":
         if args.impl != "native":
             raise SystemExit("--impl reference times the MLP workloads only")

@@ -231,6 +231,42 @@ tp_status tp_linear_row_backward(const tp_linear_desc* desc, const void* const* 
                                  void* const* dW, void* dbias, void* ws, size_t ws_bytes,
                                  void* stream);
 
+/* ---------------------------------------------------------------------------------------
+ * LayerNorm with the hidden dimension split over the shards ("Tensor Parallelism: principle
+ * and practice", section 4.2: each device computes the mean and variance of its own part and
+ * the statistics are synchronised by an All-Reduce). Shard i holds columns i*H/n ..
+ * (i+1)*H/n - 1 of every token row as its own buffer X[i] [T, H/n] (row-major), with its
+ * slices gamma[i], beta[i] [H/n]. The row statistics are the mean and the biased variance of
+ * the whole row (H columns), eps added inside the square root:
+ *   Y[i] = (X[i] - mean) / sqrt(var + eps) * gamma[i] + beta[i].
+ * On this GPU the All-Reduce is the combination of the shards' (count, mean, M2) in shard
+ * order inside the kernel (deterministic). dtype TP_BF16 or TP_F32 applies to X, Y, dY, dX,
+ * gamma and beta; mean, rstd, dgamma, dbeta are fp32. bf16 needs H/n % 8 == 0 and 16-byte
+ * aligned pointers; fp32 takes any width (16-byte accesses where rows and pointers allow).
+ * No workspace; calls enqueue on `stream`; TP_ERR_* as for the other entry points. */
+typedef struct tp_layernorm_desc {
+  int64_t tokens;     /* T (>= 0) */
+  int64_t hidden;     /* H, divisible by tp_degree */
+  int32_t tp_degree;  /* n, 1..64 */
+  int32_t dtype;      /* tp_dtype */
+  float eps;          /* > 0 */
+} tp_layernorm_desc;
+
+/* Forward. gamma / beta: arrays of n pointers, or NULL for 1 / 0. mean, rstd: fp32 [T] or NULL
+ * (not stored); the backward needs them. */
+tp_status tp_layernorm_forward(const tp_layernorm_desc* desc, const void* const* X,
+                               const void* const* gamma, const void* const* beta, void* const* Y,
+                               float* mean, float* rstd, void* stream);
+
+/* Backward for dY[i] [T, H/n]: dX[i] [T, H/n] (dtype) = rstd * (g - mean_row(g) - xhat *
+ * mean_row(g * xhat)) with g = dY * gamma and xhat = (X - mean) * rstd over the whole row;
+ * dgamma[i] = sum_t dY[i] * xhat, dbeta[i] = sum_t dY[i] (fp32 [H/n], arrays may be NULL: not
+ * computed). mean, rstd: the forward's. */
+tp_status tp_layernorm_backward(const tp_layernorm_desc* desc, const void* const* X,
+                                const void* const* gamma, const float* mean, const float* rstd,
+                                const void* const* dY, void* const* dX, float* const* dgamma,
+                                float* const* dbeta, void* stream);
+
 /* Launch tracing (profiling aid). While tracing is on, every kernel launch this library makes
  * (in any thread) is bracketed by two CUDA events recorded on the launch's stream, and the
  * launch's algorithmic work is noted: flops = 2*M*N*K per GEMM over all its shards; bytes =
@@ -246,7 +282,9 @@ typedef enum tp_kernel_kind {
   TP_K_COLSUM = 4,         /* bias gradients: column sums over tokens */
   TP_K_DACT = 5,           /* dH = dY * act'(H) */
   TP_K_SELFTEST = 6,
-  TP_K_SHARD_COPY = 7      /* token-shard gather / scatter (sequence parallel) */
+  TP_K_SHARD_COPY = 7,     /* token-shard gather / scatter (sequence parallel) */
+  TP_K_LAYERNORM = 8,      /* hidden-split LayerNorm: row statistics + normalise (fwd, bwd dX) */
+  TP_K_LN_PARAM_GRAD = 9   /* hidden-split LayerNorm: dgamma, dbeta column sums */
 } tp_kernel_kind;
 
 typedef enum tp_trace_tag {
@@ -261,7 +299,10 @@ typedef enum tp_trace_tag {
   TP_TAG_ACT_GRAD = 9,     /* stand-alone dH = dY * act'(H) */
   TP_TAG_OTHER = 10,
   TP_TAG_SP_GATHER = 11,   /* all-gather of token shards */
-  TP_TAG_SP_SCATTER = 12   /* scatter of the summed rows to token shards */
+  TP_TAG_SP_SCATTER = 12,  /* scatter of the summed rows to token shards */
+  TP_TAG_LN_FWD = 13,      /* LayerNorm forward */
+  TP_TAG_LN_DGRAD = 14,    /* LayerNorm input gradient */
+  TP_TAG_LN_PARAM_GRAD = 15 /* LayerNorm dgamma, dbeta */
 } tp_trace_tag;
 
 typedef struct tp_trace_record {

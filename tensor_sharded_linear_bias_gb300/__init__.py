@@ -22,7 +22,8 @@ __all__ = [
     "tp_linear_row_forward", "tp_linear_row_backward", "tp_selftest_wait_timeout",
     "new_workspace", "EXPORTED_SYMBOLS", "tp_trace_start", "tp_trace_stop", "TraceRecord",
     "KERNEL_NAMES", "TAG_NAMES", "tp_linear_row_forward_noalloc", "tp_mlp_sp_workspace_size",
-    "tp_mlp_forward_sp", "tp_mlp_backward_sp",
+    "tp_mlp_forward_sp", "tp_mlp_backward_sp", "LayerNormDesc", "tp_layernorm_forward",
+    "tp_layernorm_backward",
 ]
 
 TP_F32, TP_BF16 = 0, 1
@@ -43,7 +44,7 @@ EXPORTED_SYMBOLS = (
     "tp_linear_column_forward", "tp_linear_column_backward", "tp_linear_row_forward",
     "tp_linear_row_backward", "tp_selftest_wait_timeout", "tp_trace_start", "tp_trace_stop",
     "tp_linear_row_forward_noalloc", "tp_mlp_sp_workspace_size", "tp_mlp_forward_sp",
-    "tp_mlp_backward_sp",
+    "tp_mlp_backward_sp", "tp_layernorm_forward", "tp_layernorm_backward",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -66,6 +67,12 @@ class MlpDesc(ctypes.Structure):
                 ("act", ctypes.c_int32), ("reduce", ctypes.c_int32)]
 
 
+class LayerNormDesc(ctypes.Structure):
+    _fields_ = [("tokens", ctypes.c_int64), ("hidden", ctypes.c_int64),
+                ("tp_degree", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("eps", ctypes.c_float)]
+
+
 class LinearDesc(ctypes.Structure):
     _fields_ = [("tokens", ctypes.c_int64), ("in_features", ctypes.c_int64),
                 ("out_features", ctypes.c_int64), ("tp_degree", ctypes.c_int32),
@@ -79,10 +86,11 @@ class TraceRecord(ctypes.Structure):
 
 
 KERNEL_NAMES = {1: "gemm_tc", 2: "gemm_ffma", 3: "shard_reduce", 4: "colsum", 5: "dact",
-                6: "selftest", 7: "shard_copy"}
+                6: "selftest", 7: "shard_copy", 8: "layernorm", 9: "ln_param_grad"}
 TAG_NAMES = {1: "column_fwd", 2: "row_fwd", 3: "row_dgrad", 4: "row_wgrad", 5: "column_wgrad",
              6: "column_dgrad", 7: "reduce", 8: "bias_grad", 9: "act_grad", 10: "other",
-             11: "sp_gather", 12: "sp_scatter"}
+             11: "sp_gather", 12: "sp_scatter", 13: "ln_fwd", 14: "ln_dgrad",
+             15: "ln_param_grad"}
 
 _P = ctypes.c_void_p
 _PP = ctypes.POINTER(ctypes.c_void_p)
@@ -117,6 +125,10 @@ _SIGS = {
                                                      _P, _P]),
     "tp_trace_stop": (ctypes.c_int, [ctypes.POINTER(TraceRecord), ctypes.c_int32,
                                      ctypes.POINTER(ctypes.c_int32)]),
+    "tp_layernorm_forward": (ctypes.c_int, [ctypes.POINTER(LayerNormDesc), _PP, _PP, _PP, _PP,
+                                            _P, _P, _P]),
+    "tp_layernorm_backward": (ctypes.c_int, [ctypes.POINTER(LayerNormDesc), _PP, _PP, _P, _P,
+                                             _PP, _PP, _PP, _PP, _P]),
 }
 
 
@@ -184,6 +196,10 @@ def _desc_mlp(d) -> MlpDesc:
 
 def _desc_lin(d) -> LinearDesc:
     return d if isinstance(d, LinearDesc) else LinearDesc(**d)
+
+
+def _desc_ln(d) -> LayerNormDesc:
+    return d if isinstance(d, LayerNormDesc) else LayerNormDesc(**d)
 
 
 # ------------------------------------------------------------------ entry points
@@ -299,3 +315,20 @@ def tp_trace_stop(capacity: int = 100000):
     return [{"kernel": KERNEL_NAMES.get(r.kernel, str(r.kernel)),
              "tag": TAG_NAMES.get(r.tag, str(r.tag)), "flops": r.flops, "bytes": r.bytes,
              "ms": r.ms, "groups": r.groups} for r in buf[:cnt.value]]
+
+
+def tp_layernorm_forward(desc, X, gamma, beta, Y, mean, rstd, stream=None):
+    """LayerNorm over a hidden dimension split into desc.tp_degree column shards: lists of
+    per-shard tensors X [T, H/n], gamma/beta [H/n] (or None), Y [T, H/n]; mean, rstd fp32 [T]
+    (or None)."""
+    _check(lib.tp_layernorm_forward(ctypes.byref(_desc_ln(desc)), _arr(X), _arr(gamma),
+                                    _arr(beta), _arr(Y), _ptr(mean), _ptr(rstd),
+                                    _stream(stream)))
+
+
+def tp_layernorm_backward(desc, X, gamma, mean, rstd, dY, dX, dgamma, dbeta, stream=None):
+    """Backward of tp_layernorm_forward: dX [T, H/n] per shard; dgamma, dbeta fp32 [H/n] per
+    shard (lists, or None)."""
+    _check(lib.tp_layernorm_backward(ctypes.byref(_desc_ln(desc)), _arr(X), _arr(gamma),
+                                     _ptr(mean), _ptr(rstd), _arr(dY), _arr(dX), _arr(dgamma),
+                                     _arr(dbeta), _stream(stream)))

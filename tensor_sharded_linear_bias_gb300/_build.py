@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", "libtpmlp")
 LIB = os.path.join(PKG, "libtpmlp.so")
 
-SOURCES = ["tp_api.cu", "tc_launch.cu", "tc_gemm_kmn.cu", "tc_gemm_kk.cu", "tc_gemm_mnmn.cu",
+SOURCES = ["tp_api.cu", "layernorm.cu", "tc_launch.cu", "tc_gemm_kmn.cu", "tc_gemm_kk.cu", "tc_gemm_mnmn.cu",
            "simt_gemm.cu", "reduce.cu", "noalloc.cu"]
 HEADERS = ["internal.h", "device_common.cuh", "tc_gemm.cuh", "tc2_gemm.cuh"]
 

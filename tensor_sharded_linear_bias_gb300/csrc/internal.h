@@ -103,6 +103,28 @@ cudaError_t launch_dact(const void* const* dY, int64_t ld_dy, const void* const*
                         void* const* dH, int n, int64_t T, int64_t w, int act, int bf16,
                         cudaStream_t st);
 
+// LayerNorm over a hidden dimension split into n column shards of Hs columns (dtype bf16 or
+// fp32 for X, Y, dY, gamma, beta; mean, rstd, dgamma, dbeta fp32). Arrays of n pointers;
+// gamma, beta, dgamma, dbeta may be NULL arrays.
+struct LnArgs {
+  const void* const* X = nullptr;
+  const void* const* gamma = nullptr;
+  const void* const* beta = nullptr;
+  void* const* Y = nullptr;  // forward: Y; backward: dX
+  const void* const* dY = nullptr;
+  float* const* dgamma = nullptr;
+  float* const* dbeta = nullptr;
+  float* mean = nullptr;
+  float* rstd = nullptr;
+  int64_t T = 0, Hs = 0;
+  int n = 0;
+  float eps = 0.f;
+  int bf16 = 0;
+};
+cudaError_t launch_ln_forward(const LnArgs& a, cudaStream_t st);
+cudaError_t launch_ln_backward_dx(const LnArgs& a, cudaStream_t st);
+cudaError_t launch_ln_param_grads(const LnArgs& a, cudaStream_t st);
+
 // One-block self-test of the bounded wait (see tp_selftest_wait_timeout).
 cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t st);
 

@@ -1,0 +1,353 @@
+// LayerNorm with the hidden dimension split into tp_degree column shards ("Tensor Parallelism:
+// principle and practice", section 4.2: each device computes the mean and variance of its own
+// part and the statistics are synchronised by an All-Reduce). All shards live on this GPU as
+// separate buffers; the All-Reduce of the statistics is a combination, in shard order, inside
+// the warp that owns the token row.
+//
+// Forward, one warp per token row:
+//   1. per shard i: every lane sums x - k_i and (x - k_i)^2 over its elements (k_i = the
+//      shard's first element of the row: a shift that keeps the sums well conditioned), the
+//      warp adds the lanes in a fixed butterfly, giving the shard's count, mean and M2;
+//   2. the shards' (count, mean, M2) are combined in shard order 0..n-1 with the pairwise
+//      update of Chan, Golub and LeVeque ("Updating formulae and a pairwise algorithm for
+//      computing sample variances", 1979): the row's mean and biased variance;
+//   3. y = (x - mean) * rstd * gamma + beta for every shard (the row's bytes are re-read from
+//      L1/L2), and mean, rstd are stored for the backward.
+// Backward dX, one warp per row: the row statistics sum(dY*gamma) and sum(dY*gamma*xhat) are
+// summed per shard, then over the shards in order, and dX = rstd * (g - (s1 + xhat s2) / H).
+// Backward dgamma, dbeta: column sums over the tokens, split over the blocks of a cluster and
+// combined in block order through distributed shared memory (deterministic, no atomics).
+#include <cooperative_groups.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace tpk {
+namespace {
+
+constexpr int kLnWarps = 8;  // token rows per block (one per warp)
+
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T>
+__device__ __forceinline__ T from_f(float v);
+template <>
+__device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// VEC consecutive elements of one row: one 16-byte access when VEC * sizeof(T) == 16.
+template <typename T, int VEC>
+struct Vec {
+  T v[VEC];
+};
+template <typename T, int VEC>
+__device__ __forceinline__ void load_vec(const T* p, float* out) {
+  const Vec<T, VEC> r = *reinterpret_cast<const Vec<T, VEC>*>(p);
+#pragma unroll
+  for (int j = 0; j < VEC; ++j) out[j] = to_f(r.v[j]);
+}
+template <typename T, int VEC>
+__device__ __forceinline__ void store_vec(T* p, const float* in) {
+  Vec<T, VEC> r;
+#pragma unroll
+  for (int j = 0; j < VEC; ++j) r.v[j] = from_f<T>(in[j]);
+  *reinterpret_cast<Vec<T, VEC>*>(p) = r;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+struct LnParams {
+  const void* X[kMaxShards];
+  const void* gamma[kMaxShards];
+  const void* beta[kMaxShards];
+  void* Y[kMaxShards];   // forward output / backward dX
+  const void* dY[kMaxShards];
+  float* dgamma[kMaxShards];
+  float* dbeta[kMaxShards];
+  float* mean;
+  float* rstd;
+  long long T, Hs;
+  int n;
+  float eps;
+};
+
+template <typename T, int VEC>
+__global__ void __launch_bounds__(kLnWarps * 32) ln_forward_kernel(const __grid_constant__ LnParams p) {
+  const int lane = threadIdx.x & 31;
+  const long long t = static_cast<long long>(blockIdx.x) * kLnWarps + (threadIdx.x >> 5);
+  if (t >= p.T) return;  // whole warp
+  const long long row = t * p.Hs;
+  // 1 + 2: per-shard shifted sums, combined over the shards in order
+  float cnt = 0.f, mean = 0.f, m2 = 0.f;
+  for (int i = 0; i < p.n; ++i) {
+    const T* x = static_cast<const T*>(p.X[i]) + row;
+    const float k = to_f(x[0]);
+    float s1 = 0.f, s2 = 0.f;
+    for (long long c = static_cast<long long>(lane) * VEC; c < p.Hs; c += 32LL * VEC) {
+      float v[VEC];
+      load_vec<T, VEC>(x + c, v);
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) {
+        const float d = v[j] - k;
+        s1 += d;
+        s2 = fmaf(d, d, s2);
+      }
+    }
+    s1 = warp_sum(s1);
+    s2 = warp_sum(s2);
+    const float ci = static_cast<float>(p.Hs);
+    const float mi = k + s1 / ci;
+    const float m2i = fmaxf(s2 - s1 * (s1 / ci), 0.f);
+    const float c2 = cnt + ci;
+    const float d = mi - mean;
+    mean += d * (ci / c2);
+    m2 += m2i + d * d * (cnt * ci / c2);
+    cnt = c2;
+  }
+  const float rstd = rsqrtf(m2 / cnt + p.eps);
+  if (lane == 0) {
+    if (p.mean != nullptr) p.mean[t] = mean;
+    if (p.rstd != nullptr) p.rstd[t] = rstd;
+  }
+  // 3: normalise, scale, shift
+  for (int i = 0; i < p.n; ++i) {
+    const T* x = static_cast<const T*>(p.X[i]) + row;
+    T* y = static_cast<T*>(p.Y[i]) + row;
+    const T* g = static_cast<const T*>(p.gamma[i]);
+    const T* b = static_cast<const T*>(p.beta[i]);
+    for (long long c = static_cast<long long>(lane) * VEC; c < p.Hs; c += 32LL * VEC) {
+      float v[VEC], gv[VEC], bv[VEC];
+      load_vec<T, VEC>(x + c, v);
+      if (g != nullptr) load_vec<T, VEC>(g + c, gv);
+      if (b != nullptr) load_vec<T, VEC>(b + c, bv);
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) {
+        const float h = (v[j] - mean) * rstd;
+        v[j] = fmaf(h, g != nullptr ? gv[j] : 1.f, b != nullptr ? bv[j] : 0.f);
+      }
+      store_vec<T, VEC>(y + c, v);
+    }
+  }
+}
+
+template <typename T, int VEC>
+__global__ void __launch_bounds__(kLnWarps * 32) ln_backward_dx_kernel(const __grid_constant__ LnParams p) {
+  const int lane = threadIdx.x & 31;
+  const long long t = static_cast<long long>(blockIdx.x) * kLnWarps + (threadIdx.x >> 5);
+  if (t >= p.T) return;
+  const long long row = t * p.Hs;
+  const float mean = p.mean[t], rstd = p.rstd[t];
+  // the two row statistics: per shard, then summed over the shards in order
+  float s1 = 0.f, s2 = 0.f;
+  for (int i = 0; i < p.n; ++i) {
+    const T* x = static_cast<const T*>(p.X[i]) + row;
+    const T* dy = static_cast<const T*>(p.dY[i]) + row;
+    const T* g = static_cast<const T*>(p.gamma[i]);
+    float a1 = 0.f, a2 = 0.f;
+    for (long long c = static_cast<long long>(lane) * VEC; c < p.Hs; c += 32LL * VEC) {
+      float v[VEC], d[VEC], gv[VEC];
+      load_vec<T, VEC>(x + c, v);
+      load_vec<T, VEC>(dy + c, d);
+      if (g != nullptr) load_vec<T, VEC>(g + c, gv);
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) {
+        const float gg = d[j] * (g != nullptr ? gv[j] : 1.f);
+        a1 += gg;
+        a2 = fmaf(gg, (v[j] - mean) * rstd, a2);
+      }
+    }
+    s1 += warp_sum(a1);
+    s2 += warp_sum(a2);
+  }
+  const float inv_h = 1.f / static_cast<float>(p.Hs * p.n);
+  const float m1 = s1 * inv_h, m2 = s2 * inv_h;
+  for (int i = 0; i < p.n; ++i) {
+    const T* x = static_cast<const T*>(p.X[i]) + row;
+    const T* dy = static_cast<const T*>(p.dY[i]) + row;
+    const T* g = static_cast<const T*>(p.gamma[i]);
+    T* dx = static_cast<T*>(p.Y[i]) + row;
+    for (long long c = static_cast<long long>(lane) * VEC; c < p.Hs; c += 32LL * VEC) {
+      float v[VEC], d[VEC], gv[VEC];
+      load_vec<T, VEC>(x + c, v);
+      load_vec<T, VEC>(dy + c, d);
+      if (g != nullptr) load_vec<T, VEC>(g + c, gv);
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) {
+        const float gg = d[j] * (g != nullptr ? gv[j] : 1.f);
+        const float h = (v[j] - mean) * rstd;
+        v[j] = rstd * (gg - m1 - h * m2);
+      }
+      store_vec<T, VEC>(dx + c, v);
+    }
+  }
+}
+
+// dgamma_i[c] = sum_t dY_i[t,c] * xhat[t,c], dbeta_i[c] = sum_t dY_i[t,c]. blockIdx.x: a strip
+// of 256 columns of one shard (strips of shard i are consecutive); blockIdx.y = q: tokens
+// [q T / R, (q+1) T / R) of a cluster of R blocks; thread = one column.
+template <typename T>
+__global__ void __launch_bounds__(256) ln_param_grads_kernel(const __grid_constant__ LnParams p) {
+  __shared__ float part[2][256];
+  const long long strips = (p.Hs + 255) / 256;
+  const int i = static_cast<int>(blockIdx.x / strips);
+  const long long c = (blockIdx.x % strips) * 256 + threadIdx.x;
+  const int R = static_cast<int>(gridDim.y), q = static_cast<int>(blockIdx.y);
+  const long long t0 = p.T * q / R, t1 = p.T * (q + 1) / R;
+  float sg = 0.f, sb = 0.f;
+  if (c < p.Hs) {
+    const T* x = static_cast<const T*>(p.X[i]) + c;
+    const T* dy = static_cast<const T*>(p.dY[i]) + c;
+    for (long long t = t0; t < t1; ++t) {
+      const float d = to_f(dy[t * p.Hs]);
+      sg = fmaf(d, (to_f(x[t * p.Hs]) - p.mean[t]) * p.rstd[t], sg);
+      sb += d;
+    }
+  }
+  if (R == 1) {
+    if (c < p.Hs) {
+      if (p.dgamma[i] != nullptr) p.dgamma[i][c] = sg;
+      if (p.dbeta[i] != nullptr) p.dbeta[i][c] = sb;
+    }
+    return;
+  }
+  part[0][threadIdx.x] = sg;
+  part[1][threadIdx.x] = sb;
+  cg::cluster_group cluster = cg::this_cluster();
+  cluster.sync();
+  if (q == 0 && c < p.Hs) {
+    float g = 0.f, b = 0.f;
+    for (int r = 0; r < R; ++r) {
+      const float* o = cluster.map_shared_rank(&part[0][0], r);
+      g += o[threadIdx.x];
+      b += o[256 + threadIdx.x];
+    }
+    if (p.dgamma[i] != nullptr) p.dgamma[i][c] = g;
+    if (p.dbeta[i] != nullptr) p.dbeta[i][c] = b;
+  }
+  cluster.sync();
+}
+
+bool aligned16(const void* ptr) { return reinterpret_cast<uintptr_t>(ptr) % 16 == 0; }
+
+// Vector width usable for every row of every shard (16-byte accesses need 16-byte-aligned
+// shard bases and rows whose byte length is a multiple of 16).
+template <typename T>
+int vec_width(const LnParams& p, bool backward) {
+  constexpr int V = 16 / sizeof(T);
+  if (p.Hs % V != 0) return 1;
+  for (int i = 0; i < p.n; ++i) {
+    if (!aligned16(p.X[i]) || !aligned16(p.Y[i])) return 1;
+    if (p.gamma[i] != nullptr && !aligned16(p.gamma[i])) return 1;
+    if (!backward && p.beta[i] != nullptr && !aligned16(p.beta[i])) return 1;
+    if (backward && !aligned16(p.dY[i])) return 1;
+  }
+  return V;
+}
+
+template <typename T>
+cudaError_t launch_rows(const LnParams& p, bool backward, cudaStream_t st) {
+  constexpr int V = 16 / sizeof(T);
+  const long long blocks = (p.T + kLnWarps - 1) / kLnWarps;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(blocks));
+  const bool vec = vec_width<T>(p, backward) == V;
+  if (!backward) {
+    if (vec)
+      ln_forward_kernel<T, V><<<grid, kLnWarps * 32, 0, st>>>(p);
+    else
+      ln_forward_kernel<T, 1><<<grid, kLnWarps * 32, 0, st>>>(p);
+  } else {
+    if (vec)
+      ln_backward_dx_kernel<T, V><<<grid, kLnWarps * 32, 0, st>>>(p);
+    else
+      ln_backward_dx_kernel<T, 1><<<grid, kLnWarps * 32, 0, st>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_param_grads(const LnParams& p, cudaStream_t st) {
+  const long long strips = ((p.Hs + 255) / 256) * p.n;
+  if (strips > 0x7fffffffLL) return cudaErrorInvalidValue;
+  // blocks per strip: about four per SM in all, at least 64 tokens each, a portable cluster
+  const long long want = (4LL * device_sm_count() + strips - 1) / strips;
+  const int R = static_cast<int>(std::max(1LL, std::min({want, p.T / 64, 8LL})));
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(strips), static_cast<unsigned>(R), 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = static_cast<unsigned>(R);
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, ln_param_grads_kernel<T>, p);
+}
+
+LnParams make(const LnArgs& a) {
+  LnParams p{};
+  for (int i = 0; i < a.n; ++i) {
+    p.X[i] = a.X[i];
+    p.gamma[i] = a.gamma ? a.gamma[i] : nullptr;
+    p.beta[i] = a.beta ? a.beta[i] : nullptr;
+    p.Y[i] = a.Y ? a.Y[i] : nullptr;
+    p.dY[i] = a.dY ? a.dY[i] : nullptr;
+    p.dgamma[i] = a.dgamma ? a.dgamma[i] : nullptr;
+    p.dbeta[i] = a.dbeta ? a.dbeta[i] : nullptr;
+  }
+  p.mean = a.mean;
+  p.rstd = a.rstd;
+  p.T = a.T;
+  p.Hs = a.Hs;
+  p.n = a.n;
+  p.eps = a.eps;
+  return p;
+}
+
+}  // namespace
+
+cudaError_t launch_ln_forward(const LnArgs& a, cudaStream_t st) {
+  if (a.T == 0) return cudaSuccess;
+  const LnParams p = make(a);
+  return a.bf16 ? launch_rows<__nv_bfloat16>(p, false, st) : launch_rows<float>(p, false, st);
+}
+
+cudaError_t launch_ln_backward_dx(const LnArgs& a, cudaStream_t st) {
+  if (a.T == 0) return cudaSuccess;
+  const LnParams p = make(a);
+  return a.bf16 ? launch_rows<__nv_bfloat16>(p, true, st) : launch_rows<float>(p, true, st);
+}
+
+cudaError_t launch_ln_param_grads(const LnArgs& a, cudaStream_t st) {
+  const LnParams p = make(a);
+  if (a.T == 0) {
+    for (int i = 0; i < a.n; ++i) {
+      if (p.dgamma[i] != nullptr) {
+        cudaError_t e = cudaMemsetAsync(p.dgamma[i], 0, size_t(a.Hs) * 4, st);
+        if (e != cudaSuccess) return e;
+      }
+      if (p.dbeta[i] != nullptr) {
+        cudaError_t e = cudaMemsetAsync(p.dbeta[i], 0, size_t(a.Hs) * 4, st);
+        if (e != cudaSuccess) return e;
+      }
+    }
+    return cudaSuccess;
+  }
+  return a.bf16 ? launch_param_grads<__nv_bfloat16>(p, st) : launch_param_grads<float>(p, st);
+}
+
+}  // namespace tpk

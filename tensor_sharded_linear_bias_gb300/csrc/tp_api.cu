@@ -3,6 +3,7 @@
 // host code only checks arguments and enqueues launches on the caller's stream.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <algorithm>
@@ -1057,6 +1058,115 @@ tp_status tp_linear_row_backward(const tp_linear_desc* desc, const void* const* 
     ColsumSeg seg{dZ, static_cast<float*>(dbias), z.N, z.N};
     TP_TRY(colsums(dt, z.T, &seg, 1, st));
   }
+  return ok();
+}
+
+// ------------------------------------------------------------------ hidden-split LayerNorm
+}  // extern "C"
+
+namespace {
+
+tp_status ln_validate(const tp_layernorm_desc* d, int64_t* Hs) {
+  if (d == nullptr) return fail(TP_ERR_NULL, "desc is NULL");
+  TP_TRY(check_common(d->tokens, d->tp_degree, d->dtype, TP_ACT_NONE, TP_REDUCE_FUSED));
+  TP_TRY(check_dim("hidden", d->hidden));
+  if (d->hidden % d->tp_degree != 0)
+    return fail(TP_ERR_INDIVISIBLE, "hidden %lld is not divisible by tp_degree %d",
+                static_cast<long long>(d->hidden), d->tp_degree);
+  if (!(d->eps > 0.0f) || !std::isfinite(d->eps)) return fail(TP_ERR_SHAPE, "eps must be > 0");
+  *Hs = d->hidden / d->tp_degree;
+  TP_TRY(check_width(d->dtype, "hidden / tp_degree", *Hs));
+  return TP_OK;
+}
+
+tp_status check_f32_ptr(const char* name, const void* p, bool required) {
+  return check_ptr(TP_F32, name, p, required);
+}
+
+}  // namespace
+
+extern "C" {
+
+tp_status tp_layernorm_forward(const tp_layernorm_desc* desc, const void* const* X,
+                               const void* const* gamma, const void* const* beta, void* const* Y,
+                               float* mean, float* rstd, void* stream) {
+  int64_t Hs = 0;
+  TP_TRY(ln_validate(desc, &Hs));
+  const int dt = desc->dtype, n = desc->tp_degree;
+  const int64_t T = desc->tokens;
+  TP_TRY(check_ptr_array(dt, "X", X, n, T > 0, T > 0));
+  TP_TRY(check_ptr_array(dt, "gamma", gamma, n, false));
+  TP_TRY(check_ptr_array(dt, "beta", beta, n, false));
+  TP_TRY(check_ptr_array(dt, "Y", reinterpret_cast<const void* const*>(Y), n, T > 0, T > 0));
+  TP_TRY(check_f32_ptr("mean", mean, false));
+  TP_TRY(check_f32_ptr("rstd", rstd, false));
+  TP_TRY(check_arch());
+  if (T == 0) return ok();
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  LnArgs a;
+  a.X = X;
+  a.gamma = gamma;
+  a.beta = beta;
+  a.Y = Y;
+  a.mean = mean;
+  a.rstd = rstd;
+  a.T = T;
+  a.Hs = Hs;
+  a.n = n;
+  a.eps = desc->eps;
+  a.bf16 = dt == TP_BF16;
+  const double e = elem_size(dt), H = double(Hs) * n;
+  const double bytes = double(T) * H * 2.0 * e + ((gamma ? 1 : 0) + (beta ? 1 : 0)) * H * e +
+                       (mean ? 4.0 * T : 0.0) + (rstd ? 4.0 * T : 0.0);
+  TP_CUDA(traced(TP_K_LAYERNORM, TP_TAG_LN_FWD, n, 0.0, bytes, st,
+                 [&] { return launch_ln_forward(a, st); }),
+          "LayerNorm forward");
+  return ok();
+}
+
+tp_status tp_layernorm_backward(const tp_layernorm_desc* desc, const void* const* X,
+                                const void* const* gamma, const float* mean, const float* rstd,
+                                const void* const* dY, void* const* dX, float* const* dgamma,
+                                float* const* dbeta, void* stream) {
+  int64_t Hs = 0;
+  TP_TRY(ln_validate(desc, &Hs));
+  const int dt = desc->dtype, n = desc->tp_degree;
+  const int64_t T = desc->tokens;
+  TP_TRY(check_ptr_array(dt, "X", X, n, T > 0, T > 0));
+  TP_TRY(check_ptr_array(dt, "gamma", gamma, n, false));
+  TP_TRY(check_ptr_array(dt, "dY", dY, n, T > 0, T > 0));
+  TP_TRY(check_ptr_array(dt, "dX", reinterpret_cast<const void* const*>(dX), n, T > 0, T > 0));
+  TP_TRY(check_ptr_array(TP_F32, "dgamma", reinterpret_cast<const void* const*>(dgamma), n, false));
+  TP_TRY(check_ptr_array(TP_F32, "dbeta", reinterpret_cast<const void* const*>(dbeta), n, false));
+  TP_TRY(check_f32_ptr("mean", mean, T > 0));
+  TP_TRY(check_f32_ptr("rstd", rstd, T > 0));
+  TP_TRY(check_arch());
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  LnArgs a;
+  a.X = X;
+  a.gamma = gamma;
+  a.Y = dX;
+  a.dY = dY;
+  a.dgamma = dgamma;
+  a.dbeta = dbeta;
+  a.mean = const_cast<float*>(mean);
+  a.rstd = const_cast<float*>(rstd);
+  a.T = T;
+  a.Hs = Hs;
+  a.n = n;
+  a.eps = desc->eps;
+  a.bf16 = dt == TP_BF16;
+  const double e = elem_size(dt), H = double(Hs) * n;
+  if (T > 0)
+    TP_CUDA(traced(TP_K_LAYERNORM, TP_TAG_LN_DGRAD, n, 0.0,
+                   double(T) * H * 3.0 * e + (gamma ? H * e : 0.0) + 8.0 * T, st,
+                   [&] { return launch_ln_backward_dx(a, st); }),
+            "LayerNorm input gradient");
+  if (dgamma != nullptr || dbeta != nullptr)
+    TP_CUDA(traced(TP_K_LN_PARAM_GRAD, TP_TAG_LN_PARAM_GRAD, n, 0.0,
+                   double(T) * H * 2.0 * e + 8.0 * T + 8.0 * H, st,
+                   [&] { return launch_ln_param_grads(a, st); }),
+            "LayerNorm parameter gradients");
   return ok();
 }
 

@@ -206,3 +206,18 @@ def test_header_tail_scratch_matches_binding(tp):
     kinds = dict((int(v), k) for k, v in re.findall(r"(TP_K_\w+) = (\d+)", text))
     assert {k: v.lower()[5:] for k, v in kinds.items()} == {
         k: v for k, v in tp.KERNEL_NAMES.items()}
+
+
+def test_layernorm_desc_validation(tp):
+    ok = dict(tokens=0, hidden=64, tp_degree=4, dtype=tp.TP_BF16, eps=1e-5)
+
+    def fwd(**kw):
+        return status_of(lambda: tp.tp_layernorm_forward(tp.LayerNormDesc(**{**ok, **kw}), None,
+                                                         None, None, None, None, None, 0))
+    assert fwd(hidden=66) == "TP_ERR_INDIVISIBLE"
+    assert fwd(hidden=4 * 12) == "TP_ERR_ALIGN"       # bf16 shard width must be a multiple of 8
+    assert fwd(eps=0.0) == "TP_ERR_SHAPE"
+    assert fwd(tp_degree=65) == "TP_ERR_SHAPE"
+    assert fwd(dtype=9) == "TP_ERR_DTYPE"
+    assert fwd(tokens=8) == "TP_ERR_NULL"              # X is required when there are tokens
+    assert fwd(dtype=tp.TP_F32, hidden=4 * 12) in ("TP_OK", "TP_ERR_ARCH")  # fp32: any width
