@@ -31,6 +31,7 @@ namespace tpk {
 namespace {
 
 constexpr int kLnWarps = 8;  // token rows per block (one per warp)
+constexpr int kUnroll = 4;   // 16-byte loads in flight per lane and operand
 
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
@@ -95,14 +96,22 @@ __global__ void __launch_bounds__(kLnWarps * 32) ln_forward_kernel(const __grid_
     const T* x = static_cast<const T*>(p.X[i]) + row;
     const float k = to_f(x[0]);
     float s1 = 0.f, s2 = 0.f;
-    for (long long c = static_cast<long long>(lane) * VEC; c < p.Hs; c += 32LL * VEC) {
-      float v[VEC];
-      load_vec<T, VEC>(x + c, v);
+    for (long long c0 = static_cast<long long>(lane) * VEC; c0 < p.Hs; c0 += 32LL * VEC * kUnroll) {
+      float v[kUnroll][VEC];
 #pragma unroll
-      for (int j = 0; j < VEC; ++j) {
-        const float d = v[j] - k;
-        s1 += d;
-        s2 = fmaf(d, d, s2);
+      for (int u = 0; u < kUnroll; ++u) {  // kUnroll loads in flight
+        const long long c = c0 + 32LL * VEC * u;
+        if (c < p.Hs) load_vec<T, VEC>(x + c, v[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        if (c0 + 32LL * VEC * u >= p.Hs) break;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+          const float d = v[u][j] - k;
+          s1 += d;
+          s2 = fmaf(d, d, s2);
+        }
       }
     }
     s1 = warp_sum(s1);
@@ -156,16 +165,28 @@ __global__ void __launch_bounds__(kLnWarps * 32) ln_backward_dx_kernel(const __g
     const T* dy = static_cast<const T*>(p.dY[i]) + row;
     const T* g = static_cast<const T*>(p.gamma[i]);
     float a1 = 0.f, a2 = 0.f;
-    for (long long c = static_cast<long long>(lane) * VEC; c < p.Hs; c += 32LL * VEC) {
-      float v[VEC], d[VEC], gv[VEC];
-      load_vec<T, VEC>(x + c, v);
-      load_vec<T, VEC>(dy + c, d);
-      if (g != nullptr) load_vec<T, VEC>(g + c, gv);
+    for (long long c0 = static_cast<long long>(lane) * VEC; c0 < p.Hs; c0 += 32LL * VEC * kUnroll) {
+      float v[kUnroll][VEC], d[kUnroll][VEC];
 #pragma unroll
-      for (int j = 0; j < VEC; ++j) {
-        const float gg = d[j] * (g != nullptr ? gv[j] : 1.f);
-        a1 += gg;
-        a2 = fmaf(gg, (v[j] - mean) * rstd, a2);
+      for (int u = 0; u < kUnroll; ++u) {
+        const long long c = c0 + 32LL * VEC * u;
+        if (c < p.Hs) {
+          load_vec<T, VEC>(x + c, v[u]);
+          load_vec<T, VEC>(dy + c, d[u]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const long long c = c0 + 32LL * VEC * u;
+        if (c >= p.Hs) break;
+        float gv[VEC];
+        if (g != nullptr) load_vec<T, VEC>(g + c, gv);
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+          const float gg = d[u][j] * (g != nullptr ? gv[j] : 1.f);
+          a1 += gg;
+          a2 = fmaf(gg, (v[u][j] - mean) * rstd, a2);
+        }
       }
     }
     s1 += warp_sum(a1);
@@ -196,9 +217,11 @@ __global__ void __launch_bounds__(kLnWarps * 32) ln_backward_dx_kernel(const __g
 
 // dgamma_i[c] = sum_t dY_i[t,c] * xhat[t,c], dbeta_i[c] = sum_t dY_i[t,c]. blockIdx.x: a strip
 // of 256 columns of one shard (strips of shard i are consecutive); blockIdx.y = q: tokens
-// [q T / R, (q+1) T / R) of a cluster of R blocks; thread = one column.
+// [q T / R, (q+1) T / R) of a cluster of R blocks; thread = one column, eight tokens' loads in
+// flight, added in token order.
 template <typename T>
 __global__ void __launch_bounds__(256) ln_param_grads_kernel(const __grid_constant__ LnParams p) {
+  constexpr int U = 8;
   __shared__ float part[2][256];
   const long long strips = (p.Hs + 255) / 256;
   const int i = static_cast<int>(blockIdx.x / strips);
@@ -209,7 +232,23 @@ __global__ void __launch_bounds__(256) ln_param_grads_kernel(const __grid_consta
   if (c < p.Hs) {
     const T* x = static_cast<const T*>(p.X[i]) + c;
     const T* dy = static_cast<const T*>(p.dY[i]) + c;
-    for (long long t = t0; t < t1; ++t) {
+    long long t = t0;
+    for (; t + U <= t1; t += U) {
+      float xv[U], dv[U], mv[U], rv[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        xv[u] = to_f(x[(t + u) * p.Hs]);
+        dv[u] = to_f(dy[(t + u) * p.Hs]);
+        mv[u] = p.mean[t + u];
+        rv[u] = p.rstd[t + u];
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        sg = fmaf(dv[u], (xv[u] - mv[u]) * rv[u], sg);
+        sb += dv[u];
+      }
+    }
+    for (; t < t1; ++t) {
       const float d = to_f(dy[t * p.Hs]);
       sg = fmaf(d, (to_f(x[t * p.Hs]) - p.mean[t]) * p.rstd[t], sg);
       sb += d;
