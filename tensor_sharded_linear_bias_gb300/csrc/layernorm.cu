@@ -44,9 +44,10 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
   return __float2bfloat16_rn(v);
 }
 
-// VEC consecutive elements of one row: one 16-byte access when VEC * sizeof(T) == 16.
+// VEC consecutive elements of one row: one 16-byte access when VEC * sizeof(T) == 16 (the
+// alignment makes the compiler emit a single vector load or store).
 template <typename T, int VEC>
-struct Vec {
+struct alignas(sizeof(T) * VEC) Vec {
   T v[VEC];
 };
 template <typename T, int VEC>
