@@ -41,6 +41,14 @@ __device__ __forceinline__ float gelu_erf_grad(float h) {
   return fmaf(h * 0.3989422804014327f, n.e, n.cdf);
 }
 
+// ------------------------------------------------------------------ L2 prefetch
+// Ask L2 for `bytes` bytes of global memory from ptr (16-byte aligned, a multiple of 16 bytes).
+__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(__cvta_generic_to_global(ptr)),
+               "r"(bytes)
+               : "memory");
+}
+
 // ------------------------------------------------------------------ bf16 packing
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

@@ -91,6 +91,11 @@ __global__ void __launch_bounds__(kLnWarps * 32) ln_forward_kernel(const __grid_
   const long long t = static_cast<long long>(blockIdx.x) * kLnWarps + (threadIdx.x >> 5);
   if (t >= p.T) return;  // whole warp
   const long long row = t * p.Hs;
+  // the whole row requested into L2 at once (one bulk prefetch per shard), so that the
+  // shard-by-shard passes below wait on L2, not on one DRAM round trip per shard
+  if (VEC > 1)
+    for (int i = lane; i < p.n; i += 32)
+      prefetch_l2(static_cast<const T*>(p.X[i]) + row, static_cast<uint32_t>(p.Hs * sizeof(T)));
   // 1 + 2: per-shard shifted sums, combined over the shards in order
   float cnt = 0.f, mean = 0.f, m2 = 0.f;
   for (int i = 0; i < p.n; ++i) {
@@ -158,6 +163,11 @@ __global__ void __launch_bounds__(kLnWarps * 32) ln_backward_dx_kernel(const __g
   const long long t = static_cast<long long>(blockIdx.x) * kLnWarps + (threadIdx.x >> 5);
   if (t >= p.T) return;
   const long long row = t * p.Hs;
+  if (VEC > 1)
+    for (int i = lane; i < p.n; i += 32) {
+      prefetch_l2(static_cast<const T*>(p.X[i]) + row, static_cast<uint32_t>(p.Hs * sizeof(T)));
+      prefetch_l2(static_cast<const T*>(p.dY[i]) + row, static_cast<uint32_t>(p.Hs * sizeof(T)));
+    }
   const float mean = p.mean[t], rstd = p.rstd[t];
   // the two row statistics: per shard, then summed over the shards in order
   float s1 = 0.f, s2 = 0.f;

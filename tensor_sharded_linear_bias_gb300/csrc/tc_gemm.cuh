@@ -295,12 +295,6 @@ __device__ __forceinline__ void warp_unpack_bf16(uint8_t* stage, const uint4* ra
   __syncwarp();
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(__cvta_generic_to_global(ptr)),
-               "r"(bytes)
-               : "memory");
-}
-
 // EPI_DACT with an activation reads the saved pre-activation at every output element.
 __device__ __forceinline__ bool dact_reads_aux(const TcParams& p) {
   return p.epi == EPI_DACT && p.act == TP_ACT_GELU_ERF;
