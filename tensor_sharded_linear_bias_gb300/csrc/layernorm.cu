@@ -4,8 +4,7 @@
 // separate buffers; the All-Reduce of the statistics is a combination, in shard order, inside
 // the warp that owns the token row.
 //
-// Forward, one warp per token row (or one block per row when the row fits the block's
-// registers, below):
+// Forward, one warp per token row:
 //   1. per shard i: every lane sums x - k_i and (x - k_i)^2 over its elements (k_i = the
 //      shard's first element of the row: a shift that keeps the sums well conditioned), the
 //      warp adds the lanes in a fixed butterfly, giving the shard's count, mean and M2;
@@ -32,7 +31,7 @@ namespace tpk {
 namespace {
 
 constexpr int kLnWarps = 8;  // token rows per block (one per warp)
-constexpr int kUnroll = 4;   // 16-byte loads in flight per lane and operand
+constexpr int kUnroll = 8;   // 16-byte loads in flight per lane and operand
 
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
@@ -290,175 +289,6 @@ __global__ void __launch_bounds__(256) ln_param_grads_kernel(const __grid_consta
   cluster.sync();
 }
 
-// ------------------------------------------------------------------ one block per row
-// When a row fits in the registers of one 256-thread block (at most kSlots 16-byte vectors per
-// thread: n * ceil(H/n / 2048) <= 8 for bf16), the whole row is loaded at once (every load in
-// flight together), reduced across the block in a fixed order, and written back from the
-// registers: one DRAM read of X per row instead of a warp's shard-by-shard round trips.
-// Thread `tid` holds, for shard i, the vectors j = tid + 256 r (r < nv = ceil(H/n/VEC/256))
-// in slot s = i * nv + r.
-constexpr int kRowThreads = 256;
-constexpr int kSlots = 8;
-
-// Sums each of K values over the block's threads in a fixed order (lanes by butterfly, then
-// warps in order); every thread gets the sums. red: kRowThreads / 32 * K floats of shared
-// memory.
-template <int K>
-__device__ __forceinline__ void block_sums(float (&v)[K], float* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int k = 0; k < K; ++k) v[k] = warp_sum(v[k]);
-  if (lane == 0) {
-#pragma unroll
-    for (int k = 0; k < K; ++k) red[warp * K + k] = v[k];
-  }
-  __syncthreads();
-#pragma unroll
-  for (int k = 0; k < K; ++k) {
-    float t = 0.f;
-#pragma unroll
-    for (int w = 0; w < kRowThreads / 32; ++w) t += red[w * K + k];
-    v[k] = t;
-  }
-  __syncthreads();
-}
-
-template <typename T, int VEC>
-__global__ void __launch_bounds__(kRowThreads) ln_forward_row_kernel(const __grid_constant__ LnParams p) {
-  __shared__ float red[kRowThreads / 32 * 2 * kSlots];
-  const long long row = static_cast<long long>(blockIdx.x) * p.Hs;
-  const int tid = threadIdx.x;
-  const long long vps = p.Hs / VEC;                       // vectors per shard row
-  const int nv = static_cast<int>((vps + kRowThreads - 1) / kRowThreads);
-  const int S = p.n * nv;                                  // slots in use (<= kSlots)
-  float v[kSlots][VEC];
-  float st[2 * kSlots];                                    // per slot: sum(x - k), sum((x - k)^2)
-  float kk[kSlots];
-#pragma unroll
-  for (int s = 0; s < kSlots; ++s) {
-    st[2 * s] = st[2 * s + 1] = 0.f;
-    kk[s] = 0.f;
-    if (s >= S) continue;
-    const int i = s / nv;
-    const long long j = tid + static_cast<long long>(kRowThreads) * (s % nv);
-    const T* x = static_cast<const T*>(p.X[i]) + row;
-    kk[s] = to_f(x[0]);                                    // the shard's shift
-    if (j < vps) load_vec<T, VEC>(x + j * VEC, v[s]);
-  }
-#pragma unroll
-  for (int s = 0; s < kSlots; ++s) {
-    if (s >= S || tid + static_cast<long long>(kRowThreads) * (s % nv) >= vps) continue;
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-      const float d = v[s][e] - kk[s];
-      st[2 * s] += d;
-      st[2 * s + 1] = fmaf(d, d, st[2 * s + 1]);
-    }
-  }
-  block_sums<2 * kSlots>(st, red);
-  // per shard: its slots' sums, then the shards combined in order (Chan et al.)
-  float cnt = 0.f, mean = 0.f, m2 = 0.f;
-  const float ci = static_cast<float>(p.Hs);
-  for (int i = 0; i < p.n; ++i) {
-    float s1 = 0.f, s2 = 0.f, k = 0.f;
-#pragma unroll
-    for (int s = 0; s < kSlots; ++s)
-      if (s / nv == i && s < S) {
-        s1 += st[2 * s];
-        s2 += st[2 * s + 1];
-        k = kk[s];
-      }
-    const float mi = k + s1 / ci;
-    const float m2i = fmaxf(s2 - s1 * (s1 / ci), 0.f);
-    const float c2 = cnt + ci;
-    const float d = mi - mean;
-    mean += d * (ci / c2);
-    m2 += m2i + d * d * (cnt * ci / c2);
-    cnt = c2;
-  }
-  const float rstd = rsqrtf(m2 / cnt + p.eps);
-  if (tid == 0) {
-    if (p.mean != nullptr) p.mean[blockIdx.x] = mean;
-    if (p.rstd != nullptr) p.rstd[blockIdx.x] = rstd;
-  }
-#pragma unroll
-  for (int s = 0; s < kSlots; ++s) {
-    if (s >= S) continue;
-    const int i = s / nv;
-    const long long j = tid + static_cast<long long>(kRowThreads) * (s % nv);
-    if (j >= vps) continue;
-    const T* g = static_cast<const T*>(p.gamma[i]);
-    const T* b = static_cast<const T*>(p.beta[i]);
-    float gv[VEC], bv[VEC];
-    if (g != nullptr) load_vec<T, VEC>(g + j * VEC, gv);
-    if (b != nullptr) load_vec<T, VEC>(b + j * VEC, bv);
-#pragma unroll
-    for (int e = 0; e < VEC; ++e)
-      v[s][e] = fmaf((v[s][e] - mean) * rstd, g != nullptr ? gv[e] : 1.f, b != nullptr ? bv[e] : 0.f);
-    store_vec<T, VEC>(static_cast<T*>(p.Y[i]) + row + j * VEC, v[s]);
-  }
-}
-
-template <typename T, int VEC>
-__global__ void __launch_bounds__(kRowThreads) ln_backward_row_kernel(const __grid_constant__ LnParams p) {
-  __shared__ float red[kRowThreads / 32 * 2 * kSlots];
-  const long long row = static_cast<long long>(blockIdx.x) * p.Hs;
-  const int tid = threadIdx.x;
-  const long long vps = p.Hs / VEC;
-  const int nv = static_cast<int>((vps + kRowThreads - 1) / kRowThreads);
-  const int S = p.n * nv;
-  const float mean = p.mean[blockIdx.x], rstd = p.rstd[blockIdx.x];
-  float h[kSlots][VEC], gd[kSlots][VEC];  // xhat and dY * gamma of the thread's vectors
-  float st[2 * kSlots];
-#pragma unroll
-  for (int s = 0; s < kSlots; ++s) {
-    st[2 * s] = st[2 * s + 1] = 0.f;
-    if (s >= S) continue;
-    const int i = s / nv;
-    const long long j = tid + static_cast<long long>(kRowThreads) * (s % nv);
-    if (j >= vps) continue;
-    load_vec<T, VEC>(static_cast<const T*>(p.X[i]) + row + j * VEC, h[s]);
-    load_vec<T, VEC>(static_cast<const T*>(p.dY[i]) + row + j * VEC, gd[s]);
-  }
-#pragma unroll
-  for (int s = 0; s < kSlots; ++s) {
-    if (s >= S) continue;
-    const int i = s / nv;
-    const long long j = tid + static_cast<long long>(kRowThreads) * (s % nv);
-    if (j >= vps) continue;
-    const T* g = static_cast<const T*>(p.gamma[i]);
-    float gv[VEC];
-    if (g != nullptr) load_vec<T, VEC>(g + j * VEC, gv);
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-      h[s][e] = (h[s][e] - mean) * rstd;
-      gd[s][e] *= g != nullptr ? gv[e] : 1.f;
-      st[2 * s] += gd[s][e];
-      st[2 * s + 1] = fmaf(gd[s][e], h[s][e], st[2 * s + 1]);
-    }
-  }
-  block_sums<2 * kSlots>(st, red);
-  float s1 = 0.f, s2 = 0.f;  // over the shards in order (slot order is shard order)
-#pragma unroll
-  for (int s = 0; s < kSlots; ++s)
-    if (s < S) {
-      s1 += st[2 * s];
-      s2 += st[2 * s + 1];
-    }
-  const float inv_h = 1.f / static_cast<float>(p.Hs * p.n);
-  const float m1 = s1 * inv_h, m2 = s2 * inv_h;
-#pragma unroll
-  for (int s = 0; s < kSlots; ++s) {
-    if (s >= S) continue;
-    const int i = s / nv;
-    const long long j = tid + static_cast<long long>(kRowThreads) * (s % nv);
-    if (j >= vps) continue;
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) gd[s][e] = rstd * (gd[s][e] - m1 - h[s][e] * m2);
-    store_vec<T, VEC>(static_cast<T*>(p.Y[i]) + row + j * VEC, gd[s]);
-  }
-}
-
 bool aligned16(const void* ptr) { return reinterpret_cast<uintptr_t>(ptr) % 16 == 0; }
 
 // Vector width usable for every row of every shard (16-byte accesses need 16-byte-aligned
@@ -483,16 +313,6 @@ cudaError_t launch_rows(const LnParams& p, bool backward, cudaStream_t st) {
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(blocks));
   const bool vec = vec_width<T>(p, backward) == V;
-  const long long nv = (p.Hs / V + kRowThreads - 1) / kRowThreads;
-  if (vec && p.n * nv <= kSlots) {  // the row fits one block's registers
-    if (p.T > 0x7fffffffLL) return cudaErrorInvalidValue;
-    const dim3 rows(static_cast<unsigned>(p.T));
-    if (!backward)
-      ln_forward_row_kernel<T, V><<<rows, kRowThreads, 0, st>>>(p);
-    else
-      ln_backward_row_kernel<T, V><<<rows, kRowThreads, 0, st>>>(p);
-    return cudaGetLastError();
-  }
   if (!backward) {
     if (vec)
       ln_forward_kernel<T, V><<<grid, kLnWarps * 32, 0, st>>>(p);

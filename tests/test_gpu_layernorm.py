@@ -80,9 +80,8 @@ class LnCase:
                                          ("bf16", 33, 16, 1), ("f32", 130, 3 * 77, 3),
                                          ("f32", 64, 8 * 96, 8), ("bf16", 40, 16 * 2048, 16)])
 def test_layernorm_matches_oracle(tp, dtype, T, H, n):
-    """One block per row when the row fits its registers (n * ceil(H/n / (256 * 16 bytes))
-    <= 8 vectors per thread), else one warp per row (the 16-shard case), and the scalar path
-    for fp32 rows that are not 16-byte multiples (77 columns per shard)."""
+    """16-byte accesses for bf16 rows and fp32 rows that allow them (up to 16 shards), and
+    the scalar path for fp32 rows that are not 16-byte multiples (77 columns per shard)."""
     errs = LnCase(tp, T, H, n, dtype).run().errors()
     assert max(errs.values()) <= (TOL_BF16 if dtype == "bf16" else TOL_F32), errs
 
