@@ -31,7 +31,7 @@ namespace tpk {
 namespace {
 
 constexpr int kLnWarps = 8;  // token rows per block (one per warp)
-constexpr int kUnroll = 8;   // 16-byte loads in flight per lane and operand
+constexpr int kUnroll = 4;   // 16-byte loads in flight per lane and operand
 
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
