@@ -2,9 +2,10 @@
 // principle and practice", section 4.2: each device computes the mean and variance of its own
 // part and the statistics are synchronised by an All-Reduce). All shards live on this GPU as
 // separate buffers; the All-Reduce of the statistics is a combination, in shard order, inside
-// the warp that owns the token row.
+// the block that owns the token row.
 //
-// Forward, one warp per token row:
+// Forward, one block per token row, its warps taking the shards in turn (warp w: shards w,
+// w + 8, ...):
 //   1. per shard i: every lane sums x - k_i and (x - k_i)^2 over its elements (k_i = the
 //      shard's first element of the row: a shift that keeps the sums well conditioned), the
 //      warp adds the lanes in a fixed butterfly, giving the shard's count, mean and M2;
@@ -13,8 +14,9 @@
 //      computing sample variances", 1979): the row's mean and biased variance;
 //   3. y = (x - mean) * rstd * gamma + beta for every shard (the row's bytes are re-read from
 //      L1/L2), and mean, rstd are stored for the backward.
-// Backward dX, one warp per row: the row statistics sum(dY*gamma) and sum(dY*gamma*xhat) are
-// summed per shard, then over the shards in order, and dX = rstd * (g - (s1 + xhat s2) / H).
+// Backward dX, one block per row likewise: the row statistics sum(dY*gamma) and
+// sum(dY*gamma*xhat) are summed per shard, then over the shards in order, and
+// dX = rstd * (g - (s1 + xhat s2) / H).
 // Backward dgamma, dbeta: column sums over the tokens, split over the blocks of a cluster and
 // combined in block order through distributed shared memory (deterministic, no atomics).
 #include <cooperative_groups.h>
@@ -30,7 +32,7 @@ namespace cg = cooperative_groups;
 namespace tpk {
 namespace {
 
-constexpr int kLnWarps = 8;  // token rows per block (one per warp)
+constexpr int kLnWarps = 8;  // warps per block (one token row per block, warps over its shards)
 constexpr int kUnroll = 4;   // 16-byte loads in flight per lane and operand
 
 __device__ __forceinline__ float to_f(float v) { return v; }
@@ -87,18 +89,12 @@ struct LnParams {
 
 template <typename T, int VEC>
 __global__ void __launch_bounds__(kLnWarps * 32) ln_forward_kernel(const __grid_constant__ LnParams p) {
-  const int lane = threadIdx.x & 31;
-  const long long t = static_cast<long long>(blockIdx.x) * kLnWarps + (threadIdx.x >> 5);
-  if (t >= p.T) return;  // whole warp
+  __shared__ float stat[kMaxShards][2];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, W = blockDim.x >> 5;
+  const long long t = blockIdx.x;
   const long long row = t * p.Hs;
-  // the whole row requested into L2 at once (one bulk prefetch per shard), so that the
-  // shard-by-shard passes below wait on L2, not on one DRAM round trip per shard
-  if (VEC > 1)
-    for (int i = lane; i < p.n; i += 32)
-      prefetch_l2(static_cast<const T*>(p.X[i]) + row, static_cast<uint32_t>(p.Hs * sizeof(T)));
-  // 1 + 2: per-shard shifted sums, combined over the shards in order
-  float cnt = 0.f, mean = 0.f, m2 = 0.f;
-  for (int i = 0; i < p.n; ++i) {
+  // 1: every warp takes shards warp, warp + W, ...: the shard's shifted sums -> (mean_i, M2_i)
+  for (int i = warp; i < p.n; i += W) {
     const T* x = static_cast<const T*>(p.X[i]) + row;
     const float k = to_f(x[0]);
     float s1 = 0.f, s2 = 0.f;
@@ -123,21 +119,29 @@ __global__ void __launch_bounds__(kLnWarps * 32) ln_forward_kernel(const __grid_
     s1 = warp_sum(s1);
     s2 = warp_sum(s2);
     const float ci = static_cast<float>(p.Hs);
-    const float mi = k + s1 / ci;
-    const float m2i = fmaxf(s2 - s1 * (s1 / ci), 0.f);
+    if (lane == 0) {
+      stat[i][0] = k + s1 / ci;
+      stat[i][1] = fmaxf(s2 - s1 * (s1 / ci), 0.f);
+    }
+  }
+  __syncthreads();
+  // 2: the shards' statistics combined in shard order (every thread, same result)
+  float cnt = 0.f, mean = 0.f, m2 = 0.f;
+  const float ci = static_cast<float>(p.Hs);
+  for (int i = 0; i < p.n; ++i) {
     const float c2 = cnt + ci;
-    const float d = mi - mean;
+    const float d = stat[i][0] - mean;
     mean += d * (ci / c2);
-    m2 += m2i + d * d * (cnt * ci / c2);
+    m2 += stat[i][1] + d * d * (cnt * ci / c2);
     cnt = c2;
   }
   const float rstd = rsqrtf(m2 / cnt + p.eps);
-  if (lane == 0) {
+  if (threadIdx.x == 0) {
     if (p.mean != nullptr) p.mean[t] = mean;
     if (p.rstd != nullptr) p.rstd[t] = rstd;
   }
-  // 3: normalise, scale, shift
-  for (int i = 0; i < p.n; ++i) {
+  // 3: normalise, scale, shift (each warp its shards again: the bytes are in L1/L2)
+  for (int i = warp; i < p.n; i += W) {
     const T* x = static_cast<const T*>(p.X[i]) + row;
     T* y = static_cast<T*>(p.Y[i]) + row;
     const T* g = static_cast<const T*>(p.gamma[i]);
@@ -159,19 +163,13 @@ __global__ void __launch_bounds__(kLnWarps * 32) ln_forward_kernel(const __grid_
 
 template <typename T, int VEC>
 __global__ void __launch_bounds__(kLnWarps * 32) ln_backward_dx_kernel(const __grid_constant__ LnParams p) {
-  const int lane = threadIdx.x & 31;
-  const long long t = static_cast<long long>(blockIdx.x) * kLnWarps + (threadIdx.x >> 5);
-  if (t >= p.T) return;
+  __shared__ float stat[kMaxShards][2];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, W = blockDim.x >> 5;
+  const long long t = blockIdx.x;
   const long long row = t * p.Hs;
-  if (VEC > 1)
-    for (int i = lane; i < p.n; i += 32) {
-      prefetch_l2(static_cast<const T*>(p.X[i]) + row, static_cast<uint32_t>(p.Hs * sizeof(T)));
-      prefetch_l2(static_cast<const T*>(p.dY[i]) + row, static_cast<uint32_t>(p.Hs * sizeof(T)));
-    }
   const float mean = p.mean[t], rstd = p.rstd[t];
-  // the two row statistics: per shard, then summed over the shards in order
-  float s1 = 0.f, s2 = 0.f;
-  for (int i = 0; i < p.n; ++i) {
+  // the two row statistics: per shard (warps over shards), then summed over the shards in order
+  for (int i = warp; i < p.n; i += W) {
     const T* x = static_cast<const T*>(p.X[i]) + row;
     const T* dy = static_cast<const T*>(p.dY[i]) + row;
     const T* g = static_cast<const T*>(p.gamma[i]);
@@ -200,12 +198,22 @@ __global__ void __launch_bounds__(kLnWarps * 32) ln_backward_dx_kernel(const __g
         }
       }
     }
-    s1 += warp_sum(a1);
-    s2 += warp_sum(a2);
+    a1 = warp_sum(a1);
+    a2 = warp_sum(a2);
+    if (lane == 0) {
+      stat[i][0] = a1;
+      stat[i][1] = a2;
+    }
+  }
+  __syncthreads();
+  float s1 = 0.f, s2 = 0.f;
+  for (int i = 0; i < p.n; ++i) {
+    s1 += stat[i][0];
+    s2 += stat[i][1];
   }
   const float inv_h = 1.f / static_cast<float>(p.Hs * p.n);
   const float m1 = s1 * inv_h, m2 = s2 * inv_h;
-  for (int i = 0; i < p.n; ++i) {
+  for (int i = warp; i < p.n; i += W) {
     const T* x = static_cast<const T*>(p.X[i]) + row;
     const T* dy = static_cast<const T*>(p.dY[i]) + row;
     const T* g = static_cast<const T*>(p.gamma[i]);
@@ -309,20 +317,20 @@ int vec_width(const LnParams& p, bool backward) {
 template <typename T>
 cudaError_t launch_rows(const LnParams& p, bool backward, cudaStream_t st) {
   constexpr int V = 16 / sizeof(T);
-  const long long blocks = (p.T + kLnWarps - 1) / kLnWarps;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  const dim3 grid(static_cast<unsigned>(blocks));
+  if (p.T > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(p.T));                 // one block per token row
+  const int threads = 32 * std::min(p.n, kLnWarps);          // one warp per shard (or more)
   const bool vec = vec_width<T>(p, backward) == V;
   if (!backward) {
     if (vec)
-      ln_forward_kernel<T, V><<<grid, kLnWarps * 32, 0, st>>>(p);
+      ln_forward_kernel<T, V><<<grid, threads, 0, st>>>(p);
     else
-      ln_forward_kernel<T, 1><<<grid, kLnWarps * 32, 0, st>>>(p);
+      ln_forward_kernel<T, 1><<<grid, threads, 0, st>>>(p);
   } else {
     if (vec)
-      ln_backward_dx_kernel<T, V><<<grid, kLnWarps * 32, 0, st>>>(p);
+      ln_backward_dx_kernel<T, V><<<grid, threads, 0, st>>>(p);
     else
-      ln_backward_dx_kernel<T, 1><<<grid, kLnWarps * 32, 0, st>>>(p);
+      ln_backward_dx_kernel<T, 1><<<grid, threads, 0, st>>>(p);
   }
   return cudaGetLastError();
 }
