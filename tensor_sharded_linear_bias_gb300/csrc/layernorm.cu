@@ -17,8 +17,9 @@
 // Backward dX, one block per row likewise: the row statistics sum(dY*gamma) and
 // sum(dY*gamma*xhat) are summed per shard, then over the shards in order, and
 // dX = rstd * (g - (s1 + xhat s2) / H).
-// Backward dgamma, dbeta: column sums over the tokens, split over the blocks of a cluster and
-// combined in block order through distributed shared memory (deterministic, no atomics).
+// Backward dgamma, dbeta: column sums over the tokens, split over the warps of a block and the
+// blocks of a cluster, combined in warp and block order (distributed shared memory for the
+// blocks): deterministic, no atomics.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
@@ -33,7 +34,8 @@ namespace tpk {
 namespace {
 
 constexpr int kLnWarps = 8;  // warps per block (one token row per block, warps over its shards)
-constexpr int kUnroll = 4;   // 16-byte loads in flight per lane and operand
+constexpr int kUnrollFwd = 8;  // 16-byte loads in flight per lane: forward (one operand)
+constexpr int kUnrollBwd = 4;  // ... and backward (two operands)
 
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
@@ -98,6 +100,7 @@ __global__ void __launch_bounds__(kLnWarps * 32) ln_forward_kernel(const __grid_
     const T* x = static_cast<const T*>(p.X[i]) + row;
     const float k = to_f(x[0]);
     float s1 = 0.f, s2 = 0.f;
+    constexpr int kUnroll = kUnrollFwd;
     for (long long c0 = static_cast<long long>(lane) * VEC; c0 < p.Hs; c0 += 32LL * VEC * kUnroll) {
       float v[kUnroll][VEC];
 #pragma unroll
@@ -174,6 +177,7 @@ __global__ void __launch_bounds__(kLnWarps * 32) ln_backward_dx_kernel(const __g
     const T* dy = static_cast<const T*>(p.dY[i]) + row;
     const T* g = static_cast<const T*>(p.gamma[i]);
     float a1 = 0.f, a2 = 0.f;
+    constexpr int kUnroll = kUnrollBwd;
     for (long long c0 = static_cast<long long>(lane) * VEC; c0 < p.Hs; c0 += 32LL * VEC * kUnroll) {
       float v[kUnroll][VEC], d[kUnroll][VEC];
 #pragma unroll
@@ -235,64 +239,94 @@ __global__ void __launch_bounds__(kLnWarps * 32) ln_backward_dx_kernel(const __g
 }
 
 // dgamma_i[c] = sum_t dY_i[t,c] * xhat[t,c], dbeta_i[c] = sum_t dY_i[t,c]. blockIdx.x: a strip
-// of 256 columns of one shard (strips of shard i are consecutive); blockIdx.y = q: tokens
-// [q T / R, (q+1) T / R) of a cluster of R blocks; thread = one column, eight tokens' loads in
-// flight, added in token order.
-template <typename T>
-__global__ void __launch_bounds__(256) ln_param_grads_kernel(const __grid_constant__ LnParams p) {
-  constexpr int U = 8;
-  __shared__ float part[2][256];
-  const long long strips = (p.Hs + 255) / 256;
+// of 32 * VEC columns of one shard (strips of shard i are consecutive); lane l of every warp
+// owns columns [strip + VEC l, strip + VEC l + VEC) (one 16-byte access per row where the rows
+// allow it). blockIdx.y = q: tokens [q T / R, (q+1) T / R) of a cluster of R blocks, of which
+// warp w takes every kPgWarps-th from the w-th, U rows' loads in flight, added in token order.
+// The warps' sums are added in warp order, then the R blocks' in block order through
+// distributed shared memory: deterministic, no atomics.
+constexpr int kPgWarps = 16;
+
+template <typename T, int VEC>
+__global__ void __launch_bounds__(kPgWarps * 32) ln_param_grads_kernel(const __grid_constant__ LnParams p) {
+  constexpr int U = 4;
+  constexpr int COLS = 32 * VEC;
+  __shared__ float part[kPgWarps][2][COLS];
+  __shared__ float blk[2][COLS];
+  const long long strips = (p.Hs + COLS - 1) / COLS;
   const int i = static_cast<int>(blockIdx.x / strips);
-  const long long c = (blockIdx.x % strips) * 256 + threadIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long c = (blockIdx.x % strips) * COLS + static_cast<long long>(lane) * VEC;
   const int R = static_cast<int>(gridDim.y), q = static_cast<int>(blockIdx.y);
   const long long t0 = p.T * q / R, t1 = p.T * (q + 1) / R;
-  float sg = 0.f, sb = 0.f;
+  float sg[VEC], sb[VEC];
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) sg[e] = sb[e] = 0.f;
   if (c < p.Hs) {
     const T* x = static_cast<const T*>(p.X[i]) + c;
     const T* dy = static_cast<const T*>(p.dY[i]) + c;
-    long long t = t0;
-    for (; t + U <= t1; t += U) {
-      float xv[U], dv[U], mv[U], rv[U];
+    long long t = t0 + warp;
+    for (; t + (U - 1) * kPgWarps < t1; t += U * kPgWarps) {
+      float xv[U][VEC], dv[U][VEC], mv[U], rv[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        xv[u] = to_f(x[(t + u) * p.Hs]);
-        dv[u] = to_f(dy[(t + u) * p.Hs]);
-        mv[u] = p.mean[t + u];
-        rv[u] = p.rstd[t + u];
+        const long long tt = t + u * kPgWarps;
+        load_vec<T, VEC>(x + tt * p.Hs, xv[u]);
+        load_vec<T, VEC>(dy + tt * p.Hs, dv[u]);
+        mv[u] = p.mean[tt];
+        rv[u] = p.rstd[tt];
       }
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        sg = fmaf(dv[u], (xv[u] - mv[u]) * rv[u], sg);
-        sb += dv[u];
-      }
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          sg[e] = fmaf(dv[u][e], (xv[u][e] - mv[u]) * rv[u], sg[e]);
+          sb[e] += dv[u][e];
+        }
     }
-    for (; t < t1; ++t) {
-      const float d = to_f(dy[t * p.Hs]);
-      sg = fmaf(d, (to_f(x[t * p.Hs]) - p.mean[t]) * p.rstd[t], sg);
-      sb += d;
+    for (; t < t1; t += kPgWarps) {
+      float xv[VEC], dv[VEC];
+      load_vec<T, VEC>(x + t * p.Hs, xv);
+      load_vec<T, VEC>(dy + t * p.Hs, dv);
+      const float m = p.mean[t], r = p.rstd[t];
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        sg[e] = fmaf(dv[e], (xv[e] - m) * r, sg[e]);
+        sb[e] += dv[e];
+      }
     }
   }
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) {
+    part[warp][0][lane * VEC + e] = sg[e];
+    part[warp][1][lane * VEC + e] = sb[e];
+  }
+  __syncthreads();
+  // the block's sums: warps in order (thread k < 2 * COLS sums one of the 2 * COLS values)
+  for (int k = threadIdx.x; k < 2 * COLS; k += kPgWarps * 32) {
+    float v = 0.f;
+    for (int w = 0; w < kPgWarps; ++w) v += part[w][k / COLS][k % COLS];
+    blk[k / COLS][k % COLS] = v;
+  }
+  auto store = [&](int k, float v) {
+    const long long col = (blockIdx.x % strips) * COLS + (k % COLS);
+    if (col >= p.Hs) return;
+    float* out = k < COLS ? p.dgamma[i] : p.dbeta[i];
+    if (out != nullptr) out[col] = v;
+  };
   if (R == 1) {
-    if (c < p.Hs) {
-      if (p.dgamma[i] != nullptr) p.dgamma[i][c] = sg;
-      if (p.dbeta[i] != nullptr) p.dbeta[i][c] = sb;
-    }
+    __syncthreads();
+    for (int k = threadIdx.x; k < 2 * COLS; k += kPgWarps * 32) store(k, blk[k / COLS][k % COLS]);
     return;
   }
-  part[0][threadIdx.x] = sg;
-  part[1][threadIdx.x] = sb;
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
-  if (q == 0 && c < p.Hs) {
-    float g = 0.f, b = 0.f;
-    for (int r = 0; r < R; ++r) {
-      const float* o = cluster.map_shared_rank(&part[0][0], r);
-      g += o[threadIdx.x];
-      b += o[256 + threadIdx.x];
+  if (q == 0) {
+    for (int k = threadIdx.x; k < 2 * COLS; k += kPgWarps * 32) {
+      float v = 0.f;
+      for (int r = 0; r < R; ++r) v += cluster.map_shared_rank(&blk[0][0], r)[k];
+      store(k, v);
     }
-    if (p.dgamma[i] != nullptr) p.dgamma[i][c] = g;
-    if (p.dbeta[i] != nullptr) p.dbeta[i][c] = b;
   }
   cluster.sync();
 }
@@ -335,16 +369,16 @@ cudaError_t launch_rows(const LnParams& p, bool backward, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <typename T>
-cudaError_t launch_param_grads(const LnParams& p, cudaStream_t st) {
-  const long long strips = ((p.Hs + 255) / 256) * p.n;
+template <typename T, int VEC>
+cudaError_t launch_param_grads_v(const LnParams& p, cudaStream_t st) {
+  const long long strips = ((p.Hs + 32LL * VEC - 1) / (32LL * VEC)) * p.n;
   if (strips > 0x7fffffffLL) return cudaErrorInvalidValue;
-  // blocks per strip: about four per SM in all, at least 64 tokens each, a portable cluster
-  const long long want = (4LL * device_sm_count() + strips - 1) / strips;
-  const int R = static_cast<int>(std::max(1LL, std::min({want, p.T / 64, 8LL})));
+  // blocks per strip: about two per SM in all, at least 256 tokens each, a portable cluster
+  const long long want = (2LL * device_sm_count() + strips - 1) / strips;
+  const int R = static_cast<int>(std::max(1LL, std::min({want, p.T / 256, 8LL})));
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(strips), static_cast<unsigned>(R), 1);
-  cfg.blockDim = dim3(256, 1, 1);
+  cfg.blockDim = dim3(kPgWarps * 32, 1, 1);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -353,7 +387,15 @@ cudaError_t launch_param_grads(const LnParams& p, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, ln_param_grads_kernel<T>, p);
+  return cudaLaunchKernelEx(&cfg, ln_param_grads_kernel<T, VEC>, p);
+}
+
+template <typename T>
+cudaError_t launch_param_grads(const LnParams& p, cudaStream_t st) {
+  constexpr int V = 16 / sizeof(T);
+  bool vec = p.Hs % V == 0;
+  for (int i = 0; i < p.n && vec; ++i) vec = aligned16(p.X[i]) && aligned16(p.dY[i]);
+  return vec ? launch_param_grads_v<T, V>(p, st) : launch_param_grads_v<T, 1>(p, st);
 }
 
 LnParams make(const LnArgs& a) {
