@@ -34,7 +34,7 @@ namespace tpk {
 namespace {
 
 constexpr int kLnWarps = 8;  // warps per block (one token row per block, warps over its shards)
-constexpr int kUnrollFwd = 8;  // 16-byte loads in flight per lane: forward (one operand)
+constexpr int kUnrollFwd = 4;  // 16-byte loads in flight per lane: forward (one operand)
 constexpr int kUnrollBwd = 4;  // ... and backward (two operands)
 
 __device__ __forceinline__ float to_f(float v) { return v; }
