@@ -114,3 +114,11 @@ def test_layernorm_zero_tokens(tp):
     c.run()
     assert all(torch.count_nonzero(g) == 0 for g in c.dg)
     assert all(torch.count_nonzero(b) == 0 for b in c.db)
+
+
+@pytest.mark.slow
+def test_layernorm_bench_size(tp):
+    """The size bench.py times (T 2048, H 12288, 8 shards, bf16), every output against the
+    oracle."""
+    errs = LnCase(tp, 2048, 12288, 8, "bf16", seed=11).run().errors()
+    assert max(errs.values()) <= TOL_BF16, errs
