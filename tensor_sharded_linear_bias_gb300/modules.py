@@ -4,8 +4,9 @@ The column-parallel linear plays the part of the custom TensorParallelLinear of 
 parallelism in practice: from theory to complete PyTorch code" (a weight of
 [in, out / world_size] per shard, a bias slice per shard, outputs gathered along the last
 dimension), except that all tp_degree shards live on the one GPU. The row-parallel linear and
-the MLP follow "Tensor Parallelism: principle and practice", section 3.1. Every computation
-runs in the library's kernels; these classes only allocate torch tensors and pass pointers.
+the MLP follow "Tensor Parallelism: principle and practice", section 3.1, the LayerNorm over a
+split hidden dimension its section 4.2. Every computation runs in the library's kernels; these
+classes only allocate torch tensors and pass pointers.
 """
 from __future__ import annotations
 
@@ -257,3 +258,58 @@ class TensorParallelMLP:
         """Synchronise and raise if a kernel reported a device-side timeout."""
         if self._ws.ws is not None:
             tp_check_status(self._ws.ws)
+
+
+class TensorParallelLayerNorm:
+    """LayerNorm over a hidden dimension split into tp_degree column shards: inputs and outputs
+    are lists of per-shard [T, hidden/n] tensors; gamma / beta are per-shard slices (1 and 0 at
+    start). The row statistics cover the whole hidden dimension (combined over the shards on
+    the device). Gradients of the last backward: ``gamma_grads``, ``beta_grads`` (fp32 per
+    shard)."""
+
+    def __init__(self, hidden: int, tp_degree: int, *, eps: float = 1e-5, dtype=None,
+                 device="cuda", affine: bool = True):
+        import torch
+
+        dtype = torch.bfloat16 if dtype is None else dtype
+        self.H, self.n, self.dtype = hidden, tp_degree, dtype
+        self.device = torch.device(device)
+        self.desc = LayerNormDesc(tokens=0, hidden=hidden, tp_degree=tp_degree,
+                                  dtype=_dtype_code(dtype), eps=eps)
+        if hidden % tp_degree != 0:
+            raise ValueError(f"hidden {hidden} is not divisible by tp_degree {tp_degree}")
+        hs = hidden // tp_degree
+        self.gamma = ([torch.ones(hs, dtype=dtype, device=self.device) for _ in range(tp_degree)]
+                      if affine else None)
+        self.beta = ([torch.zeros(hs, dtype=dtype, device=self.device) for _ in range(tp_degree)]
+                     if affine else None)
+        self._x = self._mean = self._rstd = None
+
+    def _desc(self, T):
+        d = LayerNormDesc.from_buffer_copy(self.desc)
+        d.tokens = T
+        return d
+
+    def forward(self, xs):
+        import torch
+
+        T = xs[0].shape[0]
+        f32 = dict(dtype=torch.float32, device=self.device)
+        ys = [torch.empty_like(x) for x in xs]
+        self._mean, self._rstd = torch.empty(T, **f32), torch.empty(T, **f32)
+        tp_layernorm_forward(self._desc(T), xs, self.gamma, self.beta, ys, self._mean, self._rstd)
+        self._x = list(xs)
+        return ys
+
+    def backward(self, dys):
+        import torch
+
+        T = dys[0].shape[0]
+        dxs = [torch.empty_like(d) for d in dys]
+        hs = self.H // self.n
+        f32 = dict(dtype=torch.float32, device=self.device)
+        self.gamma_grads = [torch.empty(hs, **f32) for _ in range(self.n)] if self.gamma else None
+        self.beta_grads = [torch.empty(hs, **f32) for _ in range(self.n)] if self.beta else None
+        tp_layernorm_backward(self._desc(T), self._x, self.gamma, self._mean, self._rstd, dys,
+                              dxs, self.gamma_grads, self.beta_grads)
+        return dxs

@@ -108,3 +108,27 @@ def test_mlp_and_linears_against_the_oracle(mods, dtype):
     col.check()
     # the row layer hands fp32 dY_i to the column layer, rounded to the input dtype here
     assert rel(np64(dx2), rb["dX"]) <= tol
+
+
+@pytest.mark.gpu
+def test_layernorm_module(mods):
+    import torch
+
+    T, H, n = 64, 8 * 128, 8
+    gen = torch.Generator().manual_seed(5)
+    x = torch.randn(T, H, generator=gen)
+    dy = torch.randn(T, H, generator=gen)
+    ln = mods.TensorParallelLayerNorm(H, n, dtype=torch.float32)
+    ln.gamma = [g + 0.1 * i for i, g in enumerate(ln.gamma)]
+    xs = [c.contiguous().cuda() for c in x.split(H // n, 1)]
+    ys = ln.forward(xs)
+    dxs = ln.backward([c.contiguous().cuda() for c in dy.split(H // n, 1)])
+    torch.cuda.synchronize()
+    gs = [np64(g) for g in ln.gamma]
+    f = oracle.layernorm_forward(oracle.split_hidden(x.numpy(), n), gs, None, 1e-5)
+    b = oracle.layernorm_backward(oracle.split_hidden(x.numpy(), n), gs,
+                                  oracle.split_hidden(dy.numpy(), n), 1e-5, f)
+    assert rel_shards([np64(y) for y in ys], f["Y"]) <= TOL_F32
+    assert rel_shards([np64(d) for d in dxs], b["dX"]) <= TOL_F32
+    assert rel_shards([np64(g) for g in ln.gamma_grads], b["dgamma"]) <= TOL_F32
+    assert rel_shards([np64(g) for g in ln.beta_grads], b["dbeta"]) <= TOL_F32
