@@ -13,12 +13,14 @@ from __future__ import annotations
 from typing import List, Optional
 
 from . import (TP_ACT_GELU_ERF, TP_ACT_NONE, TP_BF16, TP_COLUMN, TP_F32, TP_REDUCE_AUTO, TP_ROW,
-               LinearDesc, MlpDesc, new_workspace, tp_check_status, tp_linear_column_backward,
+               LayerNormDesc, LinearDesc, MlpDesc, new_workspace, tp_check_status,
+               tp_layernorm_backward, tp_layernorm_forward, tp_linear_column_backward,
                tp_linear_column_forward, tp_linear_row_backward, tp_linear_row_forward,
                tp_linear_workspace_size, tp_mlp_backward, tp_mlp_forward,
                tp_mlp_workspace_size)
 
-__all__ = ["ColumnParallelLinear", "RowParallelLinear", "TensorParallelMLP"]
+__all__ = ["ColumnParallelLinear", "RowParallelLinear", "TensorParallelMLP",
+           "TensorParallelLayerNorm"]
 
 
 def _dtype_code(dtype) -> int:
