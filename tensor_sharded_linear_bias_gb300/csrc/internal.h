@@ -62,9 +62,6 @@ struct GemmSpec {
   const void* zbias = nullptr;
   int* status = nullptr;
   int kslices = 1;  // FFMA GEMM: K steps split over a cluster of this many CTAs per tile (1: none)
-  // tensor-core GEMM on SM pairs: L2 policy of the A / B loads (0 none, 1 evict first for an
-  // operand streamed once, 2 evict last for one reused across the output's tiles)
-  int l2_hint_a = 0, l2_hint_b = 0;
   // tensor-core GEMM on SM pairs: scratch for split tail tiles (nullptr: never split)
   float* tail_ws = nullptr;
   int* tail_counters = nullptr;

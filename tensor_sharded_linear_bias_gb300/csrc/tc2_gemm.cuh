@@ -105,35 +105,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-// The same loads with an L2 eviction-priority policy (createpolicy) attached.
-__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap* map, int x,
-                                                      int y, uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const CUtensorMap* map, int x,
-                                                      int y, int z, uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
-      : "memory");
-}
-
-// L2 policies: 1 = evict first (streamed once), 2 = evict last (reused); 0 = none.
-__device__ __forceinline__ uint64_t l2_policy(int hint) {
-  uint64_t pol = 0;
-  if (hint == 1)
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  else if (hint == 2)
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-
 __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                                uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -302,7 +273,6 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
       uint32_t stage = 0, phase = 0;
       bool failed = false;
       long long issued = 0;
-      const uint64_t pol_a = l2_policy(p.hint_a), pol_b = l2_policy(p.hint_b);
       for (int u = cluster; u < p.num_units && !failed; u += nclusters) {
         int t, kb0, kb1, piece;
         tc::decode_unit(p, u, total_kb, t, kb0, kb1, piece);
@@ -325,10 +295,7 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
           const uint32_t sb = sa + A_BYTES;
           if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
           if (!A_MN) {
-            if (p.hint_a)
-              tma_load_2d_pair_hint(sa, &p.tmA[kg], kk, arow, fb, pol_a);
-            else
-              tma_load_2d_pair(sa, &p.tmA[kg], kk, arow, fb);
+            tma_load_2d_pair(sa, &p.tmA[kg], kk, arow, fb);
           } else if (p.a3d) {
             tma_load_3d_pair(sa, &p.tmA[kg], 0, kk, arow / 64, fb);
           } else {
@@ -337,15 +304,9 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
               tma_load_2d_pair(sa + j * MN_BOX_BYTES, &p.tmA[kg], arow + 64 * j, kk, fb);
           }
           if (!B_MN) {
-            if (p.hint_b)
-              tma_load_2d_pair_hint(sb, &p.tmB[kg], kk, bcol, fb, pol_b);
-            else
-              tma_load_2d_pair(sb, &p.tmB[kg], kk, bcol, fb);
+            tma_load_2d_pair(sb, &p.tmB[kg], kk, bcol, fb);
           } else if (p.b3d) {
-            if (p.hint_b)
-              tma_load_3d_pair_hint(sb, &p.tmB[kg], 0, kk, bcol / 64, fb, pol_b);
-            else
-              tma_load_3d_pair(sb, &p.tmB[kg], 0, kk, bcol / 64, fb);
+            tma_load_3d_pair(sb, &p.tmB[kg], 0, kk, bcol / 64, fb);
           } else {
 #pragma unroll
             for (int j = 0; j < HALF / 64; ++j)

@@ -78,7 +78,6 @@ struct __align__(128) TcParams {
   // its fp32 accumulator in tail_ws; the warp completing a (tile, 32-row block) count in
   // tail_counters adds the pieces in piece order and runs the tile's epilogue.
   int full_tiles, ksplit, num_units;
-  int hint_a, hint_b;  // L2 policy of the A / B loads (SM-pair kernel): 0 none, 1 evict first, 2 evict last
   float* tail_ws;
   int* tail_counters;
   int* status;

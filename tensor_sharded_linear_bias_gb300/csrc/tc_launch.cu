@@ -146,12 +146,6 @@ bool mn3d_enabled() {
   return true;
 }
 
-// L2 eviction-priority policies on the TMA loads; TPMLP_L2_HINTS=0 turns them off.
-bool l2_hints_enabled() {
-  if (const char* env = std::getenv("TPMLP_L2_HINTS")) return std::atoi(env) != 0;
-  return true;
-}
-
 // Split tail; TPMLP_TAIL_SPLIT=0 turns it off.
 bool tail_split_enabled() {
   if (const char* env = std::getenv("TPMLP_TAIL_SPLIT")) return std::atoi(env) != 0;
@@ -291,10 +285,6 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
   p.full_tiles = p.num_tiles;
   p.ksplit = 1;
   p.num_units = p.num_tiles;
-  if (l2_hints_enabled()) {
-    p.hint_a = s.l2_hint_a;
-    p.hint_b = s.l2_hint_b;
-  }
   if (pair) {
     const int epi_warps = pair_epi_warps(p.epi, p.act, p.kblocks * p.kpo);
     const int max_clusters = pair_clusters(layout, epi_warps);

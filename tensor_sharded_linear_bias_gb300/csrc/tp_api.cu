@@ -145,13 +145,6 @@ tp_status cuda_fail(cudaError_t e, const char* what) {
 
 int* status_word(void* ws) { return static_cast<int*>(ws); }
 
-// Products of an activation (A, K-major, reused by every column block of the output) and a
-// weight (B, read by one wave of tiles and not again): keep A in L2, let B go first.
-void weight_stream_hints(GemmSpec& s) {
-  s.l2_hint_a = 2;
-  s.l2_hint_b = 1;
-}
-
 // First byte of a call's scratch: after the status block and, for bf16, the split tail tiles.
 size_t scratch_base(int dtype) { return kStatusBytes + (dtype == TP_BF16 ? kTailBytes : 0); }
 
@@ -422,7 +415,6 @@ tp_status row_product(int dtype, int reduce, int n, int64_t T, int64_t Ks, int64
   s.ldd = N;
   s.epi = EPI_STORE_F32;
   bind_ws(s, ws, dtype);
-  weight_stream_hints(s);
   for (int i = 0; i < n; ++i) {
     s.A[i] = X[i];
     s.B[i] = W[i];
@@ -470,7 +462,6 @@ tp_status input_grad_sum(int dtype, int reduce, int n, int64_t T, int64_t w, int
   s.ldd = Kd;
   s.epi = EPI_STORE_F32;
   bind_ws(s, ws, dtype);
-  weight_stream_hints(s);
   for (int i = 0; i < n; ++i) {
     s.A[i] = dH[i];
     s.B[i] = W[i];
@@ -695,7 +686,6 @@ tp_status tp_mlp_forward(const tp_mlp_desc* desc, const void* X, const void* con
   c.epi = EPI_BIAS_ACT;
   c.act = desc->act;
   bind_ws(c, ws, dt);
-  weight_stream_hints(c);
   for (int i = 0; i < n; ++i) {
     c.A[i] = X;
     c.B[i] = A[i];
@@ -755,7 +745,6 @@ tp_status tp_mlp_backward(const tp_mlp_desc* desc, const void* X, const void* co
     s.epi = EPI_DACT;
     s.act = desc->act;
     bind_ws(s, ws, dt);
-    weight_stream_hints(s);
     for (int i = 0; i < n; ++i) {
       s.A[i] = dZ;
       s.B[i] = B[i];
@@ -931,7 +920,6 @@ tp_status tp_linear_column_forward(const tp_linear_desc* desc, const void* X,
   c.epi = EPI_BIAS_ACT;
   c.act = desc->act;
   bind_ws(c, ws, dt);
-  weight_stream_hints(c);
   for (int i = 0; i < n; ++i) {
     c.A[i] = X;
     c.B[i] = W[i];
@@ -1056,7 +1044,6 @@ tp_status tp_linear_row_backward(const tp_linear_desc* desc, const void* const* 
     s.ldd = z.Ks;
     s.epi = EPI_STORE_F32;
     bind_ws(s, ws, dt);
-    weight_stream_hints(s);
     for (int i = 0; i < n; ++i) {
       s.A[i] = dZ;
       s.B[i] = W[i];
