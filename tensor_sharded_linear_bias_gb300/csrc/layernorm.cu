@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(kLnWarps * 32) ln_forward_kernel(const __grid_
 }
 
 template <typename T, int VEC>
-__global__ void __launch_bounds__(kLnWarps * 32) ln_backward_dx_kernel(const __grid_constant__ LnParams p) {
+__global__ void __launch_bounds__(kLnWarps * 32, 3) ln_backward_dx_kernel(const __grid_constant__ LnParams p) {
   __shared__ float stat[kMaxShards][2];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, W = blockDim.x >> 5;
   const long long t = blockIdx.x;
