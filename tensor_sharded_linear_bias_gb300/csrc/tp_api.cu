@@ -119,23 +119,23 @@ tp_status check_ws(void* ws, size_t ws_bytes, size_t need) {
 }
 
 tp_status check_arch() {
-  static int verdict[64] = {};  // 0 unknown, 1 ok, 2 bad
+  static int arch_state[64] = {};  // 0 unknown, 1 ok, 2 bad
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
     cudaGetLastError();
     return fail(TP_ERR_ARCH, "no CUDA device is available");
   }
   if (dev >= 64) return fail(TP_ERR_ARCH, "device index %d out of range", dev);
-  if (verdict[dev] == 0) {
+  if (arch_state[dev] == 0) {
     int major = 0, minor = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    verdict[dev] = (major == 10 && minor == 3) ? 1 : 2;
-    if (verdict[dev] == 2)
+    arch_state[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    if (arch_state[dev] == 2)
       return fail(TP_ERR_ARCH, "device %d is sm_%d%d; this library is built for sm_103a", dev,
                   major, minor);
   }
-  if (verdict[dev] == 2) return fail(TP_ERR_ARCH, "device %d is not sm_103", dev);
+  if (arch_state[dev] == 2) return fail(TP_ERR_ARCH, "device %d is not sm_103", dev);
   return TP_OK;
 }
 
