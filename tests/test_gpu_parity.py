@@ -475,8 +475,10 @@ def test_workload_sweep_sampled(tp, n, T):
 
 
 @pytest.mark.slow
-def test_workload_attention_projections(tp):
-    """Fused QKV (column parallel over heads) and output projection (row parallel)."""
+@pytest.mark.parametrize("reduce", [0, 1, 2, 4])
+def test_workload_attention_projections(tp, reduce):
+    """Fused QKV (column parallel over heads) and output projection (row parallel), with the
+    shard sums fused, as fp32 partials, as AUTO picks them, and overlapped with the GEMM."""
     import torch
 
     w = wl.ATTN_T4096_H5120_TP8
@@ -493,9 +495,9 @@ def test_workload_attention_projections(tp):
     Wo = [t["Wo"][s * hw:(s + 1) * hw, :].contiguous() for s in range(n)]
     f32 = dict(dtype=torch.float32, device="cuda")
     col = tp.LinearDesc(tokens=T, in_features=Hm, out_features=3 * Hm, tp_degree=n,
-                        dtype=tp.TP_BF16, act=0, reduce=0, gather=0)
+                        dtype=tp.TP_BF16, act=0, reduce=reduce, gather=0)
     row = tp.LinearDesc(tokens=T, in_features=Hm, out_features=Hm, tp_degree=n,
-                        dtype=tp.TP_BF16, act=0, reduce=0, gather=0)
+                        dtype=tp.TP_BF16, act=0, reduce=reduce, gather=0)
     ws = tp.new_workspace(max(tp.tp_linear_workspace_size(col, tp.TP_COLUMN),
                               tp.tp_linear_workspace_size(row, tp.TP_ROW)))
     QKV = [torch.empty(T, 3 * hw, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
