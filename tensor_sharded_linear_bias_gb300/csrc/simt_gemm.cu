@@ -265,32 +265,21 @@ __global__ void __launch_bounds__(256) skinny_gemm_kernel(const __grid_constant_
   const int L = static_cast<int>(ke - kb);
   float* As = sk;                               // [L][kSkStride], rows m >= M are 0
   float* red = sk + max(L * kSkStride, kSkPart);
-  // stage A^T for this block's K range (consecutive threads: consecutive k of one row), eight
-  // independent loads per thread in flight at a time
+  // stage A^T for this block's K range (consecutive threads: consecutive k of one row)
   {
     const int K = static_cast<int>(p.K);
-    const int total = kSkRows * L;
-    for (int e0 = threadIdx.x; e0 < total; e0 += 256 * 8) {
-      float v[8];
-      int dst[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int e = e0 + 256 * u;
-        v[u] = 0.f;
-        dst[u] = -1;
-        if (e < total) {
-          const int m = e / L, kl = e - m * L;
-          dst[u] = kl * kSkStride + m;
-          if (m < p.M) {
-            const long long k = kb + kl;
-            const int kg = static_cast<int>(k / K);
-            v[u] = p.A[p.ksum ? kg : g][m * p.sam + (k - static_cast<long long>(kg) * K)];
-          }
+    for (int m = 0; m < kSkRows; ++m) {
+      const float* Arow = nullptr;
+      for (int kl = threadIdx.x; kl < L; kl += 256) {
+        float v = 0.f;
+        if (m < p.M) {
+          const long long k = kb + kl;
+          const int kg = static_cast<int>(k / K);
+          Arow = p.A[p.ksum ? kg : g] + m * p.sam;
+          v = Arow[k - static_cast<long long>(kg) * K];
         }
+        As[kl * kSkStride + m] = v;
       }
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (dst[u] >= 0) As[dst[u]] = v[u];
     }
   }
   __syncthreads();
