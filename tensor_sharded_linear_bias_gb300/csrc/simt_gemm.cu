@@ -266,65 +266,45 @@ __global__ void __launch_bounds__(256) skinny_gemm_kernel(const __grid_constant_
   float* As = sk;                               // [L][kSkStride], rows m >= M are 0
   float* red = sk + max(L * kSkStride, kSkPart);
   // stage A^T for this block's K range (consecutive threads: consecutive k of one row)
-  {
-    const int K = static_cast<int>(p.K);
-    for (int m = 0; m < kSkRows; ++m) {
-      const float* Arow = nullptr;
-      for (int kl = threadIdx.x; kl < L; kl += 256) {
-        float v = 0.f;
-        if (m < p.M) {
-          const long long k = kb + kl;
-          const int kg = static_cast<int>(k / K);
-          Arow = p.A[p.ksum ? kg : g] + m * p.sam;
-          v = Arow[k - static_cast<long long>(kg) * K];
-        }
-        As[kl * kSkStride + m] = v;
-      }
-    }
+  for (int e = threadIdx.x; e < kSkRows * L; e += 256) {
+    const int m = e / L, kl = e % L;
+    const long long k = kb + kl;
+    const int kg = static_cast<int>(k / p.K);
+    const long long kk = k - kg * p.K;
+    float v = 0.f;
+    if (m < p.M) v = p.A[p.ksum ? kg : g][m * p.sam + kk];
+    As[kl * kSkStride + m] = v;
   }
   __syncthreads();
-  // this warp's share of the K range, U elements' B loads in flight at a time
-  constexpr int U = 8;
+  // this warp's share of the K range
   const int w0 = L * warp / 8, w1 = L * (warp + 1) / 8;
   const long long n = n0 + 2 * lane;
-  const bool in0 = n < p.N, in1 = n + 1 < p.N;
   float acc[kSkRows][2];
 #pragma unroll
   for (int m = 0; m < kSkRows; ++m) acc[m][0] = acc[m][1] = 0.f;
   long long k = kb + w0;
   int kg = static_cast<int>(k / p.K);
   long long kk = k - kg * p.K;
-  for (int kl0 = w0; kl0 < w1; kl0 += U) {
-    float b0[U], b1[U];
+  for (int kl = w0; kl < w1; ++kl) {
+    const float* B = p.B[p.ksum ? kg : g] + kk * p.sbk;
+    const float b0 = n < p.N ? B[n] : 0.f;
+    const float b1 = n + 1 < p.N ? B[n + 1] : 0.f;
+    const float4* a4 = reinterpret_cast<const float4*>(As + kl * kSkStride);
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      b0[u] = b1[u] = 0.f;
-      if (kl0 + u < w1) {
-        const float* B = p.B[p.ksum ? kg : g] + kk * p.sbk + n;
-        if (in0) b0[u] = B[0];
-        if (in1) b1[u] = B[1];
-        if (++kk == p.K) {
-          kk = 0;
-          ++kg;
-        }
-      }
+    for (int q = 0; q < kSkRows / 4; ++q) {
+      const float4 a = a4[q];
+      acc[4 * q][0] = fmaf(a.x, b0, acc[4 * q][0]);
+      acc[4 * q][1] = fmaf(a.x, b1, acc[4 * q][1]);
+      acc[4 * q + 1][0] = fmaf(a.y, b0, acc[4 * q + 1][0]);
+      acc[4 * q + 1][1] = fmaf(a.y, b1, acc[4 * q + 1][1]);
+      acc[4 * q + 2][0] = fmaf(a.z, b0, acc[4 * q + 2][0]);
+      acc[4 * q + 2][1] = fmaf(a.z, b1, acc[4 * q + 2][1]);
+      acc[4 * q + 3][0] = fmaf(a.w, b0, acc[4 * q + 3][0]);
+      acc[4 * q + 3][1] = fmaf(a.w, b1, acc[4 * q + 3][1]);
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (kl0 + u >= w1) break;
-      const float4* a4 = reinterpret_cast<const float4*>(As + (kl0 + u) * kSkStride);
-#pragma unroll
-      for (int q = 0; q < kSkRows / 4; ++q) {
-        const float4 a = a4[q];
-        acc[4 * q][0] = fmaf(a.x, b0[u], acc[4 * q][0]);
-        acc[4 * q][1] = fmaf(a.x, b1[u], acc[4 * q][1]);
-        acc[4 * q + 1][0] = fmaf(a.y, b0[u], acc[4 * q + 1][0]);
-        acc[4 * q + 1][1] = fmaf(a.y, b1[u], acc[4 * q + 1][1]);
-        acc[4 * q + 2][0] = fmaf(a.z, b0[u], acc[4 * q + 2][0]);
-        acc[4 * q + 2][1] = fmaf(a.z, b1[u], acc[4 * q + 2][1]);
-        acc[4 * q + 3][0] = fmaf(a.w, b0[u], acc[4 * q + 3][0]);
-        acc[4 * q + 3][1] = fmaf(a.w, b1[u], acc[4 * q + 3][1]);
-      }
+    if (++kk == p.K) {
+      kk = 0;
+      ++kg;
     }
   }
   __syncthreads();  // every warp is done reading As: its space takes the partial tiles
