@@ -8,9 +8,8 @@
 // RM*ty+RM-1 (RM = TM/16) and columns 4tx .. 4tx+3; each K element costs one vector shared load
 // of A, one of B and 4*RM FFMAs.
 //
-// Products of at most 32 rows whose B is N-contiguous take skinny_gemm_kernel instead (below).
-//
-// Split K: when the output tiles alone cannot fill the GPU (few tokens), the K steps of every tile (over all summed shards) are cut into S <= 8
+// Split K: when the output tiles alone cannot fill the GPU (few tokens, as in the pages'
+// batch-32 example), the K steps of every tile (over all summed shards) are cut into S <= 8
 // contiguous ranges computed by the S CTAs of one thread-block cluster. Each CTA parks its
 // partial tile in its shared memory; after a cluster barrier, CTA q adds rows q*TM/S ..
 // (q+1)*TM/S-1 of all S partial tiles in CTA order (distributed shared memory), applies the
@@ -238,152 +237,6 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ 
   cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
-// ------------------------------------------------------------------ at most 32 rows
-// Products of at most 32 rows with A row-major (K contiguous) and B N-contiguous -- the forward
-// at few tokens, as in the pages' batch-32 example. The weights are streamed once: a block of
-// 8 warps owns 64 output columns (2 per lane) for all <= 32 rows; its K range (a slice of the
-// summed K when the cluster splits K) is staged transposed in shared memory once, each warp
-// takes an eighth of it, and per K element a lane issues 8 vector shared loads (the 32 A values,
-// broadcast), 2 B loads and 64 FFMAs. The warps' partial tiles are added in warp order, then the
-// cluster's blocks in block order through distributed shared memory, then the epilogue.
-constexpr int kSkCols = 64;          // output columns per block
-constexpr int kSkRows = 32;          // rows held (M <= 32, zero-padded)
-constexpr int kSkStride = 36;        // floats per staged K row (16-byte multiple)
-constexpr int kSkMaxK = 640;         // staged K elements per block
-constexpr int kSkPart = 8 * kSkRows * kSkCols;  // floats of the warps' partial tiles
-
-__global__ void __launch_bounds__(256) skinny_gemm_kernel(const __grid_constant__ SimtParams p) {
-  extern __shared__ __align__(16) float sk[];
-  const int S = p.slices;
-  const int g = static_cast<int>(blockIdx.z) / S;
-  const int slice = static_cast<int>(blockIdx.z) % S;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long n0 = static_cast<long long>(blockIdx.x) * kSkCols;
-  const int kgroups = p.ksum ? p.groups : 1;
-  const long long Kall = p.K * kgroups;
-  const long long kb = Kall * slice / S, ke = Kall * (slice + 1) / S;
-  const int L = static_cast<int>(ke - kb);
-  float* As = sk;                               // [L][kSkStride], rows m >= M are 0
-  float* red = sk + max(L * kSkStride, kSkPart);
-  // stage A^T for this block's K range (consecutive threads: consecutive k of one row)
-  for (int e = threadIdx.x; e < kSkRows * L; e += 256) {
-    const int m = e / L, kl = e % L;
-    const long long k = kb + kl;
-    const int kg = static_cast<int>(k / p.K);
-    const long long kk = k - kg * p.K;
-    float v = 0.f;
-    if (m < p.M) v = p.A[p.ksum ? kg : g][m * p.sam + kk];
-    As[kl * kSkStride + m] = v;
-  }
-  __syncthreads();
-  // this warp's share of the K range
-  const int w0 = L * warp / 8, w1 = L * (warp + 1) / 8;
-  const long long n = n0 + 2 * lane;
-  float acc[kSkRows][2];
-#pragma unroll
-  for (int m = 0; m < kSkRows; ++m) acc[m][0] = acc[m][1] = 0.f;
-  long long k = kb + w0;
-  int kg = static_cast<int>(k / p.K);
-  long long kk = k - kg * p.K;
-  for (int kl = w0; kl < w1; ++kl) {
-    const float* B = p.B[p.ksum ? kg : g] + kk * p.sbk;
-    const float b0 = n < p.N ? B[n] : 0.f;
-    const float b1 = n + 1 < p.N ? B[n + 1] : 0.f;
-    const float4* a4 = reinterpret_cast<const float4*>(As + kl * kSkStride);
-#pragma unroll
-    for (int q = 0; q < kSkRows / 4; ++q) {
-      const float4 a = a4[q];
-      acc[4 * q][0] = fmaf(a.x, b0, acc[4 * q][0]);
-      acc[4 * q][1] = fmaf(a.x, b1, acc[4 * q][1]);
-      acc[4 * q + 1][0] = fmaf(a.y, b0, acc[4 * q + 1][0]);
-      acc[4 * q + 1][1] = fmaf(a.y, b1, acc[4 * q + 1][1]);
-      acc[4 * q + 2][0] = fmaf(a.z, b0, acc[4 * q + 2][0]);
-      acc[4 * q + 2][1] = fmaf(a.z, b1, acc[4 * q + 2][1]);
-      acc[4 * q + 3][0] = fmaf(a.w, b0, acc[4 * q + 3][0]);
-      acc[4 * q + 3][1] = fmaf(a.w, b1, acc[4 * q + 3][1]);
-    }
-    if (++kk == p.K) {
-      kk = 0;
-      ++kg;
-    }
-  }
-  __syncthreads();  // every warp is done reading As: its space takes the partial tiles
-  float* part = sk;  // [warp][m][col]
-#pragma unroll
-  for (int m = 0; m < kSkRows; ++m) {
-    part[(warp * kSkRows + m) * kSkCols + 2 * lane] = acc[m][0];
-    part[(warp * kSkRows + m) * kSkCols + 2 * lane + 1] = acc[m][1];
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < kSkRows * kSkCols; e += 256) {
-    float v = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) v += part[w * kSkRows * kSkCols + e];
-    red[e] = v;
-  }
-  const int og = p.ksum ? 0 : g;
-  if (S == 1) {
-    __syncthreads();
-    for (int e = threadIdx.x; e < kSkRows * kSkCols; e += 256) {
-      const int m = e / kSkCols;
-      const long long c = n0 + e % kSkCols;
-      if (m < p.M && c < p.N) epilogue(p, og, m, c, red[e]);
-    }
-    return;
-  }
-  cg::cluster_group cluster = cg::this_cluster();
-  cluster.sync();
-  const int e0 = kSkRows * kSkCols * slice / S, e1 = kSkRows * kSkCols * (slice + 1) / S;
-  for (int e = e0 + static_cast<int>(threadIdx.x); e < e1; e += 256) {
-    float v = 0.f;
-    for (int q = 0; q < S; ++q) v += cluster.map_shared_rank(red, q)[e];
-    const int m = e / kSkCols;
-    const long long c = n0 + e % kSkCols;
-    if (m < p.M && c < p.N) epilogue(p, og, m, c, v);
-  }
-  cluster.sync();
-}
-
-// Blocks of the K split for the skinny kernel (0: not applicable).
-int plan_skinny(const GemmSpec& s) {
-  if (const char* env = std::getenv("TPMLP_SIMT_SKINNY"))
-    if (std::atoi(env) == 0) return 0;
-  if (s.M > kSkRows || s.a_mn || !s.b_mn) return 0;
-  const long long outs = s.ksum ? 1 : s.groups;
-  const long long blocks = ((s.N + kSkCols - 1) / kSkCols) * outs;
-  const long long Kall = s.K * (s.ksum ? s.groups : 1);
-  const long long target = 2LL * device_sm_count();
-  long long S = std::max((target + blocks - 1) / blocks, (Kall + kSkMaxK - 1) / kSkMaxK);
-  S = std::min<long long>(S, std::max(1LL, Kall / 64));  // at least 64 K elements per block
-  S = std::min<long long>(S, kMaxSplit);                  // a portable cluster
-  if ((Kall + S - 1) / S > kSkMaxK) return 0;             // the block's K range must fit
-  return static_cast<int>(std::max(1LL, S));
-}
-
-cudaError_t launch_skinny(const SimtParams& p, long long col_blocks, cudaStream_t st) {
-  const long long Kall = p.K * (p.ksum ? p.groups : 1);
-  const int L = static_cast<int>((Kall + p.slices - 1) / p.slices);
-  const int smem = static_cast<int>(sizeof(float)) *
-                   (std::max(L * kSkStride, kSkPart) + kSkRows * kSkCols);
-  cudaError_t e = cudaFuncSetAttribute(skinny_gemm_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  const unsigned zg = p.ksum ? 1u : static_cast<unsigned>(p.groups);
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(col_blocks), 1, zg * static_cast<unsigned>(p.slices));
-  cfg.blockDim = dim3(256, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = static_cast<unsigned>(p.slices);
-  cfg.attrs = attr;
-  cfg.numAttrs = p.slices > 1 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, skinny_gemm_kernel, p);
-}
-
 int tile_rows(int64_t M) { return M <= 32 ? 32 : 64; }
 
 SimtParams make_params(const GemmSpec& s) {
@@ -461,12 +314,6 @@ cudaError_t launch_simt_gemm(const GemmSpec& s, cudaStream_t st) {
   if (s.M <= 0 || s.N <= 0 || s.K <= 0) return cudaSuccess;
   if (s.groups < 1 || s.groups > kMaxShards) return cudaErrorInvalidValue;
   if (s.kslices < 1 || s.kslices > kMaxSplit) return cudaErrorInvalidValue;
-  const int skinny = plan_skinny(s);
-  if (skinny > 0) {
-    SimtParams p = make_params(s);
-    p.slices = skinny;
-    return launch_skinny(p, (s.N + kSkCols - 1) / kSkCols, st);
-  }
   SimtParams p = make_params(s);
   p.slices = s.kslices;
   const unsigned zg = s.ksum ? 1u : static_cast<unsigned>(s.groups);

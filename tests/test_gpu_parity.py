@@ -127,28 +127,6 @@ def test_p3_shapes_fp32_forward(tp):
         assert max(errs.values()) <= TOL_F32, errs
 
 
-@pytest.mark.parametrize("T,H,F,n", [(20, 72, 4 * 40, 4), (32, 200, 2 * 1000, 2), (7, 640, 8 * 72, 8)])
-def test_fp32_at_most_32_rows(tp, monkeypatch, T, H, F, n):
-    """Products of <= 32 rows with an N-contiguous B (the forward) take the skinny kernel: the
-    whole K range of a block staged once, 8 warps on K slices, clusters over K when the column
-    blocks alone cannot fill the GPU, ragged column blocks. Matches the oracle, and the general
-    FFMA kernel (TPMLP_SIMT_SKINNY=0) to fp32 rounding."""
-    import torch
-
-    w = wl.P3_FP32_FWD.with_shape(tokens=T, hidden=H, ffn=F, tp_degree=n)
-    w = wl.dataclasses.replace(w, sigma={**w.sigma, "a": 0.05, "b": 0.05})
-    case = MlpCase(w, 0).run()
-    errs = compare_full(case.outputs(), *full_reference(case))
-    assert max(errs.values()) <= TOL_F32, errs
-    Z1, Y1 = case.Z.clone(), [y.clone() for y in case.Ys]
-    case.run()
-    assert torch.equal(Z1, case.Z)
-    monkeypatch.setenv("TPMLP_SIMT_SKINNY", "0")
-    case.run()
-    assert rel(np64(case.Z), np64(Z1)) <= TOL_F32
-    assert rel_shards([np64(y) for y in case.Ys], [np64(y) for y in Y1]) <= TOL_F32
-
-
 def test_fp32_split_k(tp, monkeypatch):
     """Few tokens: the FFMA GEMMs whose tiles cannot fill the GPU cut their K range over the
     CTAs of a cluster (column forward, row forward with the shard sum, the dY GEMM with the
