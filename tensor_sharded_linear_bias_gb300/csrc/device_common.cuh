@@ -105,6 +105,23 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// The same wait for a role of a warp-specialised kernel that must also notice another role's
+// failure: 1 when the phase has completed, 0 when the CTA's abort flag went up first, -1 after
+// `limit_ns`. The flag is read only while the wait actually polls, so a wait that succeeds at
+// once costs one try_wait.
+__device__ __forceinline__ int mbar_wait_or_abort(uint32_t bar, uint32_t parity,
+                                                  const volatile int* abort_flag,
+                                                  uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return 1;
+  const uint64_t t0 = global_ns();
+  uint32_t spins = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return 1;
+    if (*abort_flag) return 0;
+    if ((++spins & 255u) == 0u && global_ns() - t0 > limit_ns) return -1;
+  }
+}
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }

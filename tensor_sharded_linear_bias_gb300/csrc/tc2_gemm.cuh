@@ -270,9 +270,14 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer (both CTAs)
+      // One thread issues every load of the CTA, so its loop is kept short: per K block one
+      // try_wait, two or three TMA issues and no division (the shard map and K offset advance
+      // incrementally); the abort flag is read only while a wait actually polls.
       uint32_t stage = 0, phase = 0;
       bool failed = false;
       long long issued = 0;
+      const uint32_t full_leader = map_to_rank(full_bar(0), 0);   // the leader's full[0]
+      const int kend = p.kblocks * BK;
       for (int u = cluster; u < p.num_units && !failed; u += nclusters) {
         int t, kb0, kb1, piece;
         tc::decode_unit(p, u, total_kb, t, kb0, kb1, piece);
@@ -280,17 +285,19 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
         tc::decode_tile(p, t, g, mb, nb);
         const int arow = mb * BM + static_cast<int>(rank) * HALF;   // this CTA's A rows
         const int bcol = nb * BN + static_cast<int>(rank) * HALF;   // this CTA's B half
+        int kg = g * p.kpo + kb0 / p.kblocks;                       // shard of block kb0
+        int kk = (kb0 % p.kblocks) * BK;                            // its K offset
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (*abort_flag) { failed = true; break; }
-          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, kWaitLimitNs)) {
-            report_status(p.status, kDevTimeoutBase | 0x40);
-            *abort_flag = 1;
+          const int w = mbar_wait_or_abort(empty_bar(stage), phase ^ 1u, abort_flag, kWaitLimitNs);
+          if (w <= 0) {
+            if (w < 0) {
+              report_status(p.status, kDevTimeoutBase | 0x40);
+              *abort_flag = 1;
+            }
             failed = true;
             break;
           }
-          const int kg = g * p.kpo + kb / p.kblocks;
-          const int kk = (kb % p.kblocks) * BK;
-          const uint32_t fb = map_to_rank(full_bar(stage), 0);   // the leader's barrier
+          const uint32_t fb = full_leader + 8u * stage;
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
           if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
@@ -313,9 +320,14 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
               tma_load_2d_pair(sb + j * MN_BOX_BYTES, &p.tmB[kg], bcol + 64 * j, kk, fb);
           }
           ++issued;
+          kk += BK;
+          if (kk == kend) { kk = 0; ++kg; }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
+      // another role may have given up after this thread's last wait: its copies in flight
+      // are then never consumed
+      if (!failed && *abort_flag) failed = true;
       if (failed && issued > 0) {
         // The copies signal the leader's barriers; give any still in flight time to land
         // before this CTA can leave.
@@ -333,19 +345,24 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
       for (int u = cluster; u < p.num_units && !failed; u += nclusters) {
         int t, kb0, kb1, piece;
         tc::decode_unit(p, u, total_kb, t, kb0, kb1, piece);
-        if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, kWaitLimitNs)) {
-          report_status(p.status, kDevTimeoutBase | 0x50);
-          *abort_flag = 1;
+        const int we = mbar_wait_or_abort(tempty_bar(acc), acc_phase ^ 1u, abort_flag, kWaitLimitNs);
+        if (we <= 0) {
+          if (we < 0) {
+            report_status(p.status, kDevTimeoutBase | 0x50);
+            *abort_flag = 1;
+          }
           failed = true;
           break;
         }
         tc::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (*abort_flag) { failed = true; break; }
-          if (!mbar_wait_bounded(full_bar(stage), phase, kWaitLimitNs)) {
-            report_status(p.status, kDevTimeoutBase | 0x51);
-            *abort_flag = 1;
+          const int w = mbar_wait_or_abort(full_bar(stage), phase, abort_flag, kWaitLimitNs);
+          if (w <= 0) {
+            if (w < 0) {
+              report_status(p.status, kDevTimeoutBase | 0x51);
+              *abort_flag = 1;
+            }
             failed = true;
             break;
           }
@@ -367,6 +384,7 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
         umma_commit_pair_multicast(tfull_bar(acc), 0x3);
         if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1u; }
       }
+      if (!failed && *abort_flag) failed = true;   // MMAs of a tile no epilogue will read
       if (failed) {
         umma_commit_pair_multicast(drain_bar, 0x1);
         mbar_wait_bounded(drain_bar, 0, 100000000ull);

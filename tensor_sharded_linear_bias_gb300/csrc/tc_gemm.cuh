@@ -513,22 +513,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer
+      // The loop is kept short (no division, the abort flag read only while a wait polls):
+      // this one thread issues every load of the CTA.
       uint32_t stage = 0, phase = 0;
       long long issued = 0;
       bool failed = false;
+      const int kend = p.kblocks * BK;
       for (int t = blockIdx.x; t < p.num_tiles && !failed; t += gridDim.x) {
         int g, mb, nb;
         decode_tile(p, t, g, mb, nb);
+        int kg = g * p.kpo, kk = 0;
         for (int kb = 0; kb < total_kb; ++kb) {
-          if (*abort_flag) { failed = true; break; }
-          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, kWaitLimitNs)) {
-            report_status(p.status, kDevTimeoutBase | 0x10);
-            *abort_flag = 1;
+          const int w = mbar_wait_or_abort(empty_bar(stage), phase ^ 1u, abort_flag, kWaitLimitNs);
+          if (w <= 0) {
+            if (w < 0) {
+              report_status(p.status, kDevTimeoutBase | 0x10);
+              *abort_flag = 1;
+            }
             failed = true;
             break;
           }
-          const int kg = g * p.kpo + kb / p.kblocks;
-          const int kk = (kb % p.kblocks) * BK;
           const uint32_t fb = full_bar(stage);
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
@@ -552,9 +556,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
               tma_load_2d(sb + j * MN_BOX_BYTES, &p.tmB[kg], nb * BN + 64 * j, kk, fb);
           }
           ++issued;
+          kk += BK;
+          if (kk == kend) { kk = 0; ++kg; }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
+      // another role may have given up after this thread's last wait
+      if (!failed && *abort_flag) failed = true;
       if (failed) {
         // Drain: wait (bounded) until every copy this thread issued has landed.
         for (int s = 0; s < STAGES; ++s) {
@@ -572,19 +580,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool failed = false;
       for (int t = blockIdx.x; t < p.num_tiles && !failed; t += gridDim.x) {
-        if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, kWaitLimitNs)) {
-          report_status(p.status, kDevTimeoutBase | 0x20);
-          *abort_flag = 1;
+        const int we = mbar_wait_or_abort(tempty_bar(acc), acc_phase ^ 1u, abort_flag, kWaitLimitNs);
+        if (we <= 0) {
+          if (we < 0) {
+            report_status(p.status, kDevTimeoutBase | 0x20);
+            *abort_flag = 1;
+          }
           failed = true;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < total_kb; ++kb) {
-          if (*abort_flag) { failed = true; break; }
-          if (!mbar_wait_bounded(full_bar(stage), phase, kWaitLimitNs)) {
-            report_status(p.status, kDevTimeoutBase | 0x21);
-            *abort_flag = 1;
+          const int w = mbar_wait_or_abort(full_bar(stage), phase, abort_flag, kWaitLimitNs);
+          if (w <= 0) {
+            if (w < 0) {
+              report_status(p.status, kDevTimeoutBase | 0x21);
+              *abort_flag = 1;
+            }
             failed = true;
             break;
           }
@@ -606,6 +619,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         umma_commit(tfull_bar(acc));
         if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1u; }
       }
+      if (!failed && *abort_flag) failed = true;   // MMAs of a tile no epilogue will read
       if (failed) {
         // Drain: all MMAs issued so far complete before TMEM is freed.
         umma_commit(drain_bar);
