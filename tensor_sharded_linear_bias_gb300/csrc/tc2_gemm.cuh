@@ -38,7 +38,8 @@ constexpr int A_BYTES = HALF * BK * 2;       // 16 KiB
 constexpr int B_BYTES = HALF * BK * 2;       // 16 KiB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int MN_BOX_BYTES = 64 * BK * 2;    // 8 KiB
-// Warp 0: TMA producer; warp 1: MMA issuer; warps 2..: EPI_W epilogue warps. A warp may only
+// Warp 0: TMA producer (A); warp 1: MMA issuer; warps 2..: EPI_W epilogue warps; the last
+// warp: TMA producer (B), so that no single thread's issue loop paces the ring. A warp may only
 // read the 32 TMEM lanes of quadrant warp % 4, so with 4 epilogue warps each takes all 256
 // columns of its 32 rows, and with 8 two warps share a quadrant and take 128 columns each
 // (for epilogue-heavy tiles, GeLU or GeLU', whose K loops are too short to hide 4 warps' work).
@@ -47,7 +48,8 @@ struct EpiShape {
   static_assert(EPI_W == 4 || EPI_W == 8, "4 or 8 epilogue warps");
   static constexpr int WARPS = EPI_W;
   static constexpr int COLS = BN * 4 / EPI_W;  // columns per epilogue warp
-  static constexpr int THREADS = 64 + 32 * EPI_W;
+  static constexpr int B_WARP = 2 + EPI_W;         // the B producer, after the epilogue warps
+  static constexpr int THREADS = 96 + 32 * EPI_W;
   static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_W * tc::STAGE_WARP_BYTES + 1024 + 256;
 };
 constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
@@ -267,12 +269,16 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
 
   const int total_kb = p.kblocks * p.kpo;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ TMA producer (both CTAs)
-      // One thread issues every load of the CTA, so its loop is kept short: per K block one
-      // try_wait, two or three TMA issues and no division (the shard map and K offset advance
-      // incrementally); the abort flag is read only while a wait actually polls.
+  if (warp == 0 || warp == E::B_WARP) {
+    // ------------------------------------------------------------ TMA producers (both CTAs)
+    // Lane 0 of warp 0 loads A (and posts the leader's expect_tx), lane 0 of the last warp
+    // loads B; with p.split_loads == 0 warp 0 loads both. Each loop is kept short: per K
+    // block one try_wait, one or two TMA issues and no division (the shard map and K offset
+    // advance incrementally); the abort flag is read only while a wait actually polls.
+    const bool b_warp = warp == E::B_WARP;
+    const bool do_a = !b_warp;
+    const bool do_b = b_warp == (p.split_loads != 0);
+    if (lane == 0 && (do_a || do_b)) {
       uint32_t stage = 0, phase = 0;
       bool failed = false;
       long long issued = 0;
@@ -300,24 +306,28 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
           const uint32_t fb = full_leader + 8u * stage;
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
-          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
-          if (!A_MN) {
-            tma_load_2d_pair(sa, &p.tmA[kg], kk, arow, fb);
-          } else if (p.a3d) {
-            tma_load_3d_pair(sa, &p.tmA[kg], 0, kk, arow / 64, fb);
-          } else {
+          if (do_a) {
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
+            if (!A_MN) {
+              tma_load_2d_pair(sa, &p.tmA[kg], kk, arow, fb);
+            } else if (p.a3d) {
+              tma_load_3d_pair(sa, &p.tmA[kg], 0, kk, arow / 64, fb);
+            } else {
 #pragma unroll
-            for (int j = 0; j < HALF / 64; ++j)
-              tma_load_2d_pair(sa + j * MN_BOX_BYTES, &p.tmA[kg], arow + 64 * j, kk, fb);
+              for (int j = 0; j < HALF / 64; ++j)
+                tma_load_2d_pair(sa + j * MN_BOX_BYTES, &p.tmA[kg], arow + 64 * j, kk, fb);
+            }
           }
-          if (!B_MN) {
-            tma_load_2d_pair(sb, &p.tmB[kg], kk, bcol, fb);
-          } else if (p.b3d) {
-            tma_load_3d_pair(sb, &p.tmB[kg], 0, kk, bcol / 64, fb);
-          } else {
+          if (do_b) {
+            if (!B_MN) {
+              tma_load_2d_pair(sb, &p.tmB[kg], kk, bcol, fb);
+            } else if (p.b3d) {
+              tma_load_3d_pair(sb, &p.tmB[kg], 0, kk, bcol / 64, fb);
+            } else {
 #pragma unroll
-            for (int j = 0; j < HALF / 64; ++j)
-              tma_load_2d_pair(sb + j * MN_BOX_BYTES, &p.tmB[kg], bcol + 64 * j, kk, fb);
+              for (int j = 0; j < HALF / 64; ++j)
+                tma_load_2d_pair(sb + j * MN_BOX_BYTES, &p.tmB[kg], bcol + 64 * j, kk, fb);
+            }
           }
           ++issued;
           kk += BK;

@@ -80,6 +80,7 @@ struct __align__(128) TcParams {
   int full_tiles, ksplit, num_units;
   float* tail_ws;
   int* tail_counters;
+  int split_loads;  // SM-pair kernel: A and B loads issued by two threads (two warps)
   int* status;
 };
 

@@ -146,6 +146,15 @@ bool mn3d_enabled() {
   return true;
 }
 
+// A and B loads of the SM-pair kernel from two producer threads: where both operands are
+// MN-major (weight gradients), whose two 3-D boxes per K block make the longest issue loop
+// (measured 1-2 % faster there, 0.5-1 % slower for the other layouts); TPMLP_SPLIT_LOADS
+// overrides.
+bool split_loads_enabled(int layout) {
+  if (const char* env = std::getenv("TPMLP_SPLIT_LOADS")) return std::atoi(env) != 0;
+  return layout == 2;
+}
+
 // Split tail; TPMLP_TAIL_SPLIT=0 turns it off.
 bool tail_split_enabled() {
   if (const char* env = std::getenv("TPMLP_TAIL_SPLIT")) return std::atoi(env) != 0;
@@ -298,6 +307,7 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
       cudaError_t e = cudaMemsetAsync(s.tail_counters, 0, counters, st);
       if (e != cudaSuccess) return e;
     }
+    p.split_loads = split_loads_enabled(layout) ? 1 : 0;
     const int clusters = std::min(p.num_units, max_clusters);
     return run_pair(layout, p, clusters, st, nullptr, epi_warps);
   }
