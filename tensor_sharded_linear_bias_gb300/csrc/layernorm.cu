@@ -24,6 +24,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "device_common.cuh"
 #include "internal.h"
@@ -238,6 +239,172 @@ __global__ void __launch_bounds__(kLnWarps * 32, 3) ln_backward_dx_kernel(const 
   }
 }
 
+// Register-resident variants for rows whose shards fit in NV 16-byte vectors per lane (one
+// warp per shard, n <= kLnWarps): every lane issues all loads of its part of the row at once
+// (one DRAM round trip per block instead of one per kUnroll vectors plus a second pass that
+// re-reads the row), keeps the raw vectors in registers for the second pass, and reads only
+// gamma / beta again (the same few KB for every row: L1 hits). The arithmetic is that of the
+// kernels above, in the same order (lane l's vectors l, l + 32, ... ascending): the results
+// are bit-identical.
+template <typename T, int NV>
+__device__ __forceinline__ void load_row_part(const T* src, long long Hs, int lane, uint4* raw) {
+  constexpr int VEC = 16 / sizeof(T);
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const long long c = static_cast<long long>(v * 32 + lane) * VEC;
+    raw[v] = c < Hs ? *reinterpret_cast<const uint4*>(src + c) : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// The VEC values of a raw 16-byte vector as fp32, with register operations only (a bf16 is
+// the upper half of the fp32 with the same bits).
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4& r, float* out);
+template <>
+__device__ __forceinline__ void unpack16<float>(const uint4& r, float* out) {
+  out[0] = __uint_as_float(r.x);
+  out[1] = __uint_as_float(r.y);
+  out[2] = __uint_as_float(r.z);
+  out[3] = __uint_as_float(r.w);
+}
+template <>
+__device__ __forceinline__ void unpack16<__nv_bfloat16>(const uint4& r, float* out) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    out[2 * q] = __uint_as_float(w[q] << 16);
+    out[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+  }
+}
+
+template <typename T, int NV>
+__global__ void __launch_bounds__(kLnWarps * 32) ln_forward_reg_kernel(const __grid_constant__ LnParams p) {
+  constexpr int VEC = 16 / sizeof(T);
+  __shared__ float stat[kLnWarps][2];
+  const int lane = threadIdx.x & 31, i = threadIdx.x >> 5;  // warp i: shard i
+  const long long t = blockIdx.x;
+  const long long row = t * p.Hs;
+  const T* x = static_cast<const T*>(p.X[i]) + row;
+  uint4 raw[NV];
+  load_row_part<T, NV>(x, p.Hs, lane, raw);
+  float first[VEC];
+  unpack16<T>(raw[0], first);
+  const float k = __shfl_sync(0xffffffffu, first[0], 0);  // the shard's first element
+  float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    if (static_cast<long long>(v * 32 + lane) * VEC >= p.Hs) break;
+    float f[VEC];
+    unpack16<T>(raw[v], f);
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) {
+      const float d = f[j] - k;
+      s1 += d;
+      s2 = fmaf(d, d, s2);
+    }
+  }
+  s1 = warp_sum(s1);
+  s2 = warp_sum(s2);
+  const float ci = static_cast<float>(p.Hs);
+  if (lane == 0) {
+    stat[i][0] = k + s1 / ci;
+    stat[i][1] = fmaxf(s2 - s1 * (s1 / ci), 0.f);
+  }
+  __syncthreads();
+  float cnt = 0.f, mean = 0.f, m2 = 0.f;
+  for (int s = 0; s < p.n; ++s) {
+    const float c2 = cnt + ci;
+    const float d = stat[s][0] - mean;
+    mean += d * (ci / c2);
+    m2 += stat[s][1] + d * d * (cnt * ci / c2);
+    cnt = c2;
+  }
+  const float rstd = rsqrtf(m2 / cnt + p.eps);
+  if (threadIdx.x == 0) {
+    if (p.mean != nullptr) p.mean[t] = mean;
+    if (p.rstd != nullptr) p.rstd[t] = rstd;
+  }
+  T* y = static_cast<T*>(p.Y[i]) + row;
+  const T* g = static_cast<const T*>(p.gamma[i]);
+  const T* b = static_cast<const T*>(p.beta[i]);
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const long long c = static_cast<long long>(v * 32 + lane) * VEC;
+    if (c >= p.Hs) break;
+    float f[VEC], gv[VEC], bv[VEC];
+    unpack16<T>(raw[v], f);
+    if (g != nullptr) load_vec<T, VEC>(g + c, gv);
+    if (b != nullptr) load_vec<T, VEC>(b + c, bv);
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) {
+      const float h = (f[j] - mean) * rstd;
+      f[j] = fmaf(h, g != nullptr ? gv[j] : 1.f, b != nullptr ? bv[j] : 0.f);
+    }
+    store_vec<T, VEC>(y + c, f);
+  }
+}
+
+template <typename T, int NV>
+__global__ void __launch_bounds__(kLnWarps * 32, 2) ln_backward_dx_reg_kernel(const __grid_constant__ LnParams p) {
+  constexpr int VEC = 16 / sizeof(T);
+  __shared__ float stat[kLnWarps][2];
+  const int lane = threadIdx.x & 31, i = threadIdx.x >> 5;
+  const long long t = blockIdx.x;
+  const long long row = t * p.Hs;
+  uint4 xr[NV], dr[NV];
+  load_row_part<T, NV>(static_cast<const T*>(p.X[i]) + row, p.Hs, lane, xr);
+  load_row_part<T, NV>(static_cast<const T*>(p.dY[i]) + row, p.Hs, lane, dr);
+  const float mean = p.mean[t], rstd = p.rstd[t];
+  const T* g = static_cast<const T*>(p.gamma[i]);
+  float a1 = 0.f, a2 = 0.f;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const long long c = static_cast<long long>(v * 32 + lane) * VEC;
+    if (c >= p.Hs) break;
+    float f[VEC], d[VEC], gv[VEC];
+    unpack16<T>(xr[v], f);
+    unpack16<T>(dr[v], d);
+    if (g != nullptr) load_vec<T, VEC>(g + c, gv);
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) {
+      const float gg = d[j] * (g != nullptr ? gv[j] : 1.f);
+      a1 += gg;
+      a2 = fmaf(gg, (f[j] - mean) * rstd, a2);
+    }
+  }
+  a1 = warp_sum(a1);
+  a2 = warp_sum(a2);
+  if (lane == 0) {
+    stat[i][0] = a1;
+    stat[i][1] = a2;
+  }
+  __syncthreads();
+  float s1 = 0.f, s2 = 0.f;
+  for (int s = 0; s < p.n; ++s) {
+    s1 += stat[s][0];
+    s2 += stat[s][1];
+  }
+  const float inv_h = 1.f / static_cast<float>(p.Hs * p.n);
+  const float m1 = s1 * inv_h, m2 = s2 * inv_h;
+  T* dx = static_cast<T*>(p.Y[i]) + row;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const long long c = static_cast<long long>(v * 32 + lane) * VEC;
+    if (c >= p.Hs) break;
+    float f[VEC], d[VEC], gv[VEC];
+    unpack16<T>(xr[v], f);
+    unpack16<T>(dr[v], d);
+    if (g != nullptr) load_vec<T, VEC>(g + c, gv);
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) {
+      const float gg = d[j] * (g != nullptr ? gv[j] : 1.f);
+      const float h = (f[j] - mean) * rstd;
+      f[j] = rstd * (gg - m1 - h * m2);
+    }
+    store_vec<T, VEC>(dx + c, f);
+  }
+}
+
 // dgamma_i[c] = sum_t dY_i[t,c] * xhat[t,c], dbeta_i[c] = sum_t dY_i[t,c]. blockIdx.x: a strip
 // of 32 * VEC columns of one shard (strips of shard i are consecutive); lane l of every warp
 // owns columns [strip + VEC l, strip + VEC l + VEC) (one 16-byte access per row where the rows
@@ -348,6 +515,20 @@ int vec_width(const LnParams& p, bool backward) {
   return V;
 }
 
+// Register-resident kernels where they apply; TPMLP_LN_REG=0 keeps the two-pass kernels.
+bool ln_reg_enabled() {
+  if (const char* env = std::getenv("TPMLP_LN_REG")) return std::atoi(env) != 0;
+  return true;
+}
+
+template <typename T, int NV>
+void launch_rows_reg(const LnParams& p, bool backward, dim3 grid, int threads, cudaStream_t st) {
+  if (!backward)
+    ln_forward_reg_kernel<T, NV><<<grid, threads, 0, st>>>(p);
+  else
+    ln_backward_dx_reg_kernel<T, NV><<<grid, threads, 0, st>>>(p);
+}
+
 template <typename T>
 cudaError_t launch_rows(const LnParams& p, bool backward, cudaStream_t st) {
   constexpr int V = 16 / sizeof(T);
@@ -355,6 +536,18 @@ cudaError_t launch_rows(const LnParams& p, bool backward, cudaStream_t st) {
   const dim3 grid(static_cast<unsigned>(p.T));                 // one block per token row
   const int threads = 32 * std::min(p.n, kLnWarps);          // one warp per shard (or more)
   const bool vec = vec_width<T>(p, backward) == V;
+  const long long nv = (p.Hs + 32LL * V - 1) / (32LL * V);    // 16-byte vectors per lane
+  if (vec && p.n <= kLnWarps && nv <= 8 && ln_reg_enabled()) {
+    if (nv <= 2)
+      launch_rows_reg<T, 2>(p, backward, grid, threads, st);
+    else if (nv <= 4)
+      launch_rows_reg<T, 4>(p, backward, grid, threads, st);
+    else if (nv <= 6)
+      launch_rows_reg<T, 6>(p, backward, grid, threads, st);
+    else
+      launch_rows_reg<T, 8>(p, backward, grid, threads, st);
+    return cudaGetLastError();
+  }
   if (!backward) {
     if (vec)
       ln_forward_kernel<T, V><<<grid, threads, 0, st>>>(p);
