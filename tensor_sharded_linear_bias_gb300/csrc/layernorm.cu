@@ -563,23 +563,54 @@ cudaError_t launch_rows(const LnParams& p, bool backward, cudaStream_t st) {
 }
 
 template <typename T, int VEC>
-cudaError_t launch_param_grads_v(const LnParams& p, cudaStream_t st) {
-  const long long strips = ((p.Hs + 32LL * VEC - 1) / (32LL * VEC)) * p.n;
-  if (strips > 0x7fffffffLL) return cudaErrorInvalidValue;
-  // blocks per strip: about two per SM in all, at least 256 tokens each, a portable cluster
-  const long long want = (2LL * device_sm_count() + strips - 1) / strips;
-  const int R = static_cast<int>(std::max(1LL, std::min({want, p.T / 256, 8LL})));
+cudaLaunchConfig_t param_grads_config(long long strips, int R, cudaStream_t st,
+                                      cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(strips), static_cast<unsigned>(R), 1);
   cfg.blockDim = dim3(kPgWarps * 32, 1, 1);
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = static_cast<unsigned>(R);
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  return cfg;
+}
+
+// How many clusters of R blocks of the column-sum kernel the device holds at once (cached per
+// device; the driver's answer, which accounts for clusters having to fit within one GPC).
+template <typename T, int VEC>
+int param_grads_max_clusters(int R) {
+  static int cache[64][9] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev][R] == 0) {
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = param_grads_config<T, VEC>(1, R, nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, ln_param_grads_kernel<T, VEC>, &cfg) != cudaSuccess)
+      n = 0;
+    cache[dev][R] = n > 0 ? n : -1;
+  }
+  return cache[dev][R];
+}
+
+template <typename T, int VEC>
+cudaError_t launch_param_grads_v(const LnParams& p, cudaStream_t st) {
+  const long long strips = ((p.Hs + 32LL * VEC - 1) / (32LL * VEC)) * p.n;
+  if (strips > 0x7fffffffLL) return cudaErrorInvalidValue;
+  // blocks per strip (a cluster): the most, up to 8 and at least 256 tokens each, for which
+  // all strips' clusters are resident at once (a second, partial wave would double the time)
+  int R = 1;
+  for (int r = static_cast<int>(std::min(8LL, std::max(1LL, p.T / 256))); r > 1; --r) {
+    if (param_grads_max_clusters<T, VEC>(r) >= strips) {
+      R = r;
+      break;
+    }
+  }
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = param_grads_config<T, VEC>(strips, R, st, attr);
   return cudaLaunchKernelEx(&cfg, ln_param_grads_kernel<T, VEC>, p);
 }
 
