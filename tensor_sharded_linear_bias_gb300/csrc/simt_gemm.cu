@@ -9,7 +9,7 @@
 // of A, one of B and 4*RM FFMAs.
 //
 // Split K: when the output tiles alone cannot fill the GPU (few tokens, as in the pages'
-// batch-32 example), the K steps of every tile (over all summed shards) are cut into S <= 8
+// batch-32 example), the K steps of every tile (over all summed shards) are cut into S <= 16
 // contiguous ranges computed by the S CTAs of one thread-block cluster. Each CTA parks its
 // partial tile in its shared memory; after a cluster barrier, CTA q adds rows q*TM/S ..
 // (q+1)*TM/S-1 of all S partial tiles in CTA order (distributed shared memory), applies the
@@ -31,7 +31,7 @@ namespace {
 
 constexpr int TN = 64, TK = 32, STAGES = 4;
 constexpr long long kMinSplitSteps = 4;  // K steps (of TK) a split slice keeps at least
-constexpr int kMaxSplit = 8;             // CTAs of a portable cluster
+constexpr int kMaxSplit = 16;            // CTAs of a cluster (above 8: non-portable size)
 
 struct SimtParams {
   const float* A[kMaxShards];
@@ -273,6 +273,10 @@ cudaError_t launch(const SimtParams& p, dim3 grid, cudaStream_t st) {
   cudaError_t e =
       cudaFuncSetAttribute(simt_gemm_kernel<TM>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  if (p.slices > 8) {
+    e = cudaFuncSetAttribute(simt_gemm_kernel<TM>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
   if (p.slices == 1) {
     simt_gemm_kernel<TM><<<grid, 256, smem, st>>>(p);
     return cudaGetLastError();
@@ -292,6 +296,40 @@ cudaError_t launch(const SimtParams& p, dim3 grid, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, simt_gemm_kernel<TM>, p);
 }
 
+// How many clusters of S CTAs of simt_gemm_kernel<TM> the device holds at once (the driver's
+// answer, which accounts for a cluster having to fit within one GPC); cached per device.
+template <int TM>
+int max_active_clusters(int S) {
+  static int cache[64][kMaxSplit + 1] = {};
+  int dev = 0;
+  if (S < 2 || S > kMaxSplit || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    return 0;
+  if (cache[dev][S] == 0) {
+    constexpr int smem = static_cast<int>(sizeof(SimtSmem<TM>));
+    int n = 0;
+    if (cudaFuncSetAttribute(simt_gemm_kernel<TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) == cudaSuccess &&
+        (S <= 8 || cudaFuncSetAttribute(simt_gemm_kernel<TM>,
+                                        cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                        1) == cudaSuccess)) {
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = dim3(1, 1, static_cast<unsigned>(S));
+      cfg.blockDim = dim3(256, 1, 1);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 1;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = static_cast<unsigned>(S);
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, simt_gemm_kernel<TM>, &cfg) != cudaSuccess) n = 0;
+    }
+    cache[dev][S] = n > 0 ? n : -1;
+  }
+  return cache[dev][S];
+}
+
 }  // namespace
 
 int plan_simt_split(const GemmSpec& s) {
@@ -307,6 +345,14 @@ int plan_simt_split(const GemmSpec& s) {
   long long S = (target + tiles - 1) / tiles;
   S = std::min(S, steps / kMinSplitSteps);  // enough K steps per slice
   S = std::min<long long>(S, kMaxSplit);
+  // every tile's cluster resident at once: a second, partial wave of clusters would take as
+  // long as the first
+  while (S > 1) {
+    const int c = TM == 32 ? max_active_clusters<32>(static_cast<int>(S))
+                           : max_active_clusters<64>(static_cast<int>(S));
+    if (c <= 0 || c >= tiles) break;  // c <= 0: no answer, keep the plan
+    --S;
+  }
   return S > 1 ? static_cast<int>(S) : 1;
 }
 
