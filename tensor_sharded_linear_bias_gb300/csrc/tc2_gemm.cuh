@@ -293,19 +293,27 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
         const int bcol = nb * BN + static_cast<int>(rank) * HALF;   // this CTA's B half
         int kg = g * p.kpo + kb0 / p.kblocks;                       // shard of block kb0
         int kk = (kb0 % p.kblocks) * BK;                            // its K offset
+        bool free_next = false;  // the next block's stage seen free by an earlier probe
         for (int kb = kb0; kb < kb1; ++kb) {
-          const int w = mbar_wait_or_abort(empty_bar(stage), phase ^ 1u, abort_flag, kWaitLimitNs);
-          if (w <= 0) {
-            if (w < 0) {
-              report_status(p.status, kDevTimeoutBase | 0x40);
-              *abort_flag = 1;
+          if (!free_next) {
+            const int w = mbar_wait_or_abort(empty_bar(stage), phase ^ 1u, abort_flag, kWaitLimitNs);
+            if (w <= 0) {
+              if (w < 0) {
+                report_status(p.status, kDevTimeoutBase | 0x40);
+                *abort_flag = 1;
+              }
+              failed = true;
+              break;
             }
-            failed = true;
-            break;
           }
+          uint32_t nstage = stage + 1, nphase = phase;
+          if (nstage == STAGES) { nstage = 0; nphase ^= 1u; }
           const uint32_t fb = full_leader + 8u * stage;
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
+          // probe the next stage between this block's loads, as the MMA issuer does
+          const bool probe = p.load_probe != 0 && kb + 1 < kb1;
+          if (!do_a && probe) free_next = mbar_try_wait(empty_bar(nstage), nphase ^ 1u);
           if (do_a) {
             if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
             if (!A_MN) {
@@ -318,6 +326,7 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
                 tma_load_2d_pair(sa + j * MN_BOX_BYTES, &p.tmA[kg], arow + 64 * j, kk, fb);
             }
           }
+          if (do_a && probe) free_next = mbar_try_wait(empty_bar(nstage), nphase ^ 1u);
           if (do_b) {
             if (!B_MN) {
               tma_load_2d_pair(sb, &p.tmB[kg], kk, bcol, fb);
@@ -332,7 +341,8 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
           ++issued;
           kk += BK;
           if (kk == kend) { kk = 0; ++kg; }
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          stage = nstage;
+          phase = nphase;
         }
       }
       // another role may have given up after this thread's last wait: its copies in flight
@@ -366,21 +376,31 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
         }
         tc::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
+        // `ready`: the next block's full barrier was seen complete by a probe issued before the
+        // current block's last MMA (its latency then hides behind the MMA issue instead of
+        // adding to the gap between blocks)
+        bool ready = false;
         for (int kb = kb0; kb < kb1; ++kb) {
-          const int w = mbar_wait_or_abort(full_bar(stage), phase, abort_flag, kWaitLimitNs);
-          if (w <= 0) {
-            if (w < 0) {
-              report_status(p.status, kDevTimeoutBase | 0x51);
-              *abort_flag = 1;
+          if (!ready) {
+            const int w = mbar_wait_or_abort(full_bar(stage), phase, abort_flag, kWaitLimitNs);
+            if (w <= 0) {
+              if (w < 0) {
+                report_status(p.status, kDevTimeoutBase | 0x51);
+                *abort_flag = 1;
+              }
+              failed = true;
+              break;
             }
-            failed = true;
-            break;
           }
           tc::tc_fence_after();
+          uint32_t nstage = stage + 1, nphase = phase;
+          if (nstage == STAGES) { nstage = 0; nphase ^= 1u; }
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
+            if (k == BK / 16 - 1)
+              ready = p.mma_probe != 0 && kb + 1 < kb1 && mbar_try_wait(full_bar(nstage), nphase);
             const uint64_t ad = A_MN ? tc::sdesc_sw128(sa + k * 2048, MN_BOX_BYTES, 1024)
                                      : tc::sdesc_sw128(sa + k * 32, 16, 1024);
             const uint64_t bd = B_MN ? tc::sdesc_sw128(sb + k * 2048, MN_BOX_BYTES, 1024)
@@ -388,7 +408,8 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
             umma_bf16_pair(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
           }
           umma_commit_pair_multicast(empty_bar(stage), 0x3);
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          stage = nstage;
+          phase = nphase;
         }
         if (failed) break;
         umma_commit_pair_multicast(tfull_bar(acc), 0x3);

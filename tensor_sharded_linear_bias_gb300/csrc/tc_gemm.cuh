@@ -81,6 +81,8 @@ struct __align__(128) TcParams {
   float* tail_ws;
   int* tail_counters;
   int split_loads;  // SM-pair kernel: A and B loads issued by two threads (two warps)
+  int mma_probe;    // SM-pair kernel: probe the next block's full barrier during the MMAs
+  int load_probe;   // ... and the next block's empty barrier between the loads
   int* status;
 };
 

@@ -155,6 +155,20 @@ bool split_loads_enabled(int layout) {
   return layout == 2;
 }
 
+// The MMA issuer's early look at the next block's barrier; TPMLP_MMA_PROBE overrides.
+bool mma_probe_enabled() {
+  if (const char* env = std::getenv("TPMLP_MMA_PROBE")) return std::atoi(env) != 0;
+  return true;
+}
+
+// The producers' early look at the next block's stage: for A K-major with B MN-major (the
+// forward GEMMs: 4-5 % faster), not for the other layouts (both K-major: 0.5-2 % slower, both
+// MN-major: no change); TPMLP_LOAD_PROBE overrides.
+bool load_probe_enabled(int layout) {
+  if (const char* env = std::getenv("TPMLP_LOAD_PROBE")) return std::atoi(env) != 0;
+  return layout == 0;
+}
+
 // Split tail; TPMLP_TAIL_SPLIT=0 turns it off.
 bool tail_split_enabled() {
   if (const char* env = std::getenv("TPMLP_TAIL_SPLIT")) return std::atoi(env) != 0;
@@ -308,6 +322,8 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
       if (e != cudaSuccess) return e;
     }
     p.split_loads = split_loads_enabled(layout) ? 1 : 0;
+    p.mma_probe = mma_probe_enabled() ? 1 : 0;
+    p.load_probe = load_probe_enabled(layout) ? 1 : 0;
     const int clusters = std::min(p.num_units, max_clusters);
     return run_pair(layout, p, clusters, st, nullptr, epi_warps);
   }

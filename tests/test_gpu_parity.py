@@ -181,27 +181,35 @@ def test_epilogue_warps(tp, monkeypatch, epi_warps, T, H, F, n):
         assert max(errs.values()) <= TOL_BF16, (reduce, errs)
 
 
+_ISSUE_VARIANTS = [{"TPMLP_SPLIT_LOADS": "1"}, {"TPMLP_SPLIT_LOADS": "0"},
+                   {"TPMLP_MMA_PROBE": "0", "TPMLP_LOAD_PROBE": "0"},
+                   {"TPMLP_MMA_PROBE": "1", "TPMLP_LOAD_PROBE": "1"}]
+
+
 @pytest.mark.parametrize("epi_warps", ["4", "8"])
-def test_split_loads(tp, monkeypatch, epi_warps):
-    """The SM-pair kernel's A and B loads issued by one producer thread or by two (warp 0 and
-    the last warp), for all three operand layouts (forward, input-gradient and weight-gradient
-    GEMMs), ragged tiles, fused and overlapped shard sums: matches the oracle, and the two
-    settings give bit-identical results (only the issuing thread differs)."""
+def test_issue_loop_variants(tp, monkeypatch, epi_warps):
+    """The SM-pair kernel's issue loops in every variant: A and B loads from one producer thread
+    or two (warp 0 and the last warp), with and without the early looks at the next block's
+    barriers (MMA issuer and producers), for all three operand layouts (forward,
+    input-gradient and weight-gradient GEMMs), ragged tiles, fused and overlapped shard sums.
+    The default matches the oracle; every variant is bit-identical to it (they change which
+    thread issues what and when, not the arithmetic)."""
     monkeypatch.setenv("TPMLP_EPI_WARPS", epi_warps)
     monkeypatch.setenv("TPMLP_GEMM_PAIR", "1")
     w = SMALL.with_shape(tokens=600, hidden=392, ffn=2 * 264, tp_degree=2)
     for reduce in (0, 4):
-        outs = {}
-        for split in ("1", "0"):
-            monkeypatch.setenv("TPMLP_SPLIT_LOADS", split)
-            case = MlpCase(w, reduce).run()
-            outs[split] = case.outputs()
-            if split == "1":
-                errs = compare_full(outs[split], *full_reference(case))
-                assert max(errs.values()) <= TOL_BF16, (reduce, errs)
-        for k, v in outs["1"].items():
-            pairs = zip(v, outs["0"][k]) if isinstance(v, list) else [(v, outs["0"][k])]
-            assert all(np.array_equal(a, b) for a, b in pairs), (reduce, k)
+        case = MlpCase(w, reduce).run()
+        base = case.outputs()
+        errs = compare_full(base, *full_reference(case))
+        assert max(errs.values()) <= TOL_BF16, (reduce, errs)
+        for env in _ISSUE_VARIANTS:
+            with monkeypatch.context() as m:
+                for k, v in env.items():
+                    m.setenv(k, v)
+                out = MlpCase(w, reduce).run().outputs()
+            for k, v in base.items():
+                pairs = zip(v, out[k]) if isinstance(v, list) else [(v, out[k])]
+                assert all(np.array_equal(a, b) for a, b in pairs), (reduce, env, k)
 
 
 _TAIL_REF = {}
