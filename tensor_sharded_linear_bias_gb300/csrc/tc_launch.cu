@@ -176,7 +176,13 @@ bool tail_split_enabled() {
 }
 
 constexpr int kMinPieceKb = 16;  // K blocks of 64 a piece keeps at least
-constexpr int kMaxSplitWaves = 8;  // deeper queues: the partly idle last wave matters little
+// Shallow tiles are split only when there are at most this many waves (in a deeper queue of
+// short tiles the partly idle last wave matters less than the pieces' round trip: the GPT-3
+// weight gradients, 121 waves of 32 K blocks, were 1 % slower split); tiles of at least
+// kDeepTileKb K blocks are split at any number of waves (the GPT-3 column forward and dY GEMMs,
+// 20 waves of 192 K blocks: 0.6-1.3 % faster; T 8192: 1-3 %).
+constexpr int kMaxSplitWaves = 8;
+constexpr int kDeepTileKb = 64;
 
 // Work units of an SM-pair launch over `clusters` pairs. Tiles are dealt to the pairs round
 // robin, so the last wave holds L = num_tiles mod clusters tiles (all of them when there are
@@ -189,7 +195,9 @@ void plan_tail(tc::TcParams& p, int clusters, int total_kb, bool have_ws) {
   p.ksplit = 1;
   p.num_units = p.num_tiles;
   if (!have_ws || !tail_split_enabled() || clusters < 2) return;
-  if (p.num_tiles > kMaxSplitWaves * clusters) return;
+  int max_waves = total_kb >= kDeepTileKb ? 1 << 20 : kMaxSplitWaves;
+  if (const char* env = std::getenv("TPMLP_TAIL_WAVES")) max_waves = std::atoi(env);
+  if (p.num_tiles > static_cast<long long>(max_waves) * clusters) return;
   const int L = p.num_tiles % clusters;
   if (L == 0) return;
   int S = clusters / L;
@@ -211,8 +219,9 @@ int plan_shard_split(int64_t M, int64_t N, int64_t K_per_group, int n) {
   }
   // Model on SM pairs (the kernel for every M > 128): 256 x 256 tiles dealt to C = SMs / 2
   // pairs; a 64-deep K block of a pair tile costs ~512 tensor cycles (~0.27 us). A last wave
-  // that leaves pairs idle costs a whole tile, unless the tail split applies (at most 8 waves,
-  // >= 32 K blocks per tile), which cuts its L tiles into P pieces (~1/P of a tile, plus a
+  // that leaves pairs idle costs a whole tile, unless the tail split applies (at most 8 waves
+  // or tiles of >= 64 K blocks; >= 32 K blocks per tile), which cuts its L tiles into P pieces
+  // (~1/P of a tile, plus a
   // little for the piece sums). A reduction of S fp32 partials moves (4 S + 4) M N bytes at
   // ~6.5 TB/s. (Measured on GB300, GPT-3-shaped step: fused 1525-1528 TFLOP/s with the tail
   // split vs 1499-1506 for S = 4 and 1499 fused without it.)
@@ -229,7 +238,8 @@ int plan_shard_split(int64_t M, int64_t N, int64_t K_per_group, int n) {
     const double tiles = S * tiles1;
     double waves = std::ceil(tiles / C);
     const double L = tiles - C * std::floor(tiles / C);
-    if (L > 0 && tiles <= kMaxSplitWaves * C && tail_split_enabled()) {
+    if (L > 0 && (tiles <= kMaxSplitWaves * C || per_tile_kb >= kDeepTileKb) &&
+        tail_split_enabled()) {
       const double P = std::min({std::floor(C / L), std::floor(per_tile_kb / kMinPieceKb),
                                  std::floor(kTailUnits / L)});
       if (P >= 2) waves = std::floor(tiles / C) + 1.0 / P + 0.05;
