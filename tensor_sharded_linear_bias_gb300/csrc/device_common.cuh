@@ -41,6 +41,41 @@ __device__ __forceinline__ float gelu_erf_grad(float h) {
   return fmaf(h * 0.3989422804014327f, n.e, n.cdf);
 }
 
+// The same two functions for two values at once with Blackwell's paired fp32 instructions
+// (__ffma2_rn, __fmul2_rn, __fadd2_rn: each half rounded exactly as the scalar operation), for
+// the epilogues that are bound by instruction issue. Every operation and its order are those
+// of normal_tail, gelu_erf and gelu_erf_grad, so the results are bit-identical to them; the
+// exponential and the fast reciprocal stay per value.
+__device__ __forceinline__ float2 splat2(float a) { return make_float2(a, a); }
+
+__device__ __forceinline__ void normal_tail2(float2 h, float2& cdf, float2& e) {
+  const float2 z = __fmul2_rn(make_float2(fabsf(h.x), fabsf(h.y)), splat2(0.7071067811865475f));
+  const float2 d = __ffma2_rn(splat2(0.3275911f), z, splat2(1.0f));
+  const float2 t = make_float2(__fdividef(1.0f, d.x), __fdividef(1.0f, d.y));
+  float2 q = __ffma2_rn(t, splat2(1.061405429f), splat2(-1.453152027f));
+  q = __ffma2_rn(t, q, splat2(1.421413741f));
+  q = __ffma2_rn(t, q, splat2(-0.284496736f));
+  q = __ffma2_rn(t, q, splat2(0.254829592f));
+  const float2 poly = __fmul2_rn(t, q);
+  const float2 nz2 = __fmul2_rn(make_float2(-z.x, -z.y), z);
+  e = make_float2(__expf(nz2.x), __expf(nz2.y));
+  const float2 lower = __fmul2_rn(__fmul2_rn(splat2(0.5f), poly), e);
+  const float2 upper = __fadd2_rn(splat2(1.0f), make_float2(-lower.x, -lower.y));
+  cdf = make_float2(h.x >= 0.0f ? upper.x : lower.x, h.y >= 0.0f ? upper.y : lower.y);
+}
+
+__device__ __forceinline__ float2 gelu_erf2(float2 h) {
+  float2 cdf, e;
+  normal_tail2(h, cdf, e);
+  return __fmul2_rn(h, cdf);
+}
+
+__device__ __forceinline__ float2 gelu_erf_grad2(float2 h) {
+  float2 cdf, e;
+  normal_tail2(h, cdf, e);
+  return __ffma2_rn(__fmul2_rn(h, splat2(0.3989422804014327f)), e, cdf);
+}
+
 // ------------------------------------------------------------------ L2 prefetch
 // Ask L2 for `bytes` bytes of global memory from ptr (16-byte aligned, a multiple of 16 bytes).
 __device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {

@@ -327,9 +327,10 @@ __device__ __forceinline__ void add_bias_bf16x32(const uint16_t* bias, int valid
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float2 f = unpack_bf16x2(w[j]);
-        v[q * 8 + 2 * j] += f.x;
-        v[q * 8 + 2 * j + 1] += f.y;
+        const float2 f = __fadd2_rn(make_float2(v[q * 8 + 2 * j], v[q * 8 + 2 * j + 1]),
+                                    unpack_bf16x2(w[j]));
+        v[q * 8 + 2 * j] = f.x;
+        v[q * 8 + 2 * j + 1] = f.y;
       }
     }
   }
@@ -412,7 +413,11 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, int g, int row
       warp_store_bf16(stage, v, static_cast<uint16_t*>(p.D[og]), p.ldd, row0, col0, p.M, valid);
     if (p.act == TP_ACT_GELU_ERF) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+      for (int i = 0; i < 32; i += 2) {
+        const float2 y = gelu_erf2(make_float2(v[i], v[i + 1]));
+        v[i] = y.x;
+        v[i + 1] = y.y;
+      }
     }
     warp_store_bf16(stage, v, static_cast<uint16_t*>(p.D2[og]), p.ldd2, row0, col0, p.M, valid);
   } else {  // EPI_DACT (aux = the saved pre-activation, read only with an activation)
@@ -422,7 +427,12 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, int g, int row
       warp_fetch_bf16(static_cast<const uint16_t*>(p.aux[og]), p.ldaux, row0, col0, p.M, valid, raw);
       warp_unpack_bf16(stage, raw, h);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] *= gelu_erf_grad(h[i]);
+      for (int i = 0; i < 32; i += 2) {
+        const float2 y = __fmul2_rn(make_float2(v[i], v[i + 1]),
+                                    gelu_erf_grad2(make_float2(h[i], h[i + 1])));
+        v[i] = y.x;
+        v[i + 1] = y.y;
+      }
     }
     warp_store_bf16(stage, v, static_cast<uint16_t*>(p.D[og]), p.ldd, row0, col0, p.M, valid);
   }
@@ -458,7 +468,12 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, int g, int row0
     tmem_ld_32cols(trow + c0, v);
     warp_unpack_bf16(stage, cur, h);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] *= gelu_erf_grad(h[i]);
+    for (int i = 0; i < 32; i += 2) {
+      const float2 y = __fmul2_rn(make_float2(v[i], v[i + 1]),
+                                  gelu_erf_grad2(make_float2(h[i], h[i + 1])));
+      v[i] = y.x;
+      v[i + 1] = y.y;
+    }
     warp_store_bf16(stage, v, static_cast<uint16_t*>(p.D[g]), p.ldd, row0, col0, p.M,
                     min(32, p.N - col0));
   }
