@@ -335,10 +335,16 @@ __global__ void __launch_bounds__(kLnWarps * 32) ln_forward_reg_kernel(const __g
     unpack16<T>(raw[v], f);
     if (g != nullptr) load_vec<T, VEC>(g + c, gv);
     if (b != nullptr) load_vec<T, VEC>(b + c, bv);
+    // the two-pass kernel's (x - mean) * rstd and fma, two columns per paired instruction
+    // (each half rounded as the scalar operation: the same results)
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) {
-      const float h = (f[j] - mean) * rstd;
-      f[j] = fmaf(h, g != nullptr ? gv[j] : 1.f, b != nullptr ? bv[j] : 0.f);
+    for (int j = 0; j < VEC; j += 2) {
+      const float2 h = __fmul2_rn(__fadd2_rn(make_float2(f[j], f[j + 1]), splat2(-mean)),
+                                  splat2(rstd));
+      const float2 y = __ffma2_rn(h, g != nullptr ? make_float2(gv[j], gv[j + 1]) : splat2(1.f),
+                                  b != nullptr ? make_float2(bv[j], bv[j + 1]) : splat2(0.f));
+      f[j] = y.x;
+      f[j + 1] = y.y;
     }
     store_vec<T, VEC>(y + c, f);
   }
