@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kLnWarps * 32) ln_forward_reg_kernel(const __g
 }
 
 template <typename T, int NV>
-__global__ void __launch_bounds__(kLnWarps * 32, 2) ln_backward_dx_reg_kernel(const __grid_constant__ LnParams p) {
+__global__ void __launch_bounds__(kLnWarps * 32, 3) ln_backward_dx_reg_kernel(const __grid_constant__ LnParams p) {
   constexpr int VEC = 16 / sizeof(T);
   __shared__ float stat[kLnWarps][2];
   const int lane = threadIdx.x & 31, i = threadIdx.x >> 5;
