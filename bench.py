@@ -179,10 +179,25 @@ def peaks():
             "source": "fallback", "ffma_f32": FFMA_F32_TFLOPS}
 
 
-def kernel_source_hash() -> str:
+def code_lines(text: str):
+    """The lines of a C++ source with // comments and blank lines removed (a comment edit does
+    not change the kernel the counters were taken on)."""
+    for line in text.splitlines():
+        code = line.split("//", 1)[0].rstrip()
+        if code:
+            yield code
+
+
+def kernel_source_hash(read=None) -> str:
+    """Hash of the code of the tensor-core GEMM's sources; `read(name)` supplies a file's text
+    (default: the working tree)."""
+    if read is None:
+        def read(f):
+            return open(os.path.join(ROOT, "tensor_sharded_linear_bias_gb300", "csrc", f)).read()
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        h.update(open(os.path.join(ROOT, "tensor_sharded_linear_bias_gb300", "csrc", f), "rb").read())
+        for line in code_lines(read(f)):
+            h.update(line.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -7,11 +7,14 @@
 // 48 KiB of the one-SM 128 x 256 tile, for the same tensor work per SM.
 //
 // Synchronisation (mbarriers; the even CTA is the "leader"):
-//   full[s]   leader only: the leader's producer posts expect_tx for both halves (64 KiB);
+//   full[s]   leader only: the leader's A producer posts expect_tx for both halves (64 KiB);
 //             both CTAs' TMA loads complete their bytes on it (.cta_group::2 loads).
 //   empty[s]  in both CTAs: the leader's MMA commit arrives on both (multicast).
 //   tfull[a]  in both CTAs: the leader's commit after a tile's last MMA (multicast).
-//   tempty[a] leader only: the 8 epilogue warps of both CTAs arrive (count 16).
+//   tempty[a] leader only: the EPI_W epilogue warps of both CTAs arrive (count 2 EPI_W).
+// The issue loops are single threads (one MMA issuer, one or two producers per CTA): each
+// keeps its per-block work short and looks at the next block's barrier while the current
+// block's last MMA (or load) issues, so that a wait that would succeed at once costs nothing.
 // TMEM (all 512 columns, two 256-column accumulators) is allocated and freed by warp 1 of
 // both CTAs together (cta_group::2). Cluster barriers after set-up and before the end keep
 // either CTA from touching the other's shared memory before it is ready or after it is gone.
