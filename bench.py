@@ -125,10 +125,22 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
+def enforced_power_limit(device_index: int):
+    """The board's enforced power limit in W (read only; None if nvidia-smi cannot say)."""
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=enforced.power.limit",
+                              "--format=csv,noheader,nounits", "-i", str(device_index)],
+                             capture_output=True, text=True, timeout=10)
+        return float(out.stdout.strip().splitlines()[0]) if out.returncode == 0 else None
+    except (OSError, ValueError, IndexError, subprocess.TimeoutExpired):
+        return None
+
+
 class ClockSampler:
     def __init__(self, device_index: int):
         self.proc = None
         self.lines = []
+        self.device_index = device_index
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={CLOCK_QUERY}", "--format=csv,noheader,nounits",
@@ -165,6 +177,7 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "power_w_median": statistics.median(power) if power else None,
+                "power_limit_w": enforced_power_limit(self.device_index),
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
