@@ -164,10 +164,16 @@ def _check(status: int):
 
 # ------------------------------------------------------------------ marshalling helpers
 def _ptr(t) -> Optional[int]:
+    """Device address of a tensor (or a raw int address). The library reads every buffer as
+    dense row-major, so a strided view (a column slice, a transpose) is refused here instead of
+    being read with the wrong layout."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_contiguous():
+        raise ValueError(f"tensor of shape {tuple(t.shape)} is not contiguous (row-major); "
+                         "pass .contiguous()")
     return t.data_ptr()
 
 

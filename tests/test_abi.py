@@ -221,3 +221,18 @@ def test_layernorm_desc_validation(tp):
     assert fwd(dtype=9) == "TP_ERR_DTYPE"
     assert fwd(tokens=8) == "TP_ERR_NULL"              # X is required when there are tokens
     assert fwd(dtype=tp.TP_F32, hidden=4 * 12) in ("TP_OK", "TP_ERR_ARCH")  # fp32: any width
+
+
+def test_binding_refuses_strided_views():
+    """Every buffer is read as dense row-major: a column slice or a transpose is refused by the
+    binding (ValueError) before any call, a contiguous tensor passes its address through."""
+    import torch
+
+    import tensor_sharded_linear_bias_gb300 as tpm
+
+    base = torch.zeros(4, 6)
+    for view in (base[:, :3], base.t(), base[:, ::2]):
+        with pytest.raises(ValueError):
+            tpm._ptr(view)
+    assert tpm._ptr(base[1:3]) == base[1:3].data_ptr()  # a row range is still dense
+    assert tpm._ptr(None) is None and tpm._ptr(1234) == 1234
