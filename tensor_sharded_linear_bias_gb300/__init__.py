@@ -165,8 +165,9 @@ def _check(status: int):
 # ------------------------------------------------------------------ marshalling helpers
 def _ptr(t) -> Optional[int]:
     """Device address of a tensor (or a raw int address). The library reads every buffer as
-    dense row-major, so a strided view (a column slice, a transpose) is refused here instead of
-    being read with the wrong layout."""
+    dense row-major device memory, so a strided view (a column slice, a transpose) or a host
+    tensor is refused here instead of being read with the wrong layout or from the wrong
+    memory."""
     if t is None:
         return None
     if isinstance(t, int):
@@ -174,7 +175,35 @@ def _ptr(t) -> Optional[int]:
     if not t.is_contiguous():
         raise ValueError(f"tensor of shape {tuple(t.shape)} is not contiguous (row-major); "
                          "pass .contiguous()")
+    if t.device.type != "cuda":
+        raise ValueError(f"tensor of shape {tuple(t.shape)} is on {t.device}; the library "
+                         "reads device memory only")
     return t.data_ptr()
+
+
+def _io_dtype(code):
+    """torch dtype of a call's inputs, weights and saved activations for a tp_dtype code."""
+    import torch
+
+    return torch.bfloat16 if code == TP_BF16 else torch.float32
+
+
+def _need(dtype, what: str, *items) -> None:
+    """Every tensor among `items` (tensors, lists of tensors, None or raw int addresses) must
+    have `dtype`: the library reads each buffer with the element size of its role (a bf16
+    buffer read as fp32 would be read past its end)."""
+    for it in items:
+        for t in (it if isinstance(it, (list, tuple)) else (it,)):
+            if t is None or isinstance(t, int):
+                continue
+            if t.dtype != dtype:
+                raise ValueError(f"{what} must be {dtype}, got {t.dtype} (shape {tuple(t.shape)})")
+
+
+def _f32():
+    import torch
+
+    return torch.float32
 
 
 def _arr(ts: Optional[Sequence]):
@@ -245,12 +274,18 @@ def tp_selftest_wait_timeout(ws, limit_us: int, stream=None):
 
 
 def tp_mlp_forward(desc, X, A, a, B, b, Z, Hsave, Ysave, ws, stream=None):
+    io = _io_dtype(_desc_mlp(desc).dtype)
+    _need(io, "X, A, a, B, b, Hsave, Ysave", X, A, a, B, b, Hsave, Ysave)
+    _need(_f32(), "Z", Z)
     p, n = _ws(ws)
     _check(lib.tp_mlp_forward(ctypes.byref(_desc_mlp(desc)), _ptr(X), _arr(A), _arr(a), _arr(B),
                               _ptr(b), _ptr(Z), _arr(Hsave), _arr(Ysave), p, n, _stream(stream)))
 
 
 def tp_mlp_backward(desc, X, A, B, Hsave, Ysave, dZ, dX, dA, da, dB, db, ws, stream=None):
+    io = _io_dtype(_desc_mlp(desc).dtype)
+    _need(io, "X, A, B, Hsave, Ysave, dZ", X, A, B, Hsave, Ysave, dZ)
+    _need(_f32(), "dX, dA, da, dB, db", dX, dA, da, dB, db)
     p, n = _ws(ws)
     _check(lib.tp_mlp_backward(ctypes.byref(_desc_mlp(desc)), _ptr(X), _arr(A), _arr(B),
                                _arr(Hsave), _arr(Ysave), _ptr(dZ), _ptr(dX), _arr(dA), _arr(da),
@@ -258,12 +293,15 @@ def tp_mlp_backward(desc, X, A, B, Hsave, Ysave, dZ, dX, dA, da, dB, db, ws, str
 
 
 def tp_linear_column_forward(desc, X, W, bias, Y, Hsave, ws, stream=None):
+    _need(_io_dtype(_desc_lin(desc).dtype), "X, W, bias, Y, Hsave", X, W, bias, Y, Hsave)
     p, n = _ws(ws)
     _check(lib.tp_linear_column_forward(ctypes.byref(_desc_lin(desc)), _ptr(X), _arr(W),
                                         _arr(bias), _arr(Y), _arr(Hsave), p, n, _stream(stream)))
 
 
 def tp_linear_column_backward(desc, X, W, Hsave, dY, dX, dW, dbias, ws, stream=None):
+    _need(_io_dtype(_desc_lin(desc).dtype), "X, W, Hsave, dY", X, W, Hsave, dY)
+    _need(_f32(), "dX, dW, dbias", dX, dW, dbias)
     p, n = _ws(ws)
     _check(lib.tp_linear_column_backward(ctypes.byref(_desc_lin(desc)), _ptr(X), _arr(W),
                                          _arr(Hsave), _arr(dY), _ptr(dX), _arr(dW), _arr(dbias),
@@ -271,18 +309,24 @@ def tp_linear_column_backward(desc, X, W, Hsave, dY, dX, dW, dbias, ws, stream=N
 
 
 def tp_linear_row_forward(desc, X, W, bias, Z, ws, stream=None):
+    _need(_io_dtype(_desc_lin(desc).dtype), "X, W, bias", X, W, bias)
+    _need(_f32(), "Z", Z)
     p, n = _ws(ws)
     _check(lib.tp_linear_row_forward(ctypes.byref(_desc_lin(desc)), _arr(X), _arr(W), _ptr(bias),
                                      _ptr(Z), p, n, _stream(stream)))
 
 
 def tp_linear_row_backward(desc, X, W, dZ, dX, dW, dbias, ws, stream=None):
+    _need(_io_dtype(_desc_lin(desc).dtype), "X, W, dZ", X, W, dZ)
+    _need(_f32(), "dX, dW, dbias", dX, dW, dbias)
     p, n = _ws(ws)
     _check(lib.tp_linear_row_backward(ctypes.byref(_desc_lin(desc)), _arr(X), _arr(W), _ptr(dZ),
                                       _arr(dX), _arr(dW), _ptr(dbias), p, n, _stream(stream)))
 
 
 def tp_linear_row_forward_noalloc(desc, X, W, bias, Z, stream=None):
+    _need(_io_dtype(_desc_lin(desc).dtype), "X, W, bias", X, W, bias)
+    _need(_f32(), "Z", Z)
     _check(lib.tp_linear_row_forward_noalloc(ctypes.byref(_desc_lin(desc)), _arr(X), _arr(W),
                                              _ptr(bias), _ptr(Z), _stream(stream)))
 
@@ -294,6 +338,9 @@ def tp_mlp_sp_workspace_size(desc) -> int:
 
 
 def tp_mlp_forward_sp(desc, X_shards, A, a, B, b, Z_shards, Hsave, Ysave, ws, stream=None):
+    io = _io_dtype(_desc_mlp(desc).dtype)
+    _need(io, "X_shards, A, a, B, b, Hsave, Ysave", X_shards, A, a, B, b, Hsave, Ysave)
+    _need(_f32(), "Z_shards", Z_shards)
     p, n = _ws(ws)
     _check(lib.tp_mlp_forward_sp(ctypes.byref(_desc_mlp(desc)), _arr(X_shards), _arr(A), _arr(a),
                                  _arr(B), _ptr(b), _arr(Z_shards), _arr(Hsave), _arr(Ysave), p,
@@ -302,6 +349,9 @@ def tp_mlp_forward_sp(desc, X_shards, A, a, B, b, Z_shards, Hsave, Ysave, ws, st
 
 def tp_mlp_backward_sp(desc, X_shards, A, B, Hsave, Ysave, dZ_shards, dX_shards, dA, da, dB, db,
                        ws, stream=None):
+    io = _io_dtype(_desc_mlp(desc).dtype)
+    _need(io, "X_shards, A, B, Hsave, Ysave, dZ_shards", X_shards, A, B, Hsave, Ysave, dZ_shards)
+    _need(_f32(), "dX_shards, dA, da, dB, db", dX_shards, dA, da, dB, db)
     p, n = _ws(ws)
     _check(lib.tp_mlp_backward_sp(ctypes.byref(_desc_mlp(desc)), _arr(X_shards), _arr(A),
                                   _arr(B), _arr(Hsave), _arr(Ysave), _arr(dZ_shards),
@@ -327,6 +377,8 @@ def tp_layernorm_forward(desc, X, gamma, beta, Y, mean, rstd, stream=None):
     """LayerNorm over a hidden dimension split into desc.tp_degree column shards: lists of
     per-shard tensors X [T, H/n], gamma/beta [H/n] (or None), Y [T, H/n]; mean, rstd fp32 [T]
     (or None)."""
+    _need(_io_dtype(_desc_ln(desc).dtype), "X, gamma, beta, Y", X, gamma, beta, Y)
+    _need(_f32(), "mean, rstd", mean, rstd)
     _check(lib.tp_layernorm_forward(ctypes.byref(_desc_ln(desc)), _arr(X), _arr(gamma),
                                     _arr(beta), _arr(Y), _ptr(mean), _ptr(rstd),
                                     _stream(stream)))
@@ -335,6 +387,8 @@ def tp_layernorm_forward(desc, X, gamma, beta, Y, mean, rstd, stream=None):
 def tp_layernorm_backward(desc, X, gamma, mean, rstd, dY, dX, dgamma, dbeta, stream=None):
     """Backward of tp_layernorm_forward: dX [T, H/n] per shard; dgamma, dbeta fp32 [H/n] per
     shard (lists, or None)."""
+    _need(_io_dtype(_desc_ln(desc).dtype), "X, gamma, dY, dX", X, gamma, dY, dX)
+    _need(_f32(), "mean, rstd, dgamma, dbeta", mean, rstd, dgamma, dbeta)
     _check(lib.tp_layernorm_backward(ctypes.byref(_desc_ln(desc)), _arr(X), _arr(gamma),
                                      _ptr(mean), _ptr(rstd), _arr(dY), _arr(dX), _arr(dgamma),
                                      _arr(dbeta), _stream(stream)))

@@ -225,14 +225,35 @@ def test_layernorm_desc_validation(tp):
 
 def test_binding_refuses_strided_views():
     """Every buffer is read as dense row-major: a column slice or a transpose is refused by the
-    binding (ValueError) before any call, a contiguous tensor passes its address through."""
+    binding (ValueError) before any call; raw int addresses and None pass through."""
     import torch
 
     import tensor_sharded_linear_bias_gb300 as tpm
 
     base = torch.zeros(4, 6)
     for view in (base[:, :3], base.t(), base[:, ::2]):
-        with pytest.raises(ValueError):
+        with pytest.raises(ValueError, match="not contiguous"):
             tpm._ptr(view)
-    assert tpm._ptr(base[1:3]) == base[1:3].data_ptr()  # a row range is still dense
+    # a row range is still dense: only the device check (no GPU here) refuses it
+    with pytest.raises(ValueError, match="device memory"):
+        tpm._ptr(base[1:3])
     assert tpm._ptr(None) is None and tpm._ptr(1234) == 1234
+
+
+def test_binding_checks_device_and_dtype():
+    """A host tensor is refused (the kernels read device memory only), and so is a tensor whose
+    dtype is not the one its role has for the call's dtype (bf16 inputs with an fp32
+    descriptor would be read past their end): ValueError before anything reaches the library."""
+    import torch
+
+    import tensor_sharded_linear_bias_gb300 as tpm
+
+    with pytest.raises(ValueError, match="device memory"):
+        tpm._ptr(torch.zeros(4, 4))
+    tpm._need(torch.bfloat16, "X", None, 7, [None, torch.zeros(2, dtype=torch.bfloat16)])
+    with pytest.raises(ValueError, match="X must be torch.bfloat16"):
+        tpm._need(torch.bfloat16, "X", [torch.zeros(2, dtype=torch.bfloat16), torch.zeros(2)])
+    d = tpm.MlpDesc(tokens=8, hidden=64, ffn=128, tp_degree=2, dtype=tpm.TP_F32, act=1, reduce=0)
+    bf = torch.zeros(8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="must be torch.float32"):
+        tpm.tp_mlp_forward(d, bf, [bf], [bf], [bf], None, bf, [bf], [bf], None)
