@@ -56,6 +56,9 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--oracle-full", action="store_true",
+                    help="time the fp64 oracle on whole workloads (comma-separated --workload "
+                         "names, attn included) on the host cores; no GPU")
     return ap.parse_args()
 
 
@@ -69,6 +72,13 @@ def workload(name: str) -> wl.MlpWorkload:
     if name.startswith("sweep:"):
         _, T, n = name.split(":")
         return wl.SWEEP_H8192_F28672.with_shape(tokens=int(T), tp_degree=int(n))
+    if name.startswith("mlp:"):
+        # a smaller case with the GPT-3-shaped slice's distributions (for profiler captures
+        # that must stay small): mlp:T:H:F:n
+        _, T, H, F, n = name.split(":")
+        w = wl.GPT3_MLP_T2048_TP8.with_shape(tokens=int(T), hidden=int(H), ffn=int(F),
+                                             tp_degree=int(n))
+        return wl.dataclasses.replace(w, name=f"mlp_bf16_T{T}_H{H}_F{F}_tp{n}")
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -120,9 +130,10 @@ def replica_throughput(work_per_step: float, steps: int, ms_local: float, world:
 
 
 # ----------------------------------------------------------------------------- clocks
-CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+CLOCK_QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+CLOCK_INTERVAL_MS = 50
 
 
 def enforced_power_limit(device_index: int):
@@ -136,18 +147,55 @@ def enforced_power_limit(device_index: int):
         return None
 
 
+def parse_clock_lines(text: str, window=None) -> dict:
+    """Clock samples (nvidia-smi CSV lines of CLOCK_QUERY) -> the summary put on the JSON line.
+    With window = (t0, t1) (host wall-clock seconds of the timed region), only samples stamped
+    inside it count for the median SM clock and the reasons; the samples before and after it
+    (an idle GPU at its highest clock) would otherwise pull the median up."""
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    rows = []
+    for line in text.strip().splitlines():
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 10:
+            continue
+        try:
+            ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+            ts += float("0." + f[0].split(".")[1]) if "." in f[0] else 0.0
+            rows.append((ts, float(f[2]), float(f[3]), float(f[4]),
+                         {nm for nm, v in zip(names, f[6:10]) if v.lower() == "active"}))
+        except (ValueError, IndexError):
+            continue
+    inside = [r for r in rows if window is None or window[0] <= r[0] <= window[1]]
+    basis = "samples inside the timed region"
+    if window is not None and not inside:
+        # a region shorter than the sampling interval: the first samples after it started
+        inside = [r for r in rows if r[0] >= window[0]][:2]
+        basis = "first samples after the timed region started (region shorter than the interval)"
+    sm = [r[1] for r in inside]
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(r[2] for r in rows) if rows else None,
+            "power_w_median": statistics.median([r[3] for r in inside]) if inside else None,
+            "samples": len(inside), "samples_total": len(rows),
+            "interval_ms": CLOCK_INTERVAL_MS, "basis": basis,
+            "reasons": sorted(set().union(*[r[4] for r in inside])) if inside else []}
+
+
 class ClockSampler:
     def __init__(self, device_index: int):
         self.proc = None
-        self.lines = []
         self.device_index = device_index
+        self.window = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={CLOCK_QUERY}", "--format=csv,noheader,nounits",
-                 "-i", str(device_index), "-lms", "200"],
+                 "-i", str(device_index), "-lms", str(CLOCK_INTERVAL_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+
+    def mark(self, t0: float, t1: float) -> None:
+        """Host wall-clock bounds of the timed region."""
+        self.window = (t0, t1)
 
     def stop(self) -> dict:
         if self.proc is None:
@@ -159,26 +207,11 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, smax, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
-                power.append(float(f[3]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "power_w_median": statistics.median(power) if power else None,
-                "power_limit_w": enforced_power_limit(self.device_index),
-                "samples": len(sm), "reasons": sorted(reasons)}
+        res = parse_clock_lines(out, self.window)
+        res["power_limit_w"] = enforced_power_limit(self.device_index)
+        if self.window is not None:
+            res["timed_region_s"] = self.window[1] - self.window[0]
+        return res
 
 
 # ----------------------------------------------------------------------------- peaks / profile
@@ -187,9 +220,10 @@ def peaks():
     if os.path.exists(path):
         p = json.load(open(path))
         return {"bf16_sustained": p["bf16_tflops_sustained"], "bf16_burst": p["bf16_tflops"],
-                "hbm_gbs": p["hbm_gbs"], "source": "measured", "ffma_f32": FFMA_F32_TFLOPS}
+                "hbm_gbs": p["hbm_gbs"], "source": "measured", "ffma_f32": FFMA_F32_TFLOPS,
+                "sm_max_mhz": p.get("sm_max_mhz", 2070.0)}
     return {"bf16_sustained": 1700.0, "bf16_burst": 1900.0, "hbm_gbs": 6800.0,
-            "source": "fallback", "ffma_f32": FFMA_F32_TFLOPS}
+            "source": "fallback", "ffma_f32": FFMA_F32_TFLOPS, "sm_max_mhz": 2070.0}
 
 
 def code_lines(text: str):
@@ -478,7 +512,10 @@ def timed_then_traced(tp, fn, steps: int, world: int, flush, trace_capacity: int
     steps with the library's per-launch trace on (per-kernel times for the roofline).
     Returns (ms of the untraced steps, trace records, clocks sampled during the untraced
     steps)."""
+    t0 = time.time()
     ms = time_steps(fn, steps, world, flush)
+    if sampler:
+        sampler.mark(t0, time.time())
     clocks = sampler.stop() if sampler else None
     tp.tp_trace_start(trace_capacity)
     time_steps(fn, steps, world, flush)
@@ -486,7 +523,57 @@ def timed_then_traced(tp, fn, steps: int, world: int, flush, trace_capacity: int
     return ms, recs, clocks
 
 
-def roofline_from_trace(recs, pk, workload_name=None):
+# Dense bf16 tensor-core rate per SM and clock: 8192 flop (a 128 x 256 x 16 MMA per 128 cycles).
+# Consistent with ncu on GB300: cuBLAS's kernel for a 2048 x 8192 x 28672 GEMM ran 2030 TFLOP/s
+# with its tensor pipe 96 % busy at ~1.65-1.7 GHz (2030e12 / (0.96 * 152 * 8192) = 1.70 GHz).
+TENSOR_FLOP_PER_CLK_SM = 8192
+NUM_SMS = 152
+BURST_REGION_S = 2.0     # longer timed regions run into the power cap: the sustained peak
+BURST_CLOCK_FRAC = 0.97  # median SM clock within 3 % of its maximum: a burst
+
+
+def tensor_peak(pk, clocks):
+    """The measured bf16 peak that matches the timed region's regime. MEASURED_PEAKS.json holds
+    a burst figure (cuBLAS timed alone, best of 10, at the maximum clock) and a sustained one
+    (cuBLAS back to back for seconds under the power cap). A short region is a burst and is
+    divided by the burst peak; only a region long enough for the power cap to pull the clock
+    down (over BURST_REGION_S, with the median clock below the maximum) is divided by the
+    sustained peak. Returns (peak, regime, note)."""
+    mhz = (clocks or {}).get("sm_mhz")
+    mx = (clocks or {}).get("sm_max_mhz") or pk.get("sm_max_mhz") or 2070.0
+    region = (clocks or {}).get("timed_region_s")
+    long_region = region is not None and region > BURST_REGION_S
+    capped = mhz is not None and mhz < BURST_CLOCK_FRAC * mx
+    if not (long_region and capped):
+        return pk["bf16_burst"], "burst", (f"MEASURED_PEAKS.json bf16_tflops (of {pk['source']}): "
+                                          f"median SM clock {mhz} of {mx} MHz over a "
+                                          f"{region if region is None else round(region, 3)} s region")
+    return pk["bf16_sustained"], "sustained", (f"MEASURED_PEAKS.json bf16_tflops_sustained (of "
+                                              f"{pk['source']}): median SM clock {mhz} of {mx} "
+                                              f"MHz over a {region if region is None else round(region, 3)} s region")
+
+
+def tensor_fractions(achieved, pk, clocks):
+    """The same achieved rate against every denominator: both measured peaks, the burst peak
+    scaled to the region's median clock (the burst ran at the maximum clock), and the tensor
+    pipe's own rate at that clock."""
+    mhz = (clocks or {}).get("sm_mhz")
+    mx = pk.get("sm_max_mhz") or 2070.0
+    out = {"frac_vs_burst": achieved / pk["bf16_burst"],
+           "frac_vs_sustained": achieved / pk["bf16_sustained"]}
+    if mhz:
+        scaled = pk["bf16_burst"] * mhz / mx
+        pipe = TENSOR_FLOP_PER_CLK_SM * NUM_SMS * mhz * 1e6 / 1e12
+        out["clock_normalised"] = {"peak": scaled, "frac": achieved / scaled, "sm_mhz": mhz,
+                                   "note": f"bf16_tflops x {mhz} / {mx} MHz (the burst peak "
+                                           f"taken at the maximum clock)"}
+        out["tensor_pipe_at_clock"] = {"peak": pipe, "frac": achieved / pipe,
+                                       "note": f"{TENSOR_FLOP_PER_CLK_SM} flop/clock/SM x "
+                                               f"{NUM_SMS} SMs x {mhz} MHz"}
+    return out
+
+
+def roofline_from_trace(recs, pk, workload_name=None, clocks=None):
     """The dominant kernel (largest total traced device time) against its roofline, and the
     per-(kernel, tag) breakdown."""
     by_kernel, by_tag = {}, {}
@@ -503,14 +590,18 @@ def roofline_from_trace(recs, pk, workload_name=None):
     dom = max(by_kernel, key=lambda k: by_kernel[k]["ms"])
     d = by_kernel[dom]
     total_ms = sum(v["ms"] for v in by_kernel.values())
-    if dom in ("gemm_tc", "gemm_ffma"):
+    if dom == "gemm_tc":
         achieved = d["flops"] / (d["ms"] / 1e3) / 1e12
-        peak = pk["bf16_sustained"] if dom == "gemm_tc" else pk["ffma_f32"]
-        roof = {"bound": "tensor" if dom == "gemm_tc" else "alu", "kernel": dom,
-                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": (f"MEASURED_PEAKS.json bf16_tflops_sustained (of {pk['source']})"
-                                if dom == "gemm_tc" else
-                                "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz")}
+        peak, regime, note = tensor_peak(pk, clocks)
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "regime": regime,
+                "peak_source": note, **tensor_fractions(achieved, pk, clocks)}
+    elif dom == "gemm_ffma":
+        achieved = d["flops"] / (d["ms"] / 1e3) / 1e12
+        peak = pk["ffma_f32"]
+        roof = {"bound": "alu", "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz"}
     else:
         achieved = d["bytes"] / (d["ms"] / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": pk["hbm_gbs"],
@@ -582,6 +673,99 @@ def cpu_baseline(w, host, seconds: float):
     value = per * reps / el / 1e12
     return {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
             "sample": f"{text}; {reps} repetitions in {el:.1f} s"}
+
+
+def mem_available_bytes():
+    """MemAvailable of the host (Linux), or None."""
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
+
+
+def timed_cpu(fn):
+    """Wall-clock seconds of fn() and the host threads it kept busy on average (process CPU
+    time / wall time)."""
+    c0, t0 = os.times(), time.perf_counter()
+    fn()
+    el = time.perf_counter() - t0
+    c1 = os.times()
+    busy = ((c1.user - c0.user) + (c1.system - c0.system)) / el if el > 0 else 0.0
+    return el, busy
+
+
+def oracle_full_line(name: str) -> dict:
+    """The fp64 oracle as it stands, on the whole workload (every output of fwd + bwd), timed
+    on the host cores. Workloads whose oracle would not fit the host's free memory (about 3x
+    the fp64 inputs and outputs) or whose full run is long (T >= 8192 in the sweep) are timed
+    on a seeded sample -- 64 token rows x 64 ffn columns per shard -- and extrapolated by
+    flops, labelled as such."""
+    import numpy as np  # noqa: F401
+
+    import oracle
+
+    if name == "attn":
+        w = wl.ATTN_T4096_H5120_TP8
+        t = {k: wl.to_bf16(v)[1] for k, v in wl.attn_tensors(w).items()}
+
+        def run():
+            oracle.attn_forward(t["X"], t["Wqkv"], t["C"], t["Wo"], w.heads, w.head_dim,
+                                w.tp_degree)
+            oracle.attn_backward(t["X"], t["Wqkv"], t["C"], t["Wo"], t["dQKV"], t["dO"],
+                                 w.heads, w.head_dim, w.tp_degree)
+
+        flops, kind, text = w.flops_fwd_bwd, "full", "whole workload, fwd+bwd, fp64 numpy"
+    else:
+        w = workload(name)
+        host = {k: (wl.to_bf16(v)[1] if w.dtype == "bf16" else v)
+                for k, v in wl.mlp_tensors(w).items()}
+        T, H, F = w.tokens, w.hidden, w.ffn
+        need = 8 * 3 * (2 * T * H + 2 * H * F + 3 * T * F + (2 * H * F if w.backward else 0))
+        avail = mem_available_bytes()
+        full = (T < 8192) and (avail is None or need < avail)
+        if full:
+            def run():
+                fwd = oracle.mlp_forward(host["X"], host["A"], host["a"], host["B"], host["b"],
+                                         w.tp_degree)
+                if w.backward:
+                    oracle.mlp_backward(host["X"], host["A"], host["a"], host["B"], host["b"],
+                                        host["dZ"], w.tp_degree, fwd)
+
+            flops = w.flops_fwd_bwd if w.backward else w.flops_fwd
+            kind = "full"
+            text = f"whole workload, {'fwd+bwd' if w.backward else 'fwd'}, fp64 numpy"
+        else:
+            run, flops, text = oracle_sample(w, host, rows=64, cols_per_shard=64)
+            kind = "extrapolated from the measured sample"
+            text += (f"; full run skipped: {'T >= 8192' if T >= 8192 else 'host memory'} "
+                     f"(needs ~{need / 1e9:.0f} GB, {0 if avail is None else avail / 1e9:.0f} GB "
+                     f"available)")
+    el, busy = timed_cpu(run)
+    if kind != "full":
+        # a sample takes a fraction of a second: repeat it for a few seconds
+        reps = max(1, int(3.0 / max(el, 1e-3)))
+        el, busy = timed_cpu(lambda: [run() for _ in range(reps)])
+        el /= reps
+    tflops = flops / el / 1e12
+    total = (w.flops_fwd_bwd if getattr(w, "backward", True) else w.flops_fwd) \
+        if name != "attn" else w.flops_fwd_bwd
+    shape = ({"tokens": w.tokens, "hidden": w.hidden, "heads": w.heads, "tp_degree": w.tp_degree}
+             if name == "attn" else {"tokens": w.tokens, "hidden": w.hidden, "ffn": w.ffn,
+                                     "tp_degree": w.tp_degree})
+    return {"impl": "oracle", "workload": w.name, **shape, "kind": kind, "value": tflops,
+            "unit": UNIT, "seconds": el, "seconds_full_workload": total / (tflops * 1e12),
+            "cores": host_cores(), "nproc": os.cpu_count(), "threads_busy": round(busy, 1),
+            "sample": text, "dtype": "f64"}
+
+
+def run_oracle_full(args):
+    """One JSON line per workload of --workload (comma-separated): the oracle's wall clock."""
+    for name in args.workload.split(","):
+        print(json.dumps(oracle_full_line(name.strip())), flush=True)
+    return 0
 
 
 def run_reference(args, w, world, rank):
@@ -686,7 +870,8 @@ def run_attention(args, world, rank, local):
     ms, value = replica_throughput(ab.flops, args.steps, ms, world)
     if rank == 0:
         pk = peaks()
-        roof, kernels = roofline_from_trace(recs, pk)
+        roof, kernels = roofline_from_trace(recs, pk, clocks=clocks)
+        peak, regime, _ = tensor_peak(pk, clocks)
         print(json.dumps({
             "metric": "attention projections (QKV split by heads + output projection) fwd+bwd "
                       "TFLOP/s (bf16)",
@@ -696,7 +881,7 @@ def run_attention(args, world, rank, local):
             "config": {"workload": w.name, "tokens": w.tokens, "hidden": w.hidden,
                        "heads": w.heads, "head_dim": w.head_dim, "tp_degree": w.tp_degree,
                        "reduce": args.reduce, "l2": l2_note},
-            "pct_of_peak": value / pk["bf16_sustained"] * 100.0, "clocks": clocks,
+            "pct_of_peak": value / peak * 100.0, "pct_of_peak_basis": regime, "clocks": clocks,
             "gpu_launches": len(recs), "roofline": roof, "kernels": kernels}), flush=True)
     return 0
 
@@ -745,7 +930,7 @@ def run_layernorm(args, world, rank, local):
     ms = max_over_ranks(ms, world)
     if rank == 0:
         pk = peaks()
-        roof, kernels = roofline_from_trace(recs, pk)
+        roof, kernels = roofline_from_trace(recs, pk, clocks=clocks)
         value = step_bytes * args.steps * world / (ms / 1e3) / 1e9
         print(json.dumps({
             "metric": "hidden-split LayerNorm fwd+bwd (8 shards, statistics combined on the "
@@ -801,6 +986,8 @@ def run_p3_column_latency(args, world, rank, local):
 # ----------------------------------------------------------------------------- main
 def main():
     args = parse_args()
+    if args.oracle_full:
+        return run_oracle_full(args)
     if args.workload == "p3col":
         world, rank, local = dist_setup(args.gpus)
         return run_p3_column_latency(args, world, rank, local)
@@ -877,7 +1064,8 @@ def main():
         return 0
 
     pk = peaks()
-    roof, kernels = roofline_from_trace(recs, pk, w.name)
+    roof, kernels = roofline_from_trace(recs, pk, w.name, clocks=clocks)
+    peak, regime, _ = tensor_peak(pk, clocks)
 
     cpu = None
     if keep_host:
@@ -897,7 +1085,9 @@ def main():
                    "l2": l2_note,
                    "timing": "throughput from untraced steps; per-kernel figures from the "
                              "same number of steps traced with per-launch events"},
-        "pct_of_peak": value / pk["bf16_sustained"] * 100.0 if w.dtype == "bf16" else None,
+        "pct_of_peak": value / peak * 100.0 if w.dtype == "bf16" else None,
+        "pct_of_peak_basis": (f"{regime} peak (see roofline.peak_source)" if w.dtype == "bf16"
+                              else None),
         "clocks": clocks,
         "e2e": e2e,
         "warm_l2": warm,

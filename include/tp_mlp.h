@@ -335,8 +335,10 @@ tp_status tp_trace_stop(tp_trace_record* out, int32_t capacity, int32_t* count);
  *  - Every call on a device shares the one array and leaves its partials there; each call
  *    clears the status word itself. Calls whose work overlaps on the GPU (on different
  *    streams, or from different threads) race on the array: order them on one stream.
- *  - A device-side wait that runs out writes its code into the array's status word, which no
- *    entry point reads back; the next call clears it.
+ *  - A device-side wait that runs out writes its code into the array's status word. With no
+ *    workspace there is no tp_check_status to read it, so the call's last launch checks the
+ *    word and, when it is set, fills Z with NaN: a timed-out call leaves Z all NaN, never a
+ *    plausible-looking sum. The next call clears the word.
  * Arguments, layouts, dtypes and the other errors are those of tp_linear_row_forward. */
 tp_status tp_linear_row_forward_noalloc(const tp_linear_desc* desc, const void* const* X,
                                         const void* const* W, const void* bias, void* Z,

@@ -23,7 +23,8 @@ __all__ = [
     "new_workspace", "EXPORTED_SYMBOLS", "tp_trace_start", "tp_trace_stop", "TraceRecord",
     "KERNEL_NAMES", "TAG_NAMES", "tp_linear_row_forward_noalloc", "tp_mlp_sp_workspace_size",
     "tp_mlp_forward_sp", "tp_mlp_backward_sp", "LayerNormDesc", "tp_layernorm_forward",
-    "tp_layernorm_backward",
+    "tp_layernorm_backward", "TUNE_KNOBS", "TP_TUNE_AUTO", "tp_tuning_set", "tp_tuning_get",
+    "tuning",
 ]
 
 TP_F32, TP_BF16 = 0, 1
@@ -44,8 +45,18 @@ EXPORTED_SYMBOLS = (
     "tp_linear_column_forward", "tp_linear_column_backward", "tp_linear_row_forward",
     "tp_linear_row_backward", "tp_selftest_wait_timeout", "tp_trace_start", "tp_trace_stop",
     "tp_linear_row_forward_noalloc", "tp_mlp_sp_workspace_size", "tp_mlp_forward_sp",
-    "tp_mlp_backward_sp", "tp_layernorm_forward", "tp_layernorm_backward",
+    "tp_mlp_backward_sp", "tp_layernorm_forward", "tp_layernorm_backward", "tp_tuning_set",
+    "tp_tuning_get",
 )
+
+# Test and measurement hook (include/tp_mlp_tuning.h): overrides of the library's measured
+# kernel choices, process-wide; TP_TUNE_AUTO gives a choice back to the library.
+TP_TUNE_AUTO = -1
+TUNE_KNOBS = {
+    "gemm_pair": 0, "epi_warps": 1, "raster": 2, "tma_3d": 3, "split_loads": 4,
+    "mma_probe": 5, "load_probe": 6, "tail_split": 7, "tail_waves": 8, "shard_split": 9,
+    "simt_split": 10, "ln_reg": 11,
+}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -129,6 +140,8 @@ _SIGS = {
                                             _P, _P, _P]),
     "tp_layernorm_backward": (ctypes.c_int, [ctypes.POINTER(LayerNormDesc), _PP, _PP, _P, _P,
                                              _PP, _PP, _PP, _PP, _P]),
+    "tp_tuning_set": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32]),
+    "tp_tuning_get": (ctypes.c_int32, [ctypes.c_int32]),
 }
 
 
@@ -160,6 +173,35 @@ def tp_last_error() -> str:
 def _check(status: int):
     if status != 0:
         raise TpError(status, tp_last_error())
+
+
+def tp_tuning_set(knob: str, value: int) -> None:
+    """Override one measured kernel choice (tests and A/B timing only)."""
+    _check(lib.tp_tuning_set(TUNE_KNOBS[knob], int(value)))
+
+
+def tp_tuning_get(knob: str) -> int:
+    return int(lib.tp_tuning_get(TUNE_KNOBS[knob]))
+
+
+class tuning:
+    """Context manager: ``with tuning(raster=1, tma_3d=0): ...`` sets the given knobs and
+    restores their previous values on exit."""
+
+    def __init__(self, **knobs):
+        self.knobs = {k: int(v) for k, v in knobs.items()}
+        self.saved = {}
+
+    def __enter__(self):
+        for k, v in self.knobs.items():
+            self.saved[k] = tp_tuning_get(k)
+            tp_tuning_set(k, v)
+        return self
+
+    def __exit__(self, *exc):
+        for k, v in self.saved.items():
+            tp_tuning_set(k, v)
+        return False
 
 
 # ------------------------------------------------------------------ marshalling helpers

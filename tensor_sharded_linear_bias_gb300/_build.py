@@ -18,7 +18,7 @@ BUILD = os.path.join(ROOT, "_build", "libtpmlp")
 LIB = os.path.join(PKG, "libtpmlp.so")
 
 SOURCES = ["tp_api.cu", "layernorm.cu", "tc_launch.cu", "tc_gemm_kmn.cu", "tc_gemm_kk.cu", "tc_gemm_mnmn.cu",
-           "simt_gemm.cu", "reduce.cu", "noalloc.cu"]
+           "simt_gemm.cu", "reduce.cu", "noalloc.cu", "tuning.cu"]
 HEADERS = ["internal.h", "device_common.cuh", "tc_gemm.cuh", "tc2_gemm.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -46,7 +46,8 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
     """Compile every CUDA translation unit for sm_103a and link the shared library."""
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
-    headers = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "tp_mlp.h")]
+    headers = [os.path.join(CSRC, h) for h in HEADERS] + [
+        os.path.join(INCLUDE, h) for h in ("tp_mlp.h", "tp_mlp_tuning.h")]
     jobs = []
     objs = []
     for src in SOURCES:

@@ -9,26 +9,39 @@ namespace tpk {
 
 // ------------------------------------------------------------------ activation
 // GeLU in its exact (erf) form and its derivative, with the normal tail computed once:
-//   Phi(-|h|) = erfc(z) / 2,  z = |h| / sqrt 2,  erfc(z) ~ P(t) exp(-z^2),  t = 1 / (1 + p z),
-// the rational approximation of Abramowitz & Stegun, Handbook of Mathematical Functions,
-// formula 7.1.26 (|error in erf| <= 1.5e-7; ~3e-7 with fp32 rounding, far below the bf16
-// outputs' resolution and the fp32 path's tolerance). exp(-z^2) = exp(-h^2 / 2) is also the
-// normal density's exponential, so GeLU' costs one exponential and one reciprocal.
+//   Phi(-|h|) = erfc(z) / 2,  z = |h| / sqrt 2,  erfc(z) ~ t Q(t) exp(-z^2),  t = 1 / (1 + p z),
+// the form of Abramowitz & Stegun, Handbook of Mathematical Functions, 7.1.26, with p = 1/2 and
+// Q of degree 8 fitted for RELATIVE error (fit_normal_tail.py, beside this file: t Q(t) is
+// within 2.1e-7 of the scaled function exp(z^2) erfc(z) for every z >= 0, so Phi(h) keeps its
+// relative accuracy far into the negative tail, where GeLU(h) = h Phi(h) is tiny; 7.1.26's
+// own degree-4 coefficients are fitted for absolute error and drift to 38 % relative error as
+// z grows). exp(-z^2) = exp(-h^2 / 2) is also the normal density's exponential, so GeLU' costs
+// one exponential and one reciprocal.
+constexpr float kTailP = 0.35355339059327373f;  // p / sqrt 2: t = 1 / (1 + kTailP |h|)
+constexpr float kTailQ0 = 2.820921728e-01f, kTailQ1 = 2.822133577e-01f,
+                kTailQ2 = 2.448138215e-01f, kTailQ3 = 1.935501536e-01f,
+                kTailQ4 = 9.956123732e-04f, kTailQ5 = 2.288727022e-01f,
+                kTailQ6 = -4.361299399e-01f, kTailQ7 = 2.560270581e-01f,
+                kTailQ8 = -5.243482750e-02f;
+
 struct NormalTail {
   float cdf;  // Phi(h)
   float e;    // exp(-h^2 / 2)
 };
 
 __device__ __forceinline__ NormalTail normal_tail(float h) {
-  const float z = fabsf(h) * 0.7071067811865475f;
-  // fast division (2 ulp): the divisor 1 + p z lies in [1, 2^126)
-  const float t = __fdividef(1.0f, fmaf(0.3275911f, z, 1.0f));
-  const float poly =
-      t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f),
-                       -0.284496736f),
-               0.254829592f);
-  const float e = __expf(-z * z);
-  const float lower = 0.5f * poly * e;  // Phi(-|h|)
+  // fast division (2 ulp): the divisor 1 + p |h| / sqrt 2 lies in [1, 2^126)
+  const float t = __fdividef(1.0f, fmaf(kTailP, fabsf(h), 1.0f));
+  float q = fmaf(t, kTailQ8, kTailQ7);
+  q = fmaf(t, q, kTailQ6);
+  q = fmaf(t, q, kTailQ5);
+  q = fmaf(t, q, kTailQ4);
+  q = fmaf(t, q, kTailQ3);
+  q = fmaf(t, q, kTailQ2);
+  q = fmaf(t, q, kTailQ1);
+  q = fmaf(t, q, kTailQ0);
+  const float e = __expf((-0.5f * h) * h);
+  const float lower = 0.5f * (t * q) * e;  // Phi(-|h|)
   return {h >= 0.0f ? 1.0f - lower : lower, e};
 }
 
@@ -49,17 +62,19 @@ __device__ __forceinline__ float gelu_erf_grad(float h) {
 __device__ __forceinline__ float2 splat2(float a) { return make_float2(a, a); }
 
 __device__ __forceinline__ void normal_tail2(float2 h, float2& cdf, float2& e) {
-  const float2 z = __fmul2_rn(make_float2(fabsf(h.x), fabsf(h.y)), splat2(0.7071067811865475f));
-  const float2 d = __ffma2_rn(splat2(0.3275911f), z, splat2(1.0f));
+  const float2 d = __ffma2_rn(splat2(kTailP), make_float2(fabsf(h.x), fabsf(h.y)), splat2(1.0f));
   const float2 t = make_float2(__fdividef(1.0f, d.x), __fdividef(1.0f, d.y));
-  float2 q = __ffma2_rn(t, splat2(1.061405429f), splat2(-1.453152027f));
-  q = __ffma2_rn(t, q, splat2(1.421413741f));
-  q = __ffma2_rn(t, q, splat2(-0.284496736f));
-  q = __ffma2_rn(t, q, splat2(0.254829592f));
-  const float2 poly = __fmul2_rn(t, q);
-  const float2 nz2 = __fmul2_rn(make_float2(-z.x, -z.y), z);
-  e = make_float2(__expf(nz2.x), __expf(nz2.y));
-  const float2 lower = __fmul2_rn(__fmul2_rn(splat2(0.5f), poly), e);
+  float2 q = __ffma2_rn(t, splat2(kTailQ8), splat2(kTailQ7));
+  q = __ffma2_rn(t, q, splat2(kTailQ6));
+  q = __ffma2_rn(t, q, splat2(kTailQ5));
+  q = __ffma2_rn(t, q, splat2(kTailQ4));
+  q = __ffma2_rn(t, q, splat2(kTailQ3));
+  q = __ffma2_rn(t, q, splat2(kTailQ2));
+  q = __ffma2_rn(t, q, splat2(kTailQ1));
+  q = __ffma2_rn(t, q, splat2(kTailQ0));
+  const float2 nh2 = __fmul2_rn(__fmul2_rn(splat2(-0.5f), h), h);
+  e = make_float2(__expf(nh2.x), __expf(nh2.y));
+  const float2 lower = __fmul2_rn(__fmul2_rn(splat2(0.5f), __fmul2_rn(t, q)), e);
   const float2 upper = __fadd2_rn(splat2(1.0f), make_float2(-lower.x, -lower.y));
   cdf = make_float2(h.x >= 0.0f ? upper.x : lower.x, h.y >= 0.0f ? upper.y : lower.y);
 }

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include "tp_mlp.h"
+#include "tp_mlp_tuning.h"
 
 namespace tpk {
 
@@ -72,7 +73,7 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st);
 // fp32 inputs, FFMA (no TF32); kslices > 1 splits every tile's K steps over a cluster.
 cudaError_t launch_simt_gemm(const GemmSpec& s, cudaStream_t st);
 // K slices (cluster size, <= 8) for an FFMA GEMM whose tiles alone would leave SMs idle
-// (1: no split). TPMLP_SIMT_SPLIT=0 turns the split off.
+// (1: no split). TP_TUNE_SIMT_SPLIT = 0 turns the split off.
 int plan_simt_split(const GemmSpec& s);
 
 // Z[T,N] = sum_{i<n} P[i][T,N] + bias (bias may be null; bias dtype: bf16 if bias_bf16).
@@ -131,6 +132,9 @@ cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t st
 // Number of partial outputs to split a shard-summed GEMM into (a divisor of n; 1 = fully
 // fused): balances the tile waves against the extra reduction traffic.
 int plan_shard_split(int64_t M, int64_t N, int64_t K_per_group, int n);
+
+// Override of a measured kernel choice (tp_mlp_tuning.h): TP_TUNE_AUTO when none is set.
+int tuning(int knob);
 
 // Device facts (cached per device).
 int device_sm_count();

@@ -24,7 +24,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <cstdlib>
 
 #include "device_common.cuh"
 #include "internal.h"
@@ -521,9 +520,9 @@ int vec_width(const LnParams& p, bool backward) {
   return V;
 }
 
-// Register-resident kernels where they apply; TPMLP_LN_REG=0 keeps the two-pass kernels.
+// Register-resident kernels where they apply; TP_TUNE_LN_REG = 0 keeps the two-pass kernels.
 bool ln_reg_enabled() {
-  if (const char* env = std::getenv("TPMLP_LN_REG")) return std::atoi(env) != 0;
+  if (const int v = tuning(TP_TUNE_LN_REG); v != TP_TUNE_AUTO) return v != 0;
   return true;
 }
 

@@ -47,6 +47,15 @@ cudaError_t scratch_on_current_device(void** out) {
   return cudaSuccess;
 }
 
+// After the shard reduction: if a GEMM wait ran out (a code in the static status word, which
+// no caller can read), Z is overwritten with NaN so that the failure cannot pass for a
+// result. One block; it reads the word and returns at once when it is zero.
+__global__ void poison_on_timeout(const int* status, float* Z, long long count) {
+  if (*reinterpret_cast<const volatile int*>(status) == 0) return;
+  const float nan = __int_as_float(0x7fc00000);
+  for (long long i = threadIdx.x; i < count; i += blockDim.x) Z[i] = nan;
+}
+
 bool aligned(const void* p, int dtype) {
   return reinterpret_cast<uintptr_t>(p) % (dtype == TP_BF16 ? 16 : 4) == 0;
 }
@@ -72,12 +81,17 @@ extern "C" tp_status tp_linear_row_forward_noalloc(const tp_linear_desc* desc,
   const int64_t Ks = K / n;
   if (dt == TP_BF16 && (Ks % 8 != 0 || N % 8 != 0))
     return fail(TP_ERR_ALIGN, "bf16 needs in_features / tp_degree and out_features to be multiples of 8");
-  const size_t need = kStatusBytes + size_t(n) * size_t(T) * size_t(N) * 4;
-  if (need > kScratchBytes) {
+  // n * T * N fp32 partials must fit behind the status block; checked factor by factor so
+  // that no product can wrap around before the comparison
+  const uint64_t max_elems = (kScratchBytes - kStatusBytes) / 4;
+  const uint64_t per_token = uint64_t(n) * uint64_t(N);  // <= 2^36: no wrap
+  if (per_token > max_elems || (T > 0 && uint64_t(T) > max_elems / per_token)) {
     std::snprintf(msg, sizeof(msg),
-                  "needs %zu bytes of scratch (n * tokens * out_features * 4 + 256); the static "
-                  "scratch of this entry point holds %zu bytes",
-                  need, kScratchBytes);
+                  "needs %llu x %lld x %lld fp32 partials (tp_degree x tokens x out_features) "
+                  "plus 256 bytes of scratch; the static scratch of this entry point holds %zu "
+                  "bytes",
+                  static_cast<unsigned long long>(n), static_cast<long long>(T),
+                  static_cast<long long>(N), kScratchBytes);
     return fail(TP_ERR_WORKSPACE, msg);
   }
   if (T > 0) {
@@ -140,6 +154,10 @@ extern "C" tp_status tp_linear_row_forward_noalloc(const tp_linear_desc* desc,
   }
   if (e == cudaSuccess)
     e = tpk::launch_shard_reduce(P, n, T, N, bias, dt == TP_BF16, static_cast<float*>(Z), st);
+  if (e == cudaSuccess) {
+    poison_on_timeout<<<1, 256, 0, st>>>(status, static_cast<float*>(Z), T * N);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) {
     std::snprintf(msg, sizeof(msg), "launch: %s", cudaGetErrorString(e));
     return fail(TP_ERR_CUDA, msg);

@@ -19,7 +19,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <cstdlib>
 
 #include "device_common.cuh"
 #include "internal.h"
@@ -334,8 +333,7 @@ int max_active_clusters(int S) {
 
 int plan_simt_split(const GemmSpec& s) {
   if (s.M <= 0 || s.N <= 0 || s.K <= 0) return 1;
-  if (const char* env = std::getenv("TPMLP_SIMT_SPLIT"))
-    if (std::atoi(env) == 0) return 1;
+  if (tuning(TP_TUNE_SIMT_SPLIT) == 0) return 1;
   const long long outs = s.ksum ? 1 : s.groups;
   const long long TM = tile_rows(s.M);
   const long long tiles = ((s.N + TN - 1) / TN) * ((s.M + TM - 1) / TM) * outs;

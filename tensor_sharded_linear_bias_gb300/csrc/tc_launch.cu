@@ -4,7 +4,6 @@
 
 #include <algorithm>
 #include <cmath>
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -60,9 +59,9 @@ bool encode_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer
 }
 
 // The SM-pair kernel computes 256-row tiles; below that the one-SM kernel's 128-row tiles
-// waste less. TPMLP_GEMM_PAIR=0/1 forces the choice (tuning and tests).
+// waste less. TP_TUNE_GEMM_PAIR forces the choice (tests and A/B timing).
 bool use_pair_kernel(int64_t M) {
-  if (const char* env = std::getenv("TPMLP_GEMM_PAIR")) return std::atoi(env) != 0;
+  if (const int v = tuning(TP_TUNE_GEMM_PAIR); v != TP_TUNE_AUTO) return v != 0;
   return M > tc::BM;
 }
 
@@ -97,9 +96,9 @@ int pair_clusters(int layout, int epi_warps = 4) {
 // 16; else 4, which is faster for deep tiles (measured on GB300, same box: the GPT-3-shaped
 // step 1494 vs 1484 TFLOP/s with 4; the 4096 x 1024 x 4096 step 753 vs 710 with 8 on its
 // GeLU / GeLU' GEMMs; weight gradients over 512 tokens 0.253 vs 0.265 ms with 8).
-// TPMLP_EPI_WARPS=4/8 forces the count.
+// TP_TUNE_EPI_WARPS forces the count.
 int pair_epi_warps(int epi, int act, int total_kb) {
-  if (const char* env = std::getenv("TPMLP_EPI_WARPS")) return std::atoi(env) == 8 ? 8 : 4;
+  if (const int v = tuning(TP_TUNE_EPI_WARPS); v != TP_TUNE_AUTO) return v == 8 ? 8 : 4;
   const bool heavy = (epi == EPI_BIAS_ACT || epi == EPI_DACT) && act == TP_ACT_GELU_ERF;
   return (heavy && total_kb <= 64) || total_kb <= 16 ? 8 : 4;
 }
@@ -109,9 +108,9 @@ int pair_epi_warps(int epi, int act, int total_kb) {
 // (C = tiles in flight); in n-fastest order, the converse. Each block is 256 x K bf16 (128 x K
 // for one-SM A blocks). Keep m fastest unless its working set exceeds half of L2 and n
 // fastest needs a quarter less. (Measured on GB300: m fastest is 5 % faster for the GPT-3-
-// shaped MLP, n fastest 1.5 % faster at 8192 tokens.) TPMLP_RASTER=0/1 forces the order.
+// shaped MLP, n fastest 1.5 % faster at 8192 tokens.) TP_TUNE_RASTER forces the order.
 int choose_raster(int tiles_m, int tiles_n, int64_t k_total, int sms, bool pair) {
-  if (const char* env = std::getenv("TPMLP_RASTER")) return std::atoi(env) != 0;
+  if (const int v = tuning(TP_TUNE_RASTER); v != TP_TUNE_AUTO) return v != 0;
   const double inflight = pair ? sms / 2.0 : double(sms);
   const double a_block = (pair ? 256.0 : 128.0) * double(k_total) * 2.0;
   const double b_block = 256.0 * double(k_total) * 2.0;
@@ -140,38 +139,38 @@ bool encode_bf16_mn3d(CUtensorMap* m, const void* ptr, uint64_t mn, uint64_t k, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// One-load MN-major tiles (3-D maps); TPMLP_TMA_3D=0 keeps the 2-D boxes.
+// One-load MN-major tiles (3-D maps); TP_TUNE_TMA_3D = 0 keeps the 2-D boxes.
 bool mn3d_enabled() {
-  if (const char* env = std::getenv("TPMLP_TMA_3D")) return std::atoi(env) != 0;
+  if (const int v = tuning(TP_TUNE_TMA_3D); v != TP_TUNE_AUTO) return v != 0;
   return true;
 }
 
 // A and B loads of the SM-pair kernel from two producer threads: where both operands are
 // MN-major (weight gradients), whose two 3-D boxes per K block make the longest issue loop
-// (measured 1-2 % faster there, 0.5-1 % slower for the other layouts); TPMLP_SPLIT_LOADS
+// (measured 1-2 % faster there, 0.5-1 % slower for the other layouts); TP_TUNE_SPLIT_LOADS
 // overrides.
 bool split_loads_enabled(int layout) {
-  if (const char* env = std::getenv("TPMLP_SPLIT_LOADS")) return std::atoi(env) != 0;
+  if (const int v = tuning(TP_TUNE_SPLIT_LOADS); v != TP_TUNE_AUTO) return v != 0;
   return layout == 2;
 }
 
-// The MMA issuer's early look at the next block's barrier; TPMLP_MMA_PROBE overrides.
+// The MMA issuer's early look at the next block's barrier; TP_TUNE_MMA_PROBE overrides.
 bool mma_probe_enabled() {
-  if (const char* env = std::getenv("TPMLP_MMA_PROBE")) return std::atoi(env) != 0;
+  if (const int v = tuning(TP_TUNE_MMA_PROBE); v != TP_TUNE_AUTO) return v != 0;
   return true;
 }
 
 // The producers' early look at the next block's stage: for A K-major with B MN-major (the
 // forward GEMMs: 4-5 % faster), not for the other layouts (both K-major: 0.5-2 % slower, both
-// MN-major: no change); TPMLP_LOAD_PROBE overrides.
+// MN-major: no change); TP_TUNE_LOAD_PROBE overrides.
 bool load_probe_enabled(int layout) {
-  if (const char* env = std::getenv("TPMLP_LOAD_PROBE")) return std::atoi(env) != 0;
+  if (const int v = tuning(TP_TUNE_LOAD_PROBE); v != TP_TUNE_AUTO) return v != 0;
   return layout == 0;
 }
 
-// Split tail; TPMLP_TAIL_SPLIT=0 turns it off.
+// Split tail; TP_TUNE_TAIL_SPLIT = 0 turns it off.
 bool tail_split_enabled() {
-  if (const char* env = std::getenv("TPMLP_TAIL_SPLIT")) return std::atoi(env) != 0;
+  if (const int v = tuning(TP_TUNE_TAIL_SPLIT); v != TP_TUNE_AUTO) return v != 0;
   return true;
 }
 
@@ -196,7 +195,7 @@ void plan_tail(tc::TcParams& p, int clusters, int total_kb, bool have_ws) {
   p.num_units = p.num_tiles;
   if (!have_ws || !tail_split_enabled() || clusters < 2) return;
   int max_waves = total_kb >= kDeepTileKb ? 1 << 20 : kMaxSplitWaves;
-  if (const char* env = std::getenv("TPMLP_TAIL_WAVES")) max_waves = std::atoi(env);
+  if (const int v = tuning(TP_TUNE_TAIL_WAVES); v != TP_TUNE_AUTO) max_waves = v;
   if (p.num_tiles > static_cast<long long>(max_waves) * clusters) return;
   const int L = p.num_tiles % clusters;
   if (L == 0) return;
@@ -213,8 +212,7 @@ void plan_tail(tc::TcParams& p, int clusters, int total_kb, bool have_ws) {
 
 int plan_shard_split(int64_t M, int64_t N, int64_t K_per_group, int n) {
   using namespace tc;
-  if (const char* env = std::getenv("TPMLP_SHARD_SPLIT")) {  // tuning override
-    const int v = std::atoi(env);
+  if (const int v = tuning(TP_TUNE_SHARD_SPLIT); v != TP_TUNE_AUTO) {
     if (v >= 1 && v <= n && n % v == 0) return v;
   }
   // Model on SM pairs (the kernel for every M > 128): 256 x 256 tiles dealt to C = SMs / 2

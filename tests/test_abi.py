@@ -14,6 +14,8 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "tp_mlp.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+                 if f.endswith(".h"))
 
 
 @pytest.fixture(scope="module")
@@ -27,9 +29,12 @@ def tp():
 
 
 def header_functions():
-    src = open(HEADER).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(tp_[a-z0-9_]+)\s*\(", src)))
+    """Every function declared by a header under include/."""
+    names = set()
+    for h in HEADERS:
+        src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b(tp_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
 
 
 def test_header_declares_what_the_binding_exports(tp):
@@ -257,3 +262,23 @@ def test_binding_checks_device_and_dtype():
     bf = torch.zeros(8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="must be torch.float32"):
         tpm.tp_mlp_forward(d, bf, [bf], [bf], [bf], None, bf, [bf], [bf], None)
+
+
+def test_tuning_hook_without_environment(tp):
+    """Kernel-variant overrides go through the tuning entry points only: setting and reading a
+    knob needs no GPU, unknown knobs and values are refused, and no environment variable
+    changes what the library picks."""
+    src = "".join(open(os.path.join(ROOT, "tensor_sharded_linear_bias_gb300", "csrc", f)).read()
+                  for f in os.listdir(os.path.join(ROOT, "tensor_sharded_linear_bias_gb300", "csrc"))
+                  if f.endswith((".cu", ".cuh", ".h")))
+    assert "getenv" not in src
+    for name in tp.TUNE_KNOBS:
+        assert tp.tp_tuning_get(name) == tp.TP_TUNE_AUTO
+    with tp.tuning(raster=1, tail_waves=3):
+        assert tp.tp_tuning_get("raster") == 1 and tp.tp_tuning_get("tail_waves") == 3
+    assert tp.tp_tuning_get("raster") == tp.TP_TUNE_AUTO
+    assert tp.lib.tp_tuning_set(len(tp.TUNE_KNOBS), 0) == 5       # TP_ERR_DTYPE
+    assert tp.lib.tp_tuning_set(-1, 0) == 5
+    assert tp.lib.tp_tuning_set(0, -2) == 2                        # TP_ERR_SHAPE
+    assert tp.lib.tp_tuning_get(99) == tp.TP_TUNE_AUTO - 1
+    assert tp.tp_tuning_get("gemm_pair") == tp.TP_TUNE_AUTO

@@ -111,16 +111,16 @@ def test_layernorm_deterministic_and_shard_count(tp):
                                          ("bf16", 70, 8 * 1536, 8), ("bf16", 50, 2 * 2048, 2),
                                          ("bf16", 33, 3 * 1000, 3), ("f32", 64, 8 * 96, 8),
                                          ("f32", 40, 8 * 1024, 8)])
-def test_layernorm_register_path_matches_two_pass(tp, monkeypatch, dtype, T, H, n):
+def test_layernorm_register_path_matches_two_pass(tp, tune, dtype, T, H, n):
     """Rows whose shards fit in at most 8 16-byte vectors per lane (2, 4, 6 and 8 here, ragged
     last vectors included) run in the register-resident kernels, which do the two-pass
-    kernels' arithmetic in the same order: every output bit-identical to TPMLP_LN_REG=0, and
+    kernels' arithmetic in the same order: every output bit-identical to knob ln_reg = 0, and
     within tolerance of the oracle."""
     import torch
 
     cases = {}
     for reg in ("1", "0"):
-        monkeypatch.setenv("TPMLP_LN_REG", reg)
+        tune.set("ln_reg", reg)
         cases[reg] = LnCase(tp, T, H, n, dtype, seed=3).run()
     errs = cases["1"].errors()
     assert max(errs.values()) <= (TOL_BF16 if dtype == "bf16" else TOL_F32), errs

@@ -72,11 +72,11 @@ def test_mlp_bf16_small(tp, T, H, F, n, reduce):
 
 @pytest.mark.parametrize("reduce", [2, 4])
 @pytest.mark.parametrize("split", ["1", "2", "4", "8"])
-def test_shard_sum_in_groups(tp, monkeypatch, split, reduce):
+def test_shard_sum_in_groups(tp, tune, split, reduce):
     """The shard sum split into `split` partial outputs (groups of 8 / split shards each),
     reduced after the GEMM (AUTO) or inside it (OVERLAP); twice in a row, so the second launch
     starts from counters the first one reset."""
-    monkeypatch.setenv("TPMLP_SHARD_SPLIT", split)
+    tune.set("shard_split", split)
     w = SMALL.with_shape(tokens=300, hidden=136, ffn=8 * 136, tp_degree=8)
     case = MlpCase(w, reduce).run()
     first = case.outputs()
@@ -92,15 +92,15 @@ def test_shard_sum_in_groups(tp, monkeypatch, split, reduce):
 @pytest.mark.parametrize("T,H,F,n", [(96, 72, 2 * 136, 2), (300, 136, 2 * 296, 2),
                                      (640, 264, 4 * 392, 4), (392, 192, 2 * 320, 2),
                                      (520, 320, 4 * 448, 4)])
-def test_gemm_kernel_variants(tp, monkeypatch, pair, raster, tma3d, T, H, F, n):
+def test_gemm_kernel_variants(tp, tune, pair, raster, tma3d, T, H, F, n):
     """Both tensor-core kernels on every GEMM of the MLP: one SM per 128 x 256 tile, and SM
     pairs (tcgen05 cta_group::2) per 256 x 256 tile, including pairs whose second half of
     the rows lies beyond M; in both tile orders (m fastest, n fastest)."""
-    monkeypatch.setenv("TPMLP_GEMM_PAIR", pair)
-    monkeypatch.setenv("TPMLP_RASTER", raster)
+    tune.set("gemm_pair", pair)
+    tune.set("raster", raster)
     # MN-major operands whose MN size is a multiple of 64 (H = 192, 320; F/n = 320, 448) are
     # loaded as one 3-D TMA box per tile, or as 64-wide 2-D boxes
-    monkeypatch.setenv("TPMLP_TMA_3D", tma3d)
+    tune.set("tma_3d", tma3d)
     for reduce in (0, 2):
         case = MlpCase(SMALL.with_shape(tokens=T, hidden=H, ffn=F, tp_degree=n), reduce).run()
         errs = compare_full(case.outputs(), *full_reference(case))
@@ -127,12 +127,12 @@ def test_p3_shapes_fp32_forward(tp):
         assert max(errs.values()) <= TOL_F32, errs
 
 
-def test_fp32_split_k(tp, monkeypatch):
+def test_fp32_split_k(tp, tune):
     """Few tokens: the FFMA GEMMs whose tiles cannot fill the GPU cut their K range over the
     CTAs of a cluster (column forward, row forward with the shard sum, the dY GEMM with the
     GeLU' epilogue, the input gradient) and add the partial tiles in CTA order through
     distributed shared memory. Ragged K per slice and ragged tiles match the oracle to fp32
-    accuracy; repeated runs are bit-identical; the unsplit kernel (TPMLP_SIMT_SPLIT=0) agrees
+    accuracy; repeated runs are bit-identical; the unsplit kernel (knob simt_split = 0) agrees
     to fp32 rounding but not bit for bit (the split path did run)."""
     import torch
 
@@ -144,7 +144,7 @@ def test_fp32_split_k(tp, monkeypatch):
     Z1, dX1, Y1 = case.Z.clone(), case.dX.clone(), [y.clone() for y in case.Ys]
     case.run()
     assert torch.equal(Z1, case.Z) and torch.equal(dX1, case.dX)
-    monkeypatch.setenv("TPMLP_SIMT_SPLIT", "0")
+    tune.set("simt_split", 0)
     case.run()
     assert rel(np64(case.Z), np64(Z1)) <= TOL_F32 and rel(np64(case.dX), np64(dX1)) <= TOL_F32
     assert not (torch.equal(Z1, case.Z) and torch.equal(dX1, case.dX)
@@ -169,33 +169,33 @@ def test_bias_grads_many_tokens(tp, dtype):
 
 @pytest.mark.parametrize("epi_warps", ["4", "8"])
 @pytest.mark.parametrize("T,H,F,n", [(300, 264, 2 * 392, 2), (520, 136, 4 * 136, 4)])
-def test_epilogue_warps(tp, monkeypatch, epi_warps, T, H, F, n):
+def test_epilogue_warps(tp, tune, epi_warps, T, H, F, n):
     """The SM-pair kernel with 4 epilogue warps (each on all 256 columns of its 32 rows) or 8
     (two per TMEM lane quadrant, 128 columns each), every epilogue and reduce mode, ragged
     tiles: matches the oracle."""
-    monkeypatch.setenv("TPMLP_EPI_WARPS", epi_warps)
-    monkeypatch.setenv("TPMLP_GEMM_PAIR", "1")
+    tune.set("epi_warps", epi_warps)
+    tune.set("gemm_pair", 1)
     for reduce in (0, 2, 4):
         case = MlpCase(SMALL.with_shape(tokens=T, hidden=H, ffn=F, tp_degree=n), reduce).run()
         errs = compare_full(case.outputs(), *full_reference(case))
         assert max(errs.values()) <= TOL_BF16, (reduce, errs)
 
 
-_ISSUE_VARIANTS = [{"TPMLP_SPLIT_LOADS": "1"}, {"TPMLP_SPLIT_LOADS": "0"},
-                   {"TPMLP_MMA_PROBE": "0", "TPMLP_LOAD_PROBE": "0"},
-                   {"TPMLP_MMA_PROBE": "1", "TPMLP_LOAD_PROBE": "1"}]
+_ISSUE_VARIANTS = [{"split_loads": 1}, {"split_loads": 0},
+                   {"mma_probe": 0, "load_probe": 0},
+                   {"mma_probe": 1, "load_probe": 1}]
 
 
 @pytest.mark.parametrize("epi_warps", ["4", "8"])
-def test_issue_loop_variants(tp, monkeypatch, epi_warps):
+def test_issue_loop_variants(tp, tune, epi_warps):
     """The SM-pair kernel's issue loops in every variant: A and B loads from one producer thread
     or two (warp 0 and the last warp), with and without the early looks at the next block's
     barriers (MMA issuer and producers), for all three operand layouts (forward,
     input-gradient and weight-gradient GEMMs), ragged tiles, fused and overlapped shard sums.
     The default matches the oracle; every variant is bit-identical to it (they change which
     thread issues what and when, not the arithmetic)."""
-    monkeypatch.setenv("TPMLP_EPI_WARPS", epi_warps)
-    monkeypatch.setenv("TPMLP_GEMM_PAIR", "1")
+    tune.set("epi_warps", epi_warps)
+    tune.set("gemm_pair", 1)
     w = SMALL.with_shape(tokens=600, hidden=392, ffn=2 * 264, tp_degree=2)
     for reduce in (0, 4):
         case = MlpCase(w, reduce).run()
@@ -203,9 +203,7 @@ def test_issue_loop_variants(tp, monkeypatch, epi_warps):
         errs = compare_full(base, *full_reference(case))
         assert max(errs.values()) <= TOL_BF16, (reduce, errs)
         for env in _ISSUE_VARIANTS:
-            with monkeypatch.context() as m:
-                for k, v in env.items():
-                    m.setenv(k, v)
+            with tp.tuning(**env):
                 out = MlpCase(w, reduce).run().outputs()
             for k, v in base.items():
                 pairs = zip(v, out[k]) if isinstance(v, list) else [(v, out[k])]
@@ -216,11 +214,11 @@ _TAIL_REF = {}
 
 
 @pytest.mark.parametrize("reduce", [0, 2, 4])
-def test_tail_split(tp, monkeypatch, reduce):
+def test_tail_split(tp, tune, reduce):
     """Tiles of a GEMM's partial last wave of SM pairs run as K pieces on the idle pairs and are
     added in piece order before the epilogue. Ragged tiles in M and N, ragged K per piece, and
     every epilogue (bias + GeLU, fused or grouped shard sum, overlapped sum, GeLU', plain fp32):
-    matches the oracle, matches the unsplit kernel (TPMLP_TAIL_SPLIT=0) to fp32 rounding, and
+    matches the oracle, matches the unsplit kernel (knob tail_split = 0) to fp32 rounding, and
     repeats bit for bit."""
     import torch
 
@@ -229,7 +227,7 @@ def test_tail_split(tp, monkeypatch, reduce):
     w = SMALL.with_shape(tokens=2080, hidden=2056, ffn=2 * 1040, tp_degree=2)
     outs = {}
     for split in ("1", "0"):
-        monkeypatch.setenv("TPMLP_TAIL_SPLIT", split)
+        tune.set("tail_split", split)
         case = MlpCase(w, reduce).run()
         outs[split] = case.outputs()
         if split == "1":

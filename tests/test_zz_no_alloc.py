@@ -59,6 +59,39 @@ def test_row_forward_without_allocation_matches_workspace_path(dtype):
         assert rel(got, ref) <= TOL_GPU_VS_GPU, f"call {call}"
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_row_forward_without_allocation_allocates_nothing(dtype):
+    """The entry point's contract: after a first call (which looks up the static array's
+    address and loads the kernels), further calls leave the device's free memory and torch's
+    allocator untouched -- everything is allocated before the measured call."""
+    import torch
+
+    import tensor_sharded_linear_bias_gb300 as tp
+
+    fn = tp.lib.tp_linear_row_forward_noalloc
+    T, K, N, n = 300, 4 * 64, 512, 4
+    Ks = K // n
+    desc = tp.LinearDesc(tokens=T, in_features=K, out_features=N, tp_degree=n,
+                         dtype=tp.TP_BF16 if dtype == "bf16" else tp.TP_F32, act=0,
+                         reduce=tp.TP_REDUCE_PARTIALS, gather=0)
+    t = _inputs(733, T, K, N, dtype)
+    X = [t["X"][:, i * Ks:(i + 1) * Ks].contiguous() for i in range(n)]
+    W = [t["W"][i * Ks:(i + 1) * Ks, :].contiguous() for i in range(n)]
+    Zs = [torch.empty(T, N, dtype=torch.float32, device="cuda") for _ in range(2)]
+    stream = torch.cuda.current_stream().cuda_stream
+    xs, ws, b = tp._arr(X), tp._arr(W), t["bias"].data_ptr()
+    assert fn(ctypes.byref(desc), xs, ws, b, Zs[0].data_ptr(), stream) == 0, tp.tp_last_error()
+    torch.cuda.synchronize()
+    free0, allocated0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+    reserved0 = torch.cuda.memory_reserved()
+    assert fn(ctypes.byref(desc), xs, ws, b, Zs[1].data_ptr(), stream) == 0, tp.tp_last_error()
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.cuda.memory_allocated() == allocated0
+    assert torch.cuda.memory_reserved() == reserved0
+    assert torch.equal(Zs[0], Zs[1])
+
+
 def test_row_forward_without_allocation_rejects_oversize():
     import tensor_sharded_linear_bias_gb300 as tp
 
