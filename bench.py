@@ -701,8 +701,8 @@ def oracle_full_line(name: str) -> dict:
     """The fp64 oracle as it stands, on the whole workload (every output of fwd + bwd), timed
     on the host cores. Workloads whose oracle would not fit the host's free memory (about 3x
     the fp64 inputs and outputs) or whose full run is long (T >= 8192 in the sweep) are timed
-    on a seeded sample -- 64 token rows x 64 ffn columns per shard -- and extrapolated by
-    flops, labelled as such."""
+    on their first 1024 token rows (every ffn column; the MLP restricted to those rows) and
+    extrapolated by flops, labelled as such."""
     import numpy as np  # noqa: F401
 
     import oracle
@@ -738,7 +738,7 @@ def oracle_full_line(name: str) -> dict:
             kind = "full"
             text = f"whole workload, {'fwd+bwd' if w.backward else 'fwd'}, fp64 numpy"
         else:
-            run, flops, text = oracle_sample(w, host, rows=64, cols_per_shard=64)
+            run, flops, text = oracle_sample(w, host, rows=1024, cols_per_shard=w.ffn)
             kind = "extrapolated from the measured sample"
             text += (f"; full run skipped: {'T >= 8192' if T >= 8192 else 'host memory'} "
                      f"(needs ~{need / 1e9:.0f} GB, {0 if avail is None else avail / 1e9:.0f} GB "

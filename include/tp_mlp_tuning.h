@@ -42,7 +42,10 @@ typedef enum tp_tune_knob {
                                (a divisor of tp_degree; others fall back to the library's) */
   TP_TUNE_SIMT_SPLIT = 10,  /* 0: no K split over a cluster in the fp32 FFMA GEMM */
   TP_TUNE_LN_REG = 11,      /* 0/1: two-pass / register-resident LayerNorm kernels (bit-identical) */
-  TP_TUNE_COUNT = 12
+  TP_TUNE_PDL = 12,         /* 0/1: SM-pair GEMMs and column sums launched without / with
+                               programmatic stream serialisation (default on: each launch's
+                               set-up overlaps the previous kernel's end; bit-identical) */
+  TP_TUNE_COUNT = 13
 } tp_tune_knob;
 
 /* Sets knob to value (TP_TUNE_AUTO: the library's choice). TP_ERR_DTYPE for an unknown

@@ -11,84 +11,114 @@ namespace tpk {
 // GeLU in its exact (erf) form and its derivative, with the normal tail computed once:
 //   Phi(-|h|) = erfc(z) / 2,  z = |h| / sqrt 2,  erfc(z) ~ t Q(t) exp(-z^2),  t = 1 / (1 + p z),
 // the form of Abramowitz & Stegun, Handbook of Mathematical Functions, 7.1.26, with p = 1/2 and
-// Q of degree 8 fitted for RELATIVE error (fit_normal_tail.py, beside this file: t Q(t) is
-// within 2.1e-7 of the scaled function exp(z^2) erfc(z) for every z >= 0, so Phi(h) keeps its
-// relative accuracy far into the negative tail, where GeLU(h) = h Phi(h) is tiny; 7.1.26's
-// own degree-4 coefficients are fitted for absolute error and drift to 38 % relative error as
-// z grows). exp(-z^2) = exp(-h^2 / 2) is also the normal density's exponential, so GeLU' costs
-// one exponential and one reciprocal.
+// Q fitted for RELATIVE error (fit_normal_tail.py, beside this file), so that Phi(h) keeps its
+// relative accuracy far into the negative tail, where GeLU(h) = h Phi(h) is tiny (7.1.26's own
+// degree-4 coefficients are fitted for absolute error and drift to 38 % relative error as z
+// grows). exp(-z^2) = exp(-h^2 / 2) is also the normal density's exponential, so GeLU' costs
+// one exponential and one reciprocal. Two fits:
+//  - degree 8 (t Q(t) within 2.1e-7 of exp(z^2) erfc(z) for every z >= 0) for the fp32 paths
+//    (FFMA GEMM epilogues, the activation-gradient kernel), whose tolerance is 1e-5;
+//  - degree 5 (within 5.1e-5) for the bf16 tensor-core epilogues, whose outputs are rounded
+//    to bf16 (2^-9 relative) and whose instruction count sets the pace of short-K GEMMs.
+// The coefficients below are Q's halved (exact in fp32), so that t Q(t) exp(-z^2) / 2 needs no
+// separate multiplication.
 constexpr float kTailP = 0.35355339059327373f;  // p / sqrt 2: t = 1 / (1 + kTailP |h|)
-constexpr float kTailQ0 = 2.820921728e-01f, kTailQ1 = 2.822133577e-01f,
-                kTailQ2 = 2.448138215e-01f, kTailQ3 = 1.935501536e-01f,
-                kTailQ4 = 9.956123732e-04f, kTailQ5 = 2.288727022e-01f,
-                kTailQ6 = -4.361299399e-01f, kTailQ7 = 2.560270581e-01f,
-                kTailQ8 = -5.243482750e-02f;
+namespace tail8 {
+constexpr float q0 = 0.5f * 2.820921728e-01f, q1 = 0.5f * 2.822133577e-01f,
+                q2 = 0.5f * 2.448138215e-01f, q3 = 0.5f * 1.935501536e-01f,
+                q4 = 0.5f * 9.956123732e-04f, q5 = 0.5f * 2.288727022e-01f,
+                q6 = 0.5f * -4.361299399e-01f, q7 = 0.5f * 2.560270581e-01f,
+                q8 = 0.5f * -5.243482750e-02f;
+}  // namespace tail8
+namespace tail5 {
+constexpr float q0 = 0.5f * 2.820021294e-01f, q1 = 0.5f * 2.845312988e-01f,
+                q2 = 0.5f * 2.286358539e-01f, q3 = 0.5f * 2.235169020e-01f,
+                q4 = 0.5f * 6.513961987e-02f, q5 = 0.5f * -8.387641932e-02f;
+}  // namespace tail5
+constexpr float kInvSqrt2Pi = 0.3989422804014327f;
 
+// Phi(-|h|) = lower and exp(-h^2 / 2) = e, degree-8 fit. GeLU and GeLU' then follow without a
+// branch: GeLU(h) = max(h, 0) - |h| lower, GeLU'(h) = [h >= 0] + e (h / sqrt(2 pi) -+ t Q / 2)
+// (the sign of t Q / 2 = lower / e opposite to h's), each with one final fused multiply-add.
+// Both the step and the sign are taken from h's sign bit, so h = -0 gives GeLU'(0) = 1/2 too.
 struct NormalTail {
-  float cdf;  // Phi(h)
-  float e;    // exp(-h^2 / 2)
+  float tq;  // t Q(t) / 2 = Phi(-|h|) / exp(-h^2 / 2)
+  float e;   // exp(-h^2 / 2)
 };
 
 __device__ __forceinline__ NormalTail normal_tail(float h) {
+  using namespace tail8;
   // fast division (2 ulp): the divisor 1 + p |h| / sqrt 2 lies in [1, 2^126)
   const float t = __fdividef(1.0f, fmaf(kTailP, fabsf(h), 1.0f));
-  float q = fmaf(t, kTailQ8, kTailQ7);
-  q = fmaf(t, q, kTailQ6);
-  q = fmaf(t, q, kTailQ5);
-  q = fmaf(t, q, kTailQ4);
-  q = fmaf(t, q, kTailQ3);
-  q = fmaf(t, q, kTailQ2);
-  q = fmaf(t, q, kTailQ1);
-  q = fmaf(t, q, kTailQ0);
-  const float e = __expf((-0.5f * h) * h);
-  const float lower = 0.5f * (t * q) * e;  // Phi(-|h|)
-  return {h >= 0.0f ? 1.0f - lower : lower, e};
+  float q = fmaf(t, q8, q7);
+  q = fmaf(t, q, q6);
+  q = fmaf(t, q, q5);
+  q = fmaf(t, q, q4);
+  q = fmaf(t, q, q3);
+  q = fmaf(t, q, q2);
+  q = fmaf(t, q, q1);
+  q = fmaf(t, q, q0);
+  return {t * q, __expf((-0.5f * h) * h)};
 }
 
-// GeLU(h) = h * Phi(h).
-__device__ __forceinline__ float gelu_erf(float h) { return h * normal_tail(h).cdf; }
+// GeLU(h) = h Phi(h) = max(h, 0) - |h| Phi(-|h|).
+__device__ __forceinline__ float gelu_erf(float h) {
+  const NormalTail n = normal_tail(h);
+  return fmaf(-fabsf(h), n.tq * n.e, fmaxf(h, 0.0f));
+}
 
-// d/dh GeLU(h) = Phi(h) + h * phi(h), phi(h) = exp(-h^2 / 2) / sqrt(2 pi).
+// d/dh GeLU(h) = Phi(h) + h phi(h), phi(h) = exp(-h^2 / 2) / sqrt(2 pi).
 __device__ __forceinline__ float gelu_erf_grad(float h) {
   const NormalTail n = normal_tail(h);
-  return fmaf(h * 0.3989422804014327f, n.e, n.cdf);
+  return fmaf(n.e, fmaf(kInvSqrt2Pi, h, copysignf(n.tq, -h)), signbit(h) ? 0.0f : 1.0f);
 }
 
-// The same two functions for two values at once with Blackwell's paired fp32 instructions
-// (__ffma2_rn, __fmul2_rn, __fadd2_rn: each half rounded exactly as the scalar operation), for
-// the epilogues that are bound by instruction issue. Every operation and its order are those
-// of normal_tail, gelu_erf and gelu_erf_grad, so the results are bit-identical to them; the
-// exponential and the fast reciprocal stay per value.
+// The bf16 epilogues' versions, two values at once with Blackwell's paired fp32 instructions
+// (__ffma2_rn, __fmul2_rn: each half rounded as the scalar operation), degree-5 fit; the same
+// formulas as above. The exponential and the fast reciprocal stay per value.
 __device__ __forceinline__ float2 splat2(float a) { return make_float2(a, a); }
 
-__device__ __forceinline__ void normal_tail2(float2 h, float2& cdf, float2& e) {
+__device__ __forceinline__ void normal_tail2(float2 h, float2& tq, float2& e) {
+  using namespace tail5;
   const float2 d = __ffma2_rn(splat2(kTailP), make_float2(fabsf(h.x), fabsf(h.y)), splat2(1.0f));
   const float2 t = make_float2(__fdividef(1.0f, d.x), __fdividef(1.0f, d.y));
-  float2 q = __ffma2_rn(t, splat2(kTailQ8), splat2(kTailQ7));
-  q = __ffma2_rn(t, q, splat2(kTailQ6));
-  q = __ffma2_rn(t, q, splat2(kTailQ5));
-  q = __ffma2_rn(t, q, splat2(kTailQ4));
-  q = __ffma2_rn(t, q, splat2(kTailQ3));
-  q = __ffma2_rn(t, q, splat2(kTailQ2));
-  q = __ffma2_rn(t, q, splat2(kTailQ1));
-  q = __ffma2_rn(t, q, splat2(kTailQ0));
+  float2 q = __ffma2_rn(t, splat2(q5), splat2(q4));
+  q = __ffma2_rn(t, q, splat2(q3));
+  q = __ffma2_rn(t, q, splat2(q2));
+  q = __ffma2_rn(t, q, splat2(q1));
+  q = __ffma2_rn(t, q, splat2(q0));
+  tq = __fmul2_rn(t, q);
   const float2 nh2 = __fmul2_rn(__fmul2_rn(splat2(-0.5f), h), h);
   e = make_float2(__expf(nh2.x), __expf(nh2.y));
-  const float2 lower = __fmul2_rn(__fmul2_rn(splat2(0.5f), __fmul2_rn(t, q)), e);
-  const float2 upper = __fadd2_rn(splat2(1.0f), make_float2(-lower.x, -lower.y));
-  cdf = make_float2(h.x >= 0.0f ? upper.x : lower.x, h.y >= 0.0f ? upper.y : lower.y);
 }
 
 __device__ __forceinline__ float2 gelu_erf2(float2 h) {
-  float2 cdf, e;
-  normal_tail2(h, cdf, e);
-  return __fmul2_rn(h, cdf);
+  float2 tq, e;
+  normal_tail2(h, tq, e);
+  return __ffma2_rn(make_float2(-fabsf(h.x), -fabsf(h.y)), __fmul2_rn(tq, e),
+                    make_float2(fmaxf(h.x, 0.0f), fmaxf(h.y, 0.0f)));
 }
 
 __device__ __forceinline__ float2 gelu_erf_grad2(float2 h) {
-  float2 cdf, e;
-  normal_tail2(h, cdf, e);
-  return __ffma2_rn(__fmul2_rn(h, splat2(0.3989422804014327f)), e, cdf);
+  float2 tq, e;
+  normal_tail2(h, tq, e);
+  const float2 s = __ffma2_rn(splat2(kInvSqrt2Pi), h,
+                              make_float2(copysignf(tq.x, -h.x), copysignf(tq.y, -h.y)));
+  return __ffma2_rn(e, s, make_float2(signbit(h.x) ? 0.0f : 1.0f, signbit(h.y) ? 0.0f : 1.0f));
+}
+
+// ------------------------------------------------------------------ programmatic dependent launch
+// A kernel launched with programmatic stream serialisation may start while the kernel before it
+// on the stream is still running: it does its set-up (barriers, TMEM, shared memory), then
+// waits here until that kernel has completed and its memory operations are visible, before its
+// first global load or store. Without that launch attribute the wait returns at once.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel on the stream be scheduled (it still waits in grid_dependency_wait for
+// this one to complete); called by every CTA once it is running, after its own wait.
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ L2 prefetch

@@ -211,6 +211,8 @@ __device__ __forceinline__ void load8(const void* base, int bf16, long long off,
 __global__ void __launch_bounds__(kColsumWarps * 32) colsum_kernel(const __grid_constant__ ColsumParams p) {
   __shared__ float part[kColsumWarps][256];
   __shared__ float block_sum[256];
+  grid_dependency_wait();
+  grid_dependents_launch();
   int s = 0;
   while (s + 1 < p.nseg && static_cast<int>(blockIdx.x) >= p.strip_start[s + 1]) ++s;
   const ColsumSeg seg = p.seg[s];
@@ -417,13 +419,15 @@ cudaError_t launch_colsum(const ColsumSeg* segs, int nseg, int64_t rows, int in_
   cfg.blockDim = dim3(kColsumWarps * 32, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = static_cast<unsigned>(R);
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = tuning(TP_TUNE_PDL) != 0 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, colsum_kernel, p);
 }
 

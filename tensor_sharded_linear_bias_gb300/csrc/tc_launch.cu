@@ -103,17 +103,42 @@ int pair_epi_warps(int epi, int act, int total_kb) {
   return (heavy && total_kb <= 64) || total_kb <= 16 ? 8 : 4;
 }
 
-// Tile order of a launch. The tiles running at the same time (one per SM, or per SM pair)
-// touch, in m-fastest order, all tiles_m row blocks of A plus C / tiles_m column blocks of B
-// (C = tiles in flight); in n-fastest order, the converse. Each block is 256 x K bf16 (128 x K
-// for one-SM A blocks). Keep m fastest unless its working set exceeds half of L2 and n
-// fastest needs a quarter less. (Measured on GB300: m fastest is 5 % faster for the GPT-3-
-// shaped MLP, n fastest 1.5 % faster at 8192 tokens.) TP_TUNE_RASTER forces the order.
+// Tile order of a launch (inside each output; m fastest or n fastest). Two estimates:
+//  1. Working set in flight: the tiles running at the same time (one per SM, or per SM pair)
+//     touch, in m-fastest order, all tiles_m row blocks of A plus C / tiles_m column blocks of
+//     B (C = tiles in flight); in n-fastest order, the converse. Each block is 256 x K bf16
+//     (128 x K for one-SM A blocks). m fastest unless its working set exceeds half of L2 and n
+//     fastest needs a quarter less. (Measured on GB300: m fastest is 5 % faster for the
+//     GPT-3-shaped MLP's forward and input-gradient GEMMs, n fastest 1.5 % faster at 8192
+//     tokens.)
+//  2. DRAM reads per output: the blocks of the slow axis are read once; the set of fast-axis
+//     blocks is read once if it fits in a share of L2 (kRasterL2Budget, leaving room for the
+//     streamed operand and the outputs), else once per wave that cycles through it. Where one
+//     order reads less than half of the other, that order wins over estimate 1. (The GPT-3
+//     column weight gradient: m fastest cycles 48 MB of X per column of dH_i and its 2.4 GB of
+//     fp32 output evicted X in between -- ncu read 2.16 GB for 0.25 GB of operands; n fastest
+//     keeps the shard's 24 MB of dH_i resident.)
+// TP_TUNE_RASTER forces the order.
+constexpr double kRasterL2Budget = 40.0e6;
+
+double raster_reads(double n_fast, double fast_block, double n_slow, double slow_block,
+                    double inflight) {
+  const double fast_set = n_fast * fast_block;
+  const double cycles = fast_set <= kRasterL2Budget
+                            ? 1.0
+                            : std::max(1.0, n_slow * std::min(1.0, n_fast / inflight));
+  return n_slow * slow_block + fast_set * cycles;
+}
+
 int choose_raster(int tiles_m, int tiles_n, int64_t k_total, int sms, bool pair) {
   if (const int v = tuning(TP_TUNE_RASTER); v != TP_TUNE_AUTO) return v != 0;
   const double inflight = pair ? sms / 2.0 : double(sms);
   const double a_block = (pair ? 256.0 : 128.0) * double(k_total) * 2.0;
   const double b_block = 256.0 * double(k_total) * 2.0;
+  const double reads_m = raster_reads(tiles_m, a_block, tiles_n, b_block, inflight);
+  const double reads_n = raster_reads(tiles_n, b_block, tiles_m, a_block, inflight);
+  if (reads_n < 0.5 * reads_m) return 1;
+  if (reads_m < 0.5 * reads_n) return 0;
   const double fm = std::min<double>(tiles_m, inflight) * a_block +
                     std::ceil(inflight / std::max(1, tiles_m)) * b_block;
   const double fn = std::min<double>(tiles_n, inflight) * b_block +

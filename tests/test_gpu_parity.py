@@ -183,15 +183,18 @@ def test_epilogue_warps(tp, tune, epi_warps, T, H, F, n):
 
 _ISSUE_VARIANTS = [{"split_loads": 1}, {"split_loads": 0},
                    {"mma_probe": 0, "load_probe": 0},
-                   {"mma_probe": 1, "load_probe": 1}]
+                   {"mma_probe": 1, "load_probe": 1},
+                   {"pdl": 1}, {"pdl": 0}]
 
 
 @pytest.mark.parametrize("epi_warps", ["4", "8"])
 def test_issue_loop_variants(tp, tune, epi_warps):
     """The SM-pair kernel's issue loops in every variant: A and B loads from one producer thread
     or two (warp 0 and the last warp), with and without the early looks at the next block's
-    barriers (MMA issuer and producers), for all three operand layouts (forward,
-    input-gradient and weight-gradient GEMMs), ragged tiles, fused and overlapped shard sums.
+    barriers (MMA issuer and producers), launched with and without programmatic stream
+    serialisation (set-up overlapping the previous kernel), for all three operand layouts
+    (forward, input-gradient and
+    weight-gradient GEMMs), ragged tiles, fused and overlapped shard sums.
     The default matches the oracle; every variant is bit-identical to it (they change which
     thread issues what and when, not the arithmetic)."""
     tune.set("epi_warps", epi_warps)
