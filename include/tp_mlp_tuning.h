@@ -45,7 +45,9 @@ typedef enum tp_tune_knob {
   TP_TUNE_PDL = 12,         /* 0/1: SM-pair GEMMs and column sums launched without / with
                                programmatic stream serialisation (default on: each launch's
                                set-up overlaps the previous kernel's end; bit-identical) */
-  TP_TUNE_COUNT = 13
+  TP_TUNE_STAGE_BLOCKS = 13, /* 1 or 2: 64-deep K blocks per operand-ring stage of the SM-pair
+                               GEMM (6 stages of 64 or 3 of 128; bit-identical) */
+  TP_TUNE_COUNT = 14
 } tp_tune_knob;
 
 /* Sets knob to value (TP_TUNE_AUTO: the library's choice). TP_ERR_DTYPE for an unknown

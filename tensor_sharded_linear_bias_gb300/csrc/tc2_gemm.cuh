@@ -34,12 +34,24 @@ using tc::TcParams;
 constexpr int BM = 256;                      // rows per CTA pair (128 per CTA)
 constexpr int BN = 256;                      // columns per tile (128 of B staged per CTA)
 constexpr int HALF = 128;
-constexpr int STAGES = 6;
 constexpr int ACC_BUFS = 2;
 constexpr int TMEM_COLS = ACC_BUFS * BN;     // 512
 constexpr int A_BYTES = HALF * BK * 2;       // 16 KiB
 constexpr int B_BYTES = HALF * BK * 2;       // 16 KiB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BLOCK_BYTES = A_BYTES + B_BYTES;  // one 64-deep K block of A and B per CTA: 32 KiB
+constexpr int RING_BLOCKS = 6;                  // K blocks the operand ring holds (192 KiB)
+// The ring is cut into stages of SUB K blocks (SUB = 1: 6 stages of 64; SUB = 2: 3 stages of
+// 128). Each stage has one full and one empty barrier, so the MMA issuer's fixed work per stage
+// (the barrier wait or look-ahead, the commit that releases the stage) is paid once per SUB K
+// blocks; the price is a coarser release (a stage is refilled only when all its blocks are
+// consumed). Inside a stage, block j sits at j * BLOCK_BYTES with the layout of a one-block
+// stage, so TMA boxes and MMA descriptors are the same for both.
+template <int SUB>
+struct Ring {
+  static_assert(SUB == 1 || SUB == 2, "1 or 2 K blocks per stage");
+  static constexpr int STAGES = RING_BLOCKS / SUB;
+  static constexpr int STAGE_BYTES = SUB * BLOCK_BYTES;
+};
 constexpr int MN_BOX_BYTES = 64 * BK * 2;    // 8 KiB
 // Warp 0: TMA producer (A); warp 1: MMA issuer; warps 2..: EPI_W epilogue warps; the last
 // warp: TMA producer (B), so that no single thread's issue loop paces the ring. A warp may only
@@ -53,9 +65,9 @@ struct EpiShape {
   static constexpr int COLS = BN * 4 / EPI_W;  // columns per epilogue warp
   static constexpr int B_WARP = 2 + EPI_W;         // the B producer, after the epilogue warps
   static constexpr int THREADS = 96 + 32 * EPI_W;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_W * tc::STAGE_WARP_BYTES + 1024 + 256;
+  static constexpr int SMEM = RING_BLOCKS * BLOCK_BYTES + EPI_W * tc::STAGE_WARP_BYTES + 1024 + 256;
 };
-constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
+constexpr int NUM_BARS = 2 * RING_BLOCKS + 2 * ACC_BUFS + 1;  // sized for the most stages
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -218,14 +230,16 @@ __device__ __forceinline__ void tail_fixup_rows(const TcParams& p, int g, int ro
   }
 }
 
-template <bool A_MN, bool B_MN, int EPI_W>
+template <bool A_MN, bool B_MN, int EPI_W, int SUB>
 __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ TcParams p) {
   using E = EpiShape<EPI_W>;
+  constexpr int STAGES = Ring<SUB>::STAGES;
+  constexpr int STAGE_BYTES = Ring<SUB>::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* epi_stage = smem + STAGES * STAGE_BYTES;
+  uint8_t* epi_stage = smem + RING_BLOCKS * BLOCK_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + E::WARPS * tc::STAGE_WARP_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -233,10 +247,10 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
   const uint32_t smem_base = smem_addr(smem);
   const uint32_t bar_base = smem_addr(bars);
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
-  auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
-  auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
-  auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + ACC_BUFS + a); };
-  const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 2 * ACC_BUFS);
+  auto empty_bar = [&](int s) { return bar_base + 8u * (RING_BLOCKS + s); };
+  auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * RING_BLOCKS + a); };
+  auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * RING_BLOCKS + ACC_BUFS + a); };
+  const uint32_t drain_bar = bar_base + 8u * (2 * RING_BLOCKS + 2 * ACC_BUFS);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -300,8 +314,9 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
         const int bcol = nb * BN + static_cast<int>(rank) * HALF;   // this CTA's B half
         int kg = g * p.kpo + kb0 / p.kblocks;                       // shard of block kb0
         int kk = (kb0 % p.kblocks) * BK;                            // its K offset
-        bool free_next = false;  // the next block's stage seen free by an earlier probe
-        for (int kb = kb0; kb < kb1; ++kb) {
+        bool free_next = false;  // the next stage seen free by an earlier probe
+        for (int kb = kb0; kb < kb1; kb += SUB) {
+          const int nsub = min(SUB, kb1 - kb);  // K blocks in this stage (fewer at a range's end)
           if (!free_next) {
             const int w = mbar_wait_or_abort(empty_bar(stage), phase ^ 1u, abort_flag, kWaitLimitNs);
             if (w <= 0) {
@@ -316,38 +331,45 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
           uint32_t nstage = stage + 1, nphase = phase;
           if (nstage == STAGES) { nstage = 0; nphase ^= 1u; }
           const uint32_t fb = full_leader + 8u * stage;
-          const uint32_t sa = smem_base + stage * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
-          // probe the next stage between this block's loads, as the MMA issuer does
-          const bool probe = p.load_probe != 0 && kb + 1 < kb1;
-          if (!do_a && probe) free_next = mbar_try_wait(empty_bar(nstage), nphase ^ 1u);
-          if (do_a) {
-            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
-            if (!A_MN) {
-              tma_load_2d_pair(sa, &p.tmA[kg], kk, arow, fb);
-            } else if (p.a3d) {
-              tma_load_3d_pair(sa, &p.tmA[kg], 0, kk, arow / 64, fb);
-            } else {
+          const uint32_t s0 = smem_base + stage * STAGE_BYTES;
+          // probe the next stage between the last block's loads, as the MMA issuer does
+          const bool probe = p.load_probe != 0 && kb + nsub < kb1;
+          if (!do_a && probe) free_next = mbar_test_wait(empty_bar(nstage), nphase ^ 1u);
+          if (do_a && rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * nsub * BLOCK_BYTES);
 #pragma unroll
-              for (int j = 0; j < HALF / 64; ++j)
-                tma_load_2d_pair(sa + j * MN_BOX_BYTES, &p.tmA[kg], arow + 64 * j, kk, fb);
-            }
-          }
-          if (do_a && probe) free_next = mbar_try_wait(empty_bar(nstage), nphase ^ 1u);
-          if (do_b) {
-            if (!B_MN) {
-              tma_load_2d_pair(sb, &p.tmB[kg], kk, bcol, fb);
-            } else if (p.b3d) {
-              tma_load_3d_pair(sb, &p.tmB[kg], 0, kk, bcol / 64, fb);
-            } else {
+          for (int j = 0; j < SUB; ++j) {
+            if (j < nsub) {
+              const uint32_t sa = s0 + j * BLOCK_BYTES;
+              const uint32_t sb = sa + A_BYTES;
+              if (do_a) {
+                if (!A_MN) {
+                  tma_load_2d_pair(sa, &p.tmA[kg], kk, arow, fb);
+                } else if (p.a3d) {
+                  tma_load_3d_pair(sa, &p.tmA[kg], 0, kk, arow / 64, fb);
+                } else {
 #pragma unroll
-              for (int j = 0; j < HALF / 64; ++j)
-                tma_load_2d_pair(sb + j * MN_BOX_BYTES, &p.tmB[kg], bcol + 64 * j, kk, fb);
+                  for (int c = 0; c < HALF / 64; ++c)
+                    tma_load_2d_pair(sa + c * MN_BOX_BYTES, &p.tmA[kg], arow + 64 * c, kk, fb);
+                }
+              }
+              if (do_a && probe && j == nsub - 1)
+                free_next = mbar_test_wait(empty_bar(nstage), nphase ^ 1u);
+              if (do_b) {
+                if (!B_MN) {
+                  tma_load_2d_pair(sb, &p.tmB[kg], kk, bcol, fb);
+                } else if (p.b3d) {
+                  tma_load_3d_pair(sb, &p.tmB[kg], 0, kk, bcol / 64, fb);
+                } else {
+#pragma unroll
+                  for (int c = 0; c < HALF / 64; ++c)
+                    tma_load_2d_pair(sb + c * MN_BOX_BYTES, &p.tmB[kg], bcol + 64 * c, kk, fb);
+                }
+              }
+              kk += BK;
+              if (kk == kend) { kk = 0; ++kg; }
             }
           }
           ++issued;
-          kk += BK;
-          if (kk == kend) { kk = 0; ++kg; }
           stage = nstage;
           phase = nphase;
         }
@@ -387,7 +409,8 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
         // current block's last MMA (its latency then hides behind the MMA issue instead of
         // adding to the gap between blocks)
         bool ready = false;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = kb0; kb < kb1; kb += SUB) {
+          const int nsub = min(SUB, kb1 - kb);
           if (!ready) {
             const int w = mbar_wait_or_abort(full_bar(stage), phase, abort_flag, kWaitLimitNs);
             if (w <= 0) {
@@ -402,17 +425,24 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
           tc::tc_fence_after();
           uint32_t nstage = stage + 1, nphase = phase;
           if (nstage == STAGES) { nstage = 0; nphase ^= 1u; }
-          const uint32_t sa = smem_base + stage * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
+          const uint32_t s0 = smem_base + stage * STAGE_BYTES;
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            if (k == BK / 16 - 1)
-              ready = p.mma_probe != 0 && kb + 1 < kb1 && mbar_try_wait(full_bar(nstage), nphase);
-            const uint64_t ad = A_MN ? tc::sdesc_sw128(sa + k * 2048, MN_BOX_BYTES, 1024)
-                                     : tc::sdesc_sw128(sa + k * 32, 16, 1024);
-            const uint64_t bd = B_MN ? tc::sdesc_sw128(sb + k * 2048, MN_BOX_BYTES, 1024)
-                                     : tc::sdesc_sw128(sb + k * 32, 16, 1024);
-            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+          for (int j = 0; j < SUB; ++j) {
+            if (j < nsub) {
+              const uint32_t sa = s0 + j * BLOCK_BYTES;
+              const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+              for (int k = 0; k < BK / 16; ++k) {
+                if (j == nsub - 1 && k == BK / 16 - 1)
+                  ready = p.mma_probe != 0 && kb + nsub < kb1 &&
+                          mbar_test_wait(full_bar(nstage), nphase);
+                const uint64_t ad = A_MN ? tc::sdesc_sw128(sa + k * 2048, MN_BOX_BYTES, 1024)
+                                         : tc::sdesc_sw128(sa + k * 32, 16, 1024);
+                const uint64_t bd = B_MN ? tc::sdesc_sw128(sb + k * 2048, MN_BOX_BYTES, 1024)
+                                         : tc::sdesc_sw128(sb + k * 32, 16, 1024);
+                umma_bf16_pair(d_tmem, ad, bd, idesc, (kb > kb0 || j > 0 || k > 0) ? 1u : 0u);
+              }
+            }
           }
           umma_commit_pair_multicast(empty_bar(stage), 0x3);
           stage = nstage;
@@ -503,10 +533,10 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
 }
 
 // Launch on clusters of two CTAs; max_clusters != nullptr asks for the occupancy limit only.
-template <bool A_MN, bool B_MN, int EPI_W>
+template <bool A_MN, bool B_MN, int EPI_W, int SUB>
 cudaError_t launch_pair(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters) {
   using E = EpiShape<EPI_W>;
-  auto kern = tc2_gemm_kernel<A_MN, B_MN, EPI_W>;
+  auto kern = tc2_gemm_kernel<A_MN, B_MN, EPI_W, SUB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, E::SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -534,6 +564,18 @@ cudaError_t launch_pair(const TcParams& p, int clusters, cudaStream_t st, int* m
   e = cudaLaunchKernelEx(&cfg, kern, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// The four instantiations of one operand layout: 4 or 8 epilogue warps, 1 or 2 K blocks per
+// ring stage.
+template <bool A_MN, bool B_MN>
+cudaError_t launch_pair_variant(const TcParams& p, int clusters, cudaStream_t st,
+                                int* max_clusters, int epi_warps, int sub) {
+  if (epi_warps == 8)
+    return sub == 2 ? launch_pair<A_MN, B_MN, 8, 2>(p, clusters, st, max_clusters)
+                    : launch_pair<A_MN, B_MN, 8, 1>(p, clusters, st, max_clusters);
+  return sub == 2 ? launch_pair<A_MN, B_MN, 4, 2>(p, clusters, st, max_clusters)
+                  : launch_pair<A_MN, B_MN, 4, 1>(p, clusters, st, max_clusters);
 }
 
 }  // namespace tc2

@@ -15,9 +15,8 @@ cudaError_t run_kk(const TcParams& p, int grid, cudaStream_t st) {
 // SM-pair kernel: clusters of two CTAs, 4 or 8 epilogue warps. max_clusters != nullptr asks
 // for the occupancy limit only.
 cudaError_t run_pair_kk(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters,
-                         int epi_warps) {
-  return epi_warps == 8 ? tc2::launch_pair<false, false, 8>(p, clusters, st, max_clusters)
-                        : tc2::launch_pair<false, false, 4>(p, clusters, st, max_clusters);
+                         int epi_warps, int sub) {
+  return tc2::launch_pair_variant<false, false>(p, clusters, st, max_clusters, epi_warps, sub);
 }
 
 }  // namespace tc

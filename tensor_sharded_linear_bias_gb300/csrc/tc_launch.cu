@@ -16,11 +16,11 @@ cudaError_t run_kmn(const TcParams& p, int grid, cudaStream_t st);
 cudaError_t run_kk(const TcParams& p, int grid, cudaStream_t st);
 cudaError_t run_mnmn(const TcParams& p, int grid, cudaStream_t st);
 cudaError_t run_pair_kmn(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters,
-                         int epi_warps);
+                         int epi_warps, int sub);
 cudaError_t run_pair_kk(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters,
-                        int epi_warps);
+                        int epi_warps, int sub);
 cudaError_t run_pair_mnmn(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters,
-                          int epi_warps);
+                          int epi_warps, int sub);
 }  // namespace tc
 
 namespace {
@@ -66,10 +66,26 @@ bool use_pair_kernel(int64_t M) {
 }
 
 cudaError_t run_pair(int layout, const tc::TcParams& p, int clusters, cudaStream_t st,
-                     int* max_clusters, int epi_warps) {
-  if (layout == 0) return tc::run_pair_kmn(p, clusters, st, max_clusters, epi_warps);
-  if (layout == 1) return tc::run_pair_kk(p, clusters, st, max_clusters, epi_warps);
-  return tc::run_pair_mnmn(p, clusters, st, max_clusters, epi_warps);
+                     int* max_clusters, int epi_warps, int sub = 1) {
+  if (layout == 0) return tc::run_pair_kmn(p, clusters, st, max_clusters, epi_warps, sub);
+  if (layout == 1) return tc::run_pair_kk(p, clusters, st, max_clusters, epi_warps, sub);
+  return tc::run_pair_mnmn(p, clusters, st, max_clusters, epi_warps, sub);
+}
+
+// K blocks per ring stage of the pair kernel (tc2::Ring). The single MMA-issuing thread needs
+// ~360 cycles to issue the four MMAs of a 64-deep block (~85 each, measured with cycle counters in
+// an instrumented copy) plus ~150 for the block's barrier look-ahead, wait and commit: about as
+// long as the 512 cycles the tensor pipe takes for the block, so the pipe idled ~15 %. Two blocks
+// per stage pay the barrier work once per 128; the coarser release (a stage is refilled only when
+// both blocks are consumed) costs more on short tiles. Measured on GB300, same box, alternating
+// (stage of 2 vs 1): GPT-3-shaped step 8.92-8.94 vs 9.18-9.33 ms (its forward and input-gradient
+// GEMMs 4-7 % faster, its weight gradients of 32 blocks 2 % slower); sweep T 16384 28.6 vs 30.0
+// ms (weight gradients of 256 blocks faster too); 4096 x 1024 x 4096 step slightly slower (tiles
+// of 16 blocks). So: 2 for tiles of at least 64 blocks (128 with both operands MN-major), else 1.
+// TP_TUNE_STAGE_BLOCKS overrides.
+int pair_sub_blocks(int layout, int total_kb) {
+  if (const int v = tuning(TP_TUNE_STAGE_BLOCKS); v != TP_TUNE_AUTO) return v == 2 ? 2 : 1;
+  return total_kb >= (layout == 2 ? 128 : 64) ? 2 : 1;
 }
 
 // Largest number of co-resident 2-CTA clusters of the pair kernel (cached per device, operand
@@ -358,7 +374,8 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
     p.mma_probe = mma_probe_enabled() ? 1 : 0;
     p.load_probe = load_probe_enabled(layout) ? 1 : 0;
     const int clusters = std::min(p.num_units, max_clusters);
-    return run_pair(layout, p, clusters, st, nullptr, epi_warps);
+    return run_pair(layout, p, clusters, st, nullptr, epi_warps,
+                    pair_sub_blocks(layout, p.kblocks * p.kpo));
   }
   const int grid = std::min(p.num_tiles, device_sm_count());
   if (!s.a_mn && s.b_mn) return run_kmn(p, grid, st);

@@ -184,7 +184,7 @@ def test_epilogue_warps(tp, tune, epi_warps, T, H, F, n):
 _ISSUE_VARIANTS = [{"split_loads": 1}, {"split_loads": 0},
                    {"mma_probe": 0, "load_probe": 0},
                    {"mma_probe": 1, "load_probe": 1},
-                   {"pdl": 1}, {"pdl": 0}]
+                   {"pdl": 1}, {"pdl": 0}, {"stage_blocks": 1}, {"stage_blocks": 2}]
 
 
 @pytest.mark.parametrize("epi_warps", ["4", "8"])
@@ -192,7 +192,8 @@ def test_issue_loop_variants(tp, tune, epi_warps):
     """The SM-pair kernel's issue loops in every variant: A and B loads from one producer thread
     or two (warp 0 and the last warp), with and without the early looks at the next block's
     barriers (MMA issuer and producers), launched with and without programmatic stream
-    serialisation (set-up overlapping the previous kernel), for all three operand layouts
+    serialisation (set-up overlapping the previous kernel), with one or two 64-deep K blocks
+    per operand-ring stage (odd K-block counts end on a half stage), for all three operand layouts
     (forward, input-gradient and
     weight-gradient GEMMs), ragged tiles, fused and overlapped shard sums.
     The default matches the oracle; every variant is bit-identical to it (they change which
@@ -216,8 +217,9 @@ def test_issue_loop_variants(tp, tune, epi_warps):
 _TAIL_REF = {}
 
 
+@pytest.mark.parametrize("stage_blocks", [1, 2])
 @pytest.mark.parametrize("reduce", [0, 2, 4])
-def test_tail_split(tp, tune, reduce):
+def test_tail_split(tp, tune, reduce, stage_blocks):
     """Tiles of a GEMM's partial last wave of SM pairs run as K pieces on the idle pairs and are
     added in piece order before the epilogue. Ragged tiles in M and N, ragged K per piece, and
     every epilogue (bias + GeLU, fused or grouped shard sum, overlapped sum, GeLU', plain fp32):
@@ -228,6 +230,7 @@ def test_tail_split(tp, tune, reduce):
     # 81-90 tiles of 256 x 256 per GEMM, K of 33-34 blocks: the tiles beyond the first wave of
     # pairs are split in two on a 76-pair GB300
     w = SMALL.with_shape(tokens=2080, hidden=2056, ffn=2 * 1040, tp_degree=2)
+    tune.set("stage_blocks", stage_blocks)   # pieces of odd K-block counts end on a half stage
     outs = {}
     for split in ("1", "0"):
         tune.set("tail_split", split)
