@@ -230,6 +230,18 @@ constexpr int kDeepTileKb = 64;
 // tiles is cut into S = clusters / L pieces of consecutive K blocks (capped by kMinPieceKb and
 // the kTailUnits pieces the workspace holds), which run side by side on the idle pairs: the
 // last wave takes about 1/S of a tile's time, plus the pieces' fp32 round trip through L2.
+// Pieces per split tile. The last wave takes about (tile time) / P for the pieces, plus the sum of
+// the P parked accumulators by the warp that completes a tile's count: it reads them from L2 two
+// at a time, 8 chunks of 32 columns each, ~3 us per piece (per-CTA timestamps on GB300: 19 pieces
+// of a 768-block tile ended 52-66 us after the other CTAs, 4 pieces of a 192-block tile ~30 us).
+// The sum tile/P + 3 P is smallest near P = sqrt(tile / 3 us), a 64-deep block taking ~0.28 us:
+// ~8 pieces for 768 blocks, ~4 for 192. TP_TUNE_TAIL_PIECES overrides the cap.
+int tail_pieces_cap(int total_kb) {
+  if (const int v = tuning(TP_TUNE_TAIL_PIECES); v != TP_TUNE_AUTO) return std::max(1, v);
+  const double tile_us = total_kb * 0.28;
+  return std::max(2, static_cast<int>(std::lround(std::sqrt(tile_us / 3.0))));
+}
+
 void plan_tail(tc::TcParams& p, int clusters, int total_kb, bool have_ws) {
   p.full_tiles = p.num_tiles;
   p.ksplit = 1;
@@ -243,6 +255,7 @@ void plan_tail(tc::TcParams& p, int clusters, int total_kb, bool have_ws) {
   int S = clusters / L;
   S = std::min(S, total_kb / kMinPieceKb);
   S = std::min(S, kTailUnits / L);
+  S = std::min(S, tail_pieces_cap(total_kb));
   if (S < 2) return;
   p.full_tiles = p.num_tiles - L;
   p.ksplit = S;
@@ -280,7 +293,8 @@ int plan_shard_split(int64_t M, int64_t N, int64_t K_per_group, int n) {
     if (L > 0 && (tiles <= kMaxSplitWaves * C || per_tile_kb >= kDeepTileKb) &&
         tail_split_enabled()) {
       const double P = std::min({std::floor(C / L), std::floor(per_tile_kb / kMinPieceKb),
-                                 std::floor(kTailUnits / L)});
+                                 std::floor(kTailUnits / L),
+                                 double(tail_pieces_cap(static_cast<int>(per_tile_kb)))});
       if (P >= 2) waves = std::floor(tiles / C) + 1.0 / P + 0.05;
     }
     double cost = waves * per_tile_kb * t_kb_us;
