@@ -48,9 +48,7 @@ typedef enum tp_tune_knob {
   TP_TUNE_STAGE_BLOCKS = 13, /* 1 or 2: 64-deep K blocks per operand-ring stage of the SM-pair
                                GEMM (6 stages of 64 or 3 of 128; bit-identical) */
   TP_TUNE_TAIL_PIECES = 14, /* upper bound (>= 1) on the K pieces of a split tail tile */
-  TP_TUNE_SKINNY = 15,      /* 0: fp32 GEMMs of at most 32 rows use the general FFMA kernel
-                               instead of the weight-streaming one */
-  TP_TUNE_COUNT = 16
+  TP_TUNE_COUNT = 15
 } tp_tune_knob;
 
 /* Sets knob to value (TP_TUNE_AUTO: the library's choice). TP_ERR_DTYPE for an unknown

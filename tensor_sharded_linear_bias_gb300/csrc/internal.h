@@ -72,10 +72,6 @@ struct GemmSpec {
 cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st);
 // fp32 inputs, FFMA (no TF32); kslices > 1 splits every tile's K steps over a cluster.
 cudaError_t launch_simt_gemm(const GemmSpec& s, cudaStream_t st);
-// fp32, at most 32 rows, A K-major, B MN-major, bias (+ GeLU) epilogue: the weight-streaming
-// kernel (skinny_gemm.cu). launch_simt_gemm uses it where skinny_gemm_applies.
-bool skinny_gemm_applies(const GemmSpec& s);
-cudaError_t launch_skinny_gemm(const GemmSpec& s, cudaStream_t st);
 // K slices (cluster size, <= 8) for an FFMA GEMM whose tiles alone would leave SMs idle
 // (1: no split). TP_TUNE_SIMT_SPLIT = 0 turns the split off.
 int plan_simt_split(const GemmSpec& s);

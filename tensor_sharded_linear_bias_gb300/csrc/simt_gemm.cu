@@ -357,7 +357,6 @@ int plan_simt_split(const GemmSpec& s) {
 cudaError_t launch_simt_gemm(const GemmSpec& s, cudaStream_t st) {
   if (s.M <= 0 || s.N <= 0 || s.K <= 0) return cudaSuccess;
   if (s.groups < 1 || s.groups > kMaxShards) return cudaErrorInvalidValue;
-  if (skinny_gemm_applies(s)) return launch_skinny_gemm(s, st);
   if (s.kslices < 1 || s.kslices > kMaxSplit) return cudaErrorInvalidValue;
   SimtParams p = make_params(s);
   p.slices = s.kslices;

@@ -588,60 +588,50 @@ def test_trace_records_every_launch(tp):
 @pytest.mark.parametrize("T,K,N,n", [
     (32, 768, 4 * 768, 4),     # the pages' example shapes (column: 4 x [768, 768])
     (1, 136, 4 * 72, 4),       # one token, ragged widths
-    (7, 3000, 2 * 1030, 2),    # K over 16 slices of at most 512, N % 4 != 0 (2 columns per lane)
+    (7, 3000, 2 * 1030, 2),    # long K split over a cluster, ragged N
     (32, 64, 8 * 40, 8),       # K too short to split
     (19, 1024, 1 * 520, 1),    # one shard
 ])
-def test_few_token_fp32_linears(tp, tune, T, K, N, n):
-    """fp32 products of at most 32 rows take the weight-streaming FFMA kernel (each lane all rows
-    x 2 or 4 columns, weights streamed into registers, K split over a cluster and summed in a fixed
-    order): the column linear with bias + GeLU (per-shard outputs, and gathered), the row linear
-    with the shard sum and its bias, against the oracle at the fp32 tolerance and against the
-    general FFMA kernel (knob skinny = 0); repeated calls bit-identical."""
+def test_few_token_fp32_linears(tp, T, K, N, n):
+    """fp32 linears over at most 32 tokens (the FFMA GEMM's K split over a cluster): the column
+    linear with bias + GeLU (per-shard outputs, and gathered into one buffer), the row linear
+    with the shard sum and its bias, against the oracle at the fp32 tolerance; repeated calls
+    bit-identical."""
     import torch
 
     t, f = _lin_inputs(57, T, K, N, "f32", "cuda")
     Ns, Ks = N // n, K // n if K % n == 0 else None
-    outs = {}
-    for skinny in (1, 0):
-        tune.set("skinny", skinny)
-        desc = tp.LinearDesc(tokens=T, in_features=K, out_features=N, tp_degree=n, dtype=tp.TP_F32,
-                             act=tp.TP_ACT_GELU_ERF, reduce=0, gather=0)
-        ws = tp.new_workspace(tp.tp_linear_workspace_size(desc, tp.TP_COLUMN))
-        W = [t["W"][:, i * Ns:(i + 1) * Ns].contiguous() for i in range(n)]
-        bias = [t["bias"][i * Ns:(i + 1) * Ns].contiguous() for i in range(n)]
-        Y = [torch.full((T, Ns), float("nan"), device="cuda") for _ in range(n)]
-        Hs = [torch.full((T, Ns), float("nan"), device="cuda") for _ in range(n)]
-        tp.tp_linear_column_forward(desc, t["X"], W, bias, Y, Hs, ws)
-        gdesc = tp.LinearDesc(tokens=T, in_features=K, out_features=N, tp_degree=n, dtype=tp.TP_F32,
-                              act=tp.TP_ACT_GELU_ERF, reduce=0, gather=1)
-        Yg = torch.full((T, N), float("nan"), device="cuda")
-        tp.tp_linear_column_forward(gdesc, t["X"], W, bias, [Yg], None, ws)
-        rec = {"Y": [np64(y) for y in Y], "H": [np64(h) for h in Hs], "Yg": np64(Yg)}
-        if Ks is not None:
-            rdesc = tp.LinearDesc(tokens=T, in_features=K, out_features=N, tp_degree=n,
-                                  dtype=tp.TP_F32, act=0, reduce=0, gather=0)
-            Xs = [t["X"][:, i * Ks:(i + 1) * Ks].contiguous() for i in range(n)]
-            Wr = [t["W"][i * Ks:(i + 1) * Ks, :].contiguous() for i in range(n)]
-            Z = torch.full((T, N), float("nan"), device="cuda")
-            tp.tp_linear_row_forward(rdesc, Xs, Wr, t["bias"], Z, ws)
-            Z2 = torch.empty_like(Z)
-            tp.tp_linear_row_forward(rdesc, Xs, Wr, t["bias"], Z2, ws)
-            tp.tp_check_status(ws)
-            torch.cuda.synchronize()
-            assert torch.equal(Z, Z2)
-            rec["Z"] = np64(Z)
-        tp.tp_check_status(ws)
-        torch.cuda.synchronize()
-        outs[skinny] = rec
-
+    desc = tp.LinearDesc(tokens=T, in_features=K, out_features=N, tp_degree=n, dtype=tp.TP_F32,
+                         act=tp.TP_ACT_GELU_ERF, reduce=0, gather=0)
+    ws = tp.new_workspace(tp.tp_linear_workspace_size(desc, tp.TP_COLUMN))
+    W = [t["W"][:, i * Ns:(i + 1) * Ns].contiguous() for i in range(n)]
+    bias = [t["bias"][i * Ns:(i + 1) * Ns].contiguous() for i in range(n)]
+    Y = [torch.full((T, Ns), float("nan"), device="cuda") for _ in range(n)]
+    Hs = [torch.full((T, Ns), float("nan"), device="cuda") for _ in range(n)]
+    tp.tp_linear_column_forward(desc, t["X"], W, bias, Y, Hs, ws)
+    gdesc = tp.LinearDesc(tokens=T, in_features=K, out_features=N, tp_degree=n, dtype=tp.TP_F32,
+                          act=tp.TP_ACT_GELU_ERF, reduce=0, gather=1)
+    Yg = torch.full((T, N), float("nan"), device="cuda")
+    Hg = [torch.empty(T, Ns, device="cuda") for _ in range(n)]
+    tp.tp_linear_column_forward(gdesc, t["X"], W, bias, [Yg], Hg, ws)
     Wc = oracle.split_columns(f["W"], n)
     Hr, Yr = oracle.column_parallel_forward(f["X"], Wc, oracle.split_vector(f["bias"], n), "gelu")
-    a, b = outs[1], outs[0]
-    assert rel_shards(a["Y"], Yr) <= TOL_F32 and rel_shards(a["H"], Hr) <= TOL_F32
-    assert rel(a["Yg"], oracle.concat_columns(Yr)) <= TOL_F32
-    assert rel_shards(a["Y"], b["Y"]) <= TOL_F32 and rel(a["Yg"], b["Yg"]) <= TOL_F32
     if Ks is not None:
+        rdesc = tp.LinearDesc(tokens=T, in_features=K, out_features=N, tp_degree=n,
+                              dtype=tp.TP_F32, act=0, reduce=0, gather=0)
+        Xs = [t["X"][:, i * Ks:(i + 1) * Ks].contiguous() for i in range(n)]
+        Wr = [t["W"][i * Ks:(i + 1) * Ks, :].contiguous() for i in range(n)]
+        Z = torch.full((T, N), float("nan"), device="cuda")
+        tp.tp_linear_row_forward(rdesc, Xs, Wr, t["bias"], Z, ws)
+        Z2 = torch.empty_like(Z)
+        tp.tp_linear_row_forward(rdesc, Xs, Wr, t["bias"], Z2, ws)
+    tp.tp_check_status(ws)
+    torch.cuda.synchronize()
+    assert rel_shards([np64(y) for y in Y], Yr) <= TOL_F32
+    assert rel_shards([np64(h) for h in Hs], Hr) <= TOL_F32
+    assert rel(np64(Yg), oracle.concat_columns(Yr)) <= TOL_F32
+    if Ks is not None:
+        assert torch.equal(Z, Z2)
         Zr = oracle.row_parallel_forward(oracle.split_columns(f["X"], n), oracle.split_rows(f["W"], n),
                                          f["bias"])
-        assert rel(a["Z"], Zr) <= TOL_F32 and rel(a["Z"], b["Z"]) <= TOL_F32
+        assert rel(np64(Z), Zr) <= TOL_F32
