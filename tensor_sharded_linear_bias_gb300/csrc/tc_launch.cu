@@ -372,9 +372,21 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
   p.ksplit = 1;
   p.num_units = p.num_tiles;
   if (pair) {
-    const int epi_warps = pair_epi_warps(p.epi, p.act, p.kblocks * p.kpo);
-    const int max_clusters = pair_clusters(layout, epi_warps);
+    int epi_warps = pair_epi_warps(p.epi, p.act, p.kblocks * p.kpo);
+    int max_clusters = pair_clusters(layout, epi_warps);
     plan_tail(p, max_clusters, p.kblocks * p.kpo, s.tail_ws != nullptr && s.tail_counters != nullptr);
+    // 8 epilogue warps also where the epilogue work is exposed at the end of the launch: split
+    // tail tiles, whose pieces the completing warps sum (with 8 warps each sums half as many
+    // columns), and launches of at most one tile per pair (no next tile hides the epilogue).
+    // Measured on GB300, same box: the GPT-3-shaped forward and input-gradient GEMMs 1-2 %
+    // faster, the 4096 x 1024 x 4096 step 0.2317 vs 0.2346 ms.
+    if (epi_warps == 4 && tuning(TP_TUNE_EPI_WARPS) == TP_TUNE_AUTO &&
+        (p.ksplit > 1 || p.num_units <= max_clusters)) {
+      epi_warps = 8;
+      max_clusters = pair_clusters(layout, epi_warps);
+      if (p.ksplit > 1 && max_clusters != pair_clusters(layout, 4))
+        plan_tail(p, max_clusters, p.kblocks * p.kpo, true);
+    }
     if (p.ksplit > 1) {
       p.tail_ws = s.tail_ws;
       p.tail_counters = s.tail_counters;
