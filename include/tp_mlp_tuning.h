@@ -4,8 +4,8 @@
  * The library picks, per launch, among kernel variants by measurement on GB300: SM-pair or
  * one-SM tensor-core GEMM, 4 or 8 epilogue warps, tile order, one 3-D or several 2-D TMA
  * boxes, one or two producer threads, the issue loops' barrier probes, the K split of a
- * last partial wave, the shard-sum grouping, the fp32 GEMM's K split over a cluster, and the
- * LayerNorm kernels. Every variant computes the same operation (none of them is a different
+ * last partial wave, the shard-sum grouping, the fp32 GEMM kernel for few rows and its K split
+ * over a cluster, and the LayerNorm kernels. Every variant computes the same operation (none of them is a different
  * reading of the pages); those marked "bit-identical" give the same bits as the default, the
  * others differ from it only in the fp32 summation order. The tests pin each variant against
  * the default and the oracle through this hook, and A/B timings use it.
@@ -48,7 +48,9 @@ typedef enum tp_tune_knob {
   TP_TUNE_STAGE_BLOCKS = 13, /* 1 or 2: 64-deep K blocks per operand-ring stage of the SM-pair
                                GEMM (6 stages of 64 or 3 of 128; bit-identical) */
   TP_TUNE_TAIL_PIECES = 14, /* upper bound (>= 1) on the K pieces of a split tail tile */
-  TP_TUNE_COUNT = 15
+  TP_TUNE_FEW_ROWS = 15,    /* 0: fp32 products of <= 32 rows on the general FFMA kernel instead
+                               of the bulk-copy one (forward layouts) */
+  TP_TUNE_COUNT = 16
 } tp_tune_knob;
 
 /* Sets knob to value (TP_TUNE_AUTO: the library's choice). TP_ERR_DTYPE for an unknown

@@ -55,7 +55,7 @@ TP_TUNE_AUTO = -1
 TUNE_KNOBS = {
     "gemm_pair": 0, "epi_warps": 1, "raster": 2, "tma_3d": 3, "split_loads": 4,
     "mma_probe": 5, "load_probe": 6, "tail_split": 7, "tail_waves": 8, "shard_split": 9,
-    "simt_split": 10, "ln_reg": 11, "pdl": 12, "stage_blocks": 13, "tail_pieces": 14,
+    "simt_split": 10, "ln_reg": 11, "pdl": 12, "stage_blocks": 13, "tail_pieces": 14, "few_rows": 15,
 }
 
 _HERE = os.path.dirname(os.path.abspath(__file__))

@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "tp_mlp.h"
@@ -72,6 +73,15 @@ struct GemmSpec {
 cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st);
 // fp32 inputs, FFMA (no TF32); kslices > 1 splits every tile's K steps over a cluster.
 cudaError_t launch_simt_gemm(const GemmSpec& s, cudaStream_t st);
+// Tensor map of a 2-D fp32 row-major array [outer][inner] (row pitch ld elements), no swizzle,
+// box box_outer x box_inner; false if the driver rejects it (alignment, sizes).
+bool encode_f32_rows(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
+                     uint32_t box_inner, uint32_t box_outer);
+// fp32 FFMA GEMM for at most 32 rows with bulk-copied operands (forward layouts: A K-major, B
+// N-contiguous; K % 64 == 0, N % 4 == 0, 16-byte aligned rows; epilogue bias (+ act) only).
+// few_rows_eligible says whether s fits it (and TP_TUNE_FEW_ROWS is not 0).
+bool few_rows_eligible(const GemmSpec& s);
+cudaError_t launch_few_rows_gemm(const GemmSpec& s, cudaStream_t st);
 // K slices (cluster size, <= 8) for an FFMA GEMM whose tiles alone would leave SMs idle
 // (1: no split). TP_TUNE_SIMT_SPLIT = 0 turns the split off.
 int plan_simt_split(const GemmSpec& s);

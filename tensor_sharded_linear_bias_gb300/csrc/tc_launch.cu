@@ -44,18 +44,70 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Tensor maps are encoded on the host for every launch; a launch of a few microseconds (few
+// tokens) would otherwise wait for its encodes (~1 us each). So each thread keeps the maps it
+// made, keyed by everything that goes into them (a map holds only the address, shape, strides,
+// box and modes, so a hit is exactly the map a new encode would give), in a small
+// direct-mapped table.
+struct MapKey {
+  const void* ptr;
+  cuuint64_t dims[3];
+  cuuint64_t strides[2];
+  cuuint32_t box[3];
+  uint32_t rank;
+  int dtype, swizzle;
+  bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
+};
+
+bool encode_cached(CUtensorMap* m, CUtensorMapDataType dtype, uint32_t rank, const void* ptr,
+                   const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                   CUtensorMapSwizzle swizzle) {
+  MapKey k;
+  std::memset(&k, 0, sizeof(k));  // padding too: keys compare byte for byte
+  k.ptr = ptr;
+  for (uint32_t i = 0; i < rank; ++i) {
+    k.dims[i] = dims[i];
+    k.box[i] = box[i];
+    if (i + 1 < rank) k.strides[i] = strides[i];
+  }
+  k.rank = rank;
+  k.dtype = static_cast<int>(dtype);
+  k.swizzle = static_cast<int>(swizzle);
+  uint64_t h = 1469598103934665603ull;  // FNV-1a over the key's bytes
+  const unsigned char* b = reinterpret_cast<const unsigned char*>(&k);
+  for (size_t i = 0; i < sizeof(k); ++i) h = (h ^ b[i]) * 1099511628211ull;
+  struct Entry {
+    bool valid = false;
+    MapKey key;
+    CUtensorMap map;
+  };
+  static thread_local Entry table[256];
+  Entry& e = table[h & 255u];
+  if (e.valid && e.key == k) {
+    *m = e.map;
+    return true;
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (fn(m, dtype, rank, const_cast<void*>(ptr), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  e.valid = true;
+  e.key = k;
+  e.map = *m;
+  return true;
+}
+
 // 2-D bf16 row-major tensor [outer][inner] with row pitch ld (elements), 128B swizzle.
 bool encode_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
                  uint32_t box_inner, uint32_t box_outer) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {ld * 2};
   const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // The SM-pair kernel computes 256-row tiles; below that the one-SM kernel's 128-row tiles
@@ -169,15 +221,12 @@ int choose_raster(int tiles_m, int tiles_n, int64_t k_total, int sms, bool pair)
 // partial last chunk would read past the rows). Returns false if the driver refuses it.
 bool encode_bf16_mn3d(CUtensorMap* m, const void* ptr, uint64_t mn, uint64_t k, uint64_t ld,
                       uint32_t chunks) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr || mn % 64 != 0) return false;
+  if (mn % 64 != 0) return false;
   const cuuint64_t dims[3] = {64, k, mn / 64};
   const cuuint64_t strides[2] = {ld * 2, 128};
   const cuuint32_t box[3] = {64, 64, chunks};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // One-load MN-major tiles (3-D maps); TP_TUNE_TMA_3D = 0 keeps the 2-D boxes.
@@ -263,6 +312,19 @@ void plan_tail(tc::TcParams& p, int clusters, int total_kb, bool have_ws) {
 }
 
 }  // namespace
+
+// 2-D fp32 row-major tensor [outer][inner] with row pitch ld (elements), no swizzle: a box
+// lands in shared memory as box_outer rows of box_inner consecutive floats; elements outside
+// the tensor read as zeros.
+bool encode_f32_rows(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
+                     uint32_t box_inner, uint32_t box_outer) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {ld * 4};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  return encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 
 int plan_shard_split(int64_t M, int64_t N, int64_t K_per_group, int n) {
   using namespace tc;

@@ -235,6 +235,9 @@ cudaError_t run_gemm(const GemmSpec& s, int dtype, cudaStream_t st, int tag) {
   gemm_work(s, dtype, &flops, &bytes);
   if (dtype == TP_BF16)
     return traced(TP_K_GEMM_TC, tag, s.groups, flops, bytes, st, [&] { return launch_tc_gemm(s, st); });
+  if (few_rows_eligible(s))
+    return traced(TP_K_GEMM_FFMA, tag, s.groups, flops, bytes, st,
+                  [&] { return launch_few_rows_gemm(s, st); });
   GemmSpec t = s;
   t.kslices = plan_simt_split(s);
   return traced(TP_K_GEMM_FFMA, tag, s.groups, flops, bytes, st,

@@ -585,19 +585,27 @@ def test_trace_records_every_launch(tp):
 
 
 # ----------------------------------------------------------------------------- few-token fp32
+@pytest.mark.parametrize("few_rows", [None, 0], ids=["auto", "general"])
 @pytest.mark.parametrize("T,K,N,n", [
     (32, 768, 4 * 768, 4),     # the pages' example shapes (column: 4 x [768, 768])
-    (1, 136, 4 * 72, 4),       # one token, ragged widths
+    (1, 136, 4 * 72, 4),       # one token, ragged widths (K % 64 != 0: general kernel)
     (7, 3000, 2 * 1030, 2),    # long K split over a cluster, ragged N
     (32, 64, 8 * 40, 8),       # K too short to split
     (19, 1024, 1 * 520, 1),    # one shard
+    (17, 640, 2 * 264, 2),     # ragged column tiles (264 = 4 x 64 + 8)
+    (32, 4096, 4 * 256, 4),    # many K chunks per slice: the operand ring wraps
+    (1, 64, 64, 1),            # one chunk, one tile, one token
 ])
-def test_few_token_fp32_linears(tp, T, K, N, n):
-    """fp32 linears over at most 32 tokens (the FFMA GEMM's K split over a cluster): the column
+def test_few_token_fp32_linears(tp, tune, T, K, N, n, few_rows):
+    """fp32 linears over at most 32 tokens (the bulk-copy few-row kernel where the shapes fit it,
+    else the FFMA GEMM's K split over a cluster; `general` forces the latter): the column
     linear with bias + GeLU (per-shard outputs, and gathered into one buffer), the row linear
     with the shard sum and its bias, against the oracle at the fp32 tolerance; repeated calls
     bit-identical."""
     import torch
+
+    if few_rows is not None:
+        tune.set("few_rows", few_rows)
 
     t, f = _lin_inputs(57, T, K, N, "f32", "cuda")
     Ns, Ks = N // n, K // n if K % n == 0 else None
