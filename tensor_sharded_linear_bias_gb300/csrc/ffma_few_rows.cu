@@ -365,18 +365,8 @@ cudaError_t launch_few_rows_gemm(const GemmSpec& s, cudaStream_t st) {
   p.slices = static_cast<int>(S);
   p.status = s.status;
 
-  // the shared-memory opt-in, once per device (a driver call per launch costs a few-token
-  // step measurable host time)
-  static bool opted_in[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = opt_in_dynamic_smem(reinterpret_cast<const void*>(few_rows_gemm_kernel), kFrSmem);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !opted_in[dev]) {
-    e = cudaFuncSetAttribute(few_rows_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kFrSmem);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) opted_in[dev] = true;
-  }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(S), static_cast<unsigned>(col_tiles),
                      static_cast<unsigned>(outs));

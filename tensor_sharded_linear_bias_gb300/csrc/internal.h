@@ -73,6 +73,11 @@ struct GemmSpec {
 cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st);
 // fp32 inputs, FFMA (no TF32); kslices > 1 splits every tile's K steps over a cluster.
 cudaError_t launch_simt_gemm(const GemmSpec& s, cudaStream_t st);
+// The dynamic shared memory opt-in (cudaFuncSetAttribute) of kernel `kern` for at least
+// `bytes` on the current device, made once per kernel and device: a driver call on every
+// launch costs a few-microsecond launch measurable host time.
+cudaError_t opt_in_dynamic_smem(const void* kern, int bytes);
+
 // Tensor map of a 2-D fp32 row-major array [outer][inner] (row pitch ld elements), no swizzle,
 // box box_outer x box_inner; false if the driver rejects it (alignment, sizes).
 bool encode_f32_rows(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,

@@ -269,8 +269,7 @@ SimtParams make_params(const GemmSpec& s) {
 template <int TM>
 cudaError_t launch(const SimtParams& p, dim3 grid, cudaStream_t st) {
   constexpr int smem = static_cast<int>(sizeof(SimtSmem<TM>));  // > 48 KiB: opt in
-  cudaError_t e =
-      cudaFuncSetAttribute(simt_gemm_kernel<TM>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = opt_in_dynamic_smem(reinterpret_cast<const void*>(simt_gemm_kernel<TM>), smem);
   if (e != cudaSuccess) return e;
   if (p.slices > 8) {
     e = cudaFuncSetAttribute(simt_gemm_kernel<TM>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);

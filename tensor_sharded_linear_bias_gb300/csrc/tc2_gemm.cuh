@@ -537,7 +537,7 @@ template <bool A_MN, bool B_MN, int EPI_W, int SUB>
 cudaError_t launch_pair(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters) {
   using E = EpiShape<EPI_W>;
   auto kern = tc2_gemm_kernel<A_MN, B_MN, EPI_W, SUB>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, E::SMEM);
+  cudaError_t e = opt_in_dynamic_smem(reinterpret_cast<const void*>(kern), E::SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];

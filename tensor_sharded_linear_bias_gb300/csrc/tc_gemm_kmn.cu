@@ -6,7 +6,7 @@ namespace tc {
 
 cudaError_t run_kmn(const TcParams& p, int grid, cudaStream_t st) {
   auto kern = tc_gemm_kernel<false, true>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  cudaError_t e = opt_in_dynamic_smem(reinterpret_cast<const void*>(kern), SMEM_BYTES);
   if (e != cudaSuccess) return e;
   kern<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(p);
   return cudaGetLastError();

@@ -313,6 +313,29 @@ void plan_tail(tc::TcParams& p, int clusters, int total_kb, bool have_ws) {
 
 }  // namespace
 
+cudaError_t opt_in_dynamic_smem(const void* kern, int bytes) {
+  struct Entry {
+    const void* kern;
+    int dev, bytes;
+  };
+  static std::mutex mu;
+  static Entry done[256];
+  static int n_done = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_done; ++i)
+      if (done[i].kern == kern && done[i].dev == dev && done[i].bytes >= bytes) return cudaSuccess;
+  }
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (n_done < 256) done[n_done++] = {kern, dev, bytes};
+  return cudaSuccess;
+}
+
 // 2-D fp32 row-major tensor [outer][inner] with row pitch ld (elements), no swizzle: a box
 // lands in shared memory as box_outer rows of box_inner consecutive floats; elements outside
 // the tensor read as zeros.
