@@ -321,6 +321,8 @@ bool few_rows_eligible(const GemmSpec& s) {
   if (s.epi != EPI_STORE_F32 && s.epi != EPI_BIAS_ACT) return false;
   if (s.K % kFrChunk != 0 || s.N % 4 != 0 || s.lda % 4 != 0 || s.ldb % 4 != 0) return false;
   if (s.groups < 1 || s.groups > kMaxShards) return false;
+  // outputs: one per group, or one sum of all groups (no partial grouping)
+  if (s.kpo > 1 && !(s.ksum && s.kpo == s.groups)) return false;
   if ((s.N + kFrCols - 1) / kFrCols > 65535) return false;
   for (int g = 0; g < s.groups; ++g)
     if (!aligned16(s.A[g]) || !aligned16(s.B[g]) || !aligned16(s.bias[g])) return false;
