@@ -1066,6 +1066,13 @@ def main():
     pk = peaks()
     roof, kernels = roofline_from_trace(recs, pk, w.name, clocks=clocks)
     peak, regime, _ = tensor_peak(pk, clocks)
+    # the whole step's algorithmic bytes (every launch's operands once, outputs once) per
+    # second, cold and warm L2: the HBM view of a latency-bound step (the pages' batch-32 case)
+    step_bytes = sum(r["bytes"] for r in recs) / args.steps
+    step_hbm = {"bytes_per_step": step_bytes,
+                "cold_gbs": step_bytes / (ms / args.steps / 1e3) / 1e9,
+                "warm_gbs": (step_bytes / (warm["ms_per_step"] / 1e3) / 1e9) if warm else None,
+                "peak": pk["hbm_gbs"], "unit": "GB/s"}
 
     cpu = None
     if keep_host:
@@ -1091,6 +1098,7 @@ def main():
         "clocks": clocks,
         "e2e": e2e,
         "warm_l2": warm,
+        "step_hbm_view": step_hbm,
         "gpu_launches": len(recs),
         "gpu_launches_per_step": len(recs) / args.steps,
         "roofline": roof,
