@@ -477,10 +477,13 @@ def make_flush(device, operand_bytes: int):
     return f, f.describe()
 
 
-def time_steps(fn, steps: int, world: int, flush=None):
+def time_steps(fn, steps: int, world: int, flush=None, host_ahead: bool = False):
     """Device time of `steps` calls of fn (ms), barrier + synchronize on both sides. Without a
     flush: one event pair around all steps. With one: flush, then an event pair around each
-    step; the sum of the steps' times."""
+    step; the sum of the steps' times. host_ahead (no flush): a sleep kernel runs on the stream
+    before the start event while the host enqueues every step, so that a step whose host-side
+    enqueue takes longer than its device time (a few-token step) is timed on the device, not
+    on the host."""
     import torch
 
     barrier(world)
@@ -488,6 +491,8 @@ def time_steps(fn, steps: int, world: int, flush=None):
     if flush is None:
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
+        if host_ahead and hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(int(2e6 * (1.0 + 0.2 * steps)))  # ~1 ms + 0.2 ms per step at 2 GHz
         start.record()
         for _ in range(steps):
             fn()
@@ -1036,10 +1041,11 @@ def main():
     # ---- the same steps with L2 left warm between them (only where the timed ones flush it)
     warm = None
     if flush is not None:
-        ms_w, value_w = replica_throughput(mb.flops, args.steps,
-                                           time_steps(mb.step, args.steps, world), world)
+        ms_w, value_w = replica_throughput(
+            mb.flops, args.steps, time_steps(mb.step, args.steps, world, host_ahead=True), world)
         warm = {"value": value_w, "unit": UNIT, "ms_per_step": ms_w / args.steps,
-                "l2": "not flushed: operands stay in L2 from step to step"}
+                "l2": "not flushed: operands stay in L2 from step to step; the steps are "
+                      "enqueued behind a sleep kernel, so the host's enqueue time is not in it"}
 
     # ---- end to end: host inputs in, host results out, every step
     e2e = None
