@@ -593,7 +593,8 @@ def test_trace_records_every_launch(tp):
     (32, 64, 8 * 40, 8),       # K too short to split
     (19, 1024, 1 * 520, 1),    # one shard
     (17, 640, 2 * 264, 2),     # ragged column tiles (264 = 4 x 64 + 8)
-    (32, 4096, 4 * 256, 4),    # many K chunks per slice: the operand ring wraps
+    (32, 4096, 4 * 256, 4),    # 8 K chunks per slice: the whole operand ring
+    (8, 8192, 64, 1),          # 16 K chunks per slice: the operand ring wraps twice
     (1, 64, 64, 1),            # one chunk, one tile, one token
 ])
 def test_few_token_fp32_linears(tp, tune, T, K, N, n, few_rows):
@@ -643,3 +644,42 @@ def test_few_token_fp32_linears(tp, tune, T, K, N, n, few_rows):
         Zr = oracle.row_parallel_forward(oracle.split_columns(f["X"], n), oracle.split_rows(f["W"], n),
                                          f["bias"])
         assert rel(np64(Z), Zr) <= TOL_F32
+
+
+@pytest.mark.parametrize("T,K,N,n", [(32, 768, 4 * 768, 4), (5, 1024, 2 * 264, 2)])
+def test_few_token_fp32_no_bias_no_act(tp, tune, T, K, N, n):
+    """The few-row fp32 kernel's other epilogues: the column linear without bias or
+    activation, the row linear without bias (shard sum and per-shard partials), against the
+    oracle at the fp32 tolerance, and bit-identical to themselves on a second call."""
+    import torch
+
+    t, f = _lin_inputs(91, T, K, N, "f32", "cuda")
+    Ns, Ks = N // n, K // n
+    desc = tp.LinearDesc(tokens=T, in_features=K, out_features=N, tp_degree=n, dtype=tp.TP_F32,
+                         act=0, reduce=0, gather=0)
+    ws = tp.new_workspace(max(tp.tp_linear_workspace_size(desc, tp.TP_COLUMN),
+                              tp.tp_linear_workspace_size(
+                                  tp.LinearDesc(tokens=T, in_features=K, out_features=N,
+                                                tp_degree=n, dtype=tp.TP_F32, act=0, reduce=1,
+                                                gather=0), tp.TP_ROW)))
+    W = [t["W"][:, i * Ns:(i + 1) * Ns].contiguous() for i in range(n)]
+    Y = [torch.full((T, Ns), float("nan"), device="cuda") for _ in range(n)]
+    tp.tp_linear_column_forward(desc, t["X"], W, None, Y, None, ws)
+    Wc = oracle.split_columns(f["W"], n)
+    _, Yr = oracle.column_parallel_forward(f["X"], Wc, None, "none")
+    Xs = [t["X"][:, i * Ks:(i + 1) * Ks].contiguous() for i in range(n)]
+    Wr = [t["W"][i * Ks:(i + 1) * Ks, :].contiguous() for i in range(n)]
+    Zr = oracle.row_parallel_forward(oracle.split_columns(f["X"], n), oracle.split_rows(f["W"], n),
+                                     None)
+    for reduce in (0, 1):
+        rdesc = tp.LinearDesc(tokens=T, in_features=K, out_features=N, tp_degree=n,
+                              dtype=tp.TP_F32, act=0, reduce=reduce, gather=0)
+        Z = torch.full((T, N), float("nan"), device="cuda")
+        tp.tp_linear_row_forward(rdesc, Xs, Wr, None, Z, ws)
+        Z2 = torch.empty_like(Z)
+        tp.tp_linear_row_forward(rdesc, Xs, Wr, None, Z2, ws)
+        tp.tp_check_status(ws)
+        torch.cuda.synchronize()
+        assert torch.equal(Z, Z2), reduce
+        assert rel(np64(Z), Zr) <= TOL_F32, reduce
+    assert rel_shards([np64(y) for y in Y], Yr) <= TOL_F32
