@@ -30,7 +30,8 @@ extern "C" {
 
 typedef enum tp_tune_knob {
   TP_TUNE_GEMM_PAIR = 0,    /* 0: one-SM tcgen05 GEMM, 1: SM pairs (default: pairs when M > 128) */
-  TP_TUNE_EPI_WARPS = 1,    /* 4 or 8 epilogue warps in the SM-pair GEMM (bit-identical) */
+  TP_TUNE_EPI_WARPS = 1,    /* 4, 8 or 12 epilogue warps in the SM-pair GEMM (bit-identical;
+                               12: whole tiles only, one K block per ring stage) */
   TP_TUNE_RASTER = 2,       /* tile order inside an output: 0 m fastest, 1 n fastest (bit-identical) */
   TP_TUNE_TMA_3D = 3,       /* 0/1: MN-major operands as 2-D boxes / one 3-D box (bit-identical) */
   TP_TUNE_SPLIT_LOADS = 4,  /* 0/1: A and B loads from one / two producer threads (bit-identical) */

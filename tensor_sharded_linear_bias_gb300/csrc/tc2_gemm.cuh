@@ -46,26 +46,34 @@ constexpr int RING_BLOCKS = 6;                  // K blocks the operand ring hol
 // blocks; the price is a coarser release (a stage is refilled only when all its blocks are
 // consumed). Inside a stage, block j sits at j * BLOCK_BYTES with the layout of a one-block
 // stage, so TMA boxes and MMA descriptors are the same for both.
-template <int SUB>
+template <int SUB, int BLOCKS = RING_BLOCKS>
 struct Ring {
   static_assert(SUB == 1 || SUB == 2, "1 or 2 K blocks per stage");
-  static constexpr int STAGES = RING_BLOCKS / SUB;
+  static_assert(BLOCKS % SUB == 0, "whole stages");
+  static constexpr int STAGES = BLOCKS / SUB;
   static constexpr int STAGE_BYTES = SUB * BLOCK_BYTES;
 };
 constexpr int MN_BOX_BYTES = 64 * BK * 2;    // 8 KiB
 // Warp 0: TMA producer (A); warp 1: MMA issuer; warps 2..: EPI_W epilogue warps; the last
 // warp: TMA producer (B), so that no single thread's issue loop paces the ring. A warp may only
 // read the 32 TMEM lanes of quadrant warp % 4, so with 4 epilogue warps each takes all 256
-// columns of its 32 rows, and with 8 two warps share a quadrant and take 128 columns each
-// (for epilogue-heavy tiles, GeLU or GeLU', whose K loops are too short to hide 4 warps' work).
+// columns of its 32 rows, with 8 two warps share a quadrant and take 128 columns each (for
+// epilogue-heavy tiles, GeLU or GeLU', whose K loops are too short to hide 4 warps' work), and
+// with 12 three warps take 96, 96 and 64 columns (their 12 staging buffers leave room for a
+// ring of 5 K blocks; whole tiles only, no split tail pieces).
 template <int EPI_W>
 struct EpiShape {
-  static_assert(EPI_W == 4 || EPI_W == 8, "4 or 8 epilogue warps");
+  static_assert(EPI_W == 4 || EPI_W == 8 || EPI_W == 12, "4, 8 or 12 epilogue warps");
   static constexpr int WARPS = EPI_W;
-  static constexpr int COLS = BN * 4 / EPI_W;  // columns per epilogue warp
+  static constexpr int PER_QUAD = EPI_W / 4;  // warps sharing a TMEM quadrant
+  // columns of the warp that is j-th in its quadrant (the largest: COLS)
+  static constexpr int COLS = EPI_W == 12 ? 96 : BN * 4 / EPI_W;
+  __device__ static int cofs(int j) { return j * COLS; }
+  __device__ static int ncols(int j) { return j == PER_QUAD - 1 ? BN - j * COLS : COLS; }
   static constexpr int B_WARP = 2 + EPI_W;         // the B producer, after the epilogue warps
   static constexpr int THREADS = 96 + 32 * EPI_W;
-  static constexpr int SMEM = RING_BLOCKS * BLOCK_BYTES + EPI_W * tc::STAGE_WARP_BYTES + 1024 + 256;
+  static constexpr int RING = EPI_W == 12 ? 5 : RING_BLOCKS;  // K blocks of the operand ring
+  static constexpr int SMEM = RING * BLOCK_BYTES + EPI_W * tc::STAGE_WARP_BYTES + 1024 + 256;
 };
 constexpr int NUM_BARS = 2 * RING_BLOCKS + 2 * ACC_BUFS + 1;  // sized for the most stages
 
@@ -234,12 +242,13 @@ template <bool A_MN, bool B_MN, int EPI_W, int SUB>
 __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ TcParams p) {
   using E = EpiShape<EPI_W>;
-  constexpr int STAGES = Ring<SUB>::STAGES;
-  constexpr int STAGE_BYTES = Ring<SUB>::STAGE_BYTES;
+  constexpr int RB = E::RING;
+  constexpr int STAGES = Ring<SUB, RB>::STAGES;
+  constexpr int STAGE_BYTES = Ring<SUB, RB>::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* epi_stage = smem + RING_BLOCKS * BLOCK_BYTES;
+  uint8_t* epi_stage = smem + RB * BLOCK_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + E::WARPS * tc::STAGE_WARP_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -247,10 +256,10 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
   const uint32_t smem_base = smem_addr(smem);
   const uint32_t bar_base = smem_addr(bars);
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
-  auto empty_bar = [&](int s) { return bar_base + 8u * (RING_BLOCKS + s); };
-  auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * RING_BLOCKS + a); };
-  auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * RING_BLOCKS + ACC_BUFS + a); };
-  const uint32_t drain_bar = bar_base + 8u * (2 * RING_BLOCKS + 2 * ACC_BUFS);
+  auto empty_bar = [&](int s) { return bar_base + 8u * (RB + s); };
+  auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * RB + a); };
+  auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * RB + ACC_BUFS + a); };
+  const uint32_t drain_bar = bar_base + 8u * (2 * RB + 2 * ACC_BUFS);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -461,7 +470,9 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
   } else {
     // -------------------------------------------------------------- epilogue warps 2..
     const int quad = warp & 3;
-    const int cofs = ((warp - 2) >> 2) * E::COLS;  // this warp's columns of the tile
+    const int jq = (warp - 2) >> 2;      // this warp's place among those sharing its quadrant
+    const int cofs = E::cofs(jq);        // its columns of the tile: cofs .. cofs + ncols - 1
+    const int ncols = E::ncols(jq);
     uint32_t acc = 0, acc_phase = 0;
     // With the GeLU' epilogue, each tile's pre-activation rows are requested into L2 one tile
     // ahead (the first tile's here), while the tile before it is being finished.
@@ -472,7 +483,7 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
       int t1, a0, a1, pc1, g1, mb1, nb1;
       tc::decode_unit(p, u, total_kb_e, t1, a0, a1, pc1);
       tc::decode_tile(p, t1, g1, mb1, nb1);
-      tc::prefetch_aux_rows(p, g1, mb1 * BM + my_rows, nb1 * BN + cofs, E::COLS);
+      tc::prefetch_aux_rows(p, g1, mb1 * BM + my_rows, nb1 * BN + cofs, ncols);
     };
     if (aux_ahead && cluster < p.num_units) prefetch_unit(cluster);
     for (int u = cluster; u < p.num_units; u += nclusters) {
@@ -493,11 +504,23 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + static_cast<uint32_t>(cofs);
       uint8_t* stg = epi_stage + (warp - 2) * tc::STAGE_WARP_BYTES;
       if (piece < 0) {
-        tc::epilogue_rows<E::COLS>(p, g, row0, nb * BN + cofs, trow, stg);
+        if constexpr (EPI_W == 12)
+          tc::epilogue_rows_n(p, g, row0, nb * BN + cofs, ncols, trow, stg);
+        else
+          tc::epilogue_rows<E::COLS>(p, g, row0, nb * BN + cofs, trow, stg);
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
-        if (p.epi == EPI_PARTIAL_REDUCE) tc::partial_reduce_rows(p, row0, nb, BN / E::COLS);
+        if (p.epi == EPI_PARTIAL_REDUCE) tc::partial_reduce_rows(p, row0, nb, E::PER_QUAD);
+      } else if constexpr (EPI_W == 12) {
+        // never launched with split tail tiles (their per-warp counters are laid out for 4 or
+        // 8 warps): free the accumulator and report the misuse instead of summing pieces
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+          report_status(p.status, kDevTimeoutBase | 0x6f);
+        }
       } else {
         // one piece of a split tile: park the accumulator rows, free TMEM, and finish the
         // tile's rows if this warp completes their count
@@ -512,7 +535,7 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
                        static_cast<int>(rank) * 8 + (cofs / E::COLS) * 4 + quad;
         if (tail_last_arrival(counter, p.ksplit)) {
           tail_fixup_rows<E::COLS>(p, g, row0, nb * BN, tile_ws, my_rows, cofs, stg);
-          if (p.epi == EPI_PARTIAL_REDUCE) tc::partial_reduce_rows(p, row0, nb, BN / E::COLS);
+          if (p.epi == EPI_PARTIAL_REDUCE) tc::partial_reduce_rows(p, row0, nb, E::PER_QUAD);
           __syncwarp();
           if (lane == 0) atomicExch(counter, 0);
         }
@@ -566,11 +589,12 @@ cudaError_t launch_pair(const TcParams& p, int clusters, cudaStream_t st, int* m
   return cudaGetLastError();
 }
 
-// The four instantiations of one operand layout: 4 or 8 epilogue warps, 1 or 2 K blocks per
-// ring stage.
+// The five instantiations of one operand layout: 4 or 8 epilogue warps with 1 or 2 K blocks
+// per ring stage, 12 with one.
 template <bool A_MN, bool B_MN>
 cudaError_t launch_pair_variant(const TcParams& p, int clusters, cudaStream_t st,
                                 int* max_clusters, int epi_warps, int sub) {
+  if (epi_warps == 12) return launch_pair<A_MN, B_MN, 12, 1>(p, clusters, st, max_clusters);
   if (epi_warps == 8)
     return sub == 2 ? launch_pair<A_MN, B_MN, 8, 2>(p, clusters, st, max_clusters)
                     : launch_pair<A_MN, B_MN, 8, 1>(p, clusters, st, max_clusters);

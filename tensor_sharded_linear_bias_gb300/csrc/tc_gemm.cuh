@@ -479,6 +479,47 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, int g, int row0
   }
 }
 
+// The same for a column count known only at run time (the SM-pair kernel with 12 epilogue
+// warps, whose warps take 96 or 64 columns). A separate copy, so that the loops of the
+// fixed-width form above compile as they always have.
+__device__ __forceinline__ void epilogue_rows_n(const TcParams& p, int g, int row0, int colbase,
+                                                int ncols, uint32_t trow, uint8_t* stage) {
+  if (!dact_reads_aux(p)) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < ncols; c0 += 32) {
+      const int col0 = colbase + c0;
+      if (col0 >= p.N) break;  // uniform across the warp
+      float v[32];
+      tmem_ld_32cols(trow + c0, v);
+      epilogue_chunk(p, g, row0, col0, v, stage);
+    }
+    return;
+  }
+  const uint16_t* aux = static_cast<const uint16_t*>(p.aux[g]);
+  uint4 nxt[4];
+  warp_fetch_bf16(aux, p.ldaux, row0, colbase, p.M, min(32, p.N - colbase), nxt);
+#pragma unroll 1
+  for (int c0 = 0; c0 < ncols; c0 += 32) {
+    const int col0 = colbase + c0;
+    if (col0 >= p.N) break;
+    const uint4 cur[4] = {nxt[0], nxt[1], nxt[2], nxt[3]};
+    if (c0 + 32 < ncols && col0 + 32 < p.N)
+      warp_fetch_bf16(aux, p.ldaux, row0, col0 + 32, p.M, min(32, p.N - col0 - 32), nxt);
+    float v[32], h[32];
+    tmem_ld_32cols(trow + c0, v);
+    warp_unpack_bf16(stage, cur, h);
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      const float2 y = __fmul2_rn(make_float2(v[i], v[i + 1]),
+                                  gelu_erf_grad2(make_float2(h[i], h[i + 1])));
+      v[i] = y.x;
+      v[i + 1] = y.y;
+    }
+    warp_store_bf16(stage, v, static_cast<uint16_t*>(p.D[g]), p.ldd, row0, col0, p.M,
+                    min(32, p.N - col0));
+  }
+}
+
 // ------------------------------------------------------------------ the kernel
 template <bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {

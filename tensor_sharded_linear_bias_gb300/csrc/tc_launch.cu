@@ -143,10 +143,10 @@ int pair_sub_blocks(int layout, int total_kb) {
 // Largest number of co-resident 2-CTA clusters of the pair kernel (cached per device, operand
 // layout and epilogue warp count); falls back to half the SM count.
 int pair_clusters(int layout, int epi_warps = 4) {
-  static int cached[64][3][2] = {};
+  static int cached[64][3][3] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return device_sm_count() / 2;
-  const int v = epi_warps == 8 ? 1 : 0;
+  const int v = epi_warps == 12 ? 2 : epi_warps == 8 ? 1 : 0;
   if (cached[dev][layout][v] == 0) {
     int n = 0;
     cudaError_t e = run_pair(layout, tc::TcParams{}, 0, nullptr, &n, epi_warps);
@@ -163,10 +163,11 @@ int pair_clusters(int layout, int epi_warps = 4) {
 // tile's main loop: GeLU or GeLU' tiles with at most 64 K blocks of 64, any tile with at most
 // 16; else 4, which is faster for deep tiles (measured on GB300, same box: the GPT-3-shaped
 // step 1494 vs 1484 TFLOP/s with 4; the 4096 x 1024 x 4096 step 753 vs 710 with 8 on its
-// GeLU / GeLU' GEMMs; weight gradients over 512 tokens 0.253 vs 0.265 ms with 8).
-// TP_TUNE_EPI_WARPS forces the count.
+// GeLU / GeLU' GEMMs; weight gradients over 512 tokens 0.253 vs 0.265 ms with 8). The launch
+// may raise 8 to 12 for GeLU / GeLU' tiles (see launch_tc_gemm). TP_TUNE_EPI_WARPS forces the
+// count (4, 8 or 12).
 int pair_epi_warps(int epi, int act, int total_kb) {
-  if (const int v = tuning(TP_TUNE_EPI_WARPS); v != TP_TUNE_AUTO) return v == 8 ? 8 : 4;
+  if (const int v = tuning(TP_TUNE_EPI_WARPS); v != TP_TUNE_AUTO) return v == 12 ? 12 : v == 8 ? 8 : 4;
   const bool heavy = (epi == EPI_BIAS_ACT || epi == EPI_DACT) && act == TP_ACT_GELU_ERF;
   return (heavy && total_kb <= 64) || total_kb <= 16 ? 8 : 4;
 }
@@ -459,7 +460,9 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
   if (pair) {
     int epi_warps = pair_epi_warps(p.epi, p.act, p.kblocks * p.kpo);
     int max_clusters = pair_clusters(layout, epi_warps);
-    plan_tail(p, max_clusters, p.kblocks * p.kpo, s.tail_ws != nullptr && s.tail_counters != nullptr);
+    // 12 epilogue warps take whole tiles only (no split tail pieces)
+    plan_tail(p, max_clusters, p.kblocks * p.kpo,
+              epi_warps != 12 && s.tail_ws != nullptr && s.tail_counters != nullptr);
     // 8 epilogue warps also where the epilogue work is exposed at the end of the launch: split
     // tail tiles, whose pieces the completing warps sum (with 8 warps each sums half as many
     // columns), and launches of at most one tile per pair (no next tile hides the epilogue).
@@ -471,6 +474,16 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
       max_clusters = pair_clusters(layout, epi_warps);
       if (p.ksplit > 1 && max_clusters != pair_clusters(layout, 4))
         plan_tail(p, max_clusters, p.kblocks * p.kpo, true);
+    }
+    // 12 epilogue warps for the GeLU / GeLU' tiles that 8 serve (short K) when the launch has
+    // no split tail tiles. Measured on GB300, same box, 4096 x 1024 x 4096 step: those GEMMs
+    // 3-4 % faster (column forward 46.7 vs 48.2 us, dY 50.1 vs 52.1), the step 1 % faster;
+    // forced on every GEMM, the weight gradients and the input gradient were slower.
+    if (epi_warps == 8 && p.ksplit == 1 && tuning(TP_TUNE_EPI_WARPS) == TP_TUNE_AUTO &&
+        (p.epi == EPI_BIAS_ACT || p.epi == EPI_DACT) && p.act == TP_ACT_GELU_ERF &&
+        p.kblocks * p.kpo <= 64) {
+      epi_warps = 12;
+      max_clusters = std::min(max_clusters, pair_clusters(layout, epi_warps));
     }
     if (p.ksplit > 1) {
       p.tail_ws = s.tail_ws;
@@ -486,7 +499,7 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
     p.load_probe = load_probe_enabled(layout) ? 1 : 0;
     const int clusters = std::min(p.num_units, max_clusters);
     return run_pair(layout, p, clusters, st, nullptr, epi_warps,
-                    pair_sub_blocks(layout, p.kblocks * p.kpo));
+                    epi_warps == 12 ? 1 : pair_sub_blocks(layout, p.kblocks * p.kpo));
   }
   const int grid = std::min(p.num_tiles, device_sm_count());
   if (!s.a_mn && s.b_mn) return run_kmn(p, grid, st);

@@ -167,12 +167,13 @@ def test_bias_grads_many_tokens(tp, dtype):
     assert max(errs.values()) <= tol, errs
 
 
-@pytest.mark.parametrize("epi_warps", ["4", "8"])
+@pytest.mark.parametrize("epi_warps", ["4", "8", "12"])
 @pytest.mark.parametrize("T,H,F,n", [(300, 264, 2 * 392, 2), (520, 136, 4 * 136, 4)])
 def test_epilogue_warps(tp, tune, epi_warps, T, H, F, n):
-    """The SM-pair kernel with 4 epilogue warps (each on all 256 columns of its 32 rows) or 8
-    (two per TMEM lane quadrant, 128 columns each), every epilogue and reduce mode, ragged
-    tiles: matches the oracle."""
+    """The SM-pair kernel with 4 epilogue warps (each on all 256 columns of its 32 rows), 8
+    (two per TMEM lane quadrant, 128 columns each) or 12 (three per quadrant: 96, 96 and 64
+    columns, a ring of 5 K blocks), every epilogue and reduce mode, ragged tiles: matches the
+    oracle."""
     tune.set("epi_warps", epi_warps)
     tune.set("gemm_pair", 1)
     for reduce in (0, 2, 4):
@@ -181,13 +182,30 @@ def test_epilogue_warps(tp, tune, epi_warps, T, H, F, n):
         assert max(errs.values()) <= TOL_BF16, (reduce, errs)
 
 
+def test_epilogue_warps_bit_identical(tp, tune):
+    """4, 8 and 12 epilogue warps split the same accumulators differently among warps; the
+    arithmetic is the same, so every output is bit-identical (GeLU and GeLU' epilogues, fused
+    and overlapped shard sums, a ragged last tile)."""
+    tune.set("gemm_pair", 1)
+    w = SMALL.with_shape(tokens=600, hidden=392, ffn=2 * 264, tp_degree=2)
+    for reduce in (0, 4):
+        outs = {}
+        for e in (4, 8, 12):
+            with tp.tuning(epi_warps=e):
+                outs[e] = MlpCase(w, reduce).run().outputs()
+        for e in (8, 12):
+            for k, v in outs[4].items():
+                pairs = zip(v, outs[e][k]) if isinstance(v, list) else [(v, outs[e][k])]
+                assert all(np.array_equal(a, b) for a, b in pairs), (reduce, e, k)
+
+
 _ISSUE_VARIANTS = [{"split_loads": 1}, {"split_loads": 0},
                    {"mma_probe": 0, "load_probe": 0},
                    {"mma_probe": 1, "load_probe": 1},
                    {"pdl": 1}, {"pdl": 0}, {"stage_blocks": 1}, {"stage_blocks": 2}]
 
 
-@pytest.mark.parametrize("epi_warps", ["4", "8"])
+@pytest.mark.parametrize("epi_warps", ["4", "8", "12"])
 def test_issue_loop_variants(tp, tune, epi_warps):
     """The SM-pair kernel's issue loops in every variant: A and B loads from one producer thread
     or two (warp 0 and the last warp), with and without the early looks at the next block's
