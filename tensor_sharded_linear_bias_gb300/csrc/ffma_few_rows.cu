@@ -62,6 +62,7 @@ struct FewRowsParams {
   int groups, ksum, epi, act;
   int slices;  // CTAs per cluster = K slices of every output tile (1: no cluster)
   int* status;
+  int b_early;  // B may be requested before the grid dependency wait (GemmSpec::b_early)
 };
 
 // One 2-D TMA box (x = inner coordinate, a multiple of 64 elements here) into this CTA's
@@ -119,8 +120,21 @@ __global__ void __launch_bounds__(kFrThreads, 1)
     fence_mbarrier_init();
   }
   __syncthreads();
-  // nothing above touched global memory: with a programmatic launch, the previous kernel's
-  // results are visible from here on
+  // With a programmatic launch this CTA may start while the previous kernel still runs. Where
+  // B is known not to be that kernel's output, the first chunks' B boxes are requested now
+  // (their A boxes, possibly the previous kernel's output, only after the wait below).
+  int b_pre = 0;
+  if (p.b_early && warp == kFrWarps && lane == 0) {
+    b_pre = min(nchunks, kFrStages);
+    for (int i = 0; i < b_pre; ++i) {
+      const int c = c_lo + i;
+      const int kg = c / chunks_per_group;
+      const uint32_t sb = ring_base + static_cast<uint32_t>(i) * kFrStageBytes;
+      mbar_arrive_expect_tx(full_bar(i), kFrStageBytes);
+      tma_box(sb, &p.tmB[p.ksum ? kg : og], n0, (c - kg * chunks_per_group) * kFrChunk, full_bar(i));
+    }
+  }
+  // from here on the previous kernel's results are visible
   grid_dependency_wait();
   grid_dependents_launch();
 
@@ -148,8 +162,10 @@ __global__ void __launch_bounds__(kFrThreads, 1)
       const int g = p.ksum ? kg : og;
       const uint32_t sb = ring_base + static_cast<uint32_t>(s) * kFrStageBytes;
       // full boxes land (zeros outside the arrays), so every chunk brings the same bytes
-      mbar_arrive_expect_tx(full_bar(s), kFrStageBytes);
-      tma_box(sb, &p.tmB[g], n0, kk, full_bar(s));
+      if (i >= b_pre) {
+        mbar_arrive_expect_tx(full_bar(s), kFrStageBytes);
+        tma_box(sb, &p.tmB[g], n0, kk, full_bar(s));
+      }
       tma_box(sb + kFrBBytes, &p.tmA[g], kk, 0, full_bar(s));
       ++issued;
     }
@@ -366,6 +382,7 @@ cudaError_t launch_few_rows_gemm(const GemmSpec& s, cudaStream_t st) {
   p.act = s.act;
   p.slices = static_cast<int>(S);
   p.status = s.status;
+  p.b_early = s.b_early;
 
   cudaError_t e = opt_in_dynamic_smem(reinterpret_cast<const void*>(few_rows_gemm_kernel), kFrSmem);
   if (e != cudaSuccess) return e;

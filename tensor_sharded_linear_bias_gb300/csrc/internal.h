@@ -64,6 +64,10 @@ struct GemmSpec {
   const void* zbias = nullptr;
   int* status = nullptr;
   int kslices = 1;  // FFMA GEMM: K steps split over a cluster of this many CTAs per tile (1: none)
+  // B is not written by the launch before this one on the stream (the caller knows: the row GEMM
+  // of tp_mlp_forward follows the column GEMM, which writes only H_i and Y_i), so the few-row
+  // fp32 GEMM may request B before waiting for that launch to finish
+  int b_early = 0;
   // tensor-core GEMM on SM pairs: scratch for split tail tiles (nullptr: never split)
   float* tail_ws = nullptr;
   int* tail_counters = nullptr;

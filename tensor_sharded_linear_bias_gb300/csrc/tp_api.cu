@@ -405,8 +405,10 @@ cudaError_t reduce_bf16_traced(const uint16_t* P, int n, int64_t T, int64_t N, c
 // X_i [T, Ks] (ld ldx), W_i [Ks, N] row-major (MN-major B), Z fp32 [T, N].
 tp_status row_product(int dtype, int reduce, int n, int64_t T, int64_t Ks, int64_t N,
                       const void* const* X, int64_t ldx, const void* const* W, const void* bias,
-                      float* Z, void* ws, size_t partials_off, cudaStream_t st, const char* what) {
+                      float* Z, void* ws, size_t partials_off, cudaStream_t st, const char* what,
+                      bool w_early = false) {
   GemmSpec s;
+  s.b_early = w_early ? 1 : 0;
   s.M = T;
   s.N = N;
   s.K = Ks;
@@ -701,7 +703,8 @@ tp_status tp_mlp_forward(const tp_mlp_desc* desc, const void* X, const void* con
   // Row-parallel linear: Z = sum_i Y_i B_i + b.
   TP_TRY(row_product(dt, desc->reduce, n, z.T, z.Fs, z.H,
                      reinterpret_cast<const void* const*>(Ysave), z.Fs, B, b,
-                     static_cast<float*>(Z), ws, scratch_base(dt), st, "row GEMM"));
+                     static_cast<float*>(Z), ws, scratch_base(dt), st, "row GEMM",
+                     /*w_early=*/true));
   return ok();
 }
 
