@@ -302,7 +302,9 @@ typedef enum tp_trace_tag {
   TP_TAG_SP_SCATTER = 12,  /* scatter of the summed rows to token shards */
   TP_TAG_LN_FWD = 13,      /* LayerNorm forward */
   TP_TAG_LN_DGRAD = 14,    /* LayerNorm input gradient */
-  TP_TAG_LN_PARAM_GRAD = 15 /* LayerNorm dgamma, dbeta */
+  TP_TAG_LN_PARAM_GRAD = 15, /* LayerNorm dgamma, dbeta */
+  TP_TAG_ROW_GRADS = 16,   /* dY_i (times act'(H_i)) and dB_i in one launch */
+  TP_TAG_COLUMN_GRADS = 17 /* dA_i and dX in one launch */
 } tp_trace_tag;
 
 typedef struct tp_trace_record {

@@ -56,6 +56,7 @@ TUNE_KNOBS = {
     "gemm_pair": 0, "epi_warps": 1, "raster": 2, "tma_3d": 3, "split_loads": 4,
     "mma_probe": 5, "load_probe": 6, "tail_split": 7, "tail_waves": 8, "shard_split": 9,
     "simt_split": 10, "ln_reg": 11, "pdl": 12, "stage_blocks": 13, "tail_pieces": 14, "few_rows": 15,
+    "dual": 16,
 }
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -101,7 +102,7 @@ KERNEL_NAMES = {1: "gemm_tc", 2: "gemm_ffma", 3: "shard_reduce", 4: "colsum", 5:
 TAG_NAMES = {1: "column_fwd", 2: "row_fwd", 3: "row_dgrad", 4: "row_wgrad", 5: "column_wgrad",
              6: "column_dgrad", 7: "reduce", 8: "bias_grad", 9: "act_grad", 10: "other",
              11: "sp_gather", 12: "sp_scatter", 13: "ln_fwd", 14: "ln_dgrad",
-             15: "ln_param_grad"}
+             15: "ln_param_grad", 16: "row_grads", 17: "column_grads"}
 
 _P = ctypes.c_void_p
 _PP = ctypes.POINTER(ctypes.c_void_p)

@@ -18,6 +18,7 @@ BUILD = os.path.join(ROOT, "_build", "libtpmlp")
 LIB = os.path.join(PKG, "libtpmlp.so")
 
 SOURCES = ["tp_api.cu", "layernorm.cu", "tc_launch.cu", "tc_gemm_kmn.cu", "tc_gemm_kk.cu", "tc_gemm_mnmn.cu",
+           "tc_gemm_dual.cu",
            "simt_gemm.cu", "ffma_few_rows.cu", "reduce.cu", "noalloc.cu", "tuning.cu"]
 HEADERS = ["internal.h", "device_common.cuh", "tc_gemm.cuh", "tc2_gemm.cuh"]
 

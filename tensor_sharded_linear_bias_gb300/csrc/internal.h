@@ -75,6 +75,11 @@ struct GemmSpec {
 
 // bf16 inputs, tcgen05 tensor cores (sm_103a). Returns cudaSuccess or the launch error.
 cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st);
+// Two independent bf16 GEMMs in one SM-pair launch, s0 with both operands MN-major, s1 with
+// both K-major, at most 16 groups each, no EPI_PARTIAL_REDUCE. tc_dual_eligible says whether
+// the two fit and (TP_TUNE_DUAL at AUTO) whether one launch is expected to beat two.
+bool tc_dual_eligible(const GemmSpec& s0, const GemmSpec& s1);
+cudaError_t launch_tc_gemm_dual(const GemmSpec& s0, const GemmSpec& s1, cudaStream_t st);
 // fp32 inputs, FFMA (no TF32); kslices > 1 splits every tile's K steps over a cluster.
 cudaError_t launch_simt_gemm(const GemmSpec& s, cudaStream_t st);
 // The dynamic shared memory opt-in (cudaFuncSetAttribute) of kernel `kern` for at least

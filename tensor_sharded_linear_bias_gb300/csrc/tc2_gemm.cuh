@@ -185,8 +185,8 @@ __device__ __forceinline__ bool tail_last_arrival(int* counter, int pieces) {
 // runs the tile's epilogue on the sums as for an unsplit tile. Reads are coalesced (each
 // instruction covers 4 rows x 128 bytes) and two pieces' loads are in flight at once; the
 // 32 x 32 sum is turned into one row per lane through the warp's staging buffer.
-template <int COLS>
-__device__ __forceinline__ void tail_fixup_rows(const TcParams& p, int g, int row0, int colbase,
+template <int COLS, class P>
+__device__ __forceinline__ void tail_fixup_rows(const P& p, int g, int row0, int colbase,
                                                 const float* tile_ws, int lrow0, int cofs,
                                                 uint8_t* stage) {
   const int lane = threadIdx.x & 31;
@@ -238,9 +238,45 @@ __device__ __forceinline__ void tail_fixup_rows(const TcParams& p, int g, int ro
   }
 }
 
-template <bool A_MN, bool B_MN, int EPI_W, int SUB>
-__global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
-    tc2_gemm_kernel(const __grid_constant__ TcParams p) {
+// The operand layouts of one GEMM of a launch, as a type.
+template <bool A_MN_, bool B_MN_>
+struct Layout {
+  static constexpr bool A_MN = A_MN_;
+  static constexpr bool B_MN = B_MN_;
+};
+
+// The GEMMs of one launch. visit(u, f) calls f(params, unit of that GEMM, layout) for work unit
+// u of the launch: one grouped GEMM (OneGemm), or two independent ones (TwoGemms) whose units
+// follow each other in one queue, so that the second GEMM's tiles fill the pairs the first
+// leaves idle and its epilogues overlap the other's main loops. Both GEMMs of a launch use the
+// same producer split (split_loads).
+template <bool A_MN, bool B_MN>
+struct OneGemm {
+  const TcParams& p;
+  __device__ __forceinline__ int units() const { return p.num_units; }
+  __device__ __forceinline__ int split_loads() const { return p.split_loads; }
+  template <class F>
+  __device__ __forceinline__ void visit(int u, F&& f) const {
+    f(p, u, Layout<A_MN, B_MN>{});
+  }
+};
+
+template <bool A0, bool B0, bool A1, bool B1>
+struct TwoGemms {
+  const tc::TcDual& d;
+  __device__ __forceinline__ int units() const { return d.num_units; }
+  __device__ __forceinline__ int split_loads() const { return d.q[0].split_loads; }
+  template <class F>
+  __device__ __forceinline__ void visit(int u, F&& f) const {
+    if (u < d.units0)
+      f(d.q[0], u, Layout<A0, B0>{});
+    else
+      f(d.q[1], u - d.units0, Layout<A1, B1>{});
+  }
+};
+
+template <int EPI_W, int SUB, class Set>
+__device__ __forceinline__ void pair_gemm(const Set& set) {
   using E = EpiShape<EPI_W>;
   constexpr int RB = E::RING;
   constexpr int STAGES = Ring<SUB, RB>::STAGES;
@@ -266,6 +302,7 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
   const uint32_t rank = cluster_ctarank();      // 0: leader (issues the MMAs), 1: peer
   const int cluster = static_cast<int>(cluster_id_x());
   const int nclusters = static_cast<int>(num_clusters_x());
+  const int num_units = set.units();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -297,91 +334,94 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
   grid_dependency_wait();
   grid_dependents_launch();
 
-  const int total_kb = p.kblocks * p.kpo;
-
   if (warp == 0 || warp == E::B_WARP) {
     // ------------------------------------------------------------ TMA producers (both CTAs)
     // Lane 0 of warp 0 loads A (and posts the leader's expect_tx), lane 0 of the last warp
-    // loads B; with p.split_loads == 0 warp 0 loads both. Each loop is kept short: per K
+    // loads B; with split_loads == 0 warp 0 loads both. Each loop is kept short: per K
     // block one try_wait, one or two TMA issues and no division (the shard map and K offset
     // advance incrementally); the abort flag is read only while a wait actually polls.
     const bool b_warp = warp == E::B_WARP;
     const bool do_a = !b_warp;
-    const bool do_b = b_warp == (p.split_loads != 0);
+    const bool do_b = b_warp == (set.split_loads() != 0);
     if (lane == 0 && (do_a || do_b)) {
       uint32_t stage = 0, phase = 0;
       bool failed = false;
       long long issued = 0;
       const uint32_t full_leader = map_to_rank(full_bar(0), 0);   // the leader's full[0]
-      const int kend = p.kblocks * BK;
-      for (int u = cluster; u < p.num_units && !failed; u += nclusters) {
-        int t, kb0, kb1, piece;
-        tc::decode_unit(p, u, total_kb, t, kb0, kb1, piece);
-        int g, mb, nb;
-        tc::decode_tile(p, t, g, mb, nb);
-        const int arow = mb * BM + static_cast<int>(rank) * HALF;   // this CTA's A rows
-        const int bcol = nb * BN + static_cast<int>(rank) * HALF;   // this CTA's B half
-        int kg = g * p.kpo + kb0 / p.kblocks;                       // shard of block kb0
-        int kk = (kb0 % p.kblocks) * BK;                            // its K offset
-        bool free_next = false;  // the next stage seen free by an earlier probe
-        for (int kb = kb0; kb < kb1; kb += SUB) {
-          const int nsub = min(SUB, kb1 - kb);  // K blocks in this stage (fewer at a range's end)
-          if (!free_next) {
-            const int w = mbar_wait_or_abort(empty_bar(stage), phase ^ 1u, abort_flag, kWaitLimitNs);
-            if (w <= 0) {
-              if (w < 0) {
-                report_status(p.status, kDevTimeoutBase | 0x40);
-                *abort_flag = 1;
-              }
-              failed = true;
-              break;
-            }
-          }
-          uint32_t nstage = stage + 1, nphase = phase;
-          if (nstage == STAGES) { nstage = 0; nphase ^= 1u; }
-          const uint32_t fb = full_leader + 8u * stage;
-          const uint32_t s0 = smem_base + stage * STAGE_BYTES;
-          // probe the next stage between the last block's loads, as the MMA issuer does
-          const bool probe = p.load_probe != 0 && kb + nsub < kb1;
-          if (!do_a && probe) free_next = mbar_test_wait(empty_bar(nstage), nphase ^ 1u);
-          if (do_a && rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * nsub * BLOCK_BYTES);
-#pragma unroll
-          for (int j = 0; j < SUB; ++j) {
-            if (j < nsub) {
-              const uint32_t sa = s0 + j * BLOCK_BYTES;
-              const uint32_t sb = sa + A_BYTES;
-              if (do_a) {
-                if (!A_MN) {
-                  tma_load_2d_pair(sa, &p.tmA[kg], kk, arow, fb);
-                } else if (p.a3d) {
-                  tma_load_3d_pair(sa, &p.tmA[kg], 0, kk, arow / 64, fb);
-                } else {
-#pragma unroll
-                  for (int c = 0; c < HALF / 64; ++c)
-                    tma_load_2d_pair(sa + c * MN_BOX_BYTES, &p.tmA[kg], arow + 64 * c, kk, fb);
+      for (int u = cluster; u < num_units && !failed; u += nclusters) {
+        set.visit(u, [&](const auto& p, int lu, auto lay) {
+          constexpr bool A_MN = decltype(lay)::A_MN;
+          constexpr bool B_MN = decltype(lay)::B_MN;
+          const int total_kb = p.kblocks * p.kpo;
+          const int kend = p.kblocks * BK;
+          int t, kb0, kb1, piece;
+          tc::decode_unit(p, lu, total_kb, t, kb0, kb1, piece);
+          int g, mb, nb;
+          tc::decode_tile(p, t, g, mb, nb);
+          const int arow = mb * BM + static_cast<int>(rank) * HALF;   // this CTA's A rows
+          const int bcol = nb * BN + static_cast<int>(rank) * HALF;   // this CTA's B half
+          int kg = g * p.kpo + kb0 / p.kblocks;                       // shard of block kb0
+          int kk = (kb0 % p.kblocks) * BK;                            // its K offset
+          bool free_next = false;  // the next stage seen free by an earlier probe
+          for (int kb = kb0; kb < kb1; kb += SUB) {
+            const int nsub = min(SUB, kb1 - kb);  // K blocks in this stage (fewer at a range's end)
+            if (!free_next) {
+              const int w = mbar_wait_or_abort(empty_bar(stage), phase ^ 1u, abort_flag, kWaitLimitNs);
+              if (w <= 0) {
+                if (w < 0) {
+                  report_status(p.status, kDevTimeoutBase | 0x40);
+                  *abort_flag = 1;
                 }
+                failed = true;
+                break;
               }
-              if (do_a && probe && j == nsub - 1)
-                free_next = mbar_test_wait(empty_bar(nstage), nphase ^ 1u);
-              if (do_b) {
-                if (!B_MN) {
-                  tma_load_2d_pair(sb, &p.tmB[kg], kk, bcol, fb);
-                } else if (p.b3d) {
-                  tma_load_3d_pair(sb, &p.tmB[kg], 0, kk, bcol / 64, fb);
-                } else {
-#pragma unroll
-                  for (int c = 0; c < HALF / 64; ++c)
-                    tma_load_2d_pair(sb + c * MN_BOX_BYTES, &p.tmB[kg], bcol + 64 * c, kk, fb);
-                }
-              }
-              kk += BK;
-              if (kk == kend) { kk = 0; ++kg; }
             }
+            uint32_t nstage = stage + 1, nphase = phase;
+            if (nstage == STAGES) { nstage = 0; nphase ^= 1u; }
+            const uint32_t fb = full_leader + 8u * stage;
+            const uint32_t s0 = smem_base + stage * STAGE_BYTES;
+            // probe the next stage between the last block's loads, as the MMA issuer does
+            const bool probe = p.load_probe != 0 && kb + nsub < kb1;
+            if (!do_a && probe) free_next = mbar_test_wait(empty_bar(nstage), nphase ^ 1u);
+            if (do_a && rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * nsub * BLOCK_BYTES);
+#pragma unroll
+            for (int j = 0; j < SUB; ++j) {
+              if (j < nsub) {
+                const uint32_t sa = s0 + j * BLOCK_BYTES;
+                const uint32_t sb = sa + A_BYTES;
+                if (do_a) {
+                  if (!A_MN) {
+                    tma_load_2d_pair(sa, &p.tmA[kg], kk, arow, fb);
+                  } else if (p.a3d) {
+                    tma_load_3d_pair(sa, &p.tmA[kg], 0, kk, arow / 64, fb);
+                  } else {
+#pragma unroll
+                    for (int c = 0; c < HALF / 64; ++c)
+                      tma_load_2d_pair(sa + c * MN_BOX_BYTES, &p.tmA[kg], arow + 64 * c, kk, fb);
+                  }
+                }
+                if (do_a && probe && j == nsub - 1)
+                  free_next = mbar_test_wait(empty_bar(nstage), nphase ^ 1u);
+                if (do_b) {
+                  if (!B_MN) {
+                    tma_load_2d_pair(sb, &p.tmB[kg], kk, bcol, fb);
+                  } else if (p.b3d) {
+                    tma_load_3d_pair(sb, &p.tmB[kg], 0, kk, bcol / 64, fb);
+                  } else {
+#pragma unroll
+                    for (int c = 0; c < HALF / 64; ++c)
+                      tma_load_2d_pair(sb + c * MN_BOX_BYTES, &p.tmB[kg], bcol + 64 * c, kk, fb);
+                  }
+                }
+                kk += BK;
+                if (kk == kend) { kk = 0; ++kg; }
+              }
+            }
+            ++issued;
+            stage = nstage;
+            phase = nphase;
           }
-          ++issued;
-          stage = nstage;
-          phase = nphase;
-        }
+        });
       }
       // another role may have given up after this thread's last wait: its copies in flight
       // are then never consumed
@@ -397,69 +437,73 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ------------------------------------------------------------ MMA issuer (leader)
-      constexpr uint32_t idesc = tc::idesc_bf16(BM, BN, A_MN, B_MN);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool failed = false;
-      for (int u = cluster; u < p.num_units && !failed; u += nclusters) {
-        int t, kb0, kb1, piece;
-        tc::decode_unit(p, u, total_kb, t, kb0, kb1, piece);
-        const int we = mbar_wait_or_abort(tempty_bar(acc), acc_phase ^ 1u, abort_flag, kWaitLimitNs);
-        if (we <= 0) {
-          if (we < 0) {
-            report_status(p.status, kDevTimeoutBase | 0x50);
-            *abort_flag = 1;
-          }
-          failed = true;
-          break;
-        }
-        tc::tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
-        // `ready`: the next block's full barrier was seen complete by a probe issued before the
-        // current block's last MMA (its latency then hides behind the MMA issue instead of
-        // adding to the gap between blocks)
-        bool ready = false;
-        for (int kb = kb0; kb < kb1; kb += SUB) {
-          const int nsub = min(SUB, kb1 - kb);
-          if (!ready) {
-            const int w = mbar_wait_or_abort(full_bar(stage), phase, abort_flag, kWaitLimitNs);
-            if (w <= 0) {
-              if (w < 0) {
-                report_status(p.status, kDevTimeoutBase | 0x51);
-                *abort_flag = 1;
-              }
-              failed = true;
-              break;
+      for (int u = cluster; u < num_units && !failed; u += nclusters) {
+        set.visit(u, [&](const auto& p, int lu, auto lay) {
+          constexpr bool A_MN = decltype(lay)::A_MN;
+          constexpr bool B_MN = decltype(lay)::B_MN;
+          constexpr uint32_t idesc = tc::idesc_bf16(BM, BN, A_MN, B_MN);
+          int t, kb0, kb1, piece;
+          tc::decode_unit(p, lu, p.kblocks * p.kpo, t, kb0, kb1, piece);
+          const int we = mbar_wait_or_abort(tempty_bar(acc), acc_phase ^ 1u, abort_flag, kWaitLimitNs);
+          if (we <= 0) {
+            if (we < 0) {
+              report_status(p.status, kDevTimeoutBase | 0x50);
+              *abort_flag = 1;
             }
+            failed = true;
+            return;
           }
           tc::tc_fence_after();
-          uint32_t nstage = stage + 1, nphase = phase;
-          if (nstage == STAGES) { nstage = 0; nphase ^= 1u; }
-          const uint32_t s0 = smem_base + stage * STAGE_BYTES;
-#pragma unroll
-          for (int j = 0; j < SUB; ++j) {
-            if (j < nsub) {
-              const uint32_t sa = s0 + j * BLOCK_BYTES;
-              const uint32_t sb = sa + A_BYTES;
-#pragma unroll
-              for (int k = 0; k < BK / 16; ++k) {
-                if (j == nsub - 1 && k == BK / 16 - 1)
-                  ready = p.mma_probe != 0 && kb + nsub < kb1 &&
-                          mbar_test_wait(full_bar(nstage), nphase);
-                const uint64_t ad = A_MN ? tc::sdesc_sw128(sa + k * 2048, MN_BOX_BYTES, 1024)
-                                         : tc::sdesc_sw128(sa + k * 32, 16, 1024);
-                const uint64_t bd = B_MN ? tc::sdesc_sw128(sb + k * 2048, MN_BOX_BYTES, 1024)
-                                         : tc::sdesc_sw128(sb + k * 32, 16, 1024);
-                umma_bf16_pair(d_tmem, ad, bd, idesc, (kb > kb0 || j > 0 || k > 0) ? 1u : 0u);
+          const uint32_t d_tmem = tmem_base + acc * BN;
+          // `ready`: the next block's full barrier was seen complete by a probe issued before the
+          // current block's last MMA (its latency then hides behind the MMA issue instead of
+          // adding to the gap between blocks)
+          bool ready = false;
+          for (int kb = kb0; kb < kb1; kb += SUB) {
+            const int nsub = min(SUB, kb1 - kb);
+            if (!ready) {
+              const int w = mbar_wait_or_abort(full_bar(stage), phase, abort_flag, kWaitLimitNs);
+              if (w <= 0) {
+                if (w < 0) {
+                  report_status(p.status, kDevTimeoutBase | 0x51);
+                  *abort_flag = 1;
+                }
+                failed = true;
+                break;
               }
             }
+            tc::tc_fence_after();
+            uint32_t nstage = stage + 1, nphase = phase;
+            if (nstage == STAGES) { nstage = 0; nphase ^= 1u; }
+            const uint32_t s0 = smem_base + stage * STAGE_BYTES;
+#pragma unroll
+            for (int j = 0; j < SUB; ++j) {
+              if (j < nsub) {
+                const uint32_t sa = s0 + j * BLOCK_BYTES;
+                const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k) {
+                  if (j == nsub - 1 && k == BK / 16 - 1)
+                    ready = p.mma_probe != 0 && kb + nsub < kb1 &&
+                            mbar_test_wait(full_bar(nstage), nphase);
+                  const uint64_t ad = A_MN ? tc::sdesc_sw128(sa + k * 2048, MN_BOX_BYTES, 1024)
+                                           : tc::sdesc_sw128(sa + k * 32, 16, 1024);
+                  const uint64_t bd = B_MN ? tc::sdesc_sw128(sb + k * 2048, MN_BOX_BYTES, 1024)
+                                           : tc::sdesc_sw128(sb + k * 32, 16, 1024);
+                  umma_bf16_pair(d_tmem, ad, bd, idesc, (kb > kb0 || j > 0 || k > 0) ? 1u : 0u);
+                }
+              }
+            }
+            umma_commit_pair_multicast(empty_bar(stage), 0x3);
+            stage = nstage;
+            phase = nphase;
           }
-          umma_commit_pair_multicast(empty_bar(stage), 0x3);
-          stage = nstage;
-          phase = nphase;
-        }
-        if (failed) break;
-        umma_commit_pair_multicast(tfull_bar(acc), 0x3);
-        if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1u; }
+          if (failed) return;
+          umma_commit_pair_multicast(tfull_bar(acc), 0x3);
+          if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1u; }
+        });
       }
       if (!failed && *abort_flag) failed = true;   // MMAs of a tile no epilogue will read
       if (failed) {
@@ -474,73 +518,81 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
     const int cofs = E::cofs(jq);        // its columns of the tile: cofs .. cofs + ncols - 1
     const int ncols = E::ncols(jq);
     uint32_t acc = 0, acc_phase = 0;
-    // With the GeLU' epilogue, each tile's pre-activation rows are requested into L2 one tile
-    // ahead (the first tile's here), while the tile before it is being finished.
-    const bool aux_ahead = tc::dact_reads_aux(p);
     const int my_rows = static_cast<int>(rank) * HALF + quad * 32;
-    const int total_kb_e = p.kblocks * p.kpo;
+    // With the GeLU' epilogue, each tile's pre-activation rows are requested into L2 one unit
+    // ahead (the first unit's here), while the unit before it is being finished.
     auto prefetch_unit = [&](int u) {
-      int t1, a0, a1, pc1, g1, mb1, nb1;
-      tc::decode_unit(p, u, total_kb_e, t1, a0, a1, pc1);
-      tc::decode_tile(p, t1, g1, mb1, nb1);
-      tc::prefetch_aux_rows(p, g1, mb1 * BM + my_rows, nb1 * BN + cofs, ncols);
+      set.visit(u, [&](const auto& p, int lu, auto) {
+        if (!tc::dact_reads_aux(p)) return;
+        int t1, a0, a1, pc1, g1, mb1, nb1;
+        tc::decode_unit(p, lu, p.kblocks * p.kpo, t1, a0, a1, pc1);
+        tc::decode_tile(p, t1, g1, mb1, nb1);
+        tc::prefetch_aux_rows(p, g1, mb1 * BM + my_rows, nb1 * BN + cofs, ncols);
+      });
     };
-    if (aux_ahead && cluster < p.num_units) prefetch_unit(cluster);
-    for (int u = cluster; u < p.num_units; u += nclusters) {
-      int t, kb0, kb1, piece;
-      tc::decode_unit(p, u, total_kb_e, t, kb0, kb1, piece);
-      int g, mb, nb;
-      tc::decode_tile(p, t, g, mb, nb);
-      if (aux_ahead && u + nclusters < p.num_units) prefetch_unit(u + nclusters);
-      if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, kWaitLimitNs)) {
-        if (lane == 0) report_status(p.status, kDevTimeoutBase | 0x60);
-        *abort_flag = 1;
-        break;
-      }
-      if (*abort_flag) break;
-      tc::tc_fence_after();
-      const int row0 = mb * BM + static_cast<int>(rank) * HALF + quad * 32;
-      const uint32_t trow =
-          tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + static_cast<uint32_t>(cofs);
-      uint8_t* stg = epi_stage + (warp - 2) * tc::STAGE_WARP_BYTES;
-      if (piece < 0) {
-        if constexpr (EPI_W == 12)
-          tc::epilogue_rows_n(p, g, row0, nb * BN + cofs, ncols, trow, stg);
-        else
-          tc::epilogue_rows<E::COLS>(p, g, row0, nb * BN + cofs, trow, stg);
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
-        if (p.epi == EPI_PARTIAL_REDUCE) tc::partial_reduce_rows(p, row0, nb, E::PER_QUAD);
-      } else if constexpr (EPI_W == 12) {
-        // never launched with split tail tiles (their per-warp counters are laid out for 4 or
-        // 8 warps): free the accumulator and report the misuse instead of summing pieces
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
-          report_status(p.status, kDevTimeoutBase | 0x6f);
+    if (cluster < num_units) prefetch_unit(cluster);
+    bool stop = false;
+    for (int u = cluster; u < num_units && !stop; u += nclusters) {
+      if (u + nclusters < num_units) prefetch_unit(u + nclusters);
+      set.visit(u, [&](const auto& p, int lu, auto) {
+        int t, kb0, kb1, piece;
+        tc::decode_unit(p, lu, p.kblocks * p.kpo, t, kb0, kb1, piece);
+        int g, mb, nb;
+        tc::decode_tile(p, t, g, mb, nb);
+        if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, kWaitLimitNs)) {
+          if (lane == 0) report_status(p.status, kDevTimeoutBase | 0x60);
+          *abort_flag = 1;
+          stop = true;
+          return;
         }
-      } else {
-        // one piece of a split tile: park the accumulator rows, free TMEM, and finish the
-        // tile's rows if this warp completes their count
-        const int split_tile = t - p.full_tiles;
-        float* tile_ws = p.tail_ws + static_cast<long long>(split_tile) * p.ksplit * PIECE_FLOATS;
-        store_piece_rows<E::COLS>(tile_ws + static_cast<long long>(piece) * PIECE_FLOATS, my_rows,
-                                  cofs, trow, stg);
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
-        int* counter = p.tail_counters + split_tile * TAIL_COUNTERS_PER_TILE +
-                       static_cast<int>(rank) * 8 + (cofs / E::COLS) * 4 + quad;
-        if (tail_last_arrival(counter, p.ksplit)) {
-          tail_fixup_rows<E::COLS>(p, g, row0, nb * BN, tile_ws, my_rows, cofs, stg);
-          if (p.epi == EPI_PARTIAL_REDUCE) tc::partial_reduce_rows(p, row0, nb, E::PER_QUAD);
+        if (*abort_flag) {
+          stop = true;
+          return;
+        }
+        tc::tc_fence_after();
+        const int row0 = mb * BM + static_cast<int>(rank) * HALF + quad * 32;
+        const uint32_t trow =
+            tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + static_cast<uint32_t>(cofs);
+        uint8_t* stg = epi_stage + (warp - 2) * tc::STAGE_WARP_BYTES;
+        if (piece < 0) {
+          if constexpr (EPI_W == 12)
+            tc::epilogue_rows_n(p, g, row0, nb * BN + cofs, ncols, trow, stg);
+          else
+            tc::epilogue_rows<E::COLS>(p, g, row0, nb * BN + cofs, trow, stg);
+          tc::tc_fence_before();
           __syncwarp();
-          if (lane == 0) atomicExch(counter, 0);
+          if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+          if (p.epi == EPI_PARTIAL_REDUCE) tc::partial_reduce_rows(p, row0, nb, E::PER_QUAD);
+        } else if constexpr (EPI_W == 12) {
+          // never launched with split tail tiles (their per-warp counters are laid out for 4 or
+          // 8 warps): free the accumulator and report the misuse instead of summing pieces
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+            report_status(p.status, kDevTimeoutBase | 0x6f);
+          }
+        } else {
+          // one piece of a split tile: park the accumulator rows, free TMEM, and finish the
+          // tile's rows if this warp completes their count
+          const int split_tile = t - p.full_tiles;
+          float* tile_ws = p.tail_ws + static_cast<long long>(split_tile) * p.ksplit * PIECE_FLOATS;
+          store_piece_rows<E::COLS>(tile_ws + static_cast<long long>(piece) * PIECE_FLOATS, my_rows,
+                                    cofs, trow, stg);
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+          int* counter = p.tail_counters + split_tile * TAIL_COUNTERS_PER_TILE +
+                         static_cast<int>(rank) * 8 + (cofs / E::COLS) * 4 + quad;
+          if (tail_last_arrival(counter, p.ksplit)) {
+            tail_fixup_rows<E::COLS>(p, g, row0, nb * BN, tile_ws, my_rows, cofs, stg);
+            if (p.epi == EPI_PARTIAL_REDUCE) tc::partial_reduce_rows(p, row0, nb, E::PER_QUAD);
+            __syncwarp();
+            if (lane == 0) atomicExch(counter, 0);
+          }
         }
-      }
-      if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1u; }
+        if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1u; }
+      });
     }
   }
 
@@ -555,11 +607,26 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
   }
 }
 
-// Launch on clusters of two CTAs; max_clusters != nullptr asks for the occupancy limit only.
 template <bool A_MN, bool B_MN, int EPI_W, int SUB>
-cudaError_t launch_pair(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters) {
+__global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
+    tc2_gemm_kernel(const __grid_constant__ TcParams p) {
+  pair_gemm<EPI_W, SUB>(OneGemm<A_MN, B_MN>{p});
+}
+
+// Two GEMMs in one launch: the first with both operands MN-major (weight gradients), the second
+// with both K-major (input gradients). One K block per ring stage.
+template <int EPI_W>
+__global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
+    tc2_dual_kernel(const __grid_constant__ tc::TcDual d) {
+  pair_gemm<EPI_W, 1>(TwoGemms<true, true, false, false>{d});
+}
+
+// Launch `kern` on clusters of two CTAs; max_clusters != nullptr asks for the occupancy limit
+// only.
+template <int EPI_W, class Kern, class Params>
+cudaError_t launch_pair_kernel(Kern kern, const Params& p, int clusters, cudaStream_t st,
+                               int* max_clusters) {
   using E = EpiShape<EPI_W>;
-  auto kern = tc2_gemm_kernel<A_MN, B_MN, EPI_W, SUB>;
   cudaError_t e = opt_in_dynamic_smem(reinterpret_cast<const void*>(kern), E::SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -587,6 +654,17 @@ cudaError_t launch_pair(const TcParams& p, int clusters, cudaStream_t st, int* m
   e = cudaLaunchKernelEx(&cfg, kern, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+template <bool A_MN, bool B_MN, int EPI_W, int SUB>
+cudaError_t launch_pair(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters) {
+  return launch_pair_kernel<EPI_W>(tc2_gemm_kernel<A_MN, B_MN, EPI_W, SUB>, p, clusters, st,
+                                   max_clusters);
+}
+
+template <int EPI_W>
+cudaError_t launch_dual(const tc::TcDual& d, int clusters, cudaStream_t st, int* max_clusters) {
+  return launch_pair_kernel<EPI_W>(tc2_dual_kernel<EPI_W>, d, clusters, st, max_clusters);
 }
 
 // The five instantiations of one operand layout: 4 or 8 epilogue warps with 1 or 2 K blocks

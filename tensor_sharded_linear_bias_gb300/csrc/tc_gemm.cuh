@@ -49,13 +49,17 @@ constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
 constexpr int EPI_WARPS = 4;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_WARPS * 32 * 128 + 1024 + 256;
 
-struct __align__(128) TcParams {
-  CUtensorMap tmA[kMaxShards];
-  CUtensorMap tmB[kMaxShards];
-  void* D[kMaxShards];
-  void* D2[kMaxShards];
-  const void* bias[kMaxShards];
-  const void* aux[kMaxShards];
+// The parameters of one grouped GEMM, for up to NM groups (tensor maps, outputs, bias and aux
+// pointers per group). A launch of one GEMM takes NM = kMaxShards; a launch of two
+// (TcDual) takes two blocks of kDualMaxShards, so that both fit in the kernel parameter space.
+template <int NM>
+struct __align__(128) TcParamsT {
+  CUtensorMap tmA[NM];
+  CUtensorMap tmB[NM];
+  void* D[NM];
+  void* D2[NM];
+  const void* bias[NM];
+  const void* aux[NM];
   long long ldd, ldd2, ldaux;
   int M, N;
   int kblocks;      // K blocks of 64 per group
@@ -84,6 +88,16 @@ struct __align__(128) TcParams {
   int mma_probe;    // SM-pair kernel: probe the next block's full barrier during the MMAs
   int load_probe;   // ... and the next block's empty barrier between the loads
   int* status;
+};
+using TcParams = TcParamsT<kMaxShards>;
+
+// Two independent GEMMs in one SM-pair launch: work units [0, units0) are q[0]'s, the rest
+// q[1]'s (unit u of the launch is unit u - units0 of q[1]); one queue deals them all to the pairs.
+constexpr int kDualMaxShards = 16;
+struct __align__(128) TcDual {
+  TcParamsT<kDualMaxShards> q[2];
+  int units0;
+  int num_units;
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -171,7 +185,8 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, float* v) {
 // ------------------------------------------------------------------ tile decode
 // Tile t -> output index og, m block, n block. With m fastest, the tiles running at the same
 // time share B blocks and sweep all of A; with n fastest, they share A blocks and sweep B.
-__device__ __forceinline__ void decode_tile(const TcParams& p, int t, int& g, int& mb, int& nb) {
+template <class P>
+__device__ __forceinline__ void decode_tile(const P& p, int t, int& g, int& mb, int& nb) {
   const int per = p.tiles_m * p.tiles_n;
   g = t / per;
   const int r = t - g * per;
@@ -185,7 +200,8 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int t, int& g, in
 }
 
 // Work unit u -> tile t and its K blocks [kb0, kb1); piece = -1 for a whole tile.
-__device__ __forceinline__ void decode_unit(const TcParams& p, int u, int total_kb, int& t,
+template <class P>
+__device__ __forceinline__ void decode_unit(const P& p, int u, int total_kb, int& t,
                                             int& kb0, int& kb1, int& piece) {
   if (u < p.full_tiles) {
     t = u;
@@ -299,14 +315,16 @@ __device__ __forceinline__ void warp_unpack_bf16(uint8_t* stage, const uint4* ra
 }
 
 // EPI_DACT with an activation reads the saved pre-activation at every output element.
-__device__ __forceinline__ bool dact_reads_aux(const TcParams& p) {
+template <class P>
+__device__ __forceinline__ bool dact_reads_aux(const P& p) {
   return p.epi == EPI_DACT && p.act == TP_ACT_GELU_ERF;
 }
 
 // Lane l asks L2 for row row0 + l of the pre-activation block [row0.., col0.., up to ncols
 // columns] of group g: one bulk prefetch per row (16-byte aligned start, a multiple of 16
 // bytes long: bf16 rows and N are multiples of 8, col0 of 256).
-__device__ __forceinline__ void prefetch_aux_rows(const TcParams& p, int g, int row0, int col0,
+template <class P>
+__device__ __forceinline__ void prefetch_aux_rows(const P& p, int g, int row0, int col0,
                                                   int ncols) {
   const int lane = threadIdx.x & 31;
   const int row = row0 + lane;
@@ -351,7 +369,8 @@ __device__ __forceinline__ float4 ld_cg_f4(const float* p) {
 // itself in for the block; the warp that completes the count (one per block, whichever
 // partial it computed) reads the nsplit partials of the block in partial order, adds the bias
 // and writes Z, then resets the counter for the next launch. No warp waits for another.
-__device__ __forceinline__ void partial_reduce_rows(const TcParams& p, int row0, int nb,
+template <class P>
+__device__ __forceinline__ void partial_reduce_rows(const P& p, int row0, int nb,
                                                    int warps_per_block = 1) {
   const int lane = threadIdx.x & 31;
   if (row0 >= p.M) return;  // no rows of this block exist (edge tile): nothing was stored
@@ -397,7 +416,8 @@ __device__ __forceinline__ void partial_reduce_rows(const TcParams& p, int row0,
 }
 
 // Warp-wide: all 32 lanes call this for the same (row0, col0).
-__device__ __forceinline__ void epilogue_chunk(const TcParams& p, int g, int row0, int col0,
+template <class P>
+__device__ __forceinline__ void epilogue_chunk(const P& p, int g, int row0, int col0,
                                                float* v, uint8_t* stage) {
   const int valid = min(32, p.N - col0);  // a multiple of 8 (N % 8 == 0)
   const int og = g;
@@ -442,8 +462,8 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, int g, int row
 // trow, 32 columns at a time. With EPI_DACT + activation, the pre-activation loads of the
 // next 32 columns are issued before the current ones are used, so each chunk's DRAM/L2 round
 // trip overlaps the previous chunk's work instead of stalling the warp.
-template <int NCOLS>
-__device__ __forceinline__ void epilogue_rows(const TcParams& p, int g, int row0, int colbase,
+template <int NCOLS, class P>
+__device__ __forceinline__ void epilogue_rows(const P& p, int g, int row0, int colbase,
                                               uint32_t trow, uint8_t* stage) {
   if (!dact_reads_aux(p)) {
     for (int c0 = 0; c0 < NCOLS; c0 += 32) {
@@ -482,7 +502,8 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, int g, int row0
 // The same for a column count known only at run time (the SM-pair kernel with 12 epilogue
 // warps, whose warps take 96 or 64 columns). A separate copy, so that the loops of the
 // fixed-width form above compile as they always have.
-__device__ __forceinline__ void epilogue_rows_n(const TcParams& p, int g, int row0, int colbase,
+template <class P>
+__device__ __forceinline__ void epilogue_rows_n(const P& p, int g, int row0, int colbase,
                                                 int ncols, uint32_t trow, uint8_t* stage) {
   if (!dact_reads_aux(p)) {
 #pragma unroll 1

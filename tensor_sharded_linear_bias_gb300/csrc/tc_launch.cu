@@ -21,6 +21,8 @@ cudaError_t run_pair_kk(const TcParams& p, int clusters, cudaStream_t st, int* m
                         int epi_warps, int sub);
 cudaError_t run_pair_mnmn(const TcParams& p, int clusters, cudaStream_t st, int* max_clusters,
                           int epi_warps, int sub);
+cudaError_t run_pair_dual(const TcDual& d, int clusters, cudaStream_t st, int* max_clusters,
+                          int epi_warps);
 }  // namespace tc
 
 namespace {
@@ -393,14 +395,14 @@ int plan_shard_split(int64_t M, int64_t N, int64_t K_per_group, int n) {
   return best;
 }
 
-cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
-  using namespace tc;
-  if (s.M <= 0 || s.N <= 0 || s.K <= 0) return cudaSuccess;
-  if (s.groups < 1 || s.groups > kMaxShards) return cudaErrorInvalidValue;
-  static_assert(sizeof(TcParams) <= 32764, "kernel parameter block too large");
+namespace {
 
-  const bool pair = use_pair_kernel(s.M);
-  alignas(128) static thread_local TcParams p;
+// The kernel parameters of GEMM s (tensor maps, outputs, tile counts, tile order), for the
+// SM-pair kernel (pair) or the one-SM kernel; *layout = 0 (A K-major, B MN-major), 1 (both
+// K-major) or 2 (both MN-major). p holds at least s.groups groups (checked by the caller).
+template <class P>
+cudaError_t fill_tc_params(P& p, const GemmSpec& s, bool pair, int* layout) {
+  using namespace tc;
   std::memset(static_cast<void*>(&p), 0, sizeof(p));
   // K-major boxes: 128 rows of A; 256 rows of B (one SM) or 128 (each SM of a pair).
   const uint32_t b_rows = pair ? static_cast<uint32_t>(tc2::HALF) : static_cast<uint32_t>(BN);
@@ -451,12 +453,26 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
   p.raster = choose_raster(p.tiles_m, p.tiles_n, s.K * p.kpo,
                            pair ? 2 * pair_clusters(0) : device_sm_count(), pair);
   p.status = s.status;
-
-  const int layout = (!s.a_mn && s.b_mn) ? 0 : (!s.a_mn && !s.b_mn) ? 1 : (s.a_mn && s.b_mn) ? 2 : -1;
-  if (layout < 0) return cudaErrorNotSupported;
+  *layout = (!s.a_mn && s.b_mn) ? 0 : (!s.a_mn && !s.b_mn) ? 1 : (s.a_mn && s.b_mn) ? 2 : -1;
+  if (*layout < 0) return cudaErrorNotSupported;
   p.full_tiles = p.num_tiles;
   p.ksplit = 1;
   p.num_units = p.num_tiles;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
+  using namespace tc;
+  if (s.M <= 0 || s.N <= 0 || s.K <= 0) return cudaSuccess;
+  if (s.groups < 1 || s.groups > kMaxShards) return cudaErrorInvalidValue;
+  static_assert(sizeof(TcParams) <= 32764, "kernel parameter block too large");
+
+  const bool pair = use_pair_kernel(s.M);
+  alignas(128) static thread_local TcParams p;
+  int layout = -1;
+  if (const cudaError_t e = fill_tc_params(p, s, pair, &layout); e != cudaSuccess) return e;
   if (pair) {
     int epi_warps = pair_epi_warps(p.epi, p.act, p.kblocks * p.kpo);
     int max_clusters = pair_clusters(layout, epi_warps);
@@ -506,6 +522,87 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
   if (!s.a_mn && !s.b_mn) return run_kk(p, grid, st);
   if (s.a_mn && s.b_mn) return run_mnmn(p, grid, st);
   return cudaErrorNotSupported;
+}
+
+
+// ---------------------------------------------------------------- two GEMMs in one launch
+namespace {
+
+// Largest number of co-resident 2-CTA clusters of the two-GEMM kernel (cached per device and
+// epilogue warp count); falls back to half the SM count.
+int dual_clusters(int epi_warps) {
+  static int cached[64][2] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return device_sm_count() / 2;
+  const int v = epi_warps == 12 ? 1 : 0;
+  if (cached[dev][v] == 0) {
+    alignas(128) static tc::TcDual probe;  // only the kernel's resources matter here
+    int n = 0;
+    cudaError_t e = tc::run_pair_dual(probe, 0, nullptr, &n, epi_warps);
+    if (e != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = device_sm_count() / 2;
+    }
+    cached[dev][v] = n;
+  }
+  return cached[dev][v];
+}
+
+int64_t pair_tiles(const GemmSpec& s) {
+  const int kpo = s.kpo > 0 ? s.kpo : (s.ksum ? s.groups : 1);
+  return int64_t(s.groups / std::max(1, kpo)) * ((s.M + tc2::BM - 1) / tc2::BM) *
+         ((s.N + tc2::BN - 1) / tc2::BN);
+}
+
+// A shared launch pays off where a GEMM alone leaves pairs idle: one of the two has at most
+// one wave of tiles (its launch ramp, its partly idle wave and its last, exposed epilogue are
+// then a large part of its time), and together they make few waves (with many waves there is
+// nothing to fill, and the one-GEMM launch keeps its split tail tiles).
+constexpr int kDualMaxWaves = 8;
+
+}  // namespace
+
+bool tc_dual_eligible(const GemmSpec& s0, const GemmSpec& s1) {
+  const int v = tuning(TP_TUNE_DUAL);
+  if (v == 0) return false;
+  const auto fits = [](const GemmSpec& s) {
+    const int kpo = s.kpo > 0 ? s.kpo : (s.ksum ? s.groups : 1);
+    return s.M > 0 && s.N > 0 && s.K > 0 && s.groups >= 1 && s.groups <= tc::kDualMaxShards &&
+           s.groups % kpo == 0 && use_pair_kernel(s.M) && s.epi != EPI_PARTIAL_REDUCE;
+  };
+  if (!(s0.a_mn && s0.b_mn && !s1.a_mn && !s1.b_mn && fits(s0) && fits(s1))) return false;
+  if (v != TP_TUNE_AUTO) return true;
+  const int64_t C = std::max(1, device_sm_count() / 2);
+  const int64_t t0 = pair_tiles(s0), t1 = pair_tiles(s1);
+  return std::min(t0, t1) <= C && t0 + t1 <= kDualMaxWaves * C;
+}
+
+cudaError_t launch_tc_gemm_dual(const GemmSpec& s0, const GemmSpec& s1, cudaStream_t st) {
+  using namespace tc;
+  static_assert(sizeof(TcDual) <= 32764, "kernel parameter block too large");
+  alignas(128) static thread_local TcDual d;
+  int l0 = -1, l1 = -1;
+  if (const cudaError_t e = fill_tc_params(d.q[0], s0, true, &l0); e != cudaSuccess) return e;
+  if (const cudaError_t e = fill_tc_params(d.q[1], s1, true, &l1); e != cudaSuccess) return e;
+  if (l0 != 2 || l1 != 1) return cudaErrorNotSupported;
+  // 12 epilogue warps when either GEMM has GeLU / GeLU' tiles of at most 64 K blocks (as for
+  // one GEMM), else 8; both GEMMs load A and B from two producer threads
+  const auto heavy = [](const TcParamsT<kDualMaxShards>& q) {
+    return (q.epi == EPI_BIAS_ACT || q.epi == EPI_DACT) && q.act == TP_ACT_GELU_ERF &&
+           q.kblocks * q.kpo <= 64;
+  };
+  int epi_warps = heavy(d.q[0]) || heavy(d.q[1]) ? 12 : 8;
+  if (const int v = tuning(TP_TUNE_EPI_WARPS); v == 8 || v == 12) epi_warps = v;
+  for (int i = 0; i < 2; ++i) {
+    d.q[i].split_loads = 1;
+    d.q[i].mma_probe = mma_probe_enabled() ? 1 : 0;
+    d.q[i].load_probe = load_probe_enabled(i == 0 ? l0 : l1) ? 1 : 0;
+  }
+  d.units0 = d.q[0].num_units;
+  d.num_units = d.q[0].num_units + d.q[1].num_units;
+  if (d.num_units == 0) return cudaSuccess;
+  const int clusters = std::min(d.num_units, dual_clusters(epi_warps));
+  return run_pair_dual(d, clusters, st, nullptr, epi_warps);
 }
 
 }  // namespace tpk

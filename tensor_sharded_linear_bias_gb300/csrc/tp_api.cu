@@ -244,6 +244,16 @@ cudaError_t run_gemm(const GemmSpec& s, int dtype, cudaStream_t st, int tag) {
                 [&] { return launch_simt_gemm(t, st); });
 }
 
+// Two independent bf16 GEMMs in one launch (tc_dual_eligible), traced as one launch.
+cudaError_t run_gemm_dual(const GemmSpec& s0, const GemmSpec& s1, int dtype, cudaStream_t st,
+                          int tag) {
+  double f0 = 0, b0 = 0, f1 = 0, b1 = 0;
+  gemm_work(s0, dtype, &f0, &b0);
+  gemm_work(s1, dtype, &f1, &b1);
+  return traced(TP_K_GEMM_TC, tag, s0.groups + s1.groups, f0 + f1, b0 + b1, st,
+                [&] { return launch_tc_gemm_dual(s0, s1, st); });
+}
+
 // Zero `rows` x `cols` fp32 outputs (a GEMM over zero tokens).
 cudaError_t zero_f32(void* p, int64_t count, cudaStream_t st) {
   if (p == nullptr || count == 0) return cudaSuccess;
@@ -452,9 +462,10 @@ tp_status row_product(int dtype, int reduce, int n, int64_t T, int64_t Ks, int64
 }
 
 // dX = sum_i dH_i W_i^T, dH_i [T, w] (ld ldh), W_i [Kd, w] row-major (K-major B).
-tp_status input_grad_sum(int dtype, int reduce, int n, int64_t T, int64_t w, int64_t Kd,
-                         const void* const* dH, int64_t ldh, const void* const* W, float* dX,
-                         void* ws, size_t partials_off, cudaStream_t st) {
+// dX = sum_i dH_i W_i^T before its outputs are set: dH_i [T, w] (ld ldh), W_i [Kd, w], both
+// K-major operands.
+GemmSpec dgrad_spec(int dtype, int n, int64_t T, int64_t w, int64_t Kd, const void* const* dH,
+                    int64_t ldh, const void* const* W, void* ws) {
   GemmSpec s;
   s.M = T;
   s.N = Kd;
@@ -471,6 +482,13 @@ tp_status input_grad_sum(int dtype, int reduce, int n, int64_t T, int64_t w, int
     s.A[i] = dH[i];
     s.B[i] = W[i];
   }
+  return s;
+}
+
+tp_status input_grad_sum(int dtype, int reduce, int n, int64_t T, int64_t w, int64_t Kd,
+                         const void* const* dH, int64_t ldh, const void* const* W, float* dX,
+                         void* ws, size_t partials_off, cudaStream_t st) {
+  GemmSpec s = dgrad_spec(dtype, n, T, w, Kd, dH, ldh, W, ws);
   const int S = shard_split(reduce, dtype, T, Kd, w, n);
   if (S == 1) {
     s.ksum = 1;
@@ -499,13 +517,8 @@ tp_status input_grad_sum(int dtype, int reduce, int n, int64_t T, int64_t w, int
 
 // dW_i = Xa_i^T Gb_i for every shard: Xa_i [T, M] (ld lda), Gb_i [T, N] (ld ldb): both
 // MN-major operands of a GEMM over the T tokens. dW_i fp32 [M, N].
-tp_status weight_grads(int dtype, int n, int64_t T, int64_t M, int64_t N,
-                       const void* const* Xa, int64_t lda, const void* const* Gb, int64_t ldb,
-                       void* const* dW, void* ws, cudaStream_t st, int tag) {
-  if (T == 0) {
-    for (int i = 0; i < n; ++i) TP_CUDA(zero_f32(dW[i], M * N, st), "zeroing weight gradient");
-    return TP_OK;
-  }
+GemmSpec wgrad_spec(int dtype, int n, int64_t T, int64_t M, int64_t N, const void* const* Xa,
+                    int64_t lda, const void* const* Gb, int64_t ldb, void* const* dW, void* ws) {
   GemmSpec s;
   s.M = M;
   s.N = N;
@@ -523,6 +536,17 @@ tp_status weight_grads(int dtype, int n, int64_t T, int64_t M, int64_t N,
     s.B[i] = Gb[i];
     s.D[i] = dW[i];
   }
+  return s;
+}
+
+tp_status weight_grads(int dtype, int n, int64_t T, int64_t M, int64_t N,
+                       const void* const* Xa, int64_t lda, const void* const* Gb, int64_t ldb,
+                       void* const* dW, void* ws, cudaStream_t st, int tag) {
+  if (T == 0) {
+    for (int i = 0; i < n; ++i) TP_CUDA(zero_f32(dW[i], M * N, st), "zeroing weight gradient");
+    return TP_OK;
+  }
+  const GemmSpec s = wgrad_spec(dtype, n, T, M, N, Xa, lda, Gb, ldb, dW, ws);
   TP_CUDA(run_gemm(s, dtype, st, tag), "weight-gradient GEMM");
   return TP_OK;
 }
@@ -736,6 +760,13 @@ tp_status tp_mlp_backward(const tp_mlp_desc* desc, const void* X, const void* co
   // dH_i = (dZ B_i^T) * act'(H_i), kept in the workspace in the input dtype.
   const size_t dh_off = scratch_base(dt);
   const void* dHp[kMaxShards] = {};
+  const void* dZs[kMaxShards] = {};
+  const void* Xs[kMaxShards] = {};
+  for (int i = 0; i < n; ++i) {
+    dZs[i] = dZ;
+    Xs[i] = X;
+  }
+  bool dB_done = false;
   if (z.T > 0) {
     GemmSpec s;
     s.M = z.T;
@@ -758,23 +789,41 @@ tp_status tp_mlp_backward(const tp_mlp_desc* desc, const void* X, const void* co
       s.aux[i] = Hsave ? Hsave[i] : nullptr;
       dHp[i] = s.D[i];
     }
-    TP_CUDA(run_gemm(s, dt, st, TP_TAG_ROW_DGRAD), "dY GEMM");
+    // dB_i = Y_i^T dZ needs only the forward's values: where the two fit one launch, its tiles
+    // and dH_i's share the pairs
+    const GemmSpec sb = wgrad_spec(dt, n, z.T, z.Fs, z.H, Ysave, z.Fs, dZs, z.H, dB, ws);
+    if (dt == TP_BF16 && tc_dual_eligible(sb, s)) {
+      TP_CUDA(run_gemm_dual(sb, s, dt, st, TP_TAG_ROW_GRADS), "dB and dY GEMMs");
+      dB_done = true;
+    } else {
+      TP_CUDA(run_gemm(s, dt, st, TP_TAG_ROW_DGRAD), "dY GEMM");
+    }
   } else {
     for (int i = 0; i < n; ++i) dHp[i] = ws_at<char>(ws, dh_off);
   }
 
   // dB_i = Y_i^T dZ.
-  const void* dZs[kMaxShards] = {};
-  for (int i = 0; i < n; ++i) dZs[i] = dZ;
-  TP_TRY(weight_grads(dt, n, z.T, z.Fs, z.H, Ysave, z.Fs, dZs, z.H, dB, ws, st, TP_TAG_ROW_WGRAD));
-  // dA_i = X^T dH_i.
-  const void* Xs[kMaxShards] = {};
-  for (int i = 0; i < n; ++i) Xs[i] = X;
-  TP_TRY(weight_grads(dt, n, z.T, z.H, z.Fs, Xs, z.H, dHp, z.Fs, dA, ws, st, TP_TAG_COLUMN_WGRAD));
-  // dX = sum_i dH_i A_i^T.
-  if (z.T > 0)
-    TP_TRY(input_grad_sum(dt, desc->reduce, n, z.T, z.Fs, z.H, dHp, z.Fs, A,
-                          static_cast<float*>(dX), ws, dh_off + z.dH, st));
+  if (!dB_done)
+    TP_TRY(weight_grads(dt, n, z.T, z.Fs, z.H, Ysave, z.Fs, dZs, z.H, dB, ws, st, TP_TAG_ROW_WGRAD));
+  // dA_i = X^T dH_i and dX = sum_i dH_i A_i^T: both need only dH_i; one launch where they fit
+  // it and the shard sum stays inside the dX GEMM's accumulator.
+  bool column_done = false;
+  if (z.T > 0 && dt == TP_BF16 && shard_split(desc->reduce, dt, z.T, z.H, z.Fs, n) == 1) {
+    const GemmSpec sa = wgrad_spec(dt, n, z.T, z.H, z.Fs, Xs, z.H, dHp, z.Fs, dA, ws);
+    GemmSpec sx = dgrad_spec(dt, n, z.T, z.Fs, z.H, dHp, z.Fs, A, ws);
+    sx.ksum = 1;
+    sx.D[0] = dX;
+    if (tc_dual_eligible(sa, sx)) {
+      TP_CUDA(run_gemm_dual(sa, sx, dt, st, TP_TAG_COLUMN_GRADS), "dA and dX GEMMs");
+      column_done = true;
+    }
+  }
+  if (!column_done) {
+    TP_TRY(weight_grads(dt, n, z.T, z.H, z.Fs, Xs, z.H, dHp, z.Fs, dA, ws, st, TP_TAG_COLUMN_WGRAD));
+    if (z.T > 0)
+      TP_TRY(input_grad_sum(dt, desc->reduce, n, z.T, z.Fs, z.H, dHp, z.Fs, A,
+                            static_cast<float*>(dX), ws, dh_off + z.dH, st));
+  }
   // db = sum_t dZ, da_i = sum_t dH_i.
   ColsumSeg segs[kMaxShards + 1];
   int nseg = 0;

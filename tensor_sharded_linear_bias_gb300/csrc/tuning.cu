@@ -11,8 +11,8 @@ std::atomic<int> g_tune[TP_TUNE_COUNT] = {
     {TP_TUNE_AUTO}, {TP_TUNE_AUTO}, {TP_TUNE_AUTO}, {TP_TUNE_AUTO},
     {TP_TUNE_AUTO}, {TP_TUNE_AUTO}, {TP_TUNE_AUTO}, {TP_TUNE_AUTO},
     {TP_TUNE_AUTO}, {TP_TUNE_AUTO}, {TP_TUNE_AUTO}, {TP_TUNE_AUTO}, {TP_TUNE_AUTO},
-    {TP_TUNE_AUTO}, {TP_TUNE_AUTO}, {TP_TUNE_AUTO}};
-static_assert(TP_TUNE_COUNT == 16, "one initialiser per knob");
+    {TP_TUNE_AUTO}, {TP_TUNE_AUTO}, {TP_TUNE_AUTO}, {TP_TUNE_AUTO}};
+static_assert(TP_TUNE_COUNT == 17, "one initialiser per knob");
 }  // namespace
 
 int tuning(int knob) { return g_tune[knob].load(std::memory_order_relaxed); }

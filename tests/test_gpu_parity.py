@@ -232,6 +232,37 @@ def test_issue_loop_variants(tp, tune, epi_warps):
                 assert all(np.array_equal(a, b) for a, b in pairs), (reduce, env, k)
 
 
+@pytest.mark.parametrize("T,H,F,n", [
+    (300, 136, 2 * 296, 2),    # ragged M, N and K in all four GEMMs
+    (600, 392, 2 * 264, 2),
+    (520, 264, 4 * 136, 4),
+    (257, 200, 16 * 136, 16),  # 16 shards: the most one shared launch takes
+])
+def test_two_gemm_launches(tp, tune, T, H, F, n):
+    """The backward's independent GEMMs in one SM-pair launch (dB_i with dY_i, dA_i with dX and
+    its shard sum), with the GeLU' epilogue and without an activation: matches the oracle, and
+    is bit-identical to separate launches (every tile runs the same K loop and epilogue; the
+    split tail, which adds K pieces in another order, is off in both)."""
+    tune.set("tail_split", 0)
+    w = SMALL.with_shape(tokens=T, hidden=H, ffn=F, tp_degree=n)
+    for act in (None, tp.TP_ACT_NONE):
+        outs = {}
+        for dual in (0, 1):
+            with tp.tuning(dual=dual):
+                case = MlpCase(w, 0, act=act)
+                tp.tp_trace_start(64)
+                case.run()
+                tags = [r["tag"] for r in tp.tp_trace_stop(64)]
+            assert ("row_grads" in tags and "column_grads" in tags) == bool(dual), (dual, tags)
+            outs[dual] = case.outputs()
+            if act is None and dual:
+                errs = compare_full(outs[dual], *full_reference(case))
+                assert max(errs.values()) <= TOL_BF16, errs
+        for k, v in outs[0].items():
+            pairs = zip(v, outs[1][k]) if isinstance(v, list) else [(v, outs[1][k])]
+            assert all(np.array_equal(a, b) for a, b in pairs), (act, k)
+
+
 _TAIL_REF = {}
 
 
@@ -593,13 +624,24 @@ def test_workload_attention_projections(tp, reduce):
 def test_trace_records_every_launch(tp):
     T, H, F, n = 256, 128, 2 * 256, 2
     c = MlpCase(SMALL.with_shape(tokens=T, hidden=H, ffn=F, tp_degree=n), 0)
-    tp.tp_trace_start(64)
-    c.run()
-    recs = tp.tp_trace_stop(64)
+    with tp.tuning(dual=0):
+        tp.tp_trace_start(64)
+        c.run()
+        recs = tp.tp_trace_stop(64)
     assert [r["tag"] for r in recs] == ["column_fwd", "row_fwd", "row_dgrad", "row_wgrad",
                                         "column_wgrad", "column_dgrad", "bias_grad"]
     assert sum(r["flops"] for r in recs if r["kernel"] == "gemm_tc") == 12 * T * H * F
     assert all(r["ms"] > 0 for r in recs)
+    # the backward's independent GEMMs in shared launches: dB_i with dY_i, dA_i with dX
+    H = 256
+    c = MlpCase(SMALL.with_shape(tokens=T, hidden=H, ffn=F, tp_degree=n), 0)
+    with tp.tuning(dual=1):
+        tp.tp_trace_start(64)
+        c.run()
+        recs = tp.tp_trace_stop(64)
+    assert [r["tag"] for r in recs] == ["column_fwd", "row_fwd", "row_grads", "column_grads",
+                                        "bias_grad"]
+    assert sum(r["flops"] for r in recs if r["kernel"] == "gemm_tc") == 12 * T * H * F
 
 
 # ----------------------------------------------------------------------------- few-token fp32
