@@ -613,12 +613,12 @@ __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
   pair_gemm<EPI_W, SUB>(OneGemm<A_MN, B_MN>{p});
 }
 
-// Two GEMMs in one launch: the first with both operands MN-major (weight gradients), the second
-// with both K-major (input gradients). One K block per ring stage.
-template <int EPI_W>
+// Two GEMMs in one launch with the given operand layouts (A0/B0 of the first, A1/B1 of the
+// second; true = MN-major). One K block per ring stage.
+template <bool A0, bool B0, bool A1, bool B1, int EPI_W>
 __global__ void __launch_bounds__(EpiShape<EPI_W>::THREADS, 1)
     tc2_dual_kernel(const __grid_constant__ tc::TcDual d) {
-  pair_gemm<EPI_W, 1>(TwoGemms<true, true, false, false>{d});
+  pair_gemm<EPI_W, 1>(TwoGemms<A0, B0, A1, B1>{d});
 }
 
 // Launch `kern` on clusters of two CTAs; max_clusters != nullptr asks for the occupancy limit
@@ -662,9 +662,10 @@ cudaError_t launch_pair(const TcParams& p, int clusters, cudaStream_t st, int* m
                                    max_clusters);
 }
 
-template <int EPI_W>
+template <bool A0, bool B0, bool A1, bool B1, int EPI_W>
 cudaError_t launch_dual(const tc::TcDual& d, int clusters, cudaStream_t st, int* max_clusters) {
-  return launch_pair_kernel<EPI_W>(tc2_dual_kernel<EPI_W>, d, clusters, st, max_clusters);
+  return launch_pair_kernel<EPI_W>(tc2_dual_kernel<A0, B0, A1, B1, EPI_W>, d, clusters, st,
+                                   max_clusters);
 }
 
 // The five instantiations of one operand layout: 4 or 8 epilogue warps with 1 or 2 K blocks

@@ -8,8 +8,9 @@ namespace tc {
 // 8 or 12 epilogue warps; max_clusters != nullptr asks for the occupancy limit only.
 cudaError_t run_pair_dual(const TcDual& d, int clusters, cudaStream_t st, int* max_clusters,
                           int epi_warps) {
-  if (epi_warps == 12) return tc2::launch_dual<12>(d, clusters, st, max_clusters);
-  return tc2::launch_dual<8>(d, clusters, st, max_clusters);
+  if (epi_warps == 12)
+    return tc2::launch_dual<true, true, false, false, 12>(d, clusters, st, max_clusters);
+  return tc2::launch_dual<true, true, false, false, 8>(d, clusters, st, max_clusters);
 }
 
 }  // namespace tc

@@ -492,12 +492,16 @@ cudaError_t launch_tc_gemm(const GemmSpec& s, cudaStream_t st) {
         plan_tail(p, max_clusters, p.kblocks * p.kpo, true);
     }
     // 12 epilogue warps for the GeLU / GeLU' tiles that 8 serve (short K) when the launch has
-    // no split tail tiles. Measured on GB300, same box, 4096 x 1024 x 4096 step: those GEMMs
-    // 3-4 % faster (column forward 46.7 vs 48.2 us, dY 50.1 vs 52.1), the step 1 % faster;
-    // forced on every GEMM, the weight gradients and the input gradient were slower.
+    // no split tail tiles, and for launches of at most one tile per pair (whose one epilogue is
+    // all exposed). Measured on GB300, same box, 4096 x 1024 x 4096 step: the GeLU / GeLU' GEMMs
+    // 3-4 % faster (column forward 46.7 vs 48.2 us, dY 50.1 vs 52.1), the step 1 % faster; its
+    // row GEMM (64 tiles of 64 K blocks) 33.8 vs 35.0 us. Forced on every GEMM of many tiles,
+    // the weight gradients and the input gradient were slower.
+    const bool one_tile_each = p.num_units <= pair_clusters(layout, 12);
     if (epi_warps == 8 && p.ksplit == 1 && tuning(TP_TUNE_EPI_WARPS) == TP_TUNE_AUTO &&
-        (p.epi == EPI_BIAS_ACT || p.epi == EPI_DACT) && p.act == TP_ACT_GELU_ERF &&
-        p.kblocks * p.kpo <= 64) {
+        (((p.epi == EPI_BIAS_ACT || p.epi == EPI_DACT) && p.act == TP_ACT_GELU_ERF &&
+          p.kblocks * p.kpo <= 64) ||
+         one_tile_each)) {
       epi_warps = 12;
       max_clusters = std::min(max_clusters, pair_clusters(layout, epi_warps));
     }
@@ -585,14 +589,10 @@ cudaError_t launch_tc_gemm_dual(const GemmSpec& s0, const GemmSpec& s1, cudaStre
   if (const cudaError_t e = fill_tc_params(d.q[0], s0, true, &l0); e != cudaSuccess) return e;
   if (const cudaError_t e = fill_tc_params(d.q[1], s1, true, &l1); e != cudaSuccess) return e;
   if (l0 != 2 || l1 != 1) return cudaErrorNotSupported;
-  // 12 epilogue warps when either GEMM has GeLU / GeLU' tiles of at most 64 K blocks (as for
-  // one GEMM), else 8; both GEMMs load A and B from two producer threads
-  const auto heavy = [](const TcParamsT<kDualMaxShards>& q) {
-    return (q.epi == EPI_BIAS_ACT || q.epi == EPI_DACT) && q.act == TP_ACT_GELU_ERF &&
-           q.kblocks * q.kpo <= 64;
-  };
-  int epi_warps = heavy(d.q[0]) || heavy(d.q[1]) ? 12 : 8;
-  if (const int v = tuning(TP_TUNE_EPI_WARPS); v == 8 || v == 12) epi_warps = v;
+  // 12 epilogue warps: GeLU' tiles of few K blocks are paced by their epilogues, and the last
+  // tiles' epilogues are exposed (measured on GB300, 4096 x 1024 x 4096 step: 0.2065 vs
+  // 0.2131 ms with 8). Both GEMMs load A and B from two producer threads.
+  const int epi_warps = tuning(TP_TUNE_EPI_WARPS) == 8 ? 8 : 12;
   for (int i = 0; i < 2; ++i) {
     d.q[i].split_loads = 1;
     d.q[i].mma_probe = mma_probe_enabled() ? 1 : 0;
