@@ -35,7 +35,7 @@ import workloads as wl  # noqa: E402
 METRIC = "TP-sharded MLP fwd+bwd TFLOP/s (bf16) on 1 GB300 and % of tensor-core peak"
 UNIT = "TFLOP/s"
 KERNEL_SOURCES = ["tc_gemm.cuh", "tc2_gemm.cuh", "tc_launch.cu", "tc_gemm_kmn.cu", "tc_gemm_kk.cu",
-                  "tc_gemm_mnmn.cu", "device_common.cuh"]
+                  "tc_gemm_mnmn.cu", "tc_gemm_dual.cu", "device_common.cuh"]
 # fp32 FFMA peak: 152 SMs x 128 lanes x 2 flops per FFMA x 2.07 GHz (maximum SM clock).
 FFMA_F32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 TRACE_PER_STEP = 24  # trace slots per step (launches per step are at most 16)
