@@ -237,6 +237,7 @@ def test_issue_loop_variants(tp, tune, epi_warps):
     (600, 392, 2 * 264, 2),
     (520, 264, 4 * 136, 4),
     (257, 200, 16 * 136, 16),  # 16 shards: the most one shared launch takes
+    (2048, 512, 2 * 1024, 2),  # more units than pairs: some pairs take two
 ])
 def test_two_gemm_launches(tp, tune, T, H, F, n):
     """The backward's independent GEMMs in one SM-pair launch (dB_i with dY_i, dA_i with dX and
