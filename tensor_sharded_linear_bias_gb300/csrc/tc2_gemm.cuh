@@ -1,10 +1,12 @@
 // The same grouped bf16 GEMM on pairs of SMs: tcgen05.mma.cta_group::2.
 //
 // A cluster of two CTAs (one per SM) computes a 256 x 256 output tile. Each CTA stages its own
-// 128 rows of A and its own 128-column half of B (32 KiB per stage, 6 stages); one MMA issued
-// by the even CTA reads both CTAs' shared memory and writes each CTA's 128 accumulator rows
-// (all 256 columns) into that CTA's TMEM. Per k block an SM takes in 32 KiB instead of the
-// 48 KiB of the one-SM 128 x 256 tile, for the same tensor work per SM.
+// 128 rows of A and its own 128-column half of B (32 KiB per 64-deep K block, a ring of 6
+// blocks, 5 with 12 epilogue warps); one MMA issued by the even CTA reads both CTAs' shared
+// memory and writes each CTA's 128 accumulator rows (all 256 columns) into that CTA's TMEM. Per
+// k block an SM takes in 32 KiB instead of the 48 KiB of the one-SM 128 x 256 tile, for the
+// same tensor work per SM. The clusters are persistent and walk a queue of work units (tiles,
+// or K pieces of split tail tiles) of one grouped GEMM, or of two independent GEMMs.
 //
 // Synchronisation (mbarriers; the even CTA is the "leader"):
 //   full[s]   leader only: the leader's A producer posts expect_tx for both halves (64 KiB);
