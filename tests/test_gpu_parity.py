@@ -273,6 +273,40 @@ def test_two_gemm_launches(tp, tune, T, H, F, n):
             assert all(np.array_equal(a, b) for a, b in pairs), (act, k)
 
 
+@pytest.mark.parametrize("dtype,T,H,F,n", [("bf16", 600, 392, 2 * 264, 2),     # shared backward launches
+                                           ("bf16", 2048, 512, 8 * 512, 8),    # split tail tiles
+                                           ("f32", 32, 768, 4 * 768, 4)])      # few-row fp32 kernel
+def test_step_captures_into_a_cuda_graph(tp, dtype, T, H, F, n):
+    """A whole step (forward and, for bf16, backward) can be captured into a CUDA graph: the
+    library makes no host synchronisation, allocation or device query on the launch path once
+    a first call has run, and a replay gives the eager step's outputs bit for bit."""
+    import torch
+
+    base = wl.P3_FP32_FWD if dtype == "f32" else SMALL
+    w = base.with_shape(tokens=T, hidden=H, ffn=F, tp_degree=n)
+    case = MlpCase(w, 2)
+    backward = dtype == "bf16"
+    case.run(backward=backward)
+    eager = case.outputs(backward=backward)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        case.forward()
+        if backward:
+            case.backward()
+    torch.cuda.synchronize()
+    for t in [case.Z, case.dX] + case.dA + case.dB + case.da + [case.db]:
+        t.fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
+    tp.tp_check_status(case.ws)
+    replayed = case.outputs(backward=backward)
+    for k, v in eager.items():
+        pairs = zip(v, replayed[k]) if isinstance(v, list) else [(v, replayed[k])]
+        assert all(np.array_equal(a, b) for a, b in pairs), k
+
+
 _TAIL_REF = {}
 
 
