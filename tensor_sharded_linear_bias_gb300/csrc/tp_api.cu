@@ -1035,10 +1035,25 @@ tp_status tp_linear_column_backward(const tp_linear_desc* desc, const void* X,
   }
   const void* Xs[kMaxShards] = {};
   for (int i = 0; i < n; ++i) Xs[i] = X;
-  TP_TRY(weight_grads(dt, n, z.T, z.K, z.Ns, Xs, z.K, dHp, ldh, dW, ws, st, TP_TAG_COLUMN_WGRAD));
-  if (z.T > 0)
-    TP_TRY(input_grad_sum(dt, desc->reduce, n, z.T, z.Ns, z.K, dHp, ldh, W,
-                          static_cast<float*>(dX), ws, dh_off + z.dH, st));
+  // dW_i = X^T dH_i and dX = sum_i dH_i W_i^T: one launch where they fit it and the shard sum
+  // stays inside the dX GEMM's accumulator (tc_dual_eligible)
+  bool shared = false;
+  if (z.T > 0 && dt == TP_BF16 && shard_split(desc->reduce, dt, z.T, z.K, z.Ns, n) == 1) {
+    const GemmSpec sw = wgrad_spec(dt, n, z.T, z.K, z.Ns, Xs, z.K, dHp, ldh, dW, ws);
+    GemmSpec sx = dgrad_spec(dt, n, z.T, z.Ns, z.K, dHp, ldh, W, ws);
+    sx.ksum = 1;
+    sx.D[0] = dX;
+    if (tc_dual_eligible(sw, sx)) {
+      TP_CUDA(run_gemm_dual(sw, sx, dt, st, TP_TAG_COLUMN_GRADS), "dW and dX GEMMs");
+      shared = true;
+    }
+  }
+  if (!shared) {
+    TP_TRY(weight_grads(dt, n, z.T, z.K, z.Ns, Xs, z.K, dHp, ldh, dW, ws, st, TP_TAG_COLUMN_WGRAD));
+    if (z.T > 0)
+      TP_TRY(input_grad_sum(dt, desc->reduce, n, z.T, z.Ns, z.K, dHp, ldh, W,
+                            static_cast<float*>(dX), ws, dh_off + z.dH, st));
+  }
   if (dbias != nullptr) {
     ColsumSeg segs[kMaxShards];
     for (int i = 0; i < n; ++i) segs[i] = ColsumSeg{dHp[i], static_cast<float*>(dbias[i]), z.Ns, ldh};
@@ -1103,6 +1118,18 @@ tp_status tp_linear_row_backward(const tp_linear_desc* desc, const void* const* 
       s.A[i] = dZ;
       s.B[i] = W[i];
       s.D[i] = dX[i];
+    }
+    // dW_i = X_i^T dZ needs only the inputs: one launch with dX_i where they fit it
+    const void* dZs[kMaxShards] = {};
+    for (int i = 0; i < n; ++i) dZs[i] = dZ;
+    const GemmSpec sw = wgrad_spec(dt, n, z.T, z.Ks, z.N, X, z.Ks, dZs, z.N, dW, ws);
+    if (dt == TP_BF16 && tc_dual_eligible(sw, s)) {
+      TP_CUDA(run_gemm_dual(sw, s, dt, st, TP_TAG_ROW_GRADS), "dW and dX GEMMs");
+      if (dbias != nullptr) {
+        ColsumSeg seg{dZ, static_cast<float*>(dbias), z.N, z.N};
+        TP_TRY(colsums(dt, z.T, &seg, 1, st));
+      }
+      return ok();
     }
     TP_CUDA(run_gemm(s, dt, st, TP_TAG_ROW_DGRAD), "row input-gradient GEMM");
   }

@@ -561,6 +561,78 @@ def test_row_linear(tp, dtype, reduce):
     assert rel(np64(db), dbr) <= tol
 
 
+@pytest.mark.parametrize("kind,gather,act", [("column", 0, 0), ("column", 1, 1), ("column", 0, 1),
+                                             ("row", 0, 0)])
+def test_linear_backward_shared_launches(tp, tune, kind, gather, act):
+    """The linear layers' backward with its weight-gradient and input-gradient GEMMs in one
+    SM-pair launch (column: dW_i with dX and its shard sum; row: dW_i with dX_i), gathered or
+    per-shard dY, with and without the activation: bit-identical to separate launches, and the
+    oracle's values."""
+    import torch
+
+    tune.set("tail_split", 0)
+    n = 4
+    if kind == "column":
+        T, K, N = 520, 264, 4 * 200
+    else:
+        T, K, N = 300, 4 * 136, 264
+    t, f = _lin_inputs(53, T, K, N, "bf16", "cuda")
+    desc = tp.LinearDesc(tokens=T, in_features=K, out_features=N, tp_degree=n, dtype=tp.TP_BF16,
+                         act=act, reduce=0, gather=gather)
+    ws = tp.new_workspace(tp.tp_linear_workspace_size(desc, tp.TP_COLUMN if kind == "column" else tp.TP_ROW))
+    f32 = dict(dtype=torch.float32, device="cuda")
+    outs = {}
+    for dual in (0, 1):
+        with tp.tuning(dual=dual):
+            tp.tp_trace_start(16)
+            if kind == "column":
+                Ns = N // n
+                W = [t["W"][:, i * Ns:(i + 1) * Ns].contiguous() for i in range(n)]
+                bias = [t["bias"][i * Ns:(i + 1) * Ns].contiguous() for i in range(n)]
+                Y = [torch.empty(T, N, dtype=torch.bfloat16, device="cuda")] if gather else \
+                    [torch.empty(T, Ns, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+                Hs = [torch.empty(T, Ns, dtype=torch.bfloat16, device="cuda") for _ in range(n)] if act else None
+                tp.tp_linear_column_forward(desc, t["X"], W, bias, Y, Hs, ws)
+                G = t["G"]
+                dY = [G] if gather else [G[:, i * Ns:(i + 1) * Ns].contiguous() for i in range(n)]
+                dX = torch.full((T, K), float("nan"), **f32)
+                dW = [torch.full((K, Ns), float("nan"), **f32) for _ in range(n)]
+                db = [torch.full((Ns,), float("nan"), **f32) for _ in range(n)]
+                tp.tp_linear_column_backward(desc, t["X"], W, Hs, dY, dX, dW, db, ws)
+                got = [dX] + dW + db
+            else:
+                Ks = K // n
+                X = [t["X"][:, i * Ks:(i + 1) * Ks].contiguous() for i in range(n)]
+                W = [t["W"][i * Ks:(i + 1) * Ks, :].contiguous() for i in range(n)]
+                dX = [torch.full((T, Ks), float("nan"), **f32) for _ in range(n)]
+                dW = [torch.full((Ks, N), float("nan"), **f32) for _ in range(n)]
+                db = torch.full((N,), float("nan"), **f32)
+                tp.tp_linear_row_backward(desc, X, W, t["G"], dX, dW, db, ws)
+                got = dX + dW + [db]
+            tags = [r["tag"] for r in tp.tp_trace_stop(16)]
+        tp.tp_check_status(ws)
+        torch.cuda.synchronize()
+        want = "column_grads" if kind == "column" else "row_grads"
+        assert (want in tags) == bool(dual), (dual, tags)
+        outs[dual] = [np64(x) for x in got]
+    assert all(np.array_equal(a, b) for a, b in zip(outs[0], outs[1]))
+    a = "gelu" if act else "none"
+    if kind == "column":
+        Wr = oracle.split_columns(f["W"], n)
+        Hr, _ = oracle.column_parallel_forward(f["X"], Wr, oracle.split_vector(f["bias"], n), a)
+        dXr, dWr, dbr, _ = oracle.column_parallel_backward(f["X"], Wr, Hr,
+                                                           oracle.split_columns(f["G"], n), a)
+        assert rel(outs[1][0], dXr) <= TOL_BF16
+        assert rel_shards(outs[1][1:1 + n], dWr) <= TOL_BF16
+        assert rel_shards(outs[1][1 + n:], dbr) <= TOL_BF16
+    else:
+        Xr, Wr = oracle.split_columns(f["X"], n), oracle.split_rows(f["W"], n)
+        dXr, dWr, dbr = oracle.row_parallel_backward(Xr, Wr, f["G"])
+        assert rel_shards(outs[1][:n], dXr) <= TOL_BF16
+        assert rel_shards(outs[1][n:2 * n], dWr) <= TOL_BF16
+        assert rel(outs[1][-1], dbr) <= TOL_BF16
+
+
 def test_many_shards(tp):
     w = SMALL.with_shape(tokens=96, hidden=64, ffn=64 * 8, tp_degree=64)
     case = MlpCase(w, 0).run()
