@@ -51,10 +51,10 @@ typedef enum tp_tune_knob {
   TP_TUNE_TAIL_PIECES = 14, /* upper bound (>= 1) on the K pieces of a split tail tile */
   TP_TUNE_FEW_ROWS = 15,    /* 0: fp32 products of <= 32 rows on the general FFMA kernel instead
                                of the bulk-copy one (forward layouts) */
-  TP_TUNE_DUAL = 16,        /* 0/1: the backward's independent bf16 GEMMs (dY_i with dB_i, dA_i with
-                               dX) in separate launches / in one SM-pair launch wherever they fit
-                               it (default: where one of them has at most one wave of tiles;
-                               bit-identical) */
+  TP_TUNE_DUAL = 16,        /* 0/1: the backward's independent bf16 GEMMs (MLP: dY_i with dB_i, dA_i
+                               with dX; linear layers: dW_i with dX) in separate launches / in one
+                               SM-pair launch wherever they fit it (default: where one of them has
+                               at most one wave of tiles; bit-identical) */
   TP_TUNE_COUNT = 17
 } tp_tune_knob;
 
